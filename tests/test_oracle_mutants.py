@@ -1,0 +1,62 @@
+"""The oracle's pins have teeth: plant plausible mistakes in copies of the
+oracle source (CPU only), rebuild, and check that a pin fails for each."""
+import ctypes
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
+
+# (name, original text, mutated text, pin that must fail)
+MUTANTS = [
+    ("ds_sign", "const double ds = p * (dp - Di);", "const double ds = p * (dp + Di);", "dense_fd"),
+    ("ds_dropped_D", "const double ds = p * (dp - Di);", "const double ds = p * dp;", "dense_fd"),
+    ("dk_no_scale", "dkj[x] += pb->scale * ds * qi[x];", "dkj[x] += ds * qi[x];", "dense_fd"),
+    ("dp_transposed_operand", "const double dp = dot(doi, vj, d);", "const double dp = dot(doi, kj, d);",
+     "dense_fd"),
+    ("causal_off_by_one", "if (mask == 1) return j <= i;", "if (mask == 1) return j < i;", "mask_bitmap"),
+    ("bottom_right_shift", "if (mask == 2) return j <= i + (lkv - lq);",
+     "if (mask == 2) return j <= i + (lq - lkv);", "mask_bitmap"),
+    ("nsa_scatter_index", "c->dk[((k0 + rows[r]) * pb->n2 + g) * d + x] += dksel[r * d + x];",
+     "c->dk[((k0 + r) * pb->n2 + g) * d + x] += dksel[r * d + x];", "nsa_fd"),
+    ("nsa_sum_ignored", "const double p = exp(pb->scale * dot(qi, ksel + r * d, d) - mx) / sm;",
+     "const double p = exp(pb->scale * dot(qi, ksel + r * d, d) - mx);", "nsa_fd"),
+]
+
+
+def _build_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new, 1))
+    so = tmp_path / f"{name}.so"
+    subprocess.check_call(["gcc", "-std=c11", "-O1", "-fPIC", "-shared", "-pthread",
+                           "-D_POSIX_C_SOURCE=200809L", "-o", str(so), str(path), "-lm"])
+    return ctypes.CDLL(str(so))
+
+
+def _run_pin(pin):
+    if pin == "dense_fd":
+        pins._check_dense_fd([5], [7], h=2, h_kv=1, d=3, scale=0.7, mask=oracle.CAUSAL_BOTTOM_RIGHT, seed=3)
+    elif pin == "mask_bitmap":
+        for mask, key in ((oracle.CAUSAL_TOP_LEFT, "top_left"), (oracle.CAUSAL_BOTTOM_RIGHT, "bottom_right")):
+            pins.test_mask_bitmaps(mask, key)
+    elif pin == "nsa_fd":
+        pins.test_nsa_finite_differences(0)
+    else:
+        raise ValueError(pin)
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name,old,new,pin", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pin_catches_mutant(tmp_path, monkeypatch, name, old, new, pin):
+    _run_pin(pin)  # the real oracle passes this pin
+    monkeypatch.setattr(oracle, "_lib", _build_mutant(tmp_path, name, old, new))
+    with pytest.raises(AssertionError):
+        _run_pin(pin)
