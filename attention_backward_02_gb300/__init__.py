@@ -1,0 +1,168 @@
+"""GB300 (sm_103a) SDPA backward (FlashAttention-2 form) and NSA selected-attention
+backward behind a C ABI (include/attnbwd.h).
+
+The functions here marshal torch CUDA tensors into the C ABI: pointers,
+strides, the caller's stream and a caller-sized workspace.  PyTorch only
+provides device memory and streams; all arithmetic runs in the library's
+CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+from . import _lib
+from ._lib import (ATTN_BF16, ATTN_CAUSAL_BOTTOM_RIGHT, ATTN_CAUSAL_TOP_LEFT, ATTN_F16, ATTN_MASK_NONE,
+                   AttnError, attn_nsa_desc_t, attn_sdpa_desc_t, attn_view_t, check)
+
+__all__ = ["sdpa_desc", "nsa_desc", "view_bhsd", "view_tnd", "sdpa_workspace_size", "sdpa_fwd_stats",
+           "sdpa_bwd", "nsa_workspace_size", "nsa_selected_attn_bwd", "nsa_block_lists",
+           "attn_query_status", "AttnError", "ATTN_F16", "ATTN_BF16", "ATTN_MASK_NONE",
+           "ATTN_CAUSAL_TOP_LEFT", "ATTN_CAUSAL_BOTTOM_RIGHT"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError(f"fp16 or bf16 expected, got {t.dtype}")
+
+
+def _stream_ptr(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+class _Keep:
+    """Holds ctypes arrays alive for the duration of a call."""
+
+    def __init__(self):
+        self.items = []
+
+
+def _cu_array(keep, cu):
+    if cu is None:
+        return None
+    arr = (C.c_int64 * len(cu))(*[int(x) for x in cu])
+    keep.items.append(arr)
+    return C.cast(arr, C.POINTER(C.c_int64))
+
+
+def sdpa_desc(*, dtype, b, h, h_kv, s_q, s_kv, d, scale, mask=ATTN_MASK_NONE, cu_seqlens_q=None,
+              cu_seqlens_kv=None, deterministic=False, dq_splits=0, _keep=None):
+    keep = _keep if _keep is not None else _Keep()
+    desc = attn_sdpa_desc_t(int(dtype), int(b), int(h), int(h_kv), int(s_q), int(s_kv), int(d), float(scale),
+                            int(mask), _cu_array(keep, cu_seqlens_q), _cu_array(keep, cu_seqlens_kv),
+                            int(bool(deterministic)), int(dq_splits))
+    desc._keep = keep
+    return desc
+
+
+def nsa_desc(*, dtype, cu_seqlens_q, cu_seqlens_kv, n1, n2, d, scale, block_size, block_count, sparse_mode,
+             deterministic=False):
+    keep = _Keep()
+    desc = attn_nsa_desc_t(int(dtype), len(cu_seqlens_q), _cu_array(keep, cu_seqlens_q),
+                           _cu_array(keep, cu_seqlens_kv), int(n1), int(n2), int(d), float(scale),
+                           int(block_size), int(block_count), int(sparse_mode), int(bool(deterministic)))
+    desc._keep = keep
+    return desc
+
+
+def view_bhsd(t) -> attn_view_t:
+    """A [B, H, S, D] tensor (any strides, innermost 1) as an attn_view_t."""
+    if t.dim() != 4 or (t.shape[-1] > 1 and t.stride(-1) != 1):
+        raise ValueError("expected a [B,H,S,D] tensor with unit innermost stride")
+    sb, sh, ss, _ = t.stride()
+    return attn_view_t(t.data_ptr(), sb, sh, ss)
+
+
+def view_tnd(t) -> attn_view_t:
+    """A packed [T, H, D] tensor as an attn_view_t (token stride = ss)."""
+    if t.dim() != 3 or (t.shape[-1] > 1 and t.stride(-1) != 1):
+        raise ValueError("expected a [T,H,D] tensor with unit innermost stride")
+    st, sh, _ = t.stride()
+    return attn_view_t(t.data_ptr(), 0, sh, st)
+
+
+def sdpa_workspace_size(desc):
+    fwd, bwd = C.c_size_t(), C.c_size_t()
+    check(_lib.load().sdpa_workspace_size(C.byref(desc), C.byref(fwd), C.byref(bwd)), "sdpa_workspace_size")
+    return fwd.value, bwd.value
+
+
+def _workspace(nbytes, device, workspace):
+    torch = _torch()
+    if workspace is not None:
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def sdpa_fwd_stats(desc, q, k, v, o, lse, *, workspace=None, stream=None):
+    """q, k, v, o: views (attn_view_t) or tensors; lse: fp32 CUDA tensor."""
+    fwd, _ = sdpa_workspace_size(desc)
+    ws = _workspace(fwd, lse.device, workspace)
+    vq, vk, vv, vo = (x if isinstance(x, attn_view_t) else view_bhsd(x) for x in (q, k, v, o))
+    st = _lib.load().sdpa_fwd_stats(C.byref(desc), vq, vk, vv, vo,
+                                    C.cast(C.c_void_p(lse.data_ptr()), C.POINTER(C.c_float)),
+                                    C.c_void_p(ws.data_ptr()), C.c_size_t(ws.numel()), C.c_void_p(_stream_ptr(stream)))
+    check(st, "sdpa_fwd_stats")
+    return ws
+
+
+def sdpa_bwd(desc, q, k, v, o, dO, lse, dQ, dK, dV, *, workspace=None, stream=None):
+    _, bwd = sdpa_workspace_size(desc)
+    ws = _workspace(bwd, lse.device, workspace)
+    views = [x if isinstance(x, attn_view_t) else view_bhsd(x) for x in (q, k, v, o, dO, dQ, dK, dV)]
+    st = _lib.load().sdpa_bwd(C.byref(desc), *views[:5],
+                              C.cast(C.c_void_p(lse.data_ptr()), C.POINTER(C.c_float)), *views[5:],
+                              C.c_void_p(ws.data_ptr()), C.c_size_t(ws.numel()), C.c_void_p(_stream_ptr(stream)))
+    check(st, "sdpa_bwd")
+    return ws
+
+
+def nsa_workspace_size(desc):
+    n = C.c_size_t()
+    check(_lib.load().nsa_workspace_size(C.byref(desc), C.byref(n)), "nsa_workspace_size")
+    return n.value
+
+
+def nsa_selected_attn_bwd(desc, q, k, v, o, dO, softmax_max, softmax_sum, topk, dq, dk, dv, *, workspace=None,
+                          stream=None):
+    ws = _workspace(nsa_workspace_size(desc), q.device, workspace)
+    fp = lambda t: C.cast(C.c_void_p(t.data_ptr()), C.POINTER(C.c_float))
+    st = _lib.load().nsa_selected_attn_bwd(
+        C.byref(desc), *(C.c_void_p(t.data_ptr()) for t in (q, k, v, o, dO)), fp(softmax_max), fp(softmax_sum),
+        C.cast(C.c_void_p(topk.data_ptr()), C.POINTER(C.c_int32)),
+        *(C.c_void_p(t.data_ptr()) for t in (dq, dk, dv)), C.c_void_p(ws.data_ptr()), C.c_size_t(ws.numel()),
+        C.c_void_p(_stream_ptr(stream)))
+    check(st, "nsa_selected_attn_bwd")
+    return ws
+
+
+def nsa_block_lists(desc, topk, offsets, tokens, *, workspace=None, stream=None):
+    """Fills device int32 tensors offsets / tokens; returns nblk_max."""
+    ws = _workspace(nsa_workspace_size(desc), topk.device, workspace)
+    ip = lambda t: C.cast(C.c_void_p(t.data_ptr()), C.POINTER(C.c_int32))
+    nblk = C.c_int64()
+    st = _lib.load().nsa_block_lists(C.byref(desc), ip(topk), ip(offsets), ip(tokens), C.byref(nblk),
+                                     C.c_void_p(ws.data_ptr()), C.c_size_t(ws.numel()),
+                                     C.c_void_p(_stream_ptr(stream)))
+    check(st, "nsa_block_lists")
+    return nblk.value, ws
+
+
+def attn_query_status(workspace, stream=None):
+    """Synchronises the stream; returns the device status bits (0 = clean)."""
+    flags = C.c_uint32()
+    st = _lib.load().attn_query_status(C.c_void_p(workspace.data_ptr()), C.c_void_p(_stream_ptr(stream)),
+                                       C.byref(flags))
+    if st not in (_lib.ATTN_OK, _lib.ATTN_ERR_DEVICE):
+        check(st, "attn_query_status")
+    return flags.value

@@ -1,0 +1,108 @@
+// common.cuh -- types and small device helpers shared by the kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attnbwd.h"
+
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxSeq = 256;  // sequences a packed (varlen) call may hold
+
+// ---------------------------------------------------------------- 16-bit I/O
+template <class T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<__half>(__half x) { return __half2float(x); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <class T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// two floats -> packed pair of 16-bit values (low half = a), round to nearest even
+template <class T> __device__ __forceinline__ uint32_t pack2(float a, float b);
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b)
+{
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// packed pair -> two floats
+template <class T> __device__ __forceinline__ float2 unpack2(uint32_t u);
+template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t u)
+{
+    __half2 h = *reinterpret_cast<__half2 *>(&u);
+    return __half22float2(h);
+}
+template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t u)
+{
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&u);
+    return __bfloat1622float2(h);
+}
+
+// ------------------------------------------------------- sequence geometry
+// A fixed-length batch: sequence b covers query rows [b*s_q, (b+1)*s_q) of the
+// token-major index space.  Packed: starts from inclusive cumulative lengths.
+struct FixedGeo {
+    int64_t nseq, s_q, s_kv;
+    __host__ __device__ int64_t q_start(int64_t b) const { return b * s_q; }
+    __host__ __device__ int64_t kv_start(int64_t b) const { return b * s_kv; }
+    __host__ __device__ int64_t q_len(int64_t) const { return s_q; }
+    __host__ __device__ int64_t kv_len(int64_t) const { return s_kv; }
+};
+
+struct PackedGeo {
+    int64_t nseq;
+    int64_t cu_q[kMaxSeq + 1];   // cu_q[0] = 0, cu_q[b+1] = end of sequence b
+    int64_t cu_kv[kMaxSeq + 1];
+    __host__ __device__ int64_t q_start(int64_t b) const { return cu_q[b]; }
+    __host__ __device__ int64_t kv_start(int64_t b) const { return cu_kv[b]; }
+    __host__ __device__ int64_t q_len(int64_t b) const { return cu_q[b + 1] - cu_q[b]; }
+    __host__ __device__ int64_t kv_len(int64_t b) const { return cu_kv[b + 1] - cu_kv[b]; }
+};
+
+// Visibility of key j to query i (both local to their sequence).
+__host__ __device__ __forceinline__ bool visible(int mask, int64_t i, int64_t j, int64_t lq, int64_t lkv)
+{
+    if (mask == ATTN_CAUSAL_TOP_LEFT) return j <= i;
+    if (mask == ATTN_CAUSAL_BOTTOM_RIGHT) return j <= i + (lkv - lq);
+    return true;
+}
+
+// Largest key index visible to query i, or lkv-1 with no mask (may be < 0).
+__host__ __device__ __forceinline__ int64_t last_visible_key(int mask, int64_t i, int64_t lq, int64_t lkv)
+{
+    if (mask == ATTN_CAUSAL_TOP_LEFT) return i < lkv - 1 ? i : lkv - 1;
+    if (mask == ATTN_CAUSAL_BOTTOM_RIGHT) {
+        int64_t j = i + (lkv - lq);
+        return j < lkv - 1 ? j : lkv - 1;
+    }
+    return lkv - 1;
+}
+
+// First query that sees key j (queries before it see nothing of column j).
+__host__ __device__ __forceinline__ int64_t first_query_seeing(int mask, int64_t j, int64_t lq, int64_t lkv)
+{
+    if (mask == ATTN_CAUSAL_TOP_LEFT) return j;
+    if (mask == ATTN_CAUSAL_BOTTOM_RIGHT) {
+        int64_t i = j - (lkv - lq);
+        return i > 0 ? i : 0;
+    }
+    return 0;
+}
+
+// ----------------------------------------------------------- status word
+__device__ __forceinline__ void raise_flag(uint32_t *status, uint32_t bit)
+{
+    if (status) atomicOr(status, bit);
+}
+
+}  // namespace attn

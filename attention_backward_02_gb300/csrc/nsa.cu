@@ -1,0 +1,346 @@
+// nsa.cu -- NSA selected-attention backward (Ascend CANN page
+// "aclnnNsaSelectedAttentionGrad", Function / Formula):
+//   selectedKey = Gather(key, topkIndices), selectedValue = Gather(value, ...)
+//   then the attention backward on the gathered rows, with dK / dV of every
+//   gathered row added back to the key / value row it came from.
+//
+// Kernels:
+//   nsa_preprocess   LSE2 = (softmaxMax + ln softmaxSum) * log2 e (lane 0 of the
+//                    8-wide stats), D = rowsum(dO * O), zeroed dK/dV accumulators
+//   block lists      per (sequence, kv head, block): ascending list of the
+//                    tokens that selected the block and see at least one of
+//                    its keys (bitmap -> count -> scan -> ordered emit), with
+//                    validation of every index (range, duplicates)
+//   nsa_bwd_simt     CUDA-core backward: one CTA per (token, kv head)
+//   nsa_finalize     dK, dV = cast(fp32 accumulators)
+#include <math.h>
+
+#include "plan.h"
+
+namespace attn {
+
+__device__ __forceinline__ int64_t seq_of_token(const PackedGeo &g, int64_t t)
+{
+    int64_t lo = 0, hi = g.nseq - 1;  // first b with t < cu_q[b+1]
+    while (lo < hi) {
+        int64_t mid = (lo + hi) / 2;
+        if (t < g.cu_q[mid + 1]) hi = mid;
+        else lo = mid + 1;
+    }
+    return lo;
+}
+
+// ------------------------------------------------------------- preprocess
+// grid (ceil(t1_pad / 128), n1), 256 threads, 16 threads per 128-wide row.
+template <class T>
+__global__ void __launch_bounds__(256) nsa_preprocess_kernel(NsaArgs a)
+{
+    const int64_t h = blockIdx.y;
+    const int lane = threadIdx.x % 16;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.status = 0u;
+    for (int r = threadIdx.x / 16; r < 128; r += 16) {
+        const int64_t t = int64_t(blockIdx.x) * 128 + r;
+        const bool live = t < a.t1_pad;  // no early exit: the row's threads shuffle below
+        const int64_t row = h * a.t1_pad + t;
+        float dsum = 0.f;
+        if (t < a.t1) {
+            const int64_t off = (t * a.n1 + h) * a.d + lane * 8;
+            uint4 ov = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.o) + off);
+            uint4 dv = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.dO) + off);
+            const uint32_t *op = &ov.x, *dp = &dv.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float2 of = unpack2<T>(op[e]), df = unpack2<T>(dp[e]);
+                dsum += of.x * df.x + of.y * df.y;
+            }
+        }
+        for (int off = 8; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+        if (!live) continue;
+        if (lane == 0) {
+            float lse2 = INFINITY;
+            if (t < a.t1) {
+                const float mx = a.smax[(t * a.n1 + h) * 8], sm = a.ssum[(t * a.n1 + h) * 8];
+                if (sm > 0.f && mx != -INFINITY) lse2 = (mx + logf(sm)) * kLog2e;
+            }
+            a.lse2[row] = lse2;
+            a.dvec[row] = t < a.t1 ? dsum : 0.f;
+        }
+    }
+}
+
+// ------------------------------------------------------------ block lists
+// Mark: one thread per (token, kv head).
+__global__ void nsa_mark_kernel(NsaArgs a, PackedGeo geo)
+{
+    const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= a.t1 * a.n2) return;
+    const int64_t t = idx / a.n2, g = idx % a.n2;
+    const int64_t b = seq_of_token(geo, t);
+    const int64_t i = t - geo.cu_q[b], lq = geo.q_len(b), lkv = geo.kv_len(b);
+    const int64_t nblk = lkv / a.bs;
+    const int32_t *ids = a.topk + idx * a.cnt;
+    for (int64_t c = 0; c < a.cnt; ++c) {
+        const int32_t blk = ids[c];
+        if (blk < 0 || blk >= nblk) {
+            raise_flag(a.status, ATTN_DEV_INDEX_RANGE);
+            continue;
+        }
+        bool dup = false;
+        for (int64_t c2 = 0; c2 < c; ++c2) dup |= ids[c2] == blk;
+        if (dup) {
+            raise_flag(a.status, ATTN_DEV_INDEX_DUP);
+            continue;
+        }
+        // the block's first key is the one most likely to be visible
+        if (a.sparse_mode == 2 && !visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, int64_t(blk) * a.bs, lq, lkv)) continue;
+        const int64_t row = (b * a.n2 + g) * a.nblk_max + blk;
+        atomicOr(a.bitmap + row * a.words_max + i / 32, 1u << (i % 32));
+    }
+}
+
+// Count: one warp per row; counts land in offsets[row + 1].
+__global__ void nsa_count_kernel(NsaArgs a)
+{
+    const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= a.nrows) return;
+    int n = 0;
+    for (int64_t w = lane; w < a.words_max; w += 32) n += __popc(a.bitmap[row * a.words_max + w]);
+    for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+    if (lane == 0) a.offsets[row + 1] = n;
+    if (row == 0 && lane == 0) a.offsets[0] = 0;
+}
+
+// Scan: one CTA of 1024 threads, inclusive scan of offsets[1..nrows] in chunks.
+__global__ void __launch_bounds__(1024) nsa_scan_kernel(NsaArgs a)
+{
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
+    for (int64_t base = 0; base < a.nrows; base += 1024) {
+        const int64_t r = base + threadIdx.x;
+        int32_t v = r < a.nrows ? a.offsets[r + 1] : 0;
+        for (int off = 1; off < 32; off <<= 1) {
+            int32_t u = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += u;
+        }
+        if (lane == 31) warp_tot[wid] = v;
+        __syncthreads();
+        if (wid == 0) {
+            int32_t w = warp_tot[lane];
+            for (int off = 1; off < 32; off <<= 1) {
+                int32_t u = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += u;
+            }
+            warp_tot[lane] = w;
+        }
+        __syncthreads();
+        const int32_t prefix = carry + (wid ? warp_tot[wid - 1] : 0);
+        if (r < a.nrows) a.offsets[r + 1] = prefix + v;
+        __syncthreads();
+        if (threadIdx.x == 1023) carry = prefix + v;
+        __syncthreads();
+    }
+}
+
+// Emit: one warp per row walks its bitmap words in order (stable by token).
+__global__ void nsa_emit_kernel(NsaArgs a, PackedGeo geo)
+{
+    const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= a.nrows) return;
+    const int64_t b = row / (a.n2 * a.nblk_max);
+    int32_t pos = a.offsets[row];
+    for (int64_t w0 = 0; w0 < a.words_max; w0 += 32) {
+        const int64_t w = w0 + lane;
+        uint32_t bits = w < a.words_max ? a.bitmap[row * a.words_max + w] : 0u;
+        int n = __popc(bits), incl = n;
+        for (int off = 1; off < 32; off <<= 1) {
+            int u = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += u;
+        }
+        int32_t my = pos + incl - n;
+        while (bits) {
+            int bit = __ffs(bits) - 1;
+            bits &= bits - 1;
+            a.tokens[my++] = int32_t(geo.cu_q[b] + w * 32 + bit);
+        }
+        pos += __shfl_sync(0xffffffffu, incl, 31);
+    }
+}
+
+// ------------------------------------------------------------ main (CUDA cores)
+// One CTA per (token, kv head); loops over the selected blocks.  dQ rows of
+// the token are owned by the CTA; dK / dV go to fp32 accumulators.
+template <class T>
+__global__ void __launch_bounds__(256) nsa_bwd_simt_kernel(NsaArgs a, PackedGeo geo)
+{
+    constexpr int D = 128, LD = D + 1;
+    extern __shared__ float smem[];
+    const int G = int(a.n1 / a.n2), BS = int(a.bs);
+    float(*Ks)[LD] = reinterpret_cast<float(*)[LD]>(smem);
+    float(*Vs)[LD] = reinterpret_cast<float(*)[LD]>(smem + BS * LD);
+    float(*Qs)[LD] = reinterpret_cast<float(*)[LD]>(smem + 2 * BS * LD);
+    float(*dOs)[LD] = reinterpret_cast<float(*)[LD]>(smem + 2 * BS * LD + G * LD);
+    float *Ps = smem + 2 * BS * LD + 2 * G * LD;  // [G][BS]
+    float *dSs = Ps + G * BS;
+    float *lse_s = dSs + G * BS;
+    float *d_s = lse_s + G;
+
+    const int64_t t = blockIdx.x, g = blockIdx.y;
+    const int64_t b = seq_of_token(geo, t);
+    const int64_t i = t - geo.cu_q[b], lq = geo.q_len(b), lkv = geo.kv_len(b), k0 = geo.cu_kv[b];
+    const int tid = threadIdx.x;
+    const float c = a.scale * kLog2e;
+    const T *Q = static_cast<const T *>(a.q), *K = static_cast<const T *>(a.k);
+    const T *V = static_cast<const T *>(a.v), *dO = static_cast<const T *>(a.dO);
+
+    for (int e = tid; e < G * D; e += 256) {
+        int hh = e / D, x = e % D;
+        int64_t off = (t * a.n1 + g * G + hh) * D + x;
+        Qs[hh][x] = to_f32(Q[off]);
+        dOs[hh][x] = to_f32(dO[off]);
+    }
+    if (tid < G) {
+        lse_s[tid] = a.lse2[(g * G + tid) * a.t1_pad + t];
+        d_s[tid] = a.dvec[(g * G + tid) * a.t1_pad + t];
+    }
+    // thread owns dQ features of (head hh_q, x range)
+    const int per = (G * D + 255) / 256;
+    float dq[16];
+    for (int e = 0; e < 16; ++e) dq[e] = 0.f;
+    const int32_t *ids = a.topk + (t * a.n2 + g) * a.cnt;
+    const int64_t nblk = lkv / a.bs;
+    for (int64_t cc = 0; cc < a.cnt; ++cc) {
+        const int64_t blk = ids[cc];
+        if (blk < 0 || blk >= nblk) continue;  // flagged by the mark kernel
+        bool dup = false;
+        for (int64_t c2 = 0; c2 < cc; ++c2) dup |= ids[c2] == blk;
+        if (dup) continue;
+        const int64_t j0 = blk * a.bs;
+        __syncthreads();
+        for (int e = tid; e < BS * D; e += 256) {
+            int r = e / D, x = e % D;
+            Ks[r][x] = to_f32(K[((k0 + j0 + r) * a.n2 + g) * D + x]);
+            Vs[r][x] = to_f32(V[((k0 + j0 + r) * a.n2 + g) * D + x]);
+        }
+        __syncthreads();
+        for (int e = tid; e < G * BS; e += 256) {
+            int hh = e / BS, r = e % BS;
+            bool vis = a.sparse_mode != 2 || visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, j0 + r, lq, lkv);
+            float s = 0.f, dp = 0.f;
+            if (vis) {
+#pragma unroll 8
+                for (int x = 0; x < D; ++x) {
+                    s += Qs[hh][x] * Ks[r][x];
+                    dp += dOs[hh][x] * Vs[r][x];
+                }
+            }
+            float p = (vis && lse_s[hh] != INFINITY) ? exp2f(s * c - lse_s[hh]) : 0.f;
+            Ps[hh * BS + r] = p;
+            dSs[hh * BS + r] = p * (dp - d_s[hh]);
+        }
+        __syncthreads();
+        for (int e = 0; e < per; ++e) {
+            int f = tid + e * 256;
+            if (f >= G * D) break;
+            int hh = f / D, x = f % D;
+            float acc = 0.f;
+            for (int r = 0; r < BS; ++r) acc += dSs[hh * BS + r] * Ks[r][x];
+            dq[e] += acc;
+        }
+        for (int f = tid; f < BS * D; f += 256) {
+            int r = f / D, x = f % D;
+            float dk = 0.f, dv = 0.f;
+            for (int hh = 0; hh < G; ++hh) {
+                dk += dSs[hh * BS + r] * Qs[hh][x];
+                dv += Ps[hh * BS + r] * dOs[hh][x];
+            }
+            int64_t off = ((k0 + j0 + r) * a.n2 + g) * D + x;
+            atomicAdd(a.dkacc + off, dk * a.scale);
+            atomicAdd(a.dvacc + off, dv);
+        }
+    }
+    T *dQ = static_cast<T *>(a.dq);
+    for (int e = 0; e < per; ++e) {
+        int f = tid + e * 256;
+        if (f >= G * D) break;
+        int hh = f / D, x = f % D;
+        dQ[(t * a.n1 + g * G + hh) * D + x] = from_f32<T>(dq[e] * a.scale);
+    }
+}
+
+template <class T>
+__global__ void nsa_finalize_kernel(NsaArgs a)
+{
+    const int64_t n = a.t2 * a.n2 * a.d;
+    T *dK = static_cast<T *>(a.dk), *dV = static_cast<T *>(a.dv);
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += int64_t(gridDim.x) * blockDim.x) {
+        dK[e] = from_f32<T>(a.dkacc[e]);
+        dV[e] = from_f32<T>(a.dvacc[e]);
+    }
+}
+
+namespace {
+// bitmap must be zero on entry
+cudaError_t block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
+{
+    if (a.t1 > 0) nsa_mark_kernel<<<unsigned((a.t1 * a.n2 + 255) / 256), 256, 0, s>>>(a, g);
+    if (a.nrows > 0) {
+        nsa_count_kernel<<<unsigned((a.nrows * 32 + 255) / 256), 256, 0, s>>>(a);
+        nsa_scan_kernel<<<1, 1024, 0, s>>>(a);
+        nsa_emit_kernel<<<unsigned((a.nrows * 32 + 255) / 256), 256, 0, s>>>(a, g);
+    }
+    return cudaGetLastError();
+}
+
+template <class T>
+cudaError_t run_nsa(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, cudaEvent_t before, cudaEvent_t after)
+{
+    cudaError_t e;
+    if (a.t1 > 0) {
+        dim3 grid(unsigned((a.t1_pad + 127) / 128), unsigned(a.n1));
+        nsa_preprocess_kernel<T><<<grid, 256, 0, s>>>(a);
+    }
+    size_t bitmap_bytes = size_t(a.nrows) * size_t(a.words_max) * sizeof(uint32_t);
+    if (bitmap_bytes && (e = cudaMemsetAsync(a.bitmap, 0, bitmap_bytes, s)) != cudaSuccess) return e;
+    size_t acc_bytes = size_t(a.t2) * size_t(a.n2 * a.d) * sizeof(float);
+    if (acc_bytes) {
+        if ((e = cudaMemsetAsync(a.dkacc, 0, acc_bytes, s)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(a.dvacc, 0, acc_bytes, s)) != cudaSuccess) return e;
+    }
+    if ((e = block_lists(a, g, s)) != cudaSuccess) return e;
+    if (a.t1 > 0) {
+        const int G = int(a.n1 / a.n2), BS = int(a.bs), LD = 129;
+        size_t smem = sizeof(float) * (2 * BS * LD + 2 * G * LD + 2 * G * BS + 2 * G);
+        auto k = nsa_bwd_simt_kernel<T>;
+        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) != cudaSuccess)
+            return e;
+        if (before && (e = cudaEventRecord(before, s)) != cudaSuccess) return e;
+        k<<<dim3(unsigned(a.t1), unsigned(a.n2)), 256, smem, s>>>(a, g);
+        if (after && (e = cudaEventRecord(after, s)) != cudaSuccess) return e;
+    }
+    if (a.t2 > 0) nsa_finalize_kernel<T><<<1024, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_nsa_block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
+{
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s)) != cudaSuccess) return e;
+    size_t bitmap_bytes = size_t(a.nrows) * size_t(a.words_max) * sizeof(uint32_t);
+    if (bitmap_bytes && (e = cudaMemsetAsync(a.bitmap, 0, bitmap_bytes, s)) != cudaSuccess) return e;
+    return block_lists(a, g, s);
+}
+
+cudaError_t launch_nsa_bwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, cudaEvent_t before,
+                           cudaEvent_t after)
+{
+    return a.dtype == ATTN_F16 ? run_nsa<__half>(a, g, s, before, after)
+                               : run_nsa<__nv_bfloat16>(a, g, s, before, after);
+}
+
+}  // namespace attn

@@ -1,0 +1,90 @@
+// plan.h -- host-side argument bundles handed from the C ABI (api.cu) to the
+// kernel launchers.  Private to the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace attn {
+
+// A 16-bit tensor: element offset of (b, h, token) is
+//   b * sb + h * sh + (start_b + i) * ss
+// with sb = 0 and start_b from the cumulative lengths in packed mode, and
+// start_b = 0 in fixed-length mode.
+struct View {
+    void *ptr;
+    int64_t sb, sh, ss;
+};
+
+// Workspace of sdpa_bwd (all offsets 256-byte aligned):
+//   status   uint32[64]
+//   lse2     f32 [h][t_pad]          LSE * log2(e); +inf on padding rows
+//   dvec     f32 [h][t_pad]          D = rowsum(dO * O); 0 on padding rows
+//   dqacc    f32 [n_part][h][t_pad][d]
+// Row index of (head hq, token t) is hq * t_pad + t, where t is the token in
+// the packed index space (b * s_q + i for a fixed-length batch).
+struct DenseArgs {
+    int dtype;                  // ATTN_F16 / ATTN_BF16
+    int64_t nseq, h, h_kv, d;
+    int64_t t_q, t_kv, t_pad;   // total query / key tokens, padded row count
+    float scale;
+    int mask;
+    int deterministic, n_part;  // n_part partial dQ buffers (1 unless deterministic)
+    bool packed;
+    View q, k, v, o, dO, dQ, dK, dV;
+    const float *lse;           // caller's stats ([B][h][s_q] or [h][T_q])
+    float *lse_out;             // forward: where the stats go
+    uint32_t *status;
+    float *lse2, *dvec, *dqacc;
+};
+
+struct Workspace {
+    static constexpr size_t kAlign = 256;
+    static size_t align(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+};
+
+// NSA workspace (all offsets 256-byte aligned):
+//   status   uint32[64]
+//   lse2     f32 [n1][t1_pad]       (max + ln sum) * log2(e)
+//   dvec     f32 [n1][t1_pad]
+//   bitmap   uint32 [nseq][n2][nblk_max][words_max]   token bits per block
+//   counts   int32 [nrows + 1]      then offsets (exclusive scan), in place
+//   tokens   int32 [t1 * n2 * cnt]  block lists, ascending token ids
+//   dqacc    f32 [n_part][t1_pad][n1][d]
+//   dkacc    f32 [t2][n2][d], dvacc f32 [t2][n2][d]
+struct NsaArgs {
+    int dtype;
+    int64_t nseq, n1, n2, d, bs, cnt;
+    int64_t t1, t2, t1_pad;
+    int64_t nblk_max, words_max, nrows;   // nrows = nseq * n2 * nblk_max
+    float scale;
+    int sparse_mode, deterministic, n_part;
+    const void *q, *k, *v, *o, *dO;
+    const float *smax, *ssum;
+    const int32_t *topk;
+    void *dq, *dk, *dv;
+    uint32_t *status;
+    float *lse2, *dvec;
+    uint32_t *bitmap;
+    int32_t *offsets, *tokens;
+    float *dqacc, *dkacc, *dvacc;
+};
+
+// ------------------------------------------------------------ launchers
+// Each returns cudaGetLastError() of its launches.
+cudaError_t launch_dense_preprocess(const DenseArgs &a, const FixedGeo &g, cudaStream_t s);
+cudaError_t launch_dense_preprocess(const DenseArgs &a, const PackedGeo &g, cudaStream_t s);
+cudaError_t launch_dense_bwd_main(const DenseArgs &a, const FixedGeo &g, cudaStream_t s);
+cudaError_t launch_dense_bwd_main(const DenseArgs &a, const PackedGeo &g, cudaStream_t s);
+cudaError_t launch_dq_finalize(const DenseArgs &a, const FixedGeo &g, cudaStream_t s);
+cudaError_t launch_dq_finalize(const DenseArgs &a, const PackedGeo &g, cudaStream_t s);
+cudaError_t launch_dense_fwd(const DenseArgs &a, const FixedGeo &g, cudaStream_t s);
+cudaError_t launch_dense_fwd(const DenseArgs &a, const PackedGeo &g, cudaStream_t s);
+
+cudaError_t launch_nsa_bwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, cudaEvent_t before,
+                           cudaEvent_t after);
+cudaError_t launch_nsa_block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s);
+
+}  // namespace attn

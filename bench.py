@@ -1,0 +1,427 @@
+"""Benchmark of the SDPA backward (and the NSA selected-attention backward).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 1..4]
+
+Default workload 1: dense SDPA backward, fp16, b4 h12 s1024 d64, scale 1/8,
+causal, BSHD storage viewed as BHSD (the GPT-2 sizes of the cuDNN-frontend
+SDPA-backward sample).  A step is one sdpa_bwd call (preprocess, main
+backward, dQ finalize) on inputs resident in HBM; the L2 is flushed between
+steps by writing a 512 MB buffer outside the timed events.  FLOPs are
+counted as 10 b h s_q s_kv d, halved for causal; NSA counts
+10 T1 n1 (count * size) d over the selected slots.
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+replica of the workload (independent problems, no data-path collective) and
+value is the total over ranks divided by the slowest rank's time.
+--impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes as C
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "SDPA backward TFLOPS and fraction of GB300 FP16/BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ workloads
+
+def workload_info(idx):
+    p = synth.workload(idx)
+    if isinstance(p, synth.NsaProblem):
+        flops = 10.0 * p.t1 * p.n1 * p.block_count * p.block_size * p.d
+        name = (f"nsa_bwd_bf16_tnd_{len(p.cu_q)}x{p.t1 // len(p.cu_q)}_n1{p.n1}_n2{p.n2}_d{p.d}"
+                f"_bs{p.block_size}x{p.block_count}_sparse{p.sparse_mode}")
+        cfg = {"workload": name, "tokens": p.t1, "n1": p.n1, "n2": p.n2, "d": p.d, "block_size": p.block_size,
+               "block_count": p.block_count, "sparse_mode": p.sparse_mode, "layout": "TND"}
+        return p, flops, cfg
+    lq = np.diff(np.concatenate([[0], p.cu_q]))
+    lkv = np.diff(np.concatenate([[0], p.cu_kv]))
+    flops = 10.0 * p.h * float((lq * lkv).sum()) * p.d * (0.5 if p.mask else 1.0)
+    dt = "fp16" if p.dtype == synth.F16 else "bf16"
+    if p.varlen:
+        name = f"dense_bwd_{dt}_varlen{p.b}_h{p.h}_hkv{p.h_kv}_d{p.d}_causal_br_tnd"
+        cfg = {"workload": name, "seqlens": [int(x) for x in lq], "h": p.h, "h_kv": p.h_kv, "d": p.d,
+               "mask": "causal_bottom_right", "layout": "TND"}
+    else:
+        name = f"dense_bwd_{dt}_b{p.b}_h{p.h}_s{p.s_q}_d{p.d}_{'causal' if p.mask else 'full'}_bshd"
+        cfg = {"workload": name, "b": p.b, "h": p.h, "h_kv": p.h_kv, "s_q": p.s_q, "s_kv": p.s_kv, "d": p.d,
+               "scale": p.scale, "mask": ["none", "causal_top_left", "causal_bottom_right"][p.mask],
+               "layout": "BSHD storage viewed as BHSD"}
+    return p, flops, cfg
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_backward_02_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel_tag):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (profiles/<tag>.txt with source_hash and
+    dram_bytes_per_launch lines); else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------- clock sampling
+
+class ClockSampler:
+    """Polls NVML (the library nvidia-smi reads) for the SM clock and the
+    clock-event reasons of one GPU while running; read-only."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
+
+    def __init__(self, pci_bus_id, period_s=0.002):
+        self.samples, self.period, self.ok = [], period_s, False
+        self._stop = threading.Event()
+        try:
+            self.nvml = C.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.handle = C.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), C.byref(self.handle)) != 0:
+                return
+            self.reasons_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.max_mhz = C.c_uint()
+            self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, C.byref(self.max_mhz))  # NVML_CLOCK_SM
+            self.ok = True
+        except (OSError, AttributeError):
+            return
+
+    def _run(self):
+        clk, reasons = C.c_uint(), C.c_ulonglong()
+        while not self._stop.is_set():
+            self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, C.byref(clk))
+            self.reasons_fn(self.handle, C.byref(reasons))
+            self.samples.append((clk.value, reasons.value))
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self.thread.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": float(statistics.median(c for c, _ in self.samples)),
+                "sm_max_mhz": float(self.max_mhz.value), "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": "NVML (nvidia-smi's library), polled every 2 ms"}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_dense_sample(p, rows_per_head=None, batch=0):
+    """One batch element, every head, query rows [s - r, s) against keys
+    [0, s): causal bottom-right sub-problem of workload p.  Returns the
+    callable and its FLOPs by the same 10 d per visible pair convention."""
+    import oracle
+    s, d = p.s_q, p.d
+    r = s if rows_per_head is None else max(1, min(s, int(rows_per_head)))
+    t0 = batch * s
+    q = p.f64("q")[t0 + s - r: t0 + s]
+    do = p.f64("do")[t0 + s - r: t0 + s]
+    k = p.f64("k")[batch * p.s_kv: batch * p.s_kv + s]
+    v = p.f64("v")[batch * p.s_kv: batch * p.s_kv + s]
+    mask = oracle.CAUSAL_BOTTOM_RIGHT if p.mask else oracle.MASK_NONE
+    o, lse = oracle.dense_fwd(q, k, v, [r], [s], p.scale, mask)
+    pairs = sum(range(s - r + 1, s + 1)) if p.mask else r * s
+    flops = 10.0 * p.h * pairs * d
+
+    def run():
+        oracle.dense_bwd(q, k, v, o, do, lse, [r], [s], p.scale, mask)
+
+    return run, flops, f"batch element {batch}, all {p.h} heads, last {r} of {s} query rows, fp64"
+
+
+def oracle_nsa_sample(p, tokens=None):
+    import oracle
+    t = p.t1 if tokens is None else max(1, min(p.t1, int(tokens)))
+    L = int(p.cu_q[0])
+    t = min(t, L)
+    q, do = p.f64("q")[L - t:L], p.f64("do")[L - t:L]
+    k, v = p.f64("k")[:L], p.f64("v")[:L]
+    topk = p.topk[L - t:L]
+    o, mx, sm = oracle.nsa_fwd(q, k, v, topk, [t], [L], p.scale, p.block_size, p.sparse_mode)
+    flops = 10.0 * t * p.n1 * p.block_count * p.block_size * p.d
+
+    def run():
+        oracle.nsa_bwd(q, k, v, o, do, mx, sm, topk, [t], [L], p.scale, p.block_size, p.sparse_mode)
+
+    return run, flops, f"sequence 0, last {t} of {L} tokens, all {p.n1} heads, fp64"
+
+
+def cpu_sample(p, target_s):
+    """A sample of the workload whose oracle run takes about target_s."""
+    if isinstance(p, synth.NsaProblem):
+        run, flops, _ = oracle_nsa_sample(p, 64)
+        t0 = time.perf_counter(); run(); dt = time.perf_counter() - t0
+        return oracle_nsa_sample(p, 64 * max(1.0, target_s / max(dt, 1e-6)))
+    run, flops, _ = oracle_dense_sample(p, 64)
+    t0 = time.perf_counter(); run(); dt = time.perf_counter() - t0
+    full_pairs = sum(range(1, p.s_q + 1)) if p.mask else p.s_q * p.s_kv
+    want_pairs = (flops / (10.0 * p.h * p.d)) * target_s / max(dt, 1e-6)
+    rows = p.s_q
+    if want_pairs < full_pairs:  # smallest r whose last-r-rows pair count reaches want_pairs
+        rows, acc = 0, 0
+        while acc < want_pairs and rows < p.s_q:
+            acc += p.s_q - rows
+            rows += 1
+    return oracle_dense_sample(p, rows)
+
+
+def run_reference(args, info):
+    import oracle
+    p, _, cfg = info
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_step = min(30.0, 120.0 / max(1, args.steps + args.warmup))
+    run, flops, desc = cpu_sample(p, per_step)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter(); run(); times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.thread_count(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- GPU arm
+
+def run_ours(args, info):
+    import torch
+    import attention_backward_02_gb300 as ab
+    from tests import harness as H
+
+    p, flops, cfg = info
+    rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    ab._lib.load()
+    lib = ab._lib.load()
+    stream = torch.cuda.current_stream()
+    nsa = isinstance(p, synth.NsaProblem)
+
+    # ---- inputs resident in HBM (O and the stats from the forward) ----
+    if nsa:
+        o_bits, mx, sm = H.nsa_oracle_inputs(p)
+        q, k, v, do, o = (H.bits_to_gpu(x, p.dtype) for x in (p.q, p.k, p.v, p.do, o_bits))
+        mx8 = torch.from_numpy(np.repeat(mx[..., None], 8, -1)).cuda()
+        sm8 = torch.from_numpy(np.repeat(sm[..., None], 8, -1)).cuda()
+        topk = torch.from_numpy(p.topk).cuda()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        desc = H.nsa_desc(p)
+        ws = torch.empty(ab.nsa_workspace_size(desc), dtype=torch.uint8, device="cuda")
+        inputs = [q, k, v, o, do, mx8, sm8, topk]
+        outputs = [dq, dk, dv]
+        launches_per_step = 7
+
+        def step():
+            ab.nsa_selected_attn_bwd(desc, q, k, v, o, do, mx8, sm8, topk, dq, dk, dv, workspace=ws, stream=stream)
+    else:
+        q, k, v, do = (H.bits_to_gpu(x, p.dtype) for x in (p.q, p.k, p.v, p.do))
+        o = torch.empty_like(q)
+        lse = torch.empty(p.t_q * p.h, dtype=torch.float32, device="cuda")
+        desc = H.dense_desc(p)
+        vq, vk, vv, vo = H.dense_views(p, (q, k, v, o))
+        ab.sdpa_fwd_stats(desc, vq, vk, vv, vo, lse)  # O and LSE from the library's forward
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        vdo, vdq, vdk, vdv = H.dense_views(p, (do, dq, dk, dv))
+        ws = torch.empty(ab.sdpa_workspace_size(desc)[1], dtype=torch.uint8, device="cuda")
+        inputs = [q, k, v, o, do, lse]
+        outputs = [dq, dk, dv]
+        launches_per_step = 3
+
+        def step():
+            ab.sdpa_bwd(desc, vq, vk, vv, vo, vdo, lse, vdq, vdk, vdv, workspace=ws, stream=stream)
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        step()
+        flush.fill_(1)
+    assert ab.attn_query_status(ws) == 0, "device status flagged during warm-up"
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for e in ev:  # instantiate the events before the timed region
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(local)
+    bus = getattr(props, "pci_bus_id", None)
+    pci = (f"{getattr(props, 'pci_domain_id', 0):08x}:{getattr(props, 'pci_bus_id', 0):02x}:"
+           f"{getattr(props, 'pci_device_id', 0):02x}.0") if bus is not None else "00000000:00:00.0"
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(pci) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            e_call0, e_main0, e_main1, e_call1 = ev[i]
+            lib.attn_set_main_kernel_events(C.c_void_p(e_main0.cuda_event), C.c_void_p(e_main1.cuda_event))
+            e_call0.record(stream)
+            step()
+            e_call1.record(stream)
+            lib.attn_set_main_kernel_events(None, None)
+            flush.fill_(1)  # L2 flush outside the timed events
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    call_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps)]
+    main_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    total_ms = sum(call_ms)
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert ab.attn_query_status(ws) == 0, "device status flagged during the timed steps"
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    main_mean = statistics.mean(main_ms)
+
+    # ---- end to end through the C ABI with host buffers ----
+    host_in = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x) for x in inputs]
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outputs]
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    e2e_steps = max(1, min(args.steps, 50))
+    e2e_ms = []
+    for i in range(e2e_steps):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for dst, src in zip(inputs, host_in):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(host_out, outputs):
+            dst.copy_(src, non_blocking=True)
+        a1.record(stream)
+        a1.synchronize()
+        e2e_ms.append(a0.elapsed_time(a1))
+        flush.fill_(1)
+    e2e_val = world * flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    pk, pk_src = peaks()
+    peak = float(pk["bf16_tflops"])  # fp16 and bf16 share one dense rate
+    achieved = flops / (main_mean * 1e-3) / 1e12
+    tag = "nsa_bwd_main" if nsa else "dense_bwd_main"
+    traffic = profile_traffic(f"{tag}_workload{args.workload}")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16" if p.dtype == synth.F16 else "bf16", "data": "synthetic",
+        "config": dict(cfg, l2="flushed: 512 MB buffer written between timed steps, outside the events",
+                       inputs="N(0,1) seeded; O and stats from the library forward" if not nsa else
+                       "N(0,1) seeded; O and softmax stats from the oracle sparse forward",
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": tag, "kernel_ms": main_mean,
+                     "peak_source": f"{pk_src} bf16_tflops (burst; fp16 has the same dense rate)",
+                     "whole_call_frac": value / world / peak},
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": statistics.mean(e2e_ms)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        run, cflops, desc_s = cpu_sample(p, 10.0)
+        t0 = time.perf_counter(); run(); dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": cflops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.thread_count(),
+                                "kind": "oracle", "sample": desc_s, "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=1, choices=[1, 2, 3, 4])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    info = workload_info(args.workload)
+    if args.impl == "reference":
+        run_reference(args, info)
+    else:
+        run_ours(args, info)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * attnbwd.h -- C ABI of the GB300 (sm_103a) attention-backward library.
+ *
+ * Three computations, each a stateless, asynchronous call on the caller's
+ * CUDA stream (passed as void*; NULL is the legacy default stream):
+ *
+ *   sdpa_fwd_stats          O and the fp32 log-sum-exp stats of scaled dot
+ *                           product attention (training-mode forward).
+ *   sdpa_bwd                dQ, dK, dV of the same attention, FlashAttention-2
+ *                           form: P is recomputed from the saved stats.
+ *   nsa_selected_attn_bwd   dQ, dK, dV of NSA selected attention, where every
+ *                           query token attends to selectedBlockCount blocks of
+ *                           selectedBlockSize keys chosen by int32 topkIndices.
+ *
+ * Definitions.  With s_ij = scale * q_i . k_j over the visible keys,
+ *   LSE_i = log sum_j exp(s_ij),  P_ij = exp(s_ij - LSE_i),  O_i = sum_j P_ij v_j,
+ *   D_i = rowsum(dO_i * O_i),  dP = dO V^T,  dS = P * (dP - D),
+ *   dV = P^T dO,  dQ = scale dS K,  dK = scale dS^T Q.
+ * Sources: the cuDNN-frontend sample "51_scaled_dot_product_attention_backward"
+ * (training forward emitting a (B,H,S,1) float32 stats tensor, backward from
+ * those stats by FlashAttention-2, multiplicative attn_scale, causal mask,
+ * half-precision I/O with float intermediates and compute, BSHD physical /
+ * BHSD logical strides) and the Ascend CANN page "aclnnNsaSelectedAttentionGrad"
+ * (Function / Formula: gather of the selected key / value blocks, dV = P^T dY,
+ * dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d); Constraints: TND layout,
+ * cumulative actual sequence lengths, G = N1/N2 <= 32, block size <= 128 and a
+ * multiple of 16, block count in [1,128], deterministic mode opt-in; the
+ * two-phase workspace-size-then-run API and its status codes).
+ *
+ * Conventions shared by every call.
+ *  - Tensors are caller-owned device memory.  The library allocates nothing,
+ *    keeps no state between calls, and fully overwrites its outputs.
+ *  - The workspace is caller-owned device memory of at least the size the
+ *    matching *_workspace_size call returns, 256-byte aligned.  Its contents
+ *    need not be initialised.  Two calls in flight at once must not share it.
+ *  - Every argument check runs on the host before anything is launched; a
+ *    call that returns an error has launched nothing.  Errors the device
+ *    finds (an index out of range, a duplicate selected block, a bounded wait
+ *    that ran out) never trap: they set bits in a status word inside the
+ *    workspace that attn_query_status reads back.
+ *  - 16-bit tensors (fp16 or bf16, one type per call) must start on a 16-byte
+ *    boundary and have element strides that are multiples of 8 (16 bytes);
+ *    the innermost (head-dim) stride is 1.  Otherwise ATTN_ERR_ALIGN.
+ *  - Query head hq uses key/value head hq / (h / h_kv).
+ *  - A query row that sees no key (possible only when a bottom-right causal
+ *    mask meets s_q > s_kv) has O = 0, LSE = +inf and zero gradients.
+ */
+#ifndef ATTNBWD_H
+#define ATTNBWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULLPTR = 1,     /* a required pointer is NULL                    */
+    ATTN_ERR_INVALID = 2,     /* a size, dtype, mode or stride is not valid    */
+    ATTN_ERR_UNSUPPORTED = 3, /* valid, but outside what the kernels cover     */
+    ATTN_ERR_WORKSPACE = 4,   /* workspace NULL, too small or misaligned       */
+    ATTN_ERR_ALIGN = 5,       /* a tensor breaks the 16-byte rule above        */
+    ATTN_ERR_CUDA = 6,        /* a CUDA runtime / driver call failed           */
+    ATTN_ERR_DEVICE = 7       /* attn_query_status: the device flagged an error */
+} attn_status_t;
+
+/* Bits of the device status word (attn_query_status).                        */
+#define ATTN_DEV_TIMEOUT      0x1u  /* a bounded barrier wait ran out; the CTA quit */
+#define ATTN_DEV_INDEX_RANGE  0x2u  /* a topk index outside [0, S2_b / block_size)   */
+#define ATTN_DEV_INDEX_DUP    0x4u  /* a block listed twice for one (token, kv head) */
+
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+/* Causal alignment.  Top-left: key j is visible to query i iff j <= i.
+ * Bottom-right: iff j <= i + (s_kv - s_q).  Both coincide when s_q == s_kv.   */
+typedef enum {
+    ATTN_MASK_NONE = 0,
+    ATTN_CAUSAL_TOP_LEFT = 1,
+    ATTN_CAUSAL_BOTTOM_RIGHT = 2
+} attn_mask_t;
+
+/* A 16-bit tensor seen as logical [B, H, S, D] with element strides
+ * (sb, sh, ss, 1).  The sample's BSHD storage viewed as BHSD has
+ * (S*H*D, D, H*D, 1).  In packed (varlen, TND) mode token t of head h is at
+ * ptr + t*ss + h*sh and sb is ignored.                                       */
+typedef struct {
+    void *ptr;
+    int64_t sb, sh, ss;
+} attn_view_t;
+
+typedef struct {
+    attn_dtype_t dtype;
+    int64_t b;              /* batch size (number of sequences)                */
+    int64_t h;              /* query heads                                     */
+    int64_t h_kv;           /* key/value heads; h % h_kv == 0                  */
+    int64_t s_q, s_kv;      /* fixed lengths; ignored in packed mode           */
+    int64_t d;              /* head dim: 64 or 128                             */
+    double scale;           /* multiplies q.k, e.g. 1/sqrt(d)                  */
+    attn_mask_t mask;
+    /* Packed mode: host arrays of b inclusive cumulative lengths, no leading
+     * zero (the Ascend page's actualSeqQLen / actualSeqKvLen form), b <= 256.
+     * Both NULL: fixed-length mode.                                          */
+    const int64_t *cu_seqlens_q;
+    const int64_t *cu_seqlens_kv;
+    /* sdpa_bwd only.  0: dQ accumulated with fp32 reductions whose order
+     * varies from run to run.  1: bitwise reproducible dQ: each of dq_splits
+     * partial fp32 buffers has one writer that adds in a fixed order, and the
+     * buffers are summed in index order (0 picks a default).                */
+    int deterministic;
+    int dq_splits;
+} attn_sdpa_desc_t;
+
+/* Workspace bytes for sdpa_fwd_stats and for sdpa_bwd with this descriptor.
+ * Either output pointer may be NULL.  Host only; no CUDA call.              */
+attn_status_t sdpa_workspace_size(const attn_sdpa_desc_t *desc, size_t *fwd_bytes, size_t *bwd_bytes);
+
+/* Forward in training mode.  q, o: [B,h,s_q,d] views; k, v: [B,h_kv,s_kv,d].
+ * lse (fp32, natural log, contiguous): [B][h][s_q] in fixed-length mode,
+ * [h][T_q] in packed mode (T_q = total query tokens).                        */
+attn_status_t sdpa_fwd_stats(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t k, attn_view_t v,
+                             attn_view_t o, float *lse, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/* Backward.  q, o, dO, dQ: [B,h,s_q,d] views; k, v, dK, dV: [B,h_kv,s_kv,d];
+ * lse as sdpa_fwd_stats writes it.  dQ / dK / dV may have any strides that
+ * follow the 16-byte rule (the sample allocates them empty_like the inputs).
+ * Outputs have the input dtype, rounded to nearest even.                    */
+attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t k, attn_view_t v,
+                       attn_view_t o, attn_view_t dO, const float *lse, attn_view_t dQ, attn_view_t dK,
+                       attn_view_t dV, void *workspace, size_t workspace_bytes, void *stream);
+
+typedef struct {
+    attn_dtype_t dtype;
+    int64_t b;              /* sequences; b <= 256                             */
+    const int64_t *cu_seqlens_q;   /* host, b inclusive cumulative lengths   */
+    const int64_t *cu_seqlens_kv;  /* host, b inclusive cumulative lengths   */
+    int64_t n1;             /* query heads (headNum)                          */
+    int64_t n2;             /* key/value heads; n1 % n2 == 0, n1/n2 <= 32     */
+    int64_t d;              /* head dim: 128                                  */
+    double scale;           /* scaleValue                                     */
+    int64_t block_size;     /* selectedBlockSize: 64                          */
+    int64_t block_count;    /* selectedBlockCount in [1, 128], count*size < 8192 */
+    int sparse_mode;        /* 0: only the selection; 2: also causal,
+                               bottom-right aligned per sequence              */
+    int deterministic;      /* 1: bitwise reproducible dQ                     */
+} attn_nsa_desc_t;
+
+/* Workspace bytes for nsa_selected_attn_bwd.  Host only; no CUDA call.       */
+attn_status_t nsa_workspace_size(const attn_nsa_desc_t *desc, size_t *bytes);
+
+/* NSA selected-attention backward, TND layout, all contiguous:
+ *   q, o, dO, dq : [T1][n1][d]      k, v, dk, dv : [T2][n2][d]
+ *   softmax_max, softmax_sum : [T1][n1][8] fp32 (the 8 lanes hold one value;
+ *       lane 0 is read): P = exp(scale q.k - max) / sum over the selection.
+ *   topk : [T1][n2][block_count] int32 block ids local to the token's
+ *       sequence, each in [0, S2_b / block_size), distinct per (token, head).
+ * Every selected block must lie inside its sequence: S2_b % block_size == 0
+ * and S2_b >= block_count * block_size for every sequence.                   */
+attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, const void *k,
+                                    const void *v, const void *o, const void *dO,
+                                    const float *softmax_max, const float *softmax_sum,
+                                    const int32_t *topk, void *dq, void *dk, void *dv,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* The inverted index the NSA backward builds internally, exposed so callers
+ * (and tests) can use or check it: for every (sequence b, kv head g, block k)
+ * in that order, row r = (b * n2 + g) * nblk_max + k with
+ * nblk_max = max_b S2_b / block_size, tokens[offsets[r] .. offsets[r+1]) are
+ * the ascending global ids of the query tokens whose topk lists block k and
+ * see at least one of its keys under the sparse mode.  offsets (int32,
+ * nblk_max * n2 * b + 1 entries) and tokens (int32, T1 * n2 * block_count
+ * entries) are device memory; *nblk_max_out (host) receives nblk_max.
+ * Invalid indices are skipped and flagged in the device status word.        */
+attn_status_t nsa_block_lists(const attn_nsa_desc_t *desc, const int32_t *topk, int32_t *offsets,
+                              int32_t *tokens, int64_t *nblk_max_out, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/* Waits for the stream, then reads the device status word of a workspace a
+ * previous call used (bits ATTN_DEV_*; 0 when clean) and clears it.
+ * Returns ATTN_ERR_DEVICE when any bit was set.                              */
+attn_status_t attn_query_status(void *workspace, void *stream, uint32_t *device_flags);
+
+/* Optional instrumentation for benchmarks.  While set, every sdpa_bwd and
+ * nsa_selected_attn_bwd call made from this host thread records the CUDA
+ * event `before` on its stream just before its main backward kernel and
+ * `after` just after it, so the main kernel can be timed alone.  Events are
+ * cudaEvent_t handles passed as void*; NULL, NULL clears.  Never fails.    */
+attn_status_t attn_set_main_kernel_events(void *before, void *after);
+
+/* Human-readable name of a status code (static storage).                    */
+const char *attn_status_string(attn_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNBWD_H */

@@ -1,0 +1,114 @@
+"""Host-only checks of the C ABI: the library loads, exports every declared
+symbol, sizes workspaces, and rejects bad arguments before any launch.
+No call here reaches a kernel, so none needs a GPU."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ab():
+    from attention_backward_02_gb300 import build
+    build.build()
+    import attention_backward_02_gb300 as ab
+    ab._lib.load()
+    return ab
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "attnbwd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M))
+
+
+def test_exports_every_declared_symbol(ab):
+    names = _declared()
+    assert names == set(ab._lib.EXPORTS), names
+    lib = C.CDLL(ab._lib.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _desc(ab, **kw):
+    base = dict(dtype=ab.ATTN_F16, b=4, h=12, h_kv=12, s_q=1024, s_kv=1024, d=64, scale=0.125,
+                mask=ab.ATTN_CAUSAL_TOP_LEFT)
+    base.update(kw)
+    return ab.sdpa_desc(**base)
+
+
+def _status(ab, desc):
+    f, b = C.c_size_t(), C.c_size_t()
+    return ab._lib.load().sdpa_workspace_size(C.byref(desc), C.byref(f), C.byref(b)), b.value
+
+
+def test_workspace_size(ab):
+    st, nbytes = _status(ab, _desc(ab))
+    assert st == 0
+    t_pad = 4 * 1024 + 128
+    assert nbytes >= 2 * 12 * t_pad * 4 + 12 * t_pad * 64 * 4
+    st, det = _status(ab, _desc(ab, deterministic=True, dq_splits=4))
+    assert st == 0 and det >= nbytes + 3 * 12 * t_pad * 64 * 4
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=7), 2), (dict(h=12, h_kv=5), 2), (dict(b=0), 2), (dict(d=96), 3), (dict(d=256), 3),
+    (dict(mask=5), 2), (dict(scale=float("nan")), 2), (dict(s_q=-1), 2), (dict(dq_splits=-2), 2),
+])
+def test_descriptor_rejections(ab, kw, code):
+    assert _status(ab, _desc(ab, **kw))[0] == code
+
+
+def test_varlen_descriptor(ab):
+    st, _ = _status(ab, _desc(ab, b=3, cu_seqlens_q=[10, 30, 60], cu_seqlens_kv=[10, 30, 60]))
+    assert st == 0
+    st, _ = _status(ab, _desc(ab, b=3, cu_seqlens_q=[10, 5, 60], cu_seqlens_kv=[10, 30, 60]))
+    assert st == 2
+    st, _ = _status(ab, _desc(ab, b=300, cu_seqlens_q=list(range(1, 301)), cu_seqlens_kv=list(range(1, 301))))
+    assert st == 3
+
+
+def _bwd_call(ab, desc, ptr=0x10000, stride=(8 * 1024 * 12 * 64, 64, 12 * 64), ws=0x100000, ws_bytes=1 << 40,
+              lse=0x20000):
+    v = ab.attn_view_t(ptr, *stride)
+    return ab._lib.load().sdpa_bwd(C.byref(desc), v, v, v, v, v, C.cast(C.c_void_p(lse), C.POINTER(C.c_float)),
+                                   v, v, v, C.c_void_p(ws), C.c_size_t(ws_bytes), None)
+
+
+def test_bwd_rejects_before_launch(ab):
+    d = _desc(ab)
+    assert _bwd_call(ab, d, ptr=0) == 1                      # NULL tensor
+    assert _bwd_call(ab, d, ptr=0x10008) == 5                # misaligned base
+    assert _bwd_call(ab, d, stride=(8, 4, 64)) == 5          # stride not a multiple of 16 bytes
+    assert _bwd_call(ab, d, ws=0) == 4                       # no workspace
+    assert _bwd_call(ab, d, ws_bytes=100) == 4               # short workspace
+    assert _bwd_call(ab, d, ws=0x100010) == 4                # misaligned workspace
+    assert _bwd_call(ab, d, lse=0) == 1                      # no stats
+    assert ab._lib.load().sdpa_bwd(None, *([ab.attn_view_t(0, 0, 0, 0)] * 5), None,
+                                   *([ab.attn_view_t(0, 0, 0, 0)] * 3), None, 0, None) == 1
+
+
+def _nsa(ab, **kw):
+    base = dict(dtype=ab.ATTN_BF16, cu_seqlens_q=[4096, 8192], cu_seqlens_kv=[4096, 8192], n1=16, n2=1, d=128,
+                scale=0.088, block_size=64, block_count=16, sparse_mode=2)
+    base.update(kw)
+    return ab.nsa_desc(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), 0), (dict(block_size=48), 2), (dict(block_size=256), 2), (dict(block_count=0), 2),
+    (dict(block_count=128, block_size=64), 2), (dict(n1=16, n2=3), 2), (dict(n1=64, n2=1), 2),
+    (dict(sparse_mode=1), 2), (dict(d=64), 2), (dict(d=192), 3),
+    (dict(cu_seqlens_kv=[4000, 8192]), 2), (dict(cu_seqlens_kv=[512, 1024], block_count=16), 2),
+])
+def test_nsa_descriptor_rejections(ab, kw, code):
+    n = C.c_size_t()
+    assert ab._lib.load().nsa_workspace_size(C.byref(_nsa(ab, **kw)), C.byref(n)) == code
+
+
+def test_status_strings(ab):
+    for code in range(8):
+        assert ab._lib.load().attn_status_string(code).startswith(b"ATTN_")

@@ -1,0 +1,129 @@
+"""GPU parity of the dense SDPA backward (and forward) against the fp64 oracle,
+through the C ABI.  Expected values come only from the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+F16, BF16 = synth.F16, synth.BF16
+NONE, TL, BR = oracle.MASK_NONE, oracle.CAUSAL_TOP_LEFT, oracle.CAUSAL_BOTTOM_RIGHT
+
+
+def _parity(p, deterministic=False, dq_splits=0):
+    o_bits, lse = H.oracle_forward(p)
+    dq, dk, dv = H.run_gpu_bwd(p, o_bits, lse, deterministic, dq_splits)
+    rq, rk, rv = oracle.dense_bwd(p.f64("q"), p.f64("k"), p.f64("v"), synth.bits_to_f64(o_bits, p.dtype),
+                                  p.f64("do"), lse, p.cu_q, p.cu_kv, p.scale, p.mask)
+    H.assert_close(dq, rq, "dQ")
+    H.assert_close(dk, rk, "dK")
+    H.assert_close(dv, rv, "dV")
+    return dq, dk, dv
+
+
+def test_workload0_forward_and_backward():
+    """fp16 b1 h2 s128 d64, scale 1/8, non-causal: forward O/LSE and backward."""
+    p = synth.workload(0)
+    o, lse = H.run_gpu_fwd(p)
+    ro, rlse = oracle.dense_fwd(p.f64("q"), p.f64("k"), p.f64("v"), p.cu_q, p.cu_kv, p.scale, p.mask)
+    H.assert_close(o, ro, "O")
+    np.testing.assert_allclose(lse, rlse, rtol=1e-5, atol=1e-5)
+    _parity(p)
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mask", [NONE, TL, BR])
+def test_small_shapes(dtype, d, mask):
+    """Several tiles with ragged tails on both sides; s_q != s_kv for the masks."""
+    p = synth.dense_problem("small", dtype=dtype, b=2, h=4, h_kv=2, d=d, s_q=200, s_kv=333, mask=mask,
+                            seed=100 + d + mask)
+    _parity(p)
+
+
+@pytest.mark.parametrize("s_q,s_kv", [(1, 1), (1, 257), (129, 1), (64, 64), (300, 300)])
+def test_edge_lengths(s_q, s_kv):
+    p = synth.dense_problem("edge", dtype=BF16, b=1, h=2, h_kv=1, d=128, s_q=s_q, s_kv=s_kv, mask=BR,
+                            seed=s_q * 7 + s_kv)
+    _parity(p)
+
+
+def test_varlen_gqa_small():
+    lens = np.array([1, 130, 77, 256, 5, 300])
+    p = synth.dense_problem("varlen", dtype=BF16, b=len(lens), h=8, h_kv=2, d=128, lens_q=lens, lens_kv=lens,
+                            mask=BR, seed=7)
+    _parity(p)
+
+
+def test_varlen_unequal_lengths():
+    lq = np.array([40, 200, 129]); lkv = np.array([100, 150, 129])
+    p = synth.dense_problem("varlen2", dtype=F16, b=3, h=4, h_kv=4, d=64, lens_q=lq, lens_kv=lkv, mask=BR, seed=8)
+    _parity(p)
+
+
+def test_empty_sequence_in_batch():
+    lens = np.array([64, 0, 100])
+    p = synth.dense_problem("varlen0", dtype=BF16, b=3, h=2, h_kv=2, d=128, lens_q=lens, lens_kv=lens,
+                            mask=TL, seed=9)
+    _parity(p)
+
+
+@pytest.mark.parametrize("dq_splits", [0, 3])
+def test_deterministic_mode_bitwise(dq_splits):
+    p = synth.dense_problem("det", dtype=BF16, b=2, h=4, h_kv=2, d=128, s_q=520, s_kv=520, mask=TL, seed=11)
+    o_bits, lse = H.oracle_forward(p)
+    a = H.run_gpu_bwd(p, o_bits, lse, deterministic=True, dq_splits=dq_splits)
+    b = H.run_gpu_bwd(p, o_bits, lse, deterministic=True, dq_splits=dq_splits)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    _parity(p, deterministic=True, dq_splits=dq_splits)
+
+
+def test_workload1_full():
+    """fp16 b4 h12 s1024 d64 causal, BSHD viewed as BHSD: every output element."""
+    _parity(synth.workload(1))
+
+
+def _sampled_parity(p, deterministic=False, nsample=96, seed=0):
+    o_bits, lse = H.oracle_forward(p)
+    dq, dk, dv = H.run_gpu_bwd(p, o_bits, lse, deterministic)
+    rng = np.random.default_rng(seed)
+    q_rows = rng.choice(p.t_q * p.h, nsample, replace=False)
+    kv_rows = rng.choice(p.t_kv * p.h_kv, nsample, replace=False)
+    # always include the first and last rows of every sequence
+    starts = np.concatenate([[0], p.cu_q[:-1]])
+    edge_t = np.unique(np.concatenate([starts, p.cu_q - 1]))
+    q_rows = np.unique(np.concatenate([q_rows, edge_t * p.h, edge_t * p.h + p.h - 1]))
+    kv_rows = np.unique(np.concatenate([kv_rows, edge_t * p.h_kv]))
+    rq, rk, rv = oracle.dense_bwd_rows(p.f64("q"), p.f64("k"), p.f64("v"), synth.bits_to_f64(o_bits, p.dtype),
+                                       p.f64("do"), lse, p.cu_q, p.cu_kv, p.scale, p.mask, q_rows, kv_rows)
+    H.assert_close(dq.reshape(-1, p.d)[q_rows], rq, "dQ rows")
+    H.assert_close(dk.reshape(-1, p.d)[kv_rows], rk, "dK rows")
+    H.assert_close(dv.reshape(-1, p.d)[kv_rows], rv, "dV rows")
+    # properties that hold at any size: sum_j dK_j = 0 per (sequence, kv head)
+    # up to the rounding of O to 16 bits, and sum_j dV_j = sum_i dO_i per group
+    G = p.h // p.h_kv
+    do = p.f64("do")
+    for b in range(len(p.cu_kv)):
+        s0, s1 = (0 if b == 0 else p.cu_kv[b - 1]), p.cu_kv[b]
+        q0, q1 = (0 if b == 0 else p.cu_q[b - 1]), p.cu_q[b]
+        for g in range(p.h_kv):
+            want = do[q0:q1, g * G:(g + 1) * G].sum((0, 1))
+            got = dv[s0:s1, g].sum(0)
+            assert np.abs(got - want).max() <= 0.05 * np.abs(want).max() + 0.5
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_workload2_sampled(deterministic):
+    """bf16 b2 h32 s4096 d128 causal: sampled rows, both dQ modes."""
+    _sampled_parity(synth.workload(2), deterministic)
+
+
+@pytest.mark.slow
+def test_workload3_sampled():
+    """varlen GQA bf16, h 32 / h_kv 8, d128, 8 lengths in [256, 4096], causal bottom-right."""
+    _sampled_parity(synth.workload(3))
