@@ -22,7 +22,7 @@ ATTN_MASK_NONE, ATTN_CAUSAL_TOP_LEFT, ATTN_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
 # every exported symbol of include/attnbwd.h
 EXPORTS = ("sdpa_workspace_size", "sdpa_fwd_stats", "sdpa_bwd", "nsa_workspace_size",
            "nsa_selected_attn_bwd", "nsa_block_lists", "attn_query_status", "attn_status_string",
-           "attn_set_main_kernel_events")
+           "attn_set_main_kernel_events", "sdpa_bwd_static_scratch")
 
 
 class attn_view_t(C.Structure):
@@ -67,6 +67,7 @@ def load() -> C.CDLL:
         "attn_query_status": [V, V, P(C.c_uint32)],
         "attn_status_string": [I],
         "attn_set_main_kernel_events": [V, V],
+        "sdpa_bwd_static_scratch": [D, view, view, view, view, view, P(C.c_float), view, view, view, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)

@@ -131,6 +131,29 @@ attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t 
                        attn_view_t o, attn_view_t dO, const float *lse, attn_view_t dQ, attn_view_t dK,
                        attn_view_t dV, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Allocation-free variant of sdpa_bwd.  The papers this library follows
+ * have no counterpart to it; it exists for callers that cannot allocate
+ * device memory when they run the backward (an engine or plugin that owns
+ * all device memory and forbids side allocations, a loop that must not
+ * allocate once running).  Instead of a caller workspace it uses a static
+ * scratch array of ATTN_STATIC_SCRATCH_BYTES compiled into the library;
+ * every GPU that loads the library holds those bytes until the process exits.
+ * Arguments and results are those of sdpa_bwd; the call allocates nothing.
+ *  - Problems whose sdpa_workspace_size exceeds ATTN_STATIC_SCRATCH_BYTES
+ *    are rejected with ATTN_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture begins.
+ *  - All calls share the one array, so calls that overlap on the GPU (other
+ *    streams, other host threads) race and corrupt each other's results;
+ *    serialise them.  Each call re-initialises the scratch it reads, so what
+ *    an earlier call left there does not matter.
+ *  - Device status flags land in the static array and cannot be read back. */
+#define ATTN_STATIC_SCRATCH_BYTES (16u << 20)
+attn_status_t sdpa_bwd_static_scratch(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t k, attn_view_t v,
+                                      attn_view_t o, attn_view_t dO, const float *lse, attn_view_t dQ,
+                                      attn_view_t dK, attn_view_t dV, void *stream);
+
 typedef struct {
     attn_dtype_t dtype;
     int64_t b;              /* sequences; b <= 256                             */
