@@ -14,7 +14,7 @@ using namespace attn;
 
 namespace {
 
-constexpr int64_t kTilePad = 128;       // rows a tile may run past the last token
+constexpr int64_t kTilePad = 128;       // NSA: rows a tile may run past the last token
 constexpr int kDefaultDqSplits = 8;     // deterministic dense dQ partial buffers
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -81,10 +81,19 @@ struct DenseLayout {
     int64_t t_pad;
 };
 
+// Workspace rows: every sequence's query rows rounded up to kWsRowAlign.
+int64_t ws_rows(const attn_sdpa_desc_t *d, const DenseShape &sh)
+{
+    if (!sh.packed) return d->b * ws_round(d->s_q);
+    int64_t n = 0;
+    for (int64_t b = 0; b < d->b; ++b) n += ws_round(d->cu_seqlens_q[b] - (b ? d->cu_seqlens_q[b - 1] : 0));
+    return n;
+}
+
 DenseLayout dense_layout(const attn_sdpa_desc_t *d, const DenseShape &sh)
 {
     DenseLayout L;
-    L.t_pad = sh.t_q + kTilePad;
+    L.t_pad = ws_rows(d, sh);
     size_t rows = size_t(d->h) * size_t(L.t_pad);
     L.status = 0;
     L.lse2 = Workspace::align(64 * sizeof(uint32_t));
@@ -126,10 +135,11 @@ void fill_geo(const attn_sdpa_desc_t *d, const DenseShape &sh, FixedGeo *fg, Pac
     fg->s_kv = d->s_kv;
     if (sh.packed) {
         pg->nseq = d->b;
-        pg->cu_q[0] = pg->cu_kv[0] = 0;
+        pg->cu_q[0] = pg->cu_kv[0] = pg->ws_q[0] = 0;
         for (int64_t b = 0; b < d->b; ++b) {
             pg->cu_q[b + 1] = d->cu_seqlens_q[b];
             pg->cu_kv[b + 1] = d->cu_seqlens_kv[b];
+            pg->ws_q[b + 1] = pg->ws_q[b] + ws_round(pg->cu_q[b + 1] - pg->cu_q[b]);
         }
     }
 }
@@ -186,7 +196,7 @@ attn_status_t sdpa_fwd_stats(const attn_sdpa_desc_t *desc, attn_view_t q, attn_v
     std::memset(&a, 0, sizeof a);
     a.dtype = desc->dtype;
     a.nseq = desc->b; a.h = desc->h; a.h_kv = desc->h_kv; a.d = desc->d;
-    a.t_q = sh.t_q; a.t_kv = sh.t_kv; a.t_pad = sh.t_q + kTilePad;
+    a.t_q = sh.t_q; a.t_kv = sh.t_kv; a.t_pad = ws_rows(desc, sh);
     a.scale = float(desc->scale);
     a.mask = desc->mask;
     a.packed = sh.packed;
@@ -214,6 +224,8 @@ attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t 
         return st;
     if (sh.t_q && !lse) return ATTN_ERR_NULLPTR;
     DenseLayout L = dense_layout(desc, sh);
+    // 32-bit row coordinates of the fp32 dQ accumulator inside the kernels
+    if (int64_t(dense_parts(desc)) * desc->h * L.t_pad >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
     if ((st = check_ws(workspace, workspace_bytes, L.total))) return st;
 
     DenseArgs a;

@@ -1,0 +1,560 @@
+// bwd_tc.cu -- tensor-core SDPA backward for sm_103a (tcgen05 + TMA + TMEM).
+//
+// FlashAttention-2 backward (cuDNN-frontend sample
+// "51_scaled_dot_product_attention_backward": backward from the saved
+// (B,H,S,1) stats, no stored P), with the gradient formulas of the Ascend page
+// "aclnnNsaSelectedAttentionGrad", Function / Formula (dV = P^T dY,
+// dQ = dS K scale, dK = dS^T Q scale).
+//
+// One CTA owns a tile of BN = 128 key/value rows of one (sequence, kv head)
+// and walks every (query head of the group, query tile of BM rows) that sees
+// it.  Everything is computed transposed, so the 128 key rows are the MMA M
+// dimension and the TMEM lanes:
+//   S^T  = K Q^T           M=128 (keys) N=BM  K=D    A=K  (K-major) B=Q  (K-major)
+//   dP^T = V dO^T          M=128        N=BM  K=D    A=V  (K-major) B=dO (K-major)
+//   P^T  = exp2(S^T scale log2 e - LSE log2 e),  dS^T = P^T (dP^T - D)   (CUDA cores)
+//   dV  += P^T dO          M=128        N=D   K=BM   A=P^T (smem, K-major) B=dO (MN-major)
+//   dK  += dS^T Q          M=128        N=D   K=BM   A=dS^T (K-major)      B=Q  (MN-major)
+//   dQ   = dS K     (D=64) M=BM=128     N=64  K=128  A=dS (MN-major)       B=K  (MN-major)
+//   dQ^T = K^T dS^T (D=128) M=D=128     N=BM=64 K=128 A=K^T (MN-major)     B=dS^T (MN-major)
+// dV, dK stay in TMEM for the whole tile and are written once; the dQ tile is
+// staged in shared memory and added into the fp32 accumulator with a TMA
+// reduce-add.  TMEM: S^T BM + dP^T BM + dV D + dK D + dQ 64 = 448 columns.
+//
+// Roles (320 threads): warp 0 issues TMA loads (K/V once per tile; Q, dO and
+// the LSE / D vectors through a 2-stage ring), warp 1 issues the MMAs, warps
+// 2..9 read S^T / dP^T from TMEM (warp w reads lanes 32 (w % 4) .. + 31; the
+// two warps on the same lanes split the BM columns), write P^T and dS^T as
+// 16-bit tiles in the 128-byte-swizzled layout the MMA reads, then stage dQ
+// and finally write dK, dV.
+//
+// Causal masking: query tiles entirely before the first query that sees the
+// key tile are skipped; the rest are masked per element.  Key rows past the
+// sequence end are masked by row; query rows past it have LSE = +inf in the
+// workspace and so P = 0.
+//
+// Every barrier wait is bounded (about a second).  On a timeout the thread
+// sets ATTN_DEV_TIMEOUT in the status word and an abort flag in shared
+// memory; from then on every wait of the CTA fails fast and all work is
+// skipped while the control flow (and so every named barrier) stays the same;
+// the CTA drains its in-flight copies and MMAs, frees its TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <type_traits>
+
+#include "plan.h"
+#include "sm103.cuh"
+
+namespace attn {
+using namespace sm103;
+
+template <int D>
+struct TcCfg {
+    static constexpr int BN = 128;                  // key rows per CTA tile
+    static constexpr int BM = D == 64 ? 128 : 64;   // query rows per iteration
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int PS_BYTES = BN * BM * 2;
+    static constexpr int DQ_BYTES = BM * D * 4;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + KV_BYTES;
+    static constexpr int OFF_Q = OFF_V + KV_BYTES;          // 2 stages
+    static constexpr int OFF_DO = OFF_Q + 2 * Q_BYTES;      // 2 stages
+    static constexpr int OFF_P = OFF_DO + 2 * Q_BYTES;
+    static constexpr int OFF_DS = OFF_P + PS_BYTES;
+    static constexpr int OFF_DQ = OFF_DS + PS_BYTES;
+    static constexpr int OFF_LSE = OFF_DQ + DQ_BYTES;       // 2 stages x BM floats
+    static constexpr int OFF_DVEC = OFF_LSE + 2 * BM * 4;   // 2 stages x BM floats
+    static constexpr int OFF_BAR = OFF_DVEC + 2 * BM * 4;
+    static constexpr int OFF_MISC = OFF_BAR + 16 * 8;
+    static constexpr int SMEM = OFF_MISC + 64;
+    static constexpr int SMEM_ALLOC = SMEM + 1024;          // room to align the base to 1024
+    static constexpr int T_S = 0, T_DP = BM, T_DV = 2 * BM, T_DK = 2 * BM + D, T_DQ = 2 * BM + 2 * D;
+    static constexpr int T_COLS = 512;
+    static_assert(T_DQ + 64 <= T_COLS, "TMEM budget");
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+struct TcParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq;
+    DenseArgs a;
+};
+
+namespace {
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// AND of `pred` over the threads of named barrier `id` (also a barrier).
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t nthreads, bool pred)
+{
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %3, 0;\n\t"
+        "bar.red.and.pred q, %1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(out)
+        : "r"(id), "r"(nthreads), "r"(uint32_t(pred))
+        : "memory");
+    return out != 0;
+}
+
+// K-major SW128 tile of `rows` rows stored in 64-column blocks; K step kk (16 elements).
+__device__ __forceinline__ uint64_t desc_kmaj(uint32_t base, uint32_t rows, int kk)
+{
+    return smem_desc_sw128(base + uint32_t(kk >> 2) * rows * 128u + uint32_t(kk & 3) * 32u, 16, 1024);
+}
+
+// MN-major SW128 tile whose rows are the K dimension (`krows` of them) and
+// whose 64-column blocks run along M/N; K step kk (16 rows).
+__device__ __forceinline__ uint64_t desc_mn(uint32_t base, uint32_t krows, int kk)
+{
+    return smem_desc_sw128(base + uint32_t(kk) * 2048u, krows * 128u, 1024);
+}
+
+__device__ __forceinline__ void flag_abort(volatile int *abort, uint32_t *status)
+{
+    *abort = 1;
+    raise_flag(status, ATTN_DEV_TIMEOUT);
+}
+
+// Query tiles that see the key tile starting at j0: [qt0, qt0 + nq).
+template <int BM>
+__device__ __forceinline__ void query_tiles(int mask, int64_t j0, int64_t lq, int64_t lkv, int *qt0, int *nq)
+{
+    const int64_t i_lo = first_query_seeing(mask, j0, lq, lkv);
+    if (lq <= 0 || lkv <= 0 || i_lo >= lq) {
+        *qt0 = 0;
+        *nq = 0;
+        return;
+    }
+    *qt0 = int(i_lo / BM);
+    *nq = int((lq + BM - 1) / BM) - *qt0;
+}
+
+template <class Geo> struct IsPacked : std::false_type {};
+template <> struct IsPacked<PackedGeo> : std::true_type {};
+
+}  // namespace
+
+template <class T, int D, class Geo>
+__global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_constant__ TcParams p, const Geo geo)
+{
+    using Cfg = TcCfg<D>;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN;
+    constexpr bool kPacked = IsPacked<Geo>::value;
+    constexpr int kType = std::is_same<T, __half>::value ? 0 : 1;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
+    uint64_t *kv_full = bars + 0, *kv_empty = bars + 1, *q_full = bars + 2, *q_empty = bars + 4;
+    uint64_t *s_full = bars + 6, *p_ready = bars + 7, *mma_done = bars + 8, *drain = bars + 9;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 8);
+    const DenseArgs &a = p.a;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        *abort = 0;
+        mbar_init(kv_full, 1);
+        mbar_init(kv_empty, 8);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_ready, 8);
+        mbar_init(mma_done, 1);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, Cfg::T_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // ---- work unit: (sequence b, kv head g) and its key tiles
+    const int64_t nheads = a.nseq * a.h_kv;
+    const int64_t unit = blockIdx.x;
+    const int64_t bg = unit % nheads, first_tile = unit / nheads;
+    const int64_t b = bg / a.h_kv, g = bg % a.h_kv;
+    const int64_t tile_step = a.deterministic ? a.n_part : INT64_MAX / 2;
+    const int64_t part = a.deterministic ? first_tile : 0;
+    const int64_t lq = geo.q_len(b), lkv = geo.kv_len(b);
+    const int64_t ntiles = (lkv + BN - 1) / BN;
+    const int G = int(a.h / a.h_kv);
+    const int q_b = kPacked ? 0 : int(b), kv_b = q_b;
+    const int64_t q_row0 = kPacked ? geo.q_start(b) : 0, kv_row0 = kPacked ? geo.kv_start(b) : 0;
+
+    uint8_t *sK = smem + Cfg::OFF_K, *sV = smem + Cfg::OFF_V, *sP = smem + Cfg::OFF_P, *sdS = smem + Cfg::OFF_DS;
+    uint8_t *sdQ = smem + Cfg::OFF_DQ;
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        if (elect_one()) {
+            prefetch_tmap(&p.tm_q); prefetch_tmap(&p.tm_k); prefetch_tmap(&p.tm_v); prefetch_tmap(&p.tm_do);
+            bool ok = true;
+            int64_t kt = 0, qi = 0, q_armed = 0, kv_armed = 0;  // loads started (for the drain below)
+            for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
+                const int64_t j0 = jt * BN;
+                int qt0, nq;
+                query_tiles<BM>(a.mask, j0, lq, lkv, &qt0, &nq);
+                const int n_iter = G * nq;
+                if (n_iter == 0) continue;
+                if (kt > 0 && ok && !(ok = mbar_wait(kv_empty, uint32_t(kt - 1) & 1, abort))) flag_abort(abort, a.status);
+                if (ok) {
+                    kv_armed = kt + 1;
+                    mbar_arrive_expect_tx(kv_full, 2 * Cfg::KV_BYTES);
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_load_4d(sK + c * BN * 128, &p.tm_k, kv_full, c * 64, int(kv_row0 + j0), int(g), kv_b);
+                        tma_load_4d(sV + c * BN * 128, &p.tm_v, kv_full, c * 64, int(kv_row0 + j0), int(g), kv_b);
+                    }
+                }
+                for (int it = 0; it < n_iter; ++it, ++qi) {
+                    const int st = int(qi & 1);
+                    const int64_t use = qi >> 1;
+                    if (use > 0 && ok && !(ok = mbar_wait(&q_empty[st], uint32_t(use - 1) & 1, abort)))
+                        flag_abort(abort, a.status);
+                    if (!ok) continue;
+                    const int64_t hq = g * G + it / nq, i0 = int64_t(qt0 + it % nq) * BM;
+                    uint8_t *sQ = smem + Cfg::OFF_Q + st * Cfg::Q_BYTES, *sdO = smem + Cfg::OFF_DO + st * Cfg::Q_BYTES;
+                    q_armed = qi + 1;
+                    mbar_arrive_expect_tx(&q_full[st], 2 * Cfg::Q_BYTES + 2 * BM * 4);
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_load_4d(sQ + c * BM * 128, &p.tm_q, &q_full[st], c * 64, int(q_row0 + i0), int(hq), q_b);
+                        tma_load_4d(sdO + c * BM * 128, &p.tm_do, &q_full[st], c * 64, int(q_row0 + i0), int(hq), q_b);
+                    }
+                    const int64_t wrow = hq * a.t_pad + geo.ws_start(b) + i0;
+                    bulk_load(smem + Cfg::OFF_LSE + st * BM * 4, a.lse2 + wrow, BM * 4, &q_full[st]);
+                    bulk_load(smem + Cfg::OFF_DVEC + st * BM * 4, a.dvec + wrow, BM * 4, &q_full[st]);
+                }
+                ++kt;
+            }
+            if (!ok) {
+                // let every copy this thread started land before the CTA exits
+                volatile int never = 0;
+                for (int64_t x = q_armed - 2; x < q_armed; ++x)
+                    if (x >= 0) mbar_wait(&q_full[x & 1], uint32_t(x >> 1) & 1, &never, 100000000ull);
+                if (kv_armed > 0) mbar_wait(kv_full, uint32_t(kv_armed - 1) & 1, &never, 100000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        if (elect_one()) {
+            constexpr uint32_t idS = idesc_f16(128, BM, kType, 0, 0);
+            constexpr uint32_t idDV = idesc_f16(128, D, kType, 0, 1);
+            constexpr uint32_t idDQ = idesc_f16(128, 64, kType, 1, 1);
+            const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP), adS = smem_u32(sdS);
+            bool ok = true;
+            int64_t kt = 0, qi = 0;
+            for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
+                const int64_t j0 = jt * BN;
+                int qt0, nq;
+                query_tiles<BM>(a.mask, j0, lq, lkv, &qt0, &nq);
+                const int n_iter = G * nq;
+                if (n_iter == 0) continue;
+                if (ok && !(ok = mbar_wait(kv_full, uint32_t(kt) & 1, abort))) flag_abort(abort, a.status);
+                tc_fence_after();
+                for (int it = 0; it < n_iter; ++it, ++qi) {
+                    const int st = int(qi & 1);
+                    const uint32_t aQ = smem_u32(smem + Cfg::OFF_Q + st * Cfg::Q_BYTES);
+                    const uint32_t adO = smem_u32(smem + Cfg::OFF_DO + st * Cfg::Q_BYTES);
+                    if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(qi >> 1) & 1, abort))) flag_abort(abort, a.status);
+                    tc_fence_after();
+                    if (ok) {
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_f16_ss(tmem + Cfg::T_S, desc_kmaj(aK, BN, kk), desc_kmaj(aQ, BM, kk), idS, kk > 0);
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_f16_ss(tmem + Cfg::T_DP, desc_kmaj(aV, BN, kk), desc_kmaj(adO, BM, kk), idS, kk > 0);
+                        mma_commit(s_full);
+                    }
+                    if (ok && !(ok = mbar_wait(p_ready, uint32_t(qi) & 1, abort))) flag_abort(abort, a.status);
+                    tc_fence_after();
+                    if (ok) {
+                        for (int kk = 0; kk < BM / 16; ++kk)
+                            mma_f16_ss(tmem + Cfg::T_DV, desc_kmaj(aP, BN, kk), desc_mn(adO, BM, kk), idDV,
+                                       it > 0 || kk > 0);
+                        for (int kk = 0; kk < BM / 16; ++kk)
+                            mma_f16_ss(tmem + Cfg::T_DK, desc_kmaj(adS, BN, kk), desc_mn(aQ, BM, kk), idDV,
+                                       it > 0 || kk > 0);
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            if (D == 64)
+                                mma_f16_ss(tmem + Cfg::T_DQ, desc_mn(adS, BN, kk), desc_mn(aK, BN, kk), idDQ, kk > 0);
+                            else
+                                mma_f16_ss(tmem + Cfg::T_DQ, desc_mn(aK, BN, kk), desc_mn(adS, BN, kk), idDQ, kk > 0);
+                        }
+                        mma_commit(mma_done);
+                        mma_commit(&q_empty[st]);
+                    }
+                }
+                ++kt;
+            }
+            // wait for every MMA this thread issued before TMEM is freed
+            volatile int never = 0;
+            mma_commit(drain);
+            mbar_wait(drain, 0, &never, 100000000ull);
+        }
+    } else {
+        // ================================================= P / dS, dQ, dK / dV
+        const int lg = warp & 3, half = (warp - 2) >> 2;
+        const uint32_t lane_addr = uint32_t(lg * 32) << 16;
+        const int r = lg * 32 + lane;  // TMEM lane of this thread
+        const float sc = a.scale * kLog2e;
+        const bool leader = warp == 2 && lane == 0;
+        const int64_t shift = a.mask == ATTN_CAUSAL_BOTTOM_RIGHT ? lkv - lq : 0;
+        const uint32_t aP = smem_u32(sP), adS = smem_u32(sdS), adQ = smem_u32(sdQ);
+        T *dK = static_cast<T *>(a.dK.ptr), *dV = static_cast<T *>(a.dV.ptr);
+        bool ok = true;
+        int64_t kt = 0, qi = 0;
+        for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
+            const int64_t j0 = jt * BN, j = j0 + r;
+            const bool row_ok = j < lkv;
+            const int64_t kv_tok = kv_row0 + j;
+            const int64_t offk = kv_b * a.dK.sb + g * a.dK.sh + kv_tok * a.dK.ss;
+            const int64_t offv = kv_b * a.dV.sb + g * a.dV.sh + kv_tok * a.dV.ss;
+            int qt0, nq;
+            query_tiles<BM>(a.mask, j0, lq, lkv, &qt0, &nq);
+            const int n_iter = G * nq;
+            if (n_iter == 0) {  // no query sees these keys: dK = dV = 0
+                if (row_ok)
+                    for (int x = half * (D / 2); x < (half + 1) * (D / 2); x += 8) {
+                        *reinterpret_cast<uint4 *>(dK + offk + x) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(dV + offv + x) = make_uint4(0, 0, 0, 0);
+                    }
+                continue;
+            }
+            for (int it = 0; it < n_iter; ++it, ++qi) {
+                const int st = int(qi & 1);
+                const int64_t hq = g * G + it / nq, i0 = int64_t(qt0 + it % nq) * BM;
+                if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(qi >> 1) & 1, abort))) flag_abort(abort, a.status);
+                if (ok && !(ok = mbar_wait(s_full, uint32_t(qi) & 1, abort))) flag_abort(abort, a.status);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+                if (ok) {
+                    const float *lse_s = reinterpret_cast<const float *>(smem + Cfg::OFF_LSE + st * BM * 4);
+                    const float *dvec_s = reinterpret_cast<const float *>(smem + Cfg::OFF_DVEC + st * BM * 4);
+                    // first visible query column of this key row (causal); all masked past the sequence
+                    const int64_t cmin = !row_ok ? INT64_MAX : (a.mask ? j - shift - i0 : INT64_MIN);
+#pragma unroll
+                    for (int cc = 0; cc < BM / 64; ++cc) {
+                        const int col0 = half * (BM / 2) + cc * 32;
+                        uint32_t s[32], dp[32];
+                        tmem_ld32(tmem + lane_addr + Cfg::T_S + col0, s);
+                        tmem_ld32(tmem + lane_addr + Cfg::T_DP + col0, dp);
+                        tmem_ld_wait();
+                        uint32_t pk[16], dk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int c0 = col0 + 2 * e, c1 = c0 + 1;
+                            const float p0 = c0 >= cmin ? ex2(fmaf(__uint_as_float(s[2 * e]), sc, -lse_s[c0])) : 0.f;
+                            const float p1 = c1 >= cmin ? ex2(fmaf(__uint_as_float(s[2 * e + 1]), sc, -lse_s[c1])) : 0.f;
+                            const float d0 = p0 * (__uint_as_float(dp[2 * e]) - dvec_s[c0]);
+                            const float d1 = p1 * (__uint_as_float(dp[2 * e + 1]) - dvec_s[c1]);
+                            pk[e] = pack2<T>(p0, p1);
+                            dk[e] = pack2<T>(d0, d1);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t off = sw128_offset(uint32_t(r), uint32_t(col0 + 8 * q), BN);
+                            st_shared_v4(aP + off, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                            st_shared_v4(adS + off, dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_ready);
+                if (ok && !(ok = mbar_wait(mma_done, uint32_t(qi) & 1, abort))) flag_abort(abort, a.status);
+                tc_fence_after();
+                // ---- dQ tile -> shared memory -> TMA add-reduce into the fp32 accumulator
+                if (leader) bulk_wait_read0();  // the previous reduce has read sdQ
+                ok = bar_and(1, 256, ok);
+                if (ok) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_addr + Cfg::T_DQ + half * 32, v);
+                    tmem_ld_wait();
+                    if (D == 64) {  // lane = query row r, columns = head dims [32 half, 32 half + 32)
+                        const uint32_t base = adQ + uint32_t(half * BM * 128 + r * 128);
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch)
+                            st_shared_v4(base + (uint32_t(ch ^ (r & 7)) << 4), v[4 * ch], v[4 * ch + 1], v[4 * ch + 2],
+                                         v[4 * ch + 3]);
+                    } else {  // lane = head dim r, columns = query rows [32 half, 32 half + 32)
+                        const uint32_t base = adQ + uint32_t(lg * BM * 128) + uint32_t((lane & 3) << 2);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int c = half * 32 + e;
+                            st_shared_f32(base + uint32_t(c * 128) + (uint32_t((lane >> 2) ^ (c & 7)) << 4), v[e]);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1, 256);
+                if (leader && ok) {
+                    const int64_t row0 = (part * a.h + hq) * a.t_pad + geo.ws_start(b) + i0;
+                    for (int box = 0; box < D / 32; ++box)
+                        tma_reduce_add_2d(&p.tm_dq, sdQ + box * BM * 128, box * 32, int(row0));
+                    bulk_commit();
+                }
+            }
+            // ---- dK, dV of this key tile (this thread: row r, half of the head dims)
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+#pragma unroll
+                for (int cc = 0; cc < D / 64; ++cc) {
+                    const int col0 = half * (D / 2) + cc * 32;
+                    uint32_t vv[32], kk[32];
+                    tmem_ld32(tmem + lane_addr + Cfg::T_DV + col0, vv);
+                    tmem_ld32(tmem + lane_addr + Cfg::T_DK + col0, kk);
+                    tmem_ld_wait();
+                    if (row_ok) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 ov, ok4;
+                            ov.x = pack2<T>(__uint_as_float(vv[8 * q + 0]), __uint_as_float(vv[8 * q + 1]));
+                            ov.y = pack2<T>(__uint_as_float(vv[8 * q + 2]), __uint_as_float(vv[8 * q + 3]));
+                            ov.z = pack2<T>(__uint_as_float(vv[8 * q + 4]), __uint_as_float(vv[8 * q + 5]));
+                            ov.w = pack2<T>(__uint_as_float(vv[8 * q + 6]), __uint_as_float(vv[8 * q + 7]));
+                            ok4.x = pack2<T>(__uint_as_float(kk[8 * q + 0]) * a.scale, __uint_as_float(kk[8 * q + 1]) * a.scale);
+                            ok4.y = pack2<T>(__uint_as_float(kk[8 * q + 2]) * a.scale, __uint_as_float(kk[8 * q + 3]) * a.scale);
+                            ok4.z = pack2<T>(__uint_as_float(kk[8 * q + 4]) * a.scale, __uint_as_float(kk[8 * q + 5]) * a.scale);
+                            ok4.w = pack2<T>(__uint_as_float(kk[8 * q + 6]) * a.scale, __uint_as_float(kk[8 * q + 7]) * a.scale);
+                            *reinterpret_cast<uint4 *>(dV + offv + col0 + 8 * q) = ov;
+                            *reinterpret_cast<uint4 *>(dK + offk + col0 + 8 * q) = ok4;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(kv_empty);
+            if (leader) bulk_wait0();  // this tile's dQ adds land before the next tile's (fixed order)
+            ++kt;
+        }
+        if (leader) bulk_wait0();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::T_COLS);
+    }
+}
+
+// ===================================================================== host
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// 16-bit [B][H][S][D] view (element strides) as a 4-D map (d, s, h, b), box (64, rows, 1, 1).
+bool map_view(CUtensorMap *m, const View &v, int dtype, int64_t d, int64_t s, int64_t h, int64_t b, uint32_t rows)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(s), cuuint64_t(h), cuuint64_t(b)};
+    const int64_t sb = b > 1 ? v.sb : s * v.ss;  // unused extent-1 dim: any legal stride
+    cuuint64_t strides[3] = {cuuint64_t(v.ss * 2), cuuint64_t(v.sh * 2), cuuint64_t((sb > 0 ? sb : 8) * 2)};
+    cuuint32_t box[4] = {64, rows, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, dtype == ATTN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                     v.ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool map_dqacc(CUtensorMap *m, float *base, int64_t d, int64_t rows, uint32_t box_rows)
+{
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cuuint64_t(d), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(d * 4)};
+    cuuint32_t box[2] = {32, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <class Geo> int64_t max_kv_len(const Geo &g)
+{
+    int64_t m = 0;
+    for (int64_t b = 0; b < g.nseq; ++b) m = g.kv_len(b) > m ? g.kv_len(b) : m;
+    return m;
+}
+
+template <class T, int D, class Geo> cudaError_t run_tc(const DenseArgs &a, const Geo &g, cudaStream_t s)
+{
+    using Cfg = TcCfg<D>;
+    constexpr bool packed = IsPacked<Geo>::value;
+    const int64_t ntiles = (max_kv_len(g) + Cfg::BN - 1) / Cfg::BN;
+    if (ntiles == 0) return cudaSuccess;
+    TcParams prm;
+    prm.a = a;
+    const int64_t nb = packed ? 1 : a.nseq;
+    const int64_t sq = packed ? a.t_q : (a.t_q / (a.nseq ? a.nseq : 1));
+    const int64_t skv = packed ? a.t_kv : (a.t_kv / (a.nseq ? a.nseq : 1));
+    if (sq > 0 && (!map_view(&prm.tm_q, a.q, a.dtype, D, sq, a.h, nb, Cfg::BM) ||
+                   !map_view(&prm.tm_do, a.dO, a.dtype, D, sq, a.h, nb, Cfg::BM)))
+        return cudaErrorInvalidValue;
+    if (!map_view(&prm.tm_k, a.k, a.dtype, D, skv, a.h_kv, nb, Cfg::BN) ||
+        !map_view(&prm.tm_v, a.v, a.dtype, D, skv, a.h_kv, nb, Cfg::BN))
+        return cudaErrorInvalidValue;
+    if (!map_dqacc(&prm.tm_dq, a.dqacc, D, int64_t(a.n_part) * a.h * a.t_pad, Cfg::BM)) return cudaErrorInvalidValue;
+    if (sq == 0) prm.tm_q = prm.tm_do = prm.tm_k;  // never read: no query tiles
+    auto k = dense_bwd_tc_kernel<T, D, Geo>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    const int64_t units = (a.deterministic ? a.n_part : ntiles) * a.nseq * a.h_kv;
+    k<<<unsigned(units), 320, Cfg::SMEM_ALLOC, s>>>(prm, g);
+    return cudaGetLastError();
+}
+
+template <class Geo> cudaError_t dispatch(const DenseArgs &a, const Geo &g, cudaStream_t s)
+{
+    if (a.d == 64)
+        return a.dtype == ATTN_F16 ? run_tc<__half, 64>(a, g, s) : run_tc<__nv_bfloat16, 64>(a, g, s);
+    return a.dtype == ATTN_F16 ? run_tc<__half, 128>(a, g, s) : run_tc<__nv_bfloat16, 128>(a, g, s);
+}
+
+}  // namespace
+
+cudaError_t launch_dense_bwd_main(const DenseArgs &a, const FixedGeo &g, cudaStream_t s) { return dispatch(a, g, s); }
+cudaError_t launch_dense_bwd_main(const DenseArgs &a, const PackedGeo &g, cudaStream_t s) { return dispatch(a, g, s); }
+
+}  // namespace attn

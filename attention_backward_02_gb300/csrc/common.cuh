@@ -51,22 +51,54 @@ template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t u)
 // ------------------------------------------------------- sequence geometry
 // A fixed-length batch: sequence b covers query rows [b*s_q, (b+1)*s_q) of the
 // token-major index space.  Packed: starts from inclusive cumulative lengths.
+// Workspace rows (per-query-row stats and the fp32 dQ accumulator) give
+// every sequence a run of rows rounded up to a multiple of kWsRowAlign, so a
+// query tile never straddles two sequences there and every tile starts on a
+// 256-byte boundary.
+constexpr int64_t kWsRowAlign = 128;
+__host__ __device__ constexpr int64_t ws_round(int64_t n) { return (n + kWsRowAlign - 1) / kWsRowAlign * kWsRowAlign; }
+
 struct FixedGeo {
     int64_t nseq, s_q, s_kv;
     __host__ __device__ int64_t q_start(int64_t b) const { return b * s_q; }
     __host__ __device__ int64_t kv_start(int64_t b) const { return b * s_kv; }
     __host__ __device__ int64_t q_len(int64_t) const { return s_q; }
     __host__ __device__ int64_t kv_len(int64_t) const { return s_kv; }
+    __host__ __device__ int64_t ws_start(int64_t b) const { return b * ws_round(s_q); }
+    __host__ __device__ int64_t ws_rows() const { return nseq * ws_round(s_q); }
+    // workspace row -> (sequence, position); false on padding rows
+    __host__ __device__ bool ws_locate(int64_t r, int64_t *b, int64_t *i) const
+    {
+        const int64_t per = ws_round(s_q);
+        *b = r / per;
+        *i = r - *b * per;
+        return *i < s_q;
+    }
 };
 
 struct PackedGeo {
     int64_t nseq;
     int64_t cu_q[kMaxSeq + 1];   // cu_q[0] = 0, cu_q[b+1] = end of sequence b
     int64_t cu_kv[kMaxSeq + 1];
+    int64_t ws_q[kMaxSeq + 1];   // first workspace row of sequence b; ws_q[nseq] = total
     __host__ __device__ int64_t q_start(int64_t b) const { return cu_q[b]; }
     __host__ __device__ int64_t kv_start(int64_t b) const { return cu_kv[b]; }
     __host__ __device__ int64_t q_len(int64_t b) const { return cu_q[b + 1] - cu_q[b]; }
     __host__ __device__ int64_t kv_len(int64_t b) const { return cu_kv[b + 1] - cu_kv[b]; }
+    __host__ __device__ int64_t ws_start(int64_t b) const { return ws_q[b]; }
+    __host__ __device__ int64_t ws_rows() const { return ws_q[nseq]; }
+    __host__ __device__ bool ws_locate(int64_t r, int64_t *b, int64_t *i) const
+    {
+        int64_t lo = 0, hi = nseq - 1;  // last b with ws_q[b] <= r
+        while (lo < hi) {
+            int64_t mid = (lo + hi + 1) / 2;
+            if (ws_q[mid] <= r) lo = mid;
+            else hi = mid - 1;
+        }
+        *b = lo;
+        *i = r - ws_q[lo];
+        return *i < q_len(lo);
+    }
 };
 
 // Visibility of key j to query i (both local to their sequence).

@@ -45,6 +45,8 @@ __device__ __forceinline__ int64_t lse_index(const DenseArgs &a, const PackedGeo
 
 // ------------------------------------------------------------- preprocess
 // grid (ceil(t_pad / 128), h), 256 threads; 8 elements per thread per row.
+// Covers every workspace row: padding rows get LSE2 = +inf (so P = 0) and
+// D = 0, and every partial dQ buffer is zeroed.
 template <class T, class Geo>
 __global__ void __launch_bounds__(256) dense_preprocess_kernel(DenseArgs a, Geo geo)
 {
@@ -54,11 +56,14 @@ __global__ void __launch_bounds__(256) dense_preprocess_kernel(DenseArgs a, Geo 
     const int lane_in_row = threadIdx.x % tpr;
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.status = 0u;
     for (int r = threadIdx.x / tpr; r < 128; r += rows_per_pass) {
-        const int64_t t = int64_t(blockIdx.x) * 128 + r;
-        const bool live = t < a.t_pad;  // no early exit: the row's threads shuffle below
-        const int64_t row = h * a.t_pad + t;
+        const int64_t wr = int64_t(blockIdx.x) * 128 + r;  // workspace row
+        const bool live = wr < a.t_pad;  // no early exit: the row's threads shuffle below
+        int64_t b = 0, i = 0;
+        const bool real = live && geo.ws_locate(wr, &b, &i);
+        const int64_t t = geo.q_start(b) + i;
+        const int64_t row = h * a.t_pad + wr;
         float dsum = 0.f;
-        if (t < a.t_q) {
+        if (real) {
             const uint4 ov = *reinterpret_cast<const uint4 *>(
                 static_cast<const T *>(a.o.ptr) + tok_off(a.o, geo, t, h) + lane_in_row * 8);
             const uint4 dv = *reinterpret_cast<const uint4 *>(
@@ -73,8 +78,8 @@ __global__ void __launch_bounds__(256) dense_preprocess_kernel(DenseArgs a, Geo 
         for (int off = tpr / 2; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
         if (!live) continue;
         if (lane_in_row == 0) {
-            a.dvec[row] = t < a.t_q ? dsum : 0.f;
-            a.lse2[row] = t < a.t_q ? a.lse[lse_index(a, geo, t, h)] * kLog2e : INFINITY;
+            a.dvec[row] = real ? dsum : 0.f;
+            a.lse2[row] = real ? a.lse[lse_index(a, geo, t, h)] * kLog2e : INFINITY;
         }
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int p = 0; p < a.n_part; ++p) {
@@ -95,9 +100,11 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(DenseArgs a, Geo geo)
     const int rows_per_pass = 256 / tpr;
     const int lane_in_row = threadIdx.x % tpr;
     for (int r = threadIdx.x / tpr; r < 128; r += rows_per_pass) {
-        const int64_t t = int64_t(blockIdx.x) * 128 + r;
-        if (t >= a.t_q) break;
-        const int64_t row = h * a.t_pad + t;
+        const int64_t wr = int64_t(blockIdx.x) * 128 + r;
+        int64_t b = 0, i = 0;
+        if (wr >= a.t_pad || !geo.ws_locate(wr, &b, &i)) continue;
+        const int64_t t = geo.q_start(b) + i;
+        const int64_t row = h * a.t_pad + wr;
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -236,7 +243,7 @@ template <class Geo> cudaError_t preprocess(const DenseArgs &a, const Geo &g, cu
 template <class Geo> cudaError_t finalize(const DenseArgs &a, const Geo &g, cudaStream_t s)
 {
     if (a.t_q == 0) return cudaSuccess;
-    dim3 grid(unsigned((a.t_q + 127) / 128), unsigned(a.h));
+    dim3 grid(unsigned((a.t_pad + 127) / 128), unsigned(a.h));
     if (a.dtype == ATTN_F16) dq_finalize_kernel<__half, Geo><<<grid, 256, 0, s>>>(a, g);
     else dq_finalize_kernel<__nv_bfloat16, Geo><<<grid, 256, 0, s>>>(a, g);
     return cudaGetLastError();

@@ -23,8 +23,9 @@ struct View {
 //   lse2     f32 [h][t_pad]          LSE * log2(e); +inf on padding rows
 //   dvec     f32 [h][t_pad]          D = rowsum(dO * O); 0 on padding rows
 //   dqacc    f32 [n_part][h][t_pad][d]
-// Row index of (head hq, token t) is hq * t_pad + t, where t is the token in
-// the packed index space (b * s_q + i for a fixed-length batch).
+// t_pad = sum over sequences of their query length rounded up to 128
+// (Geo::ws_start / ws_rows); the row of (head hq, sequence b, position i) is
+// hq * t_pad + ws_start(b) + i.
 struct DenseArgs {
     int dtype;                  // ATTN_F16 / ATTN_BF16
     int64_t nseq, h, h_kv, d;

@@ -48,7 +48,7 @@ def _status(ab, desc):
 def test_workspace_size(ab):
     st, nbytes = _status(ab, _desc(ab))
     assert st == 0
-    t_pad = 4 * 1024 + 128
+    t_pad = 4 * 1024  # each sequence rounded up to 128 rows
     assert nbytes >= 2 * 12 * t_pad * 4 + 12 * t_pad * 64 * 4
     st, det = _status(ab, _desc(ab, deterministic=True, dq_splits=4))
     assert st == 0 and det >= nbytes + 3 * 12 * t_pad * 64 * 4
