@@ -22,7 +22,7 @@ ATTN_MASK_NONE, ATTN_CAUSAL_TOP_LEFT, ATTN_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
 # every exported symbol of include/attnbwd.h
 EXPORTS = ("sdpa_workspace_size", "sdpa_fwd_stats", "sdpa_bwd", "nsa_workspace_size",
            "nsa_selected_attn_bwd", "nsa_block_lists", "attn_query_status", "attn_status_string",
-           "attn_set_main_kernel_events", "sdpa_bwd_static_scratch")
+           "attn_set_main_kernel_events", "sdpa_bwd_static_scratch", "attn_last_error")
 
 
 class attn_view_t(C.Structure):
@@ -66,13 +66,14 @@ def load() -> C.CDLL:
         "nsa_block_lists": [N, P(C.c_int32), P(C.c_int32), P(C.c_int32), P(C.c_int64), V, S, V],
         "attn_query_status": [V, V, P(C.c_uint32)],
         "attn_status_string": [I],
+        "attn_last_error": [],
         "attn_set_main_kernel_events": [V, V],
         "sdpa_bwd_static_scratch": [D, view, view, view, view, view, P(C.c_float), view, view, view, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
         fn.argtypes = args
-        fn.restype = C.c_char_p if name == "attn_status_string" else I
+        fn.restype = C.c_char_p if name in ("attn_status_string", "attn_last_error") else I
     _lib = lib
     return lib
 
@@ -81,7 +82,8 @@ class AttnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         name = load().attn_status_string(status).decode()
-        super().__init__(f"{where} returned {name} ({status})")
+        detail = load().attn_last_error().decode() if status == ATTN_ERR_CUDA else ""
+        super().__init__(f"{where} returned {name} ({status})" + (f": {detail}" if detail else ""))
 
 
 def check(status: int, where: str) -> None:

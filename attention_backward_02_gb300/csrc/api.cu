@@ -144,7 +144,15 @@ void fill_geo(const attn_sdpa_desc_t *d, const DenseShape &sh, FixedGeo *fg, Pac
     }
 }
 
-attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+// Text of the CUDA error behind the last ATTN_ERR_CUDA of this host thread.
+thread_local const char *g_last_error = "";
+
+attn_status_t cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return ATTN_OK;
+    g_last_error = cudaGetErrorString(e);
+    return ATTN_ERR_CUDA;
+}
 
 thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 
@@ -153,6 +161,8 @@ cudaError_t mark(cudaEvent_t ev, cudaStream_t s) { return ev ? cudaEventRecord(e
 }  // namespace
 
 extern "C" {
+
+const char *attn_last_error(void) { return g_last_error; }
 
 const char *attn_status_string(attn_status_t s)
 {
@@ -255,17 +265,17 @@ attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t 
     fill_geo(desc, sh, &fg, &pg);
     cudaError_t e;
     if (sh.packed) {
-        if ((e = launch_dense_preprocess(a, pg, s)) != cudaSuccess) return ATTN_ERR_CUDA;
-        if ((e = mark(g_ev_before, s)) != cudaSuccess) return ATTN_ERR_CUDA;
-        if ((e = launch_dense_bwd_main(a, pg, s)) != cudaSuccess) return ATTN_ERR_CUDA;
-        if ((e = mark(g_ev_after, s)) != cudaSuccess) return ATTN_ERR_CUDA;
-        if ((e = launch_dq_finalize(a, pg, s)) != cudaSuccess) return ATTN_ERR_CUDA;
+        if ((e = launch_dense_preprocess(a, pg, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = mark(g_ev_before, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = launch_dense_bwd_main(a, pg, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = mark(g_ev_after, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = launch_dq_finalize(a, pg, s)) != cudaSuccess) return cuda_status(e);
     } else {
-        if ((e = launch_dense_preprocess(a, fg, s)) != cudaSuccess) return ATTN_ERR_CUDA;
-        if ((e = mark(g_ev_before, s)) != cudaSuccess) return ATTN_ERR_CUDA;
-        if ((e = launch_dense_bwd_main(a, fg, s)) != cudaSuccess) return ATTN_ERR_CUDA;
-        if ((e = mark(g_ev_after, s)) != cudaSuccess) return ATTN_ERR_CUDA;
-        if ((e = launch_dq_finalize(a, fg, s)) != cudaSuccess) return ATTN_ERR_CUDA;
+        if ((e = launch_dense_preprocess(a, fg, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = mark(g_ev_before, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = launch_dense_bwd_main(a, fg, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = mark(g_ev_after, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = launch_dq_finalize(a, fg, s)) != cudaSuccess) return cuda_status(e);
     }
     return ATTN_OK;
 }
@@ -446,10 +456,11 @@ attn_status_t attn_query_status(void *workspace, void *stream, uint32_t *device_
 {
     if (!workspace || !device_flags) return ATTN_ERR_NULLPTR;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaError_t e;
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_status(e);
     uint32_t flags = 0;
-    if (cudaMemcpy(&flags, workspace, sizeof flags, cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (flags && cudaMemset(workspace, 0, sizeof flags) != cudaSuccess) return ATTN_ERR_CUDA;
+    if ((e = cudaMemcpy(&flags, workspace, sizeof flags, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_status(e);
+    if (flags && (e = cudaMemset(workspace, 0, sizeof flags)) != cudaSuccess) return cuda_status(e);
     *device_flags = flags;
     return flags ? ATTN_ERR_DEVICE : ATTN_OK;
 }

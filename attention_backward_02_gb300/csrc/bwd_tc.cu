@@ -10,28 +10,36 @@
 // and walks every (query head of the group, query tile of BM rows) that sees
 // it.  Everything is computed transposed, so the 128 key rows are the MMA M
 // dimension and the TMEM lanes:
-//   S^T  = K Q^T           M=128 (keys) N=BM  K=D    A=K  (K-major) B=Q  (K-major)
-//   dP^T = V dO^T          M=128        N=BM  K=D    A=V  (K-major) B=dO (K-major)
+//   S^T  = K Q^T           M=128 (keys) N=BM  K=D    A=K  (smem, K-major) B=Q  (K-major)
+//   dP^T = V dO^T          M=128        N=BM  K=D    A=V  (smem, K-major) B=dO (K-major)
 //   P^T  = exp2(S^T scale log2 e - LSE log2 e),  dS^T = P^T (dP^T - D)   (CUDA cores)
-//   dV  += P^T dO          M=128        N=D   K=BM   A=P^T (smem, K-major) B=dO (MN-major)
-//   dK  += dS^T Q          M=128        N=D   K=BM   A=dS^T (K-major)      B=Q  (MN-major)
+//   dV  += P^T dO          M=128        N=D   K=BM   A=P^T (TMEM, 16-bit)   B=dO (MN-major)
+//   dK  += dS^T Q          M=128        N=D   K=BM   A=dS^T (smem, K-major) B=Q  (MN-major)
 //   dQ   = dS K     (D=64) M=BM=128     N=64  K=128  A=dS (MN-major)       B=K  (MN-major)
 //   dQ^T = K^T dS^T (D=128) M=D=128     N=BM=64 K=128 A=K^T (MN-major)     B=dS^T (MN-major)
-// dV, dK stay in TMEM for the whole tile and are written once; the dQ tile is
-// staged in shared memory and added into the fp32 accumulator with a TMA
-// reduce-add.  TMEM: S^T BM + dP^T BM + dV D + dK D + dQ 64 = 448 columns.
+// dV, dK stay in TMEM for the whole tile and are written once; each dQ tile
+// is staged in shared memory and added into the fp32 accumulator with a TMA
+// reduce-add.  TMEM: S^T BM + dP^T BM + P^T BM/2 + dV D + dK D + dQ 64 columns
+// (512 at D = 64, 480 at D = 128).
 //
-// Roles (320 threads): warp 0 issues TMA loads (K/V once per tile; Q, dO and
-// the LSE / D vectors through a 2-stage ring), warp 1 issues the MMAs, warps
-// 2..9 read S^T / dP^T from TMEM (warp w reads lanes 32 (w % 4) .. + 31; the
-// two warps on the same lanes split the BM columns), write P^T and dS^T as
-// 16-bit tiles in the 128-byte-swizzled layout the MMA reads, then stage dQ
-// and finally write dK, dV.
+// Pipeline.  The MMA warp issues S/dP of query tile i and then dV/dK/dQ of
+// tile i-1, so the tensor cores run tile i-1's three GEMMs while the softmax
+// warps turn tile i's S/dP into P/dS.  Two 32 KB shared buffers alternate
+// per query tile: tile i writes its dS into one while tile i-1's GEMMs read
+// their dS from the other, which, once they complete, stages tile i-1's dQ
+// for the reduce-add.  P (16-bit, packed) waits in registers until tile
+// i-1's dV GEMM has released the P columns of TMEM.  Q, dO and the LSE / D
+// vectors stream through a 3-stage ring.
+//
+// Roles (320 threads): warp 0 issues TMA loads, warp 1 issues the MMAs,
+// warps 2..9 do the element-wise work (warp w reads TMEM lanes
+// 32 (w % 4) .. + 31; the two warps on the same lanes split the columns), the
+// dQ staging and the dK / dV epilogue.
 //
 // Causal masking: query tiles entirely before the first query that sees the
-// key tile are skipped; the rest are masked per element.  Key rows past the
-// sequence end are masked by row; query rows past it have LSE = +inf in the
-// workspace and so P = 0.
+// key tile are skipped; the rest are masked per element when needed.  Key
+// rows past the sequence end are masked by row; query rows past it have
+// LSE = +inf in the workspace and so P = 0.
 //
 // Every barrier wait is bounded (about a second).  On a timeout the thread
 // sets ATTN_DEV_TIMEOUT in the status word and an abort flag in shared
@@ -53,24 +61,25 @@ template <int D>
 struct TcCfg {
     static constexpr int BN = 128;                  // key rows per CTA tile
     static constexpr int BM = D == 64 ? 128 : 64;   // query rows per iteration
+    static constexpr int NST = 3;                   // Q / dO ring stages
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int Q_BYTES = BM * D * 2;
-    static constexpr int PS_BYTES = BN * BM * 2;
+    static constexpr int DS_BYTES = BN * BM * 2;
     static constexpr int DQ_BYTES = BM * D * 4;
+    static constexpr int X_BYTES = DS_BYTES > DQ_BYTES ? DS_BYTES : DQ_BYTES;  // dS / dQ buffer
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + KV_BYTES;
-    static constexpr int OFF_Q = OFF_V + KV_BYTES;          // 2 stages
-    static constexpr int OFF_DO = OFF_Q + 2 * Q_BYTES;      // 2 stages
-    static constexpr int OFF_P = OFF_DO + 2 * Q_BYTES;
-    static constexpr int OFF_DS = OFF_P + PS_BYTES;
-    static constexpr int OFF_DQ = OFF_DS + PS_BYTES;
-    static constexpr int OFF_LSE = OFF_DQ + DQ_BYTES;       // 2 stages x BM floats
-    static constexpr int OFF_DVEC = OFF_LSE + 2 * BM * 4;   // 2 stages x BM floats
-    static constexpr int OFF_BAR = OFF_DVEC + 2 * BM * 4;
-    static constexpr int OFF_MISC = OFF_BAR + 16 * 8;
+    static constexpr int OFF_Q = OFF_V + KV_BYTES;            // NST stages
+    static constexpr int OFF_DO = OFF_Q + NST * Q_BYTES;      // NST stages
+    static constexpr int OFF_X = OFF_DO + NST * Q_BYTES;      // 2 dS / dQ buffers
+    static constexpr int OFF_LSE = OFF_X + 2 * X_BYTES;       // NST x BM floats
+    static constexpr int OFF_DVEC = OFF_LSE + NST * BM * 4;   // NST x BM floats
+    static constexpr int OFF_BAR = OFF_DVEC + NST * BM * 4;
+    static constexpr int OFF_MISC = OFF_BAR + 24 * 8;
     static constexpr int SMEM = OFF_MISC + 64;
-    static constexpr int SMEM_ALLOC = SMEM + 1024;          // room to align the base to 1024
-    static constexpr int T_S = 0, T_DP = BM, T_DV = 2 * BM, T_DK = 2 * BM + D, T_DQ = 2 * BM + 2 * D;
+    static constexpr int SMEM_ALLOC = SMEM + 1024;            // room to align the base to 1024
+    static constexpr int T_S = 0, T_DP = BM, T_P = 2 * BM, T_DV = 2 * BM + BM / 2, T_DK = T_DV + D,
+                         T_DQ = T_DK + D;
     static constexpr int T_COLS = 512;
     static_assert(T_DQ + 64 <= T_COLS, "TMEM budget");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
@@ -99,6 +108,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, uint32_t v)
 {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
 }
 
 // AND of `pred` over the threads of named barrier `id` (also a barrier).
@@ -158,15 +174,17 @@ template <class T, int D, class Geo>
 __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_constant__ TcParams p, const Geo geo)
 {
     using Cfg = TcCfg<D>;
-    constexpr int BM = Cfg::BM, BN = Cfg::BN;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, NST = Cfg::NST;
+    constexpr int HC = BM / 2;  // query columns per softmax thread
     constexpr bool kPacked = IsPacked<Geo>::value;
     constexpr int kType = std::is_same<T, __half>::value ? 0 : 1;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
-    uint64_t *kv_full = bars + 0, *kv_empty = bars + 1, *q_full = bars + 2, *q_empty = bars + 4;
-    uint64_t *s_full = bars + 6, *p_ready = bars + 7, *mma_done = bars + 8, *drain = bars + 9;
+    uint64_t *kv_full = bars + 0, *kv_empty = bars + 1, *q_full = bars + 2, *q_empty = bars + 2 + NST;
+    uint64_t *s_full = bars + 2 + 2 * NST, *s_free = s_full + 1, *p_ready = s_full + 2, *mma_done = s_full + 3;
+    uint64_t *drain = s_full + 4;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 8);
     const DenseArgs &a = p.a;
@@ -176,11 +194,12 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
         *abort = 0;
         mbar_init(kv_full, 1);
         mbar_init(kv_empty, 8);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(&q_full[s], 1);
             mbar_init(&q_empty[s], 1);
         }
         mbar_init(s_full, 1);
+        mbar_init(s_free, 8);
         mbar_init(p_ready, 8);
         mbar_init(mma_done, 1);
         mbar_init(drain, 1);
@@ -205,8 +224,7 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
     const int q_b = kPacked ? 0 : int(b), kv_b = q_b;
     const int64_t q_row0 = kPacked ? geo.q_start(b) : 0, kv_row0 = kPacked ? geo.kv_start(b) : 0;
 
-    uint8_t *sK = smem + Cfg::OFF_K, *sV = smem + Cfg::OFF_V, *sP = smem + Cfg::OFF_P, *sdS = smem + Cfg::OFF_DS;
-    uint8_t *sdQ = smem + Cfg::OFF_DQ;
+    uint8_t *sK = smem + Cfg::OFF_K, *sV = smem + Cfg::OFF_V, *sX = smem + Cfg::OFF_X;
 
     if (warp == 0) {
         // ================================================= TMA producer
@@ -230,8 +248,8 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                     }
                 }
                 for (int it = 0; it < n_iter; ++it, ++qi) {
-                    const int st = int(qi & 1);
-                    const int64_t use = qi >> 1;
+                    const int st = int(qi % NST);
+                    const int64_t use = qi / NST;
                     if (use > 0 && ok && !(ok = mbar_wait(&q_empty[st], uint32_t(use - 1) & 1, abort)))
                         flag_abort(abort, a.status);
                     if (!ok) continue;
@@ -252,8 +270,8 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
             if (!ok) {
                 // let every copy this thread started land before the CTA exits
                 volatile int never = 0;
-                for (int64_t x = q_armed - 2; x < q_armed; ++x)
-                    if (x >= 0) mbar_wait(&q_full[x & 1], uint32_t(x >> 1) & 1, &never, 100000000ull);
+                for (int64_t x = q_armed - NST; x < q_armed; ++x)
+                    if (x >= 0) mbar_wait(&q_full[x % NST], uint32_t(x / NST) & 1, &never, 100000000ull);
                 if (kv_armed > 0) mbar_wait(kv_full, uint32_t(kv_armed - 1) & 1, &never, 100000000ull);
             }
         }
@@ -263,9 +281,28 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
             constexpr uint32_t idS = idesc_f16(128, BM, kType, 0, 0);
             constexpr uint32_t idDV = idesc_f16(128, D, kType, 0, 1);
             constexpr uint32_t idDQ = idesc_f16(128, 64, kType, 1, 1);
-            const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP), adS = smem_u32(sdS);
+            const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
             bool ok = true;
             int64_t kt = 0, qi = 0;
+            // dV, dK, dQ of query tile x (global index) whose P / dS are ready
+            auto grads = [&](int64_t x, bool first) {
+                const int st = int(x % NST);
+                const uint32_t adS = smem_u32(sX + (x & 1) * Cfg::X_BYTES);
+                const uint32_t aQ = smem_u32(smem + Cfg::OFF_Q + st * Cfg::Q_BYTES);
+                const uint32_t adO = smem_u32(smem + Cfg::OFF_DO + st * Cfg::Q_BYTES);
+                for (int kk = 0; kk < BM / 16; ++kk)
+                    mma_f16_ts(tmem + Cfg::T_DV, tmem + Cfg::T_P + kk * 8, desc_mn(adO, BM, kk), idDV, !first || kk > 0);
+                for (int kk = 0; kk < BM / 16; ++kk)
+                    mma_f16_ss(tmem + Cfg::T_DK, desc_kmaj(adS, BN, kk), desc_mn(aQ, BM, kk), idDV, !first || kk > 0);
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    if (D == 64)
+                        mma_f16_ss(tmem + Cfg::T_DQ, desc_mn(adS, BN, kk), desc_mn(aK, BN, kk), idDQ, kk > 0);
+                    else
+                        mma_f16_ss(tmem + Cfg::T_DQ, desc_mn(aK, BN, kk), desc_mn(adS, BN, kk), idDQ, kk > 0);
+                }
+                mma_commit(mma_done);
+                mma_commit(&q_empty[st]);
+            };
             for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
                 const int64_t j0 = jt * BN;
                 int qt0, nq;
@@ -275,10 +312,13 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                 if (ok && !(ok = mbar_wait(kv_full, uint32_t(kt) & 1, abort))) flag_abort(abort, a.status);
                 tc_fence_after();
                 for (int it = 0; it < n_iter; ++it, ++qi) {
-                    const int st = int(qi & 1);
+                    const int st = int(qi % NST);
                     const uint32_t aQ = smem_u32(smem + Cfg::OFF_Q + st * Cfg::Q_BYTES);
                     const uint32_t adO = smem_u32(smem + Cfg::OFF_DO + st * Cfg::Q_BYTES);
-                    if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(qi >> 1) & 1, abort))) flag_abort(abort, a.status);
+                    if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(qi / NST) & 1, abort))) flag_abort(abort, a.status);
+                    // S^T / dP^T of the previous query tile have been read out of TMEM
+                    if (qi > 0 && ok && !(ok = mbar_wait(s_free, uint32_t(qi - 1) & 1, abort)))
+                        flag_abort(abort, a.status);
                     tc_fence_after();
                     if (ok) {
                         for (int kk = 0; kk < D / 16; ++kk)
@@ -287,25 +327,15 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                             mma_f16_ss(tmem + Cfg::T_DP, desc_kmaj(aV, BN, kk), desc_kmaj(adO, BM, kk), idS, kk > 0);
                         mma_commit(s_full);
                     }
-                    if (ok && !(ok = mbar_wait(p_ready, uint32_t(qi) & 1, abort))) flag_abort(abort, a.status);
-                    tc_fence_after();
-                    if (ok) {
-                        for (int kk = 0; kk < BM / 16; ++kk)
-                            mma_f16_ss(tmem + Cfg::T_DV, desc_kmaj(aP, BN, kk), desc_mn(adO, BM, kk), idDV,
-                                       it > 0 || kk > 0);
-                        for (int kk = 0; kk < BM / 16; ++kk)
-                            mma_f16_ss(tmem + Cfg::T_DK, desc_kmaj(adS, BN, kk), desc_mn(aQ, BM, kk), idDV,
-                                       it > 0 || kk > 0);
-                        for (int kk = 0; kk < BN / 16; ++kk) {
-                            if (D == 64)
-                                mma_f16_ss(tmem + Cfg::T_DQ, desc_mn(adS, BN, kk), desc_mn(aK, BN, kk), idDQ, kk > 0);
-                            else
-                                mma_f16_ss(tmem + Cfg::T_DQ, desc_mn(aK, BN, kk), desc_mn(adS, BN, kk), idDQ, kk > 0);
-                        }
-                        mma_commit(mma_done);
-                        mma_commit(&q_empty[st]);
+                    if (it > 0) {
+                        if (ok && !(ok = mbar_wait(p_ready, uint32_t(qi - 1) & 1, abort))) flag_abort(abort, a.status);
+                        tc_fence_after();
+                        if (ok) grads(qi - 1, it == 1);
                     }
                 }
+                if (ok && !(ok = mbar_wait(p_ready, uint32_t(qi - 1) & 1, abort))) flag_abort(abort, a.status);
+                tc_fence_after();
+                if (ok) grads(qi - 1, n_iter == 1);
                 ++kt;
             }
             // wait for every MMA this thread issued before TMEM is freed
@@ -321,10 +351,46 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
         const float sc = a.scale * kLog2e;
         const bool leader = warp == 2 && lane == 0;
         const int64_t shift = a.mask == ATTN_CAUSAL_BOTTOM_RIGHT ? lkv - lq : 0;
-        const uint32_t aP = smem_u32(sP), adS = smem_u32(sdS), adQ = smem_u32(sdQ);
+        const uint32_t aX = smem_u32(sX);
         T *dK = static_cast<T *>(a.dK.ptr), *dV = static_cast<T *>(a.dV.ptr);
         bool ok = true;
         int64_t kt = 0, qi = 0;
+
+        // dQ of query tile x (head hq, first row i0), whose GEMMs just completed and released
+        // dS buffer x & 1 -> staged there -> TMA add-reduce into the fp32 accumulator
+        auto stage_dq = [&](int64_t x, int64_t hq, int64_t i0) {
+            const uint32_t adQ = aX + uint32_t(x & 1) * Cfg::X_BYTES;
+            uint8_t *sdQ = sX + (x & 1) * Cfg::X_BYTES;
+            ok = bar_and(1, 256, ok);
+            if (ok) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_addr + Cfg::T_DQ + half * 32, v);
+                tmem_ld_wait();
+                if (D == 64) {  // lane = query row r, columns = head dims [32 half, 32 half + 32)
+                    const uint32_t base = adQ + uint32_t(half * BM * 128 + r * 128);
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        st_shared_v4(base + (uint32_t(ch ^ (r & 7)) << 4), v[4 * ch], v[4 * ch + 1], v[4 * ch + 2],
+                                     v[4 * ch + 3]);
+                } else {  // lane = head dim r, columns = query rows [32 half, 32 half + 32)
+                    const uint32_t base = adQ + uint32_t(lg * BM * 128) + uint32_t((lane & 3) << 2);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int c = half * 32 + e;
+                        st_shared_f32(base + uint32_t(c * 128) + (uint32_t((lane >> 2) ^ (c & 7)) << 4), v[e]);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 256);
+            if (leader && ok) {
+                const int64_t row0 = (part * a.h + hq) * a.t_pad + geo.ws_start(b) + i0;
+                for (int box = 0; box < D / 32; ++box)
+                    tma_reduce_add_2d(&p.tm_dq, sdQ + box * BM * 128, box * 32, int(row0));
+                bulk_commit();
+            }
+        };
+
         for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
             const int64_t j0 = jt * BN, j = j0 + r;
             const bool row_ok = j < lkv;
@@ -342,83 +408,95 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                     }
                 continue;
             }
+            int64_t prev_hq = 0, prev_i0 = 0;
             for (int it = 0; it < n_iter; ++it, ++qi) {
-                const int st = int(qi & 1);
+                const int st = int(qi % NST);
                 const int64_t hq = g * G + it / nq, i0 = int64_t(qt0 + it % nq) * BM;
-                if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(qi >> 1) & 1, abort))) flag_abort(abort, a.status);
+                if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(qi / NST) & 1, abort))) flag_abort(abort, a.status);
                 if (ok && !(ok = mbar_wait(s_full, uint32_t(qi) & 1, abort))) flag_abort(abort, a.status);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
+                // dS buffer qi & 1 last staged dQ of tile qi - 2: that reduce must have read it
+                if (leader) bulk_wait_read0();
+                named_bar_sync(1, 256);
+                const uint32_t adS = aX + uint32_t(qi & 1) * Cfg::X_BYTES;
+                // ---- P^T (kept packed until TMEM frees) and dS^T (to shared memory now)
+                uint32_t pk[HC / 2];
                 if (ok) {
-                    const float *lse_s = reinterpret_cast<const float *>(smem + Cfg::OFF_LSE + st * BM * 4);
-                    const float *dvec_s = reinterpret_cast<const float *>(smem + Cfg::OFF_DVEC + st * BM * 4);
-                    // first visible query column of this key row (causal); all masked past the sequence
-                    const int64_t cmin = !row_ok ? INT64_MAX : (a.mask ? j - shift - i0 : INT64_MIN);
+                    const uint32_t a_lse = smem_u32(smem + Cfg::OFF_LSE + st * BM * 4);
+                    const uint32_t a_dv = smem_u32(smem + Cfg::OFF_DVEC + st * BM * 4);
+                    // first visible query column of this key row; everything is masked past the sequence
+                    const int64_t cmin64 = !row_ok ? INT64_MAX : (a.mask ? j - shift - i0 : INT64_MIN);
+                    const int cmin = int(cmin64 < -1 ? -1 : (cmin64 > BM ? BM : cmin64));
+                    const bool any_mask = __any_sync(0xffffffffu, cmin > half * HC);
 #pragma unroll
-                    for (int cc = 0; cc < BM / 64; ++cc) {
-                        const int col0 = half * (BM / 2) + cc * 32;
-                        uint32_t s[32], dp[32];
-                        tmem_ld32(tmem + lane_addr + Cfg::T_S + col0, s);
-                        tmem_ld32(tmem + lane_addr + Cfg::T_DP + col0, dp);
+                    for (int cc = 0; cc < HC / 16; ++cc) {
+                        const int col0 = half * HC + cc * 16;
+                        uint32_t s[16], dp[16];
+                        tmem_ld16(tmem + lane_addr + Cfg::T_S + col0, s);
+                        tmem_ld16(tmem + lane_addr + Cfg::T_DP + col0, dp);
+                        float lse[16], dv[16];
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const float4 l4 = ld_shared_f4(a_lse + uint32_t(col0 + 4 * q4) * 4);
+                            const float4 d4 = ld_shared_f4(a_dv + uint32_t(col0 + 4 * q4) * 4);
+                            lse[4 * q4] = l4.x; lse[4 * q4 + 1] = l4.y; lse[4 * q4 + 2] = l4.z; lse[4 * q4 + 3] = l4.w;
+                            dv[4 * q4] = d4.x; dv[4 * q4 + 1] = d4.y; dv[4 * q4 + 2] = d4.z; dv[4 * q4 + 3] = d4.w;
+                        }
                         tmem_ld_wait();
-                        uint32_t pk[16], dk[16];
+                        float pv[16], dsv[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const int c0 = col0 + 2 * e, c1 = c0 + 1;
-                            const float p0 = c0 >= cmin ? ex2(fmaf(__uint_as_float(s[2 * e]), sc, -lse_s[c0])) : 0.f;
-                            const float p1 = c1 >= cmin ? ex2(fmaf(__uint_as_float(s[2 * e + 1]), sc, -lse_s[c1])) : 0.f;
-                            const float d0 = p0 * (__uint_as_float(dp[2 * e]) - dvec_s[c0]);
-                            const float d1 = p1 * (__uint_as_float(dp[2 * e + 1]) - dvec_s[c1]);
-                            pk[e] = pack2<T>(p0, p1);
-                            dk[e] = pack2<T>(d0, d1);
+                            float pe = ex2(fmaf(__uint_as_float(s[e]), sc, -lse[e]));
+                            if (any_mask) pe = (col0 + e >= cmin) ? pe : 0.f;
+                            pv[e] = pe;
+                            dsv[e] = pe * (__uint_as_float(dp[e]) - dv[e]);
+                        }
+                        uint32_t dk[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            pk[cc * 8 + e] = pack2<T>(pv[2 * e], pv[2 * e + 1]);
+                            dk[e] = pack2<T>(dsv[2 * e], dsv[2 * e + 1]);
                         }
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
+                        for (int q = 0; q < 2; ++q) {
                             const uint32_t off = sw128_offset(uint32_t(r), uint32_t(col0 + 8 * q), BN);
-                            st_shared_v4(aP + off, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                             st_shared_v4(adS + off, dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
                         }
                     }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free);  // S^T / dP^T may be overwritten
+                // ---- the previous query tile's GEMMs have released P (TMEM) and dS (smem); its dQ is ready
+                if (it > 0) {
+                    if (ok && !(ok = mbar_wait(mma_done, uint32_t(qi - 1) & 1, abort))) flag_abort(abort, a.status);
+                    ok = __all_sync(0xffffffffu, ok);
+                    tc_fence_after();
+                    stage_dq(qi - 1, prev_hq, prev_i0);
+                }
+                if (ok) {
+#pragma unroll
+                    for (int c8 = 0; c8 < HC / 16; ++c8) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) w[e] = pk[c8 * 8 + e];
+                        tmem_st8(tmem + lane_addr + Cfg::T_P + half * (HC / 2) + c8 * 8, w);
+                    }
+                    tmem_st_wait();
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_ready);
-                if (ok && !(ok = mbar_wait(mma_done, uint32_t(qi) & 1, abort))) flag_abort(abort, a.status);
-                tc_fence_after();
-                // ---- dQ tile -> shared memory -> TMA add-reduce into the fp32 accumulator
-                if (leader) bulk_wait_read0();  // the previous reduce has read sdQ
-                ok = bar_and(1, 256, ok);
-                if (ok) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_addr + Cfg::T_DQ + half * 32, v);
-                    tmem_ld_wait();
-                    if (D == 64) {  // lane = query row r, columns = head dims [32 half, 32 half + 32)
-                        const uint32_t base = adQ + uint32_t(half * BM * 128 + r * 128);
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch)
-                            st_shared_v4(base + (uint32_t(ch ^ (r & 7)) << 4), v[4 * ch], v[4 * ch + 1], v[4 * ch + 2],
-                                         v[4 * ch + 3]);
-                    } else {  // lane = head dim r, columns = query rows [32 half, 32 half + 32)
-                        const uint32_t base = adQ + uint32_t(lg * BM * 128) + uint32_t((lane & 3) << 2);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int c = half * 32 + e;
-                            st_shared_f32(base + uint32_t(c * 128) + (uint32_t((lane >> 2) ^ (c & 7)) << 4), v[e]);
-                        }
-                    }
-                }
-                fence_proxy_async_smem();
-                named_bar_sync(1, 256);
-                if (leader && ok) {
-                    const int64_t row0 = (part * a.h + hq) * a.t_pad + geo.ws_start(b) + i0;
-                    for (int box = 0; box < D / 32; ++box)
-                        tma_reduce_add_2d(&p.tm_dq, sdQ + box * BM * 128, box * 32, int(row0));
-                    bulk_commit();
-                }
+                prev_hq = hq;
+                prev_i0 = i0;
             }
-            // ---- dK, dV of this key tile (this thread: row r, half of the head dims)
+            // ---- last query tile of this key tile: its dQ, then dK and dV
+            if (ok && !(ok = mbar_wait(mma_done, uint32_t(qi - 1) & 1, abort))) flag_abort(abort, a.status);
             ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+            stage_dq(qi - 1, prev_hq, prev_i0);
             if (ok) {
 #pragma unroll
                 for (int cc = 0; cc < D / 64; ++cc) {

@@ -212,6 +212,10 @@ attn_status_t attn_query_status(void *workspace, void *stream, uint32_t *device_
  * cudaEvent_t handles passed as void*; NULL, NULL clears.  Never fails.    */
 attn_status_t attn_set_main_kernel_events(void *before, void *after);
 
+/* Text of the CUDA runtime / driver error behind the most recent
+ * ATTN_ERR_CUDA returned to this host thread ("" if none).  Static storage. */
+const char *attn_last_error(void);
+
 /* Human-readable name of a status code (static storage).                    */
 const char *attn_status_string(attn_status_t status);
 
