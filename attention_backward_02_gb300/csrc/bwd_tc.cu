@@ -117,6 +117,30 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
     return v;
 }
 
+// P = exp2(x) and dS = P (dP - D) for two adjacent columns, packed as two
+// 16-bit values each (low half = first column).  x = S scale log2 e - LSE
+// log2 e (-inf where masked), g = dP - D.  fp16: the two exponentials run as
+// one f16x2 MUFU operation and dS as one f16x2 multiply, at the precision P
+// and dS are rounded to anyway.  bf16: fp32 exponentials and products,
+// rounded once.
+template <class T> __device__ __forceinline__ uint32_t p_and_ds(float x0, float x1, float g0, float g1, uint32_t *ds);
+template <> __device__ __forceinline__ uint32_t p_and_ds<__half>(float x0, float x1, float g0, float g1, uint32_t *ds)
+{
+    const uint32_t xh = pack2<__half>(x0, x1), gh = pack2<__half>(g0, g1);
+    uint32_t ph, dh;
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(ph) : "r"(xh));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(dh) : "r"(ph), "r"(gh));
+    *ds = dh;
+    return ph;
+}
+template <>
+__device__ __forceinline__ uint32_t p_and_ds<__nv_bfloat16>(float x0, float x1, float g0, float g1, uint32_t *ds)
+{
+    const float p0 = ex2(x0), p1 = ex2(x1);
+    *ds = pack2<__nv_bfloat16>(p0 * g0, p1 * g1);
+    return pack2<__nv_bfloat16>(p0, p1);
+}
+
 // AND of `pred` over the threads of named barrier `id` (also a barrier).
 __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t nthreads, bool pred)
 {
@@ -429,34 +453,39 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                     const int64_t cmin64 = !row_ok ? INT64_MAX : (a.mask ? j - shift - i0 : INT64_MIN);
                     const int cmin = int(cmin64 < -1 ? -1 : (cmin64 > BM ? BM : cmin64));
                     const bool any_mask = __any_sync(0xffffffffu, cmin > half * HC);
+                    // chunks of 16 columns; the TMEM loads of chunk cc + 1 are issued before
+                    // chunk cc is computed
+                    constexpr int NCH = HC / 16;
+                    uint32_t sbuf[2][16], dbuf[2][16];
+                    tmem_ld16(tmem + lane_addr + Cfg::T_S + half * HC, sbuf[0]);
+                    tmem_ld16(tmem + lane_addr + Cfg::T_DP + half * HC, dbuf[0]);
 #pragma unroll
-                    for (int cc = 0; cc < HC / 16; ++cc) {
-                        const int col0 = half * HC + cc * 16;
-                        uint32_t s[16], dp[16];
-                        tmem_ld16(tmem + lane_addr + Cfg::T_S + col0, s);
-                        tmem_ld16(tmem + lane_addr + Cfg::T_DP + col0, dp);
-                        float lse[16], dv[16];
+                    for (int cc = 0; cc < NCH; ++cc) {
+                        const int col0 = half * HC + cc * 16, cur = cc & 1;
+                        tmem_ld_wait_regs(sbuf[cur], dbuf[cur]);
+                        if (cc + 1 < NCH) {
+                            tmem_ld16(tmem + lane_addr + Cfg::T_S + col0 + 16, sbuf[cur ^ 1]);
+                            tmem_ld16(tmem + lane_addr + Cfg::T_DP + col0 + 16, dbuf[cur ^ 1]);
+                        }
+                        uint32_t dk[8];
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             const float4 l4 = ld_shared_f4(a_lse + uint32_t(col0 + 4 * q4) * 4);
                             const float4 d4 = ld_shared_f4(a_dv + uint32_t(col0 + 4 * q4) * 4);
-                            lse[4 * q4] = l4.x; lse[4 * q4 + 1] = l4.y; lse[4 * q4 + 2] = l4.z; lse[4 * q4 + 3] = l4.w;
-                            dv[4 * q4] = d4.x; dv[4 * q4 + 1] = d4.y; dv[4 * q4 + 2] = d4.z; dv[4 * q4 + 3] = d4.w;
-                        }
-                        tmem_ld_wait();
-                        float pv[16], dsv[16];
+                            const float lse4[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            float pe = ex2(fmaf(__uint_as_float(s[e]), sc, -lse[e]));
-                            if (any_mask) pe = (col0 + e >= cmin) ? pe : 0.f;
-                            pv[e] = pe;
-                            dsv[e] = pe * (__uint_as_float(dp[e]) - dv[e]);
-                        }
-                        uint32_t dk[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            pk[cc * 8 + e] = pack2<T>(pv[2 * e], pv[2 * e + 1]);
-                            dk[e] = pack2<T>(dsv[2 * e], dsv[2 * e + 1]);
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const int e = 4 * q4 + 2 * h2, c = col0 + e;
+                                float x0 = fmaf(__uint_as_float(sbuf[cur][e]), sc, -lse4[2 * h2]);
+                                float x1 = fmaf(__uint_as_float(sbuf[cur][e + 1]), sc, -lse4[2 * h2 + 1]);
+                                if (any_mask) {
+                                    x0 = c >= cmin ? x0 : -INFINITY;
+                                    x1 = c + 1 >= cmin ? x1 : -INFINITY;
+                                }
+                                const float g0 = __uint_as_float(dbuf[cur][e]) - dv4[2 * h2];
+                                const float g1 = __uint_as_float(dbuf[cur][e + 1]) - dv4[2 * h2 + 1];
+                                pk[cc * 8 + 2 * q4 + h2] = p_and_ds<T>(x0, x1, g0, g1, &dk[2 * q4 + h2]);
+                            }
                         }
 #pragma unroll
                         for (int q = 0; q < 2; ++q) {
