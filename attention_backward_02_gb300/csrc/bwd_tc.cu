@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();  // the preprocess (LSE, D, zeroed dQ accumulator) has completed
 
     // ---- work unit: (sequence b, kv head g) and its key tiles
     const int64_t nheads = a.nseq * a.h_kv;
@@ -559,6 +560,7 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
             ++kt;
         }
         if (leader) bulk_wait0();
+        pdl_trigger();  // the dQ finalize may start launching; it waits for this grid
     }
 
     tc_fence_before();
@@ -648,8 +650,7 @@ template <class T, int D, class Geo> cudaError_t run_tc(const DenseArgs &a, cons
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const int64_t units = (a.deterministic ? a.n_part : ntiles) * a.nseq * a.h_kv;
-    k<<<unsigned(units), 320, Cfg::SMEM_ALLOC, s>>>(prm, g);
-    return cudaGetLastError();
+    return launch_kernel(k, dim3(unsigned(units)), dim3(320), Cfg::SMEM_ALLOC, s, true, prm, g);
 }
 
 template <class Geo> cudaError_t dispatch(const DenseArgs &a, const Geo &g, cudaStream_t s)

@@ -131,6 +131,33 @@ __host__ __device__ __forceinline__ int64_t first_query_seeing(int mask, int64_t
     return 0;
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel of the stream still runs; it must wait here before it
+// touches anything that kernel writes.  (A no-op for an ordinary launch.)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel of the stream start launching (its blocks then wait
+// in pdl_wait until this grid has completed).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launches k on stream s, optionally with programmatic stream serialization.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                                 Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, static_cast<Args &&>(args)...);
+}
+
 // ----------------------------------------------------------- status word
 __device__ __forceinline__ void raise_flag(uint32_t *status, uint32_t bit)
 {

@@ -44,85 +44,86 @@ __device__ __forceinline__ int64_t lse_index(const DenseArgs &a, const PackedGeo
 }
 
 // ------------------------------------------------------------- preprocess
-// grid (ceil(t_pad / 128), h), 256 threads; 8 elements per thread per row.
-// Covers every workspace row: padding rows get LSE2 = +inf (so P = 0) and
-// D = 0, and every partial dQ buffer is zeroed.
+// One workspace row per group of d/8 threads (8 elements each), 256 threads
+// per block, grid (ceil(t_pad / rows per block), h).  Covers every workspace
+// row: padding rows get LSE2 = +inf (so P = 0) and D = 0, and every partial
+// dQ buffer is zeroed.  Launched normally (it overwrites what the previous
+// call's last kernel reads); lets the main kernel launch behind it.
 template <class T, class Geo>
 __global__ void __launch_bounds__(256) dense_preprocess_kernel(DenseArgs a, Geo geo)
 {
+    pdl_trigger();
     const int64_t h = blockIdx.y;
-    const int tpr = int(a.d / 8);               // threads per row
-    const int rows_per_pass = 256 / tpr;
+    const int tpr = int(a.d / 8);  // threads per row
     const int lane_in_row = threadIdx.x % tpr;
+    const int64_t wr = int64_t(blockIdx.x) * (256 / tpr) + threadIdx.x / tpr;  // workspace row
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.status = 0u;
-    for (int r = threadIdx.x / tpr; r < 128; r += rows_per_pass) {
-        const int64_t wr = int64_t(blockIdx.x) * 128 + r;  // workspace row
-        const bool live = wr < a.t_pad;  // no early exit: the row's threads shuffle below
-        int64_t b = 0, i = 0;
-        const bool real = live && geo.ws_locate(wr, &b, &i);
-        const int64_t t = geo.q_start(b) + i;
-        const int64_t row = h * a.t_pad + wr;
-        float dsum = 0.f;
-        if (real) {
-            const uint4 ov = *reinterpret_cast<const uint4 *>(
-                static_cast<const T *>(a.o.ptr) + tok_off(a.o, geo, t, h) + lane_in_row * 8);
-            const uint4 dv = *reinterpret_cast<const uint4 *>(
-                static_cast<const T *>(a.dO.ptr) + tok_off(a.dO, geo, t, h) + lane_in_row * 8);
-            const uint32_t *op = &ov.x, *dp = &dv.x;
+    const bool live = wr < a.t_pad;  // no early exit: the row's threads shuffle below
+    int64_t b = 0, i = 0;
+    const bool real = live && geo.ws_locate(wr, &b, &i);
+    const int64_t t = geo.q_start(b) + i;
+    const int64_t row = h * a.t_pad + wr;
+    float dsum = 0.f, lse = 0.f;
+    if (real) {
+        const uint4 ov = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.o.ptr) + tok_off(a.o, geo, t, h) +
+                                                          lane_in_row * 8);
+        const uint4 dv = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.dO.ptr) +
+                                                          tok_off(a.dO, geo, t, h) + lane_in_row * 8);
+        if (lane_in_row == 0) lse = a.lse[lse_index(a, geo, t, h)];
+        const uint32_t *op = &ov.x, *dp = &dv.x;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float2 of = unpack2<T>(op[e]), df = unpack2<T>(dp[e]);
-                dsum += of.x * df.x + of.y * df.y;
-            }
+        for (int e = 0; e < 4; ++e) {
+            float2 of = unpack2<T>(op[e]), df = unpack2<T>(dp[e]);
+            dsum += of.x * df.x + of.y * df.y;
         }
-        for (int off = tpr / 2; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
-        if (!live) continue;
-        if (lane_in_row == 0) {
-            a.dvec[row] = real ? dsum : 0.f;
-            a.lse2[row] = real ? a.lse[lse_index(a, geo, t, h)] * kLog2e : INFINITY;
-        }
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int p = 0; p < a.n_part; ++p) {
-            float4 *dst = reinterpret_cast<float4 *>(a.dqacc + ((int64_t(p) * a.h * a.t_pad + row) * a.d)) +
-                          lane_in_row * 2;
-            dst[0] = z;
-            dst[1] = z;
-        }
+    }
+    for (int off = tpr / 2; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+    if (!live) return;
+    if (lane_in_row == 0) {
+        a.dvec[row] = real ? dsum : 0.f;
+        a.lse2[row] = real ? lse * kLog2e : INFINITY;
+    }
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < a.n_part; ++p) {
+        float4 *dst =
+            reinterpret_cast<float4 *>(a.dqacc + ((int64_t(p) * a.h * a.t_pad + row) * a.d)) + lane_in_row * 2;
+        dst[0] = z;
+        dst[1] = z;
     }
 }
 
 // ------------------------------------------------------------ dq finalize
+// dQ = cast(scale * sum over the partial buffers, in index order).  Same row
+// mapping as the preprocess; launched behind the main kernel and waits for it.
 template <class T, class Geo>
 __global__ void __launch_bounds__(256) dq_finalize_kernel(DenseArgs a, Geo geo)
 {
     const int64_t h = blockIdx.y;
     const int tpr = int(a.d / 8);
-    const int rows_per_pass = 256 / tpr;
     const int lane_in_row = threadIdx.x % tpr;
-    for (int r = threadIdx.x / tpr; r < 128; r += rows_per_pass) {
-        const int64_t wr = int64_t(blockIdx.x) * 128 + r;
-        int64_t b = 0, i = 0;
-        if (wr >= a.t_pad || !geo.ws_locate(wr, &b, &i)) continue;
-        const int64_t t = geo.q_start(b) + i;
-        const int64_t row = h * a.t_pad + wr;
-        float acc[8];
+    const int64_t wr = int64_t(blockIdx.x) * (256 / tpr) + threadIdx.x / tpr;
+    int64_t b = 0, i = 0;
+    const bool real = wr < a.t_pad && geo.ws_locate(wr, &b, &i);
+    pdl_wait();
+    if (!real) return;
+    const int64_t t = geo.q_start(b) + i;
+    const int64_t row = h * a.t_pad + wr;
+    float acc[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int p = 0; p < a.n_part; ++p) {  // fixed order: bitwise reproducible
-            const float4 *src =
-                reinterpret_cast<const float4 *>(a.dqacc + ((int64_t(p) * a.h * a.t_pad + row) * a.d)) +
-                lane_in_row * 2;
-            float4 x0 = src[0], x1 = src[1];
-            acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
-            acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
-        }
-        uint4 out;
-        out.x = pack2<T>(acc[0] * a.scale, acc[1] * a.scale);
-        out.y = pack2<T>(acc[2] * a.scale, acc[3] * a.scale);
-        out.z = pack2<T>(acc[4] * a.scale, acc[5] * a.scale);
-        out.w = pack2<T>(acc[6] * a.scale, acc[7] * a.scale);
-        *reinterpret_cast<uint4 *>(static_cast<T *>(a.dQ.ptr) + tok_off(a.dQ, geo, t, h) + lane_in_row * 8) = out;
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int p = 0; p < a.n_part; ++p) {  // fixed order: bitwise reproducible
+        const float4 *src =
+            reinterpret_cast<const float4 *>(a.dqacc + ((int64_t(p) * a.h * a.t_pad + row) * a.d)) + lane_in_row * 2;
+        float4 x0 = src[0], x1 = src[1];
+        acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
+        acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
     }
+    uint4 out;
+    out.x = pack2<T>(acc[0] * a.scale, acc[1] * a.scale);
+    out.y = pack2<T>(acc[2] * a.scale, acc[3] * a.scale);
+    out.z = pack2<T>(acc[4] * a.scale, acc[5] * a.scale);
+    out.w = pack2<T>(acc[6] * a.scale, acc[7] * a.scale);
+    *reinterpret_cast<uint4 *>(static_cast<T *>(a.dQ.ptr) + tok_off(a.dQ, geo, t, h) + lane_in_row * 8) = out;
 }
 
 // ------------------------------------------------------------- forward
@@ -234,19 +235,19 @@ template <> int64_t max_len_q(const DenseArgs &, const PackedGeo &g)
 
 template <class Geo> cudaError_t preprocess(const DenseArgs &a, const Geo &g, cudaStream_t s)
 {
-    dim3 grid(unsigned((a.t_pad + 127) / 128), unsigned(a.h));
-    if (a.dtype == ATTN_F16) dense_preprocess_kernel<__half, Geo><<<grid, 256, 0, s>>>(a, g);
-    else dense_preprocess_kernel<__nv_bfloat16, Geo><<<grid, 256, 0, s>>>(a, g);
-    return cudaGetLastError();
+    const int64_t rows_per_block = 256 / (a.d / 8);
+    dim3 grid(unsigned((a.t_pad + rows_per_block - 1) / rows_per_block), unsigned(a.h));
+    if (a.dtype == ATTN_F16) return launch_kernel(dense_preprocess_kernel<__half, Geo>, grid, 256, 0, s, false, a, g);
+    return launch_kernel(dense_preprocess_kernel<__nv_bfloat16, Geo>, grid, 256, 0, s, false, a, g);
 }
 
 template <class Geo> cudaError_t finalize(const DenseArgs &a, const Geo &g, cudaStream_t s)
 {
     if (a.t_q == 0) return cudaSuccess;
-    dim3 grid(unsigned((a.t_pad + 127) / 128), unsigned(a.h));
-    if (a.dtype == ATTN_F16) dq_finalize_kernel<__half, Geo><<<grid, 256, 0, s>>>(a, g);
-    else dq_finalize_kernel<__nv_bfloat16, Geo><<<grid, 256, 0, s>>>(a, g);
-    return cudaGetLastError();
+    const int64_t rows_per_block = 256 / (a.d / 8);
+    dim3 grid(unsigned((a.t_pad + rows_per_block - 1) / rows_per_block), unsigned(a.h));
+    if (a.dtype == ATTN_F16) return launch_kernel(dq_finalize_kernel<__half, Geo>, grid, 256, 0, s, true, a, g);
+    return launch_kernel(dq_finalize_kernel<__nv_bfloat16, Geo>, grid, 256, 0, s, true, a, g);
 }
 
 template <class T, class Geo, int D> cudaError_t fwd_run(const DenseArgs &a, const Geo &g, dim3 grid, cudaStream_t s)

@@ -322,17 +322,25 @@ def run_ours(args, info):
     with ClockSampler(pci) as clocks:
         t_wall = time.perf_counter()
         for i in range(args.steps):
-            e_call0, e_main0, e_main1, e_call1 = ev[i]
-            lib.attn_set_main_kernel_events(C.c_void_p(e_main0.cuda_event), C.c_void_p(e_main1.cuda_event))
+            e_call0, _, _, e_call1 = ev[i]
             e_call0.record(stream)
             step()
             e_call1.record(stream)
-            lib.attn_set_main_kernel_events(None, None)
             flush.fill_(1)  # L2 flush outside the timed events
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     if dist:
         dist.barrier()
+    # second pass, same steps: events around the main kernel alone (for the
+    # roofline); events inside the call break the launch overlap, so this pass
+    # does not feed the headline number
+    for i in range(args.steps):
+        _, e_main0, e_main1, _ = ev[i]
+        lib.attn_set_main_kernel_events(C.c_void_p(e_main0.cuda_event), C.c_void_p(e_main1.cuda_event))
+        step()
+        lib.attn_set_main_kernel_events(None, None)
+        flush.fill_(1)
+    torch.cuda.synchronize()
     call_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps)]
     main_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     total_ms = sum(call_ms)
@@ -390,7 +398,7 @@ def run_ours(args, info):
                      "whole_call_frac": value / world / peak},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": statistics.mean(e2e_ms)},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step * args.steps,  # of the timed pass
         "clocks": clocks.summary(),
         "wall_s_timed_region": t_wall,
     }
