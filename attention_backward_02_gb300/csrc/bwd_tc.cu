@@ -86,7 +86,7 @@ struct TcCfg {
 };
 
 struct TcParams {
-    CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq;
+    CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq, tm_dk, tm_dv;
     DenseArgs a;
 };
 
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
     if (threadIdx.x == 0) {
         *abort = 0;
         mbar_init(kv_full, 1);
-        mbar_init(kv_empty, 8);
+        mbar_init(kv_empty, 1);
         for (int s = 0; s < NST; ++s) {
             mbar_init(&q_full[s], 1);
             mbar_init(&q_empty[s], 1);
@@ -236,18 +236,29 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
     pdl_wait();  // the preprocess (LSE, D, zeroed dQ accumulator) has completed
 
-    // ---- work unit: (sequence b, kv head g) and its key tiles
+    // ---- work units: (sequence b, kv head g) and its key tiles; unit
+    // index = first tile * (nseq * h_kv) + (b * h_kv + g), so for a causal
+    // fixed-length batch the units come heaviest first.  The CTA takes units
+    // c, 2C-1-c, 2C+c, ... (C CTAs), which evens out their total work.
     const int64_t nheads = a.nseq * a.h_kv;
-    const int64_t unit = blockIdx.x;
-    const int64_t bg = unit % nheads, first_tile = unit / nheads;
-    const int64_t b = bg / a.h_kv, g = bg % a.h_kv;
     const int64_t tile_step = a.deterministic ? a.n_part : INT64_MAX / 2;
-    const int64_t part = a.deterministic ? first_tile : 0;
-    const int64_t lq = geo.q_len(b), lkv = geo.kv_len(b);
-    const int64_t ntiles = (lkv + BN - 1) / BN;
     const int G = int(a.h / a.h_kv);
-    const int q_b = kPacked ? 0 : int(b), kv_b = q_b;
-    const int64_t q_row0 = kPacked ? geo.q_start(b) : 0, kv_row0 = kPacked ? geo.kv_start(b) : 0;
+#define ATTN_FOR_EACH_UNIT                                                                                    \
+    for (int64_t round_ = 0;; ++round_) {                                                                     \
+        const int64_t unit = round_ * gridDim.x +                                                             \
+                             ((round_ & 1) ? int64_t(gridDim.x) - 1 - blockIdx.x : int64_t(blockIdx.x));      \
+        if (unit >= a.tc_units) break;                                                                        \
+        const int64_t bg = unit % nheads, first_tile = unit / nheads;                                         \
+        const int64_t b = bg / a.h_kv, g = bg % a.h_kv;                                                       \
+        const int64_t part = a.deterministic ? first_tile : 0;                                                \
+        const int64_t lq = geo.q_len(b), lkv = geo.kv_len(b);                                                 \
+        const int64_t ntiles = (lkv + BN - 1) / BN;                                                           \
+        const int q_b = kPacked ? 0 : int(b), kv_b = q_b;                                                     \
+        const int64_t q_row0 = kPacked ? geo.q_start(b) : 0, kv_row0 = kPacked ? geo.kv_start(b) : 0;         \
+        (void)part;                                                                                           \
+        (void)q_row0;                                                                                         \
+        (void)kv_row0;
+#define ATTN_END_UNITS }
 
     uint8_t *sK = smem + Cfg::OFF_K, *sV = smem + Cfg::OFF_V, *sX = smem + Cfg::OFF_X;
 
@@ -257,12 +268,34 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
             prefetch_tmap(&p.tm_q); prefetch_tmap(&p.tm_k); prefetch_tmap(&p.tm_v); prefetch_tmap(&p.tm_do);
             bool ok = true;
             int64_t kt = 0, qi = 0, q_armed = 0, kv_armed = 0;  // loads started (for the drain below)
+            ATTN_FOR_EACH_UNIT
             for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
                 const int64_t j0 = jt * BN;
                 int qt0, nq;
                 query_tiles<BM>(a.mask, j0, lq, lkv, &qt0, &nq);
                 const int n_iter = G * nq;
                 if (n_iter == 0) continue;
+                // Q / dO of query tile `it` (global iteration index x) into its ring stage
+                auto load_q = [&](int it, int64_t x) {
+                    const int st = int(x % NST);
+                    const int64_t use = x / NST;
+                    if (use > 0 && ok && !(ok = mbar_wait(&q_empty[st], uint32_t(use - 1) & 1, abort)))
+                        flag_abort(abort, a.status);
+                    if (!ok) return;
+                    const int64_t hq = g * G + it / nq, i0 = int64_t(qt0 + it % nq) * BM;
+                    uint8_t *sQ = smem + Cfg::OFF_Q + st * Cfg::Q_BYTES, *sdO = smem + Cfg::OFF_DO + st * Cfg::Q_BYTES;
+                    q_armed = x + 1;
+                    mbar_arrive_expect_tx(&q_full[st], 2 * Cfg::Q_BYTES + 2 * BM * 4);
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_load_4d(sQ + c * BM * 128, &p.tm_q, &q_full[st], c * 64, int(q_row0 + i0), int(hq), q_b);
+                        tma_load_4d(sdO + c * BM * 128, &p.tm_do, &q_full[st], c * 64, int(q_row0 + i0), int(hq), q_b);
+                    }
+                    const int64_t wrow = hq * a.t_pad + geo.ws_start(b) + i0;
+                    bulk_load(smem + Cfg::OFF_LSE + st * BM * 4, a.lse2 + wrow, BM * 4, &q_full[st]);
+                    bulk_load(smem + Cfg::OFF_DVEC + st * BM * 4, a.dvec + wrow, BM * 4, &q_full[st]);
+                };
+                // the first query tile does not need the key tile: load it before waiting for K / V
+                load_q(0, qi);
                 if (kt > 0 && ok && !(ok = mbar_wait(kv_empty, uint32_t(kt - 1) & 1, abort))) flag_abort(abort, a.status);
                 if (ok) {
                     kv_armed = kt + 1;
@@ -272,26 +305,11 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                         tma_load_4d(sV + c * BN * 128, &p.tm_v, kv_full, c * 64, int(kv_row0 + j0), int(g), kv_b);
                     }
                 }
-                for (int it = 0; it < n_iter; ++it, ++qi) {
-                    const int st = int(qi % NST);
-                    const int64_t use = qi / NST;
-                    if (use > 0 && ok && !(ok = mbar_wait(&q_empty[st], uint32_t(use - 1) & 1, abort)))
-                        flag_abort(abort, a.status);
-                    if (!ok) continue;
-                    const int64_t hq = g * G + it / nq, i0 = int64_t(qt0 + it % nq) * BM;
-                    uint8_t *sQ = smem + Cfg::OFF_Q + st * Cfg::Q_BYTES, *sdO = smem + Cfg::OFF_DO + st * Cfg::Q_BYTES;
-                    q_armed = qi + 1;
-                    mbar_arrive_expect_tx(&q_full[st], 2 * Cfg::Q_BYTES + 2 * BM * 4);
-                    for (int c = 0; c < D / 64; ++c) {
-                        tma_load_4d(sQ + c * BM * 128, &p.tm_q, &q_full[st], c * 64, int(q_row0 + i0), int(hq), q_b);
-                        tma_load_4d(sdO + c * BM * 128, &p.tm_do, &q_full[st], c * 64, int(q_row0 + i0), int(hq), q_b);
-                    }
-                    const int64_t wrow = hq * a.t_pad + geo.ws_start(b) + i0;
-                    bulk_load(smem + Cfg::OFF_LSE + st * BM * 4, a.lse2 + wrow, BM * 4, &q_full[st]);
-                    bulk_load(smem + Cfg::OFF_DVEC + st * BM * 4, a.dvec + wrow, BM * 4, &q_full[st]);
-                }
+                ++qi;
+                for (int it = 1; it < n_iter; ++it, ++qi) load_q(it, qi);
                 ++kt;
             }
+            ATTN_END_UNITS
             if (!ok) {
                 // let every copy this thread started land before the CTA exits
                 volatile int never = 0;
@@ -328,6 +346,7 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                 mma_commit(mma_done);
                 mma_commit(&q_empty[st]);
             };
+            ATTN_FOR_EACH_UNIT
             for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
                 const int64_t j0 = jt * BN;
                 int qt0, nq;
@@ -360,9 +379,13 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                 }
                 if (ok && !(ok = mbar_wait(p_ready, uint32_t(qi - 1) & 1, abort))) flag_abort(abort, a.status);
                 tc_fence_after();
-                if (ok) grads(qi - 1, n_iter == 1);
+                if (ok) {
+                    grads(qi - 1, n_iter == 1);
+                    mma_commit(kv_empty);  // K / V free for the next tile once these GEMMs finish
+                }
                 ++kt;
             }
+            ATTN_END_UNITS
             // wait for every MMA this thread issued before TMEM is freed
             volatile int never = 0;
             mma_commit(drain);
@@ -375,7 +398,6 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
         const int r = lg * 32 + lane;  // TMEM lane of this thread
         const float sc = a.scale * kLog2e;
         const bool leader = warp == 2 && lane == 0;
-        const int64_t shift = a.mask == ATTN_CAUSAL_BOTTOM_RIGHT ? lkv - lq : 0;
         const uint32_t aX = smem_u32(sX);
         T *dK = static_cast<T *>(a.dK.ptr), *dV = static_cast<T *>(a.dV.ptr);
         bool ok = true;
@@ -383,7 +405,7 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
 
         // dQ of query tile x (head hq, first row i0), whose GEMMs just completed and released
         // dS buffer x & 1 -> staged there -> TMA add-reduce into the fp32 accumulator
-        auto stage_dq = [&](int64_t x, int64_t hq, int64_t i0) {
+        auto stage_dq = [&](int64_t x, int64_t hq, int64_t row_base, int64_t i0) {
             const uint32_t adQ = aX + uint32_t(x & 1) * Cfg::X_BYTES;
             uint8_t *sdQ = sX + (x & 1) * Cfg::X_BYTES;
             ok = bar_and(1, 256, ok);
@@ -409,13 +431,15 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
             fence_proxy_async_smem();
             named_bar_sync(1, 256);
             if (leader && ok) {
-                const int64_t row0 = (part * a.h + hq) * a.t_pad + geo.ws_start(b) + i0;
+                const int64_t row0 = row_base + hq * a.t_pad + i0;
                 for (int box = 0; box < D / 32; ++box)
                     tma_reduce_add_2d(&p.tm_dq, sdQ + box * BM * 128, box * 32, int(row0));
                 bulk_commit();
             }
         };
 
+        ATTN_FOR_EACH_UNIT
+        const int64_t shift = a.mask == ATTN_CAUSAL_BOTTOM_RIGHT ? lkv - lq : 0;
         for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
             const int64_t j0 = jt * BN, j = j0 + r;
             const bool row_ok = j < lkv;
@@ -503,7 +527,7 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                     if (ok && !(ok = mbar_wait(mma_done, uint32_t(qi - 1) & 1, abort))) flag_abort(abort, a.status);
                     ok = __all_sync(0xffffffffu, ok);
                     tc_fence_after();
-                    stage_dq(qi - 1, prev_hq, prev_i0);
+                    stage_dq(qi - 1, prev_hq, part * a.h * a.t_pad + geo.ws_start(b), prev_i0);
                 }
                 if (ok) {
 #pragma unroll
@@ -526,7 +550,14 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
             if (ok && !(ok = mbar_wait(mma_done, uint32_t(qi - 1) & 1, abort))) flag_abort(abort, a.status);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
-            stage_dq(qi - 1, prev_hq, prev_i0);
+            stage_dq(qi - 1, prev_hq, part * a.h * a.t_pad + geo.ws_start(b), prev_i0);
+            // dK, dV tiles: staged in the two dS / dQ buffers (swizzled like the loads) and
+            // written by TMA, unless the tile runs past a packed sequence's end (per-row stores)
+            const bool tma_out = !kPacked || j0 + BN <= lkv;
+            if (tma_out) {
+                if (leader) bulk_wait_read0();  // the last dQ reduce has read its buffer
+                ok = bar_and(1, 256, ok);
+            }
             if (ok) {
 #pragma unroll
                 for (int cc = 0; cc < D / 64; ++cc) {
@@ -535,34 +566,50 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                     tmem_ld32(tmem + lane_addr + Cfg::T_DV + col0, vv);
                     tmem_ld32(tmem + lane_addr + Cfg::T_DK + col0, kk);
                     tmem_ld_wait();
-                    if (row_ok) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 ov, ok4;
-                            ov.x = pack2<T>(__uint_as_float(vv[8 * q + 0]), __uint_as_float(vv[8 * q + 1]));
-                            ov.y = pack2<T>(__uint_as_float(vv[8 * q + 2]), __uint_as_float(vv[8 * q + 3]));
-                            ov.z = pack2<T>(__uint_as_float(vv[8 * q + 4]), __uint_as_float(vv[8 * q + 5]));
-                            ov.w = pack2<T>(__uint_as_float(vv[8 * q + 6]), __uint_as_float(vv[8 * q + 7]));
-                            ok4.x = pack2<T>(__uint_as_float(kk[8 * q + 0]) * a.scale, __uint_as_float(kk[8 * q + 1]) * a.scale);
-                            ok4.y = pack2<T>(__uint_as_float(kk[8 * q + 2]) * a.scale, __uint_as_float(kk[8 * q + 3]) * a.scale);
-                            ok4.z = pack2<T>(__uint_as_float(kk[8 * q + 4]) * a.scale, __uint_as_float(kk[8 * q + 5]) * a.scale);
-                            ok4.w = pack2<T>(__uint_as_float(kk[8 * q + 6]) * a.scale, __uint_as_float(kk[8 * q + 7]) * a.scale);
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 ov, ok4;
+                        ov.x = pack2<T>(__uint_as_float(vv[8 * q + 0]), __uint_as_float(vv[8 * q + 1]));
+                        ov.y = pack2<T>(__uint_as_float(vv[8 * q + 2]), __uint_as_float(vv[8 * q + 3]));
+                        ov.z = pack2<T>(__uint_as_float(vv[8 * q + 4]), __uint_as_float(vv[8 * q + 5]));
+                        ov.w = pack2<T>(__uint_as_float(vv[8 * q + 6]), __uint_as_float(vv[8 * q + 7]));
+                        ok4.x = pack2<T>(__uint_as_float(kk[8 * q + 0]) * a.scale, __uint_as_float(kk[8 * q + 1]) * a.scale);
+                        ok4.y = pack2<T>(__uint_as_float(kk[8 * q + 2]) * a.scale, __uint_as_float(kk[8 * q + 3]) * a.scale);
+                        ok4.z = pack2<T>(__uint_as_float(kk[8 * q + 4]) * a.scale, __uint_as_float(kk[8 * q + 5]) * a.scale);
+                        ok4.w = pack2<T>(__uint_as_float(kk[8 * q + 6]) * a.scale, __uint_as_float(kk[8 * q + 7]) * a.scale);
+                        if (tma_out) {
+                            const uint32_t off = sw128_offset(uint32_t(r), uint32_t(col0 + 8 * q), BN);
+                            st_shared_v4(aX + off, ov.x, ov.y, ov.z, ov.w);
+                            st_shared_v4(aX + Cfg::X_BYTES + off, ok4.x, ok4.y, ok4.z, ok4.w);
+                        } else if (row_ok) {
                             *reinterpret_cast<uint4 *>(dV + offv + col0 + 8 * q) = ov;
                             *reinterpret_cast<uint4 *>(dK + offk + col0 + 8 * q) = ok4;
                         }
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(kv_empty);
-            if (leader) bulk_wait0();  // this tile's dQ adds land before the next tile's (fixed order)
+            if (tma_out) {
+                fence_proxy_async_smem();
+                named_bar_sync(1, 256);
+                if (leader && ok) {
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_store_4d(&p.tm_dv, sX + c * BN * 128, c * 64, int(kv_row0 + j0), int(g), kv_b);
+                        tma_store_4d(&p.tm_dk, sX + Cfg::X_BYTES + c * BN * 128, c * 64, int(kv_row0 + j0), int(g), kv_b);
+                    }
+                    bulk_commit();
+                }
+            }
+            // deterministic mode: this tile's dQ adds land before the next tile's (fixed order)
+            if (leader && a.deterministic) bulk_wait0();
             ++kt;
         }
+        ATTN_END_UNITS
         if (leader) bulk_wait0();
         pdl_trigger();  // the dQ finalize may start launching; it waits for this grid
     }
 
+#undef ATTN_FOR_EACH_UNIT
+#undef ATTN_END_UNITS
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -620,6 +667,14 @@ bool map_dqacc(CUtensorMap *m, float *base, int64_t d, int64_t rows, uint32_t bo
     return r == CUDA_SUCCESS;
 }
 
+int64_t sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+
 template <class Geo> int64_t max_kv_len(const Geo &g)
 {
     int64_t m = 0;
@@ -642,14 +697,17 @@ template <class T, int D, class Geo> cudaError_t run_tc(const DenseArgs &a, cons
                    !map_view(&prm.tm_do, a.dO, a.dtype, D, sq, a.h, nb, Cfg::BM)))
         return cudaErrorInvalidValue;
     if (!map_view(&prm.tm_k, a.k, a.dtype, D, skv, a.h_kv, nb, Cfg::BN) ||
-        !map_view(&prm.tm_v, a.v, a.dtype, D, skv, a.h_kv, nb, Cfg::BN))
+        !map_view(&prm.tm_v, a.v, a.dtype, D, skv, a.h_kv, nb, Cfg::BN) ||
+        !map_view(&prm.tm_dk, a.dK, a.dtype, D, skv, a.h_kv, nb, Cfg::BN) ||
+        !map_view(&prm.tm_dv, a.dV, a.dtype, D, skv, a.h_kv, nb, Cfg::BN))
         return cudaErrorInvalidValue;
     if (!map_dqacc(&prm.tm_dq, a.dqacc, D, int64_t(a.n_part) * a.h * a.t_pad, Cfg::BM)) return cudaErrorInvalidValue;
     if (sq == 0) prm.tm_q = prm.tm_do = prm.tm_k;  // never read: no query tiles
     auto k = dense_bwd_tc_kernel<T, D, Geo>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    const int64_t units = (a.deterministic ? a.n_part : ntiles) * a.nseq * a.h_kv;
+    prm.a.tc_units = (a.deterministic ? a.n_part : ntiles) * a.nseq * a.h_kv;
+    const int64_t units = prm.a.tc_units < sm_count() ? prm.a.tc_units : sm_count();
     return launch_kernel(k, dim3(unsigned(units)), dim3(320), Cfg::SMEM_ALLOC, s, true, prm, g);
 }
 

@@ -39,6 +39,7 @@ struct DenseArgs {
     float *lse_out;             // forward: where the stats go
     uint32_t *status;
     float *lse2, *dvec, *dqacc;
+    int64_t tc_units;           // main kernel: work units (set by its launcher)
 };
 
 struct Workspace {
