@@ -322,7 +322,7 @@ attn_status_t check_nsa_desc(const attn_nsa_desc_t *d, NsaShape *sh)
 }
 
 struct NsaLayout {
-    size_t status, lse2, dvec, bitmap, offsets, tokens, dqacc, dkacc, dvacc, total;
+    size_t status, lse2, dvec, bitmap, offsets, pieces, tokens, dqacc, dkacc, dvacc, total;
     int64_t t1_pad, nrows;
 };
 
@@ -337,7 +337,8 @@ NsaLayout nsa_layout(const attn_nsa_desc_t *d, const NsaShape &sh)
     L.dvec = L.lse2 + Workspace::align(rows * sizeof(float));
     L.bitmap = L.dvec + Workspace::align(rows * sizeof(float));
     L.offsets = L.bitmap + Workspace::align(size_t(L.nrows) * size_t(sh.words_max) * sizeof(uint32_t));
-    L.tokens = L.offsets + Workspace::align(size_t(L.nrows + 1) * sizeof(int32_t));
+    L.pieces = L.offsets + Workspace::align(size_t(L.nrows + 1) * sizeof(int32_t));
+    L.tokens = L.pieces + Workspace::align(size_t(L.nrows + 1) * sizeof(int32_t));
     L.dqacc = L.tokens + Workspace::align(size_t(sh.t1) * size_t(d->n2 * d->block_count) * sizeof(int32_t) + 4);
     L.dkacc = L.dqacc + Workspace::align(rows * size_t(d->d) * sizeof(float));
     L.dvacc = L.dkacc + Workspace::align(size_t(sh.t2) * size_t(d->n2 * d->d) * sizeof(float));
@@ -397,6 +398,7 @@ attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, 
     a.bitmap = reinterpret_cast<uint32_t *>(ws + L.bitmap);
     a.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
     a.tokens = reinterpret_cast<int32_t *>(ws + L.tokens);
+    a.pieces = reinterpret_cast<int32_t *>(ws + L.pieces);
     a.dqacc = reinterpret_cast<float *>(ws + L.dqacc);
     a.dkacc = reinterpret_cast<float *>(ws + L.dkacc);
     a.dvacc = reinterpret_cast<float *>(ws + L.dvacc);

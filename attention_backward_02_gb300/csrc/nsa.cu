@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(256) nsa_preprocess_kernel(NsaArgs a)
     for (int r = threadIdx.x / 16; r < 128; r += 16) {
         const int64_t t = int64_t(blockIdx.x) * 128 + r;
         const bool live = t < a.t1_pad;  // no early exit: the row's threads shuffle below
-        const int64_t row = h * a.t1_pad + t;
+        const int64_t row = t * a.n1 + h;  // token-major
         float dsum = 0.f;
         if (t < a.t1) {
             const int64_t off = (t * a.n1 + h) * a.d + lane * 8;
@@ -204,8 +204,8 @@ __global__ void __launch_bounds__(256) nsa_bwd_simt_kernel(NsaArgs a, PackedGeo 
         dOs[hh][x] = to_f32(dO[off]);
     }
     if (tid < G) {
-        lse_s[tid] = a.lse2[(g * G + tid) * a.t1_pad + t];
-        d_s[tid] = a.dvec[(g * G + tid) * a.t1_pad + t];
+        lse_s[tid] = a.lse2[t * a.n1 + g * G + tid];
+        d_s[tid] = a.dvec[t * a.n1 + g * G + tid];
     }
     // thread owns dQ features of (head hh_q, x range)
     const int per = (G * D + 255) / 256;
@@ -272,6 +272,21 @@ __global__ void __launch_bounds__(256) nsa_bwd_simt_kernel(NsaArgs a, PackedGeo 
     }
 }
 
+// dQ = cast(scale * fp32 accumulator), tensor-core path
+template <class T>
+__global__ void nsa_dq_finalize_kernel(NsaArgs a)
+{
+    const int64_t n = a.t1 * a.n1 * a.d;
+    T *dQ = static_cast<T *>(a.dq);
+    for (int64_t e = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 4; e < n; e += int64_t(gridDim.x) * blockDim.x * 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(a.dqacc + e);
+        uint2 o;
+        o.x = pack2<T>(v.x * a.scale, v.y * a.scale);
+        o.y = pack2<T>(v.z * a.scale, v.w * a.scale);
+        *reinterpret_cast<uint2 *>(dQ + e) = o;
+    }
+}
+
 template <class T>
 __global__ void nsa_finalize_kernel(NsaArgs a)
 {
@@ -312,7 +327,14 @@ cudaError_t run_nsa(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, cudaEv
         if ((e = cudaMemsetAsync(a.dvacc, 0, acc_bytes, s)) != cudaSuccess) return e;
     }
     if ((e = block_lists(a, g, s)) != cudaSuccess) return e;
-    if (a.t1 > 0) {
+    if (nsa_tc_supported(a)) {
+        size_t dq_bytes = size_t(a.t1) * size_t(a.n1 * a.d) * sizeof(float);
+        if (dq_bytes && (e = cudaMemsetAsync(a.dqacc, 0, dq_bytes, s)) != cudaSuccess) return e;
+        if (before && (e = cudaEventRecord(before, s)) != cudaSuccess) return e;
+        if ((e = launch_nsa_tc(a, g, s)) != cudaSuccess) return e;
+        if (after && (e = cudaEventRecord(after, s)) != cudaSuccess) return e;
+        if (a.t1 > 0) nsa_dq_finalize_kernel<T><<<1024, 256, 0, s>>>(a);
+    } else if (a.t1 > 0) {
         const int G = int(a.n1 / a.n2), BS = int(a.bs), LD = 129;
         size_t smem = sizeof(float) * (2 * BS * LD + 2 * G * LD + 2 * G * BS + 2 * G);
         auto k = nsa_bwd_simt_kernel<T>;

@@ -1,0 +1,502 @@
+// nsa_tc.cu -- tensor-core NSA selected-attention backward for sm_103a.
+//
+// Ascend CANN page "aclnnNsaSelectedAttentionGrad", Function / Formula:
+// every query token gathers selectedBlockCount blocks of selectedBlockSize
+// keys / values through topkIndices, runs the attention backward on them
+// (dV = P^T dY, dQ = dS K scale, dK = dS^T Q scale) and the gathered dK / dV
+// rows go back to the key / value rows they came from.
+//
+// Block-centric: a work unit ("piece") is one (sequence, kv head, key block)
+// and up to kPieceChunks chunks of the ascending list of tokens that selected
+// the block (built by the block-list kernels).  A chunk is 128 rows: 128 / G
+// tokens x the G query heads of the kv head, which TND stores contiguously,
+// so one TMA box per token brings a token's G rows (empty slots load out of
+// bounds and arrive as zeros).  Per chunk:
+//   S   = Q K_blk^T        M=128 rows  N=64 keys K=128  A=Q (K-major)   B=K (K-major)
+//   dP  = dO V_blk^T       M=128       N=64      K=128  A=dO (K-major)  B=V (K-major)
+//   P   = exp2(S scale log2 e - LSE log2 e), dS = P (dP - D)     (LSE from max/sum)
+//   dV^T += dO^T P         M=128 (d)   N=64      K=128  A=dO (MN-major) B=P (MN-major)
+//   dK^T += Q^T dS         M=128 (d)   N=64      K=128  A=Q (MN-major)  B=dS (MN-major)
+//   dQ   = dS K_blk        M=128 rows  N=128 (d) K=64   A=dS (K-major)  B=K (MN-major)
+// dQ of each token is added into an fp32 accumulator with TMA reduce-adds
+// (one box of G rows per token), staged in the chunk's own Q / dO ring stage
+// once its GEMMs are done; dK^T / dV^T stay in TMEM for the piece and are
+// added into fp32 accumulators with coalesced reductions at its end.
+// TMEM: S 64 + dP 64 + dV^T 64 + dK^T 64 + dQ 128 = 384 columns.
+//
+// Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2..9
+// element-wise work (warp w reads TMEM lanes 32 (w % 4) .. + 31; two warps
+// per lane group split the columns).  Bounded waits as in the dense kernel.
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <type_traits>
+
+#include "plan.h"
+#include "sm103.cuh"
+#include "tc_util.cuh"
+
+namespace attn {
+using namespace sm103;
+using namespace tc;
+
+namespace {
+
+constexpr int kD = 128, kBS = 64, kRows = 128, kNst = 2, kMaxSlots = 16;
+constexpr int kPieceChunks = 32;  // chunks per work unit at most
+
+struct NsaCfg {
+    static constexpr int KV_BYTES = kBS * kD * 2;       // 16 KB
+    static constexpr int Q_BYTES = kRows * kD * 2;      // 32 KB
+    static constexpr int PS_BYTES = kRows * kBS * 2;    // 16 KB
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + KV_BYTES;
+    static constexpr int OFF_Q = OFF_V + KV_BYTES;          // kNst stages
+    static constexpr int OFF_DO = OFF_Q + kNst * Q_BYTES;   // kNst stages
+    static constexpr int OFF_P = OFF_DO + kNst * Q_BYTES;
+    static constexpr int OFF_DS = OFF_P + PS_BYTES;
+    static constexpr int OFF_LSE = OFF_DS + PS_BYTES;       // kNst x 128 floats
+    static constexpr int OFF_DVEC = OFF_LSE + kNst * kRows * 4;
+    static constexpr int OFF_SLOT = OFF_DVEC + kNst * kRows * 4;  // kNst x kMaxSlots x {local index, token}
+    static constexpr int OFF_BAR = OFF_SLOT + kNst * kMaxSlots * 8;
+    static constexpr int OFF_MISC = OFF_BAR + 16 * 8;
+    static constexpr int SMEM = OFF_MISC + 64;
+    static constexpr int SMEM_ALLOC = SMEM + 1024;
+    static constexpr int T_S = 0, T_DP = 64, T_DV = 128, T_DK = 192, T_DQ = 256;
+    static constexpr int T_COLS = 512;
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+}  // namespace
+
+struct NsaTcParams {
+    CUtensorMap tm_q, tm_do, tm_k, tm_v, tm_dq;
+    NsaArgs a;
+};
+
+// piece index -> row of the block lists (binary search over the piece offsets)
+__device__ __forceinline__ int64_t piece_row(const int32_t *piece_off, int64_t nrows, int64_t p)
+{
+    int64_t lo = 0, hi = nrows - 1;  // last row with piece_off[row] <= p
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) / 2;
+        if (piece_off[mid] <= p) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <class T>
+__global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constant__ NsaTcParams p, const PackedGeo geo)
+{
+    using Cfg = NsaCfg;
+    constexpr int kType = std::is_same<T, __half>::value ? 0 : 1;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
+    uint64_t *kv_full = bars + 0, *kv_empty = bars + 1, *q_full = bars + 2, *q_empty = bars + 2 + kNst;
+    uint64_t *s_full = bars + 2 + 2 * kNst, *p_ready = s_full + 1, *mma_done = s_full + 2, *drain = s_full + 3;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 8);
+    int32_t *slots = reinterpret_cast<int32_t *>(smem + Cfg::OFF_SLOT);  // [stage][slot][2]
+    const NsaArgs &a = p.a;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int G = int(a.n1 / a.n2), tpc = kRows / G;  // query heads per kv head, tokens per chunk
+    const int64_t n_pieces = a.pieces[a.nrows];
+
+    if (threadIdx.x == 0) {
+        *abort = 0;
+        mbar_init(kv_full, 1);
+        mbar_init(kv_empty, 1);
+        for (int s = 0; s < kNst; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_ready, 8);
+        mbar_init(mma_done, 1);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, Cfg::T_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    uint8_t *sK = smem + Cfg::OFF_K, *sV = smem + Cfg::OFF_V, *sP = smem + Cfg::OFF_P, *sdS = smem + Cfg::OFF_DS;
+
+    // the work unit of piece pc: block-list row, token range, sequence / head / block
+#define NSA_PIECE_DECODE                                                                         \
+    const int64_t row = piece_row(a.pieces, a.nrows, pc);                                       \
+    const int64_t lp = pc - a.pieces[row];                                                      \
+    const int64_t tok_begin = a.offsets[row] + lp * kPieceChunks * tpc;                         \
+    const int64_t tok_end_full = a.offsets[row + 1];                                            \
+    const int64_t tok_end = tok_begin + kPieceChunks * tpc < tok_end_full ? tok_begin + kPieceChunks * tpc : tok_end_full; \
+    const int nchunks = int((tok_end - tok_begin + tpc - 1) / tpc);                            \
+    const int64_t b = row / (a.n2 * a.nblk_max), g = (row / a.nblk_max) % a.n2, blk = row % a.nblk_max; \
+    (void)b; (void)g; (void)blk; (void)nchunks;
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        if (elect_one()) {
+            prefetch_tmap(&p.tm_q); prefetch_tmap(&p.tm_do); prefetch_tmap(&p.tm_k); prefetch_tmap(&p.tm_v);
+            bool ok = true;
+            int64_t kt = 0, ci = 0, q_armed = 0, kv_armed = 0;
+            for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
+                NSA_PIECE_DECODE
+                if (kt > 0 && ok && !(ok = mbar_wait(kv_empty, uint32_t(kt - 1) & 1, abort))) flag_abort(abort, a.status);
+                if (ok) {
+                    kv_armed = kt + 1;
+                    const int krow = int(geo.cu_kv[b] + blk * kBS);
+                    mbar_arrive_expect_tx(kv_full, 2 * Cfg::KV_BYTES);
+                    for (int c = 0; c < kD / 64; ++c) {
+                        tma_load_3d(sK + c * kBS * 128, &p.tm_k, kv_full, c * 64, int(g), krow);
+                        tma_load_3d(sV + c * kBS * 128, &p.tm_v, kv_full, c * 64, int(g), krow);
+                    }
+                }
+                for (int ch = 0; ch < nchunks; ++ch, ++ci) {
+                    const int st = int(ci % kNst);
+                    const int64_t use = ci / kNst;
+                    if (use > 0 && ok && !(ok = mbar_wait(&q_empty[st], uint32_t(use - 1) & 1, abort)))
+                        flag_abort(abort, a.status);
+                    if (!ok) continue;
+                    int32_t *sl = slots + st * kMaxSlots * 2;
+                    int valid = 0;
+                    for (int u = 0; u < tpc; ++u) {
+                        const int64_t idx = tok_begin + int64_t(ch) * tpc + u;
+                        const int32_t t = idx < tok_end ? a.tokens[idx] : -1;
+                        sl[2 * u] = t >= 0 ? int32_t(t - geo.cu_q[b]) : -1;
+                        sl[2 * u + 1] = t;
+                        valid += t >= 0;
+                    }
+                    q_armed = ci + 1;
+                    uint8_t *sQ = smem + Cfg::OFF_Q + st * Cfg::Q_BYTES, *sdO = smem + Cfg::OFF_DO + st * Cfg::Q_BYTES;
+                    mbar_arrive_expect_tx(&q_full[st], 2 * Cfg::Q_BYTES + uint32_t(valid) * G * 8);
+                    for (int u = 0; u < tpc; ++u) {
+                        const int32_t t = sl[2 * u + 1];
+                        const int qrow = t >= 0 ? int(int64_t(t) * a.n1 + g * G) : int(a.t1 * a.n1);  // past the end: zeros
+                        for (int c = 0; c < kD / 64; ++c) {
+                            tma_load_2d(sQ + c * kRows * 128 + u * G * 128, &p.tm_q, &q_full[st], c * 64, qrow);
+                            tma_load_2d(sdO + c * kRows * 128 + u * G * 128, &p.tm_do, &q_full[st], c * 64, qrow);
+                        }
+                        if (t >= 0) {
+                            bulk_load(smem + Cfg::OFF_LSE + st * kRows * 4 + u * G * 4, a.lse2 + qrow, G * 4, &q_full[st]);
+                            bulk_load(smem + Cfg::OFF_DVEC + st * kRows * 4 + u * G * 4, a.dvec + qrow, G * 4, &q_full[st]);
+                        }
+                    }
+                }
+                ++kt;
+            }
+            if (!ok) {
+                volatile int never = 0;
+                for (int64_t x = q_armed - kNst; x < q_armed; ++x)
+                    if (x >= 0) mbar_wait(&q_full[x % kNst], uint32_t(x / kNst) & 1, &never, 100000000ull);
+                if (kv_armed > 0) mbar_wait(kv_full, uint32_t(kv_armed - 1) & 1, &never, 100000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        if (elect_one()) {
+            constexpr uint32_t idS = idesc_f16(128, kBS, kType, 0, 0);     // S, dP
+            constexpr uint32_t idT = idesc_f16(128, kBS, kType, 1, 1);     // dV^T, dK^T
+            constexpr uint32_t idQ = idesc_f16(128, kD, kType, 0, 1);      // dQ
+            const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP), adS = smem_u32(sdS);
+            bool ok = true;
+            int64_t kt = 0, ci = 0;
+            for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
+                NSA_PIECE_DECODE
+                if (ok && !(ok = mbar_wait(kv_full, uint32_t(kt) & 1, abort))) flag_abort(abort, a.status);
+                tc_fence_after();
+                for (int ch = 0; ch < nchunks; ++ch, ++ci) {
+                    const int st = int(ci % kNst);
+                    const uint32_t aQ = smem_u32(smem + Cfg::OFF_Q + st * Cfg::Q_BYTES);
+                    const uint32_t adO = smem_u32(smem + Cfg::OFF_DO + st * Cfg::Q_BYTES);
+                    if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(ci / kNst) & 1, abort))) flag_abort(abort, a.status);
+                    tc_fence_after();
+                    if (ok) {
+                        for (int kk = 0; kk < kD / 16; ++kk)
+                            mma_f16_ss(tmem + Cfg::T_S, desc_kmaj(aQ, kRows, kk), desc_kmaj(aK, kBS, kk), idS, kk > 0);
+                        for (int kk = 0; kk < kD / 16; ++kk)
+                            mma_f16_ss(tmem + Cfg::T_DP, desc_kmaj(adO, kRows, kk), desc_kmaj(aV, kBS, kk), idS, kk > 0);
+                        mma_commit(s_full);
+                    }
+                    if (ok && !(ok = mbar_wait(p_ready, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
+                    tc_fence_after();
+                    if (ok) {
+                        for (int kk = 0; kk < kRows / 16; ++kk)
+                            mma_f16_ss(tmem + Cfg::T_DV, desc_mn(adO, kRows, kk), desc_mn(aP, kRows, kk), idT,
+                                       ch > 0 || kk > 0);
+                        for (int kk = 0; kk < kRows / 16; ++kk)
+                            mma_f16_ss(tmem + Cfg::T_DK, desc_mn(aQ, kRows, kk), desc_mn(adS, kRows, kk), idT,
+                                       ch > 0 || kk > 0);
+                        for (int kk = 0; kk < kBS / 16; ++kk)
+                            mma_f16_ss(tmem + Cfg::T_DQ, desc_kmaj(adS, kRows, kk), desc_mn(aK, kBS, kk), idQ, kk > 0);
+                        mma_commit(mma_done);
+                        if (ch == nchunks - 1) mma_commit(kv_empty);
+                    }
+                }
+                ++kt;
+            }
+            volatile int never = 0;
+            mma_commit(drain);
+            mbar_wait(drain, 0, &never, 100000000ull);
+        }
+    } else {
+        // ================================================= P / dS, dQ, dK / dV
+        const int lg = warp & 3, half = (warp - 2) >> 2;
+        const uint32_t lane_addr = uint32_t(lg * 32) << 16;
+        const int r = lg * 32 + lane;  // TMEM lane: chunk row (S, dP, dQ) or head dim (dV^T, dK^T)
+        const float sc = a.scale * kLog2e;
+        const bool leader = warp == 2 && lane == 0;
+        const uint32_t aP = smem_u32(sP), adS = smem_u32(sdS);
+        bool ok = true;
+        int64_t kt = 0, ci = 0;
+        for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
+            NSA_PIECE_DECODE
+            const int64_t shift = geo.kv_len(b) - geo.q_len(b);
+            for (int ch = 0; ch < nchunks; ++ch, ++ci) {
+                const int st = int(ci % kNst);
+                if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(ci / kNst) & 1, abort))) flag_abort(abort, a.status);
+                if (ok && !(ok = mbar_wait(s_full, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+                const int32_t *sl = slots + st * kMaxSlots * 2;
+                if (ok) {
+                    // this row's token: empty slot -> everything masked; sparse mode 2 -> keys past
+                    // (local index + S2 - S1) masked
+                    const int32_t i_loc = sl[2 * (r / G)];
+                    const int64_t cmax64 =
+                        i_loc < 0 ? -1 : (a.sparse_mode == 2 ? int64_t(i_loc) + shift - blk * kBS : int64_t(kBS));
+                    const int cmax = int(cmax64 < -1 ? -1 : (cmax64 > kBS ? kBS : cmax64));
+                    const bool any_mask = __any_sync(0xffffffffu, cmax < (half + 1) * 32 - 1);
+                    // an empty slot's stats were never loaded: P = 0 and dS = 0 there by construction
+                    const float lse =
+                        i_loc < 0 ? INFINITY : reinterpret_cast<const float *>(smem + Cfg::OFF_LSE + st * kRows * 4)[r];
+                    const float dvv =
+                        i_loc < 0 ? 0.f : reinterpret_cast<const float *>(smem + Cfg::OFF_DVEC + st * kRows * 4)[r];
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int col0 = half * 32 + cc * 16;
+                        uint32_t s[16], dp[16];
+                        tmem_ld16(tmem + lane_addr + Cfg::T_S + col0, s);
+                        tmem_ld16(tmem + lane_addr + Cfg::T_DP + col0, dp);
+                        tmem_ld_wait_regs(s, dp);
+                        uint32_t pk[8], dk[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int c = col0 + 2 * e;
+                            float x0 = fmaf(__uint_as_float(s[2 * e]), sc, -lse);
+                            float x1 = fmaf(__uint_as_float(s[2 * e + 1]), sc, -lse);
+                            if (any_mask) {
+                                x0 = c <= cmax ? x0 : -INFINITY;
+                                x1 = c + 1 <= cmax ? x1 : -INFINITY;
+                            }
+                            pk[e] = p_and_ds<T>(x0, x1, __uint_as_float(dp[2 * e]) - dvv,
+                                                __uint_as_float(dp[2 * e + 1]) - dvv, &dk[e]);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const uint32_t off = sw128_offset(uint32_t(r), uint32_t(col0 + 8 * q), kRows);
+                            st_shared_v4(aP + off, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                            st_shared_v4(adS + off, dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_ready);
+                // ---- dQ of this chunk -> its own (now free) Q / dO stage -> TMA add-reduce per token
+                if (ok && !(ok = mbar_wait(mma_done, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
+                ok = bar_and(1, 256, ok);
+                tc_fence_after();
+                uint8_t *stage_q = smem + Cfg::OFF_Q + st * Cfg::Q_BYTES, *stage_do = smem + Cfg::OFF_DO + st * Cfg::Q_BYTES;
+                if (ok) {
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int box = half * 2 + cc;  // head dims [32 box, 32 box + 32)
+                        uint32_t v[32];
+                        tmem_ld32(tmem + lane_addr + Cfg::T_DQ + box * 32, v);
+                        tmem_ld_wait();
+                        const uint32_t base =
+                            smem_u32(box < 2 ? stage_q + box * (kRows * 128) : stage_do + (box - 2) * (kRows * 128)) +
+                            uint32_t(r * 128);
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4)
+                            st_shared_v4(base + (uint32_t(c4 ^ (r & 7)) << 4), v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
+                                         v[4 * c4 + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1, 256);
+                if (leader) {
+                    if (ok) {
+                        for (int u = 0; u < tpc; ++u) {
+                            const int32_t t = sl[2 * u + 1];
+                            if (t < 0) continue;
+                            const int qrow = int(int64_t(t) * a.n1 + g * G);
+                            for (int box = 0; box < 4; ++box) {
+                                const uint8_t *src = (box < 2 ? stage_q + box * (kRows * 128)
+                                                              : stage_do + (box - 2) * (kRows * 128)) + u * G * 128;
+                                tma_reduce_add_2d(&p.tm_dq, src, box * 32, qrow);
+                            }
+                        }
+                        bulk_commit();
+                        bulk_wait_read0();
+                    }
+                    mbar_arrive(&q_empty[st]);  // the stage may be refilled
+                }
+            }
+            // ---- dV^T, dK^T of this piece (this thread: head dim r, 32 of the 64 keys)
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                uint32_t vv[32], kk[32];
+                tmem_ld32(tmem + lane_addr + Cfg::T_DV + half * 32, vv);
+                tmem_ld32(tmem + lane_addr + Cfg::T_DK + half * 32, kk);
+                tmem_ld_wait();
+                const int64_t key0 = geo.cu_kv[b] + blk * kBS + half * 32;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int64_t off = ((key0 + e) * a.n2 + g) * kD + r;
+                    atomicAdd(a.dvacc + off, __uint_as_float(vv[e]));
+                    atomicAdd(a.dkacc + off, __uint_as_float(kk[e]) * a.scale);
+                }
+            }
+            tc_fence_before();
+            ++kt;
+        }
+        if (leader) bulk_wait0();
+    }
+#undef NSA_PIECE_DECODE
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::T_COLS);
+    }
+}
+
+// ===================================================================== host
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 nsa_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+bool encode(CUtensorMap *m, CUtensorMapDataType type, int rank, const void *base, const cuuint64_t *dims,
+            const cuuint64_t *strides, const cuuint32_t *box)
+{
+    auto enc = nsa_encode_fn();
+    if (!enc) return false;
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, type, rank, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int nsa_sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    return n > 0 ? n : 1;
+}
+
+// Pieces per block-list row and their exclusive scan (one CTA).
+__global__ void __launch_bounds__(1024) nsa_piece_scan_kernel(NsaArgs a)
+{
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int G = int(a.n1 / a.n2), per_piece = kPieceChunks * (kRows / G);
+    const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
+    if (threadIdx.x == 0) a.pieces[0] = 0;
+    for (int64_t base = 0; base < a.nrows; base += 1024) {
+        const int64_t r = base + threadIdx.x;
+        const int32_t len = r < a.nrows ? a.offsets[r + 1] - a.offsets[r] : 0;
+        int32_t v = (len + per_piece - 1) / per_piece;
+        for (int off = 1; off < 32; off <<= 1) {
+            int32_t u = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += u;
+        }
+        if (lane == 31) warp_tot[wid] = v;
+        __syncthreads();
+        if (wid == 0) {
+            int32_t w = warp_tot[lane];
+            for (int off = 1; off < 32; off <<= 1) {
+                int32_t u = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += u;
+            }
+            warp_tot[lane] = w;
+        }
+        __syncthreads();
+        const int32_t prefix = carry + (wid ? warp_tot[wid - 1] : 0);
+        if (r < a.nrows) a.pieces[r + 1] = prefix + v;
+        __syncthreads();
+        if (threadIdx.x == 1023) carry = prefix + v;
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+bool nsa_tc_supported(const NsaArgs &a)
+{
+    const int64_t G = a.n1 / a.n2;
+    return a.d == kD && a.bs == kBS && (G == 8 || G == 16 || G == 32);
+}
+
+cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
+{
+    nsa_piece_scan_kernel<<<1, 1024, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (a.t1 == 0) return cudaSuccess;
+    NsaTcParams prm;
+    prm.a = a;
+    const int G = int(a.n1 / a.n2);
+    const CUtensorMapDataType dt = a.dtype == ATTN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    {   // Q, dO: rows (token, head) x d; box 64 x G (one token's heads of a kv head)
+        cuuint64_t dims[2] = {cuuint64_t(kD), cuuint64_t(a.t1 * a.n1)};
+        cuuint64_t strides[1] = {cuuint64_t(kD * 2)};
+        cuuint32_t box[2] = {64, cuuint32_t(G)};
+        if (!encode(&prm.tm_q, dt, 2, a.q, dims, strides, box) || !encode(&prm.tm_do, dt, 2, a.dO, dims, strides, box))
+            return cudaErrorInvalidValue;
+    }
+    {   // K, V: (d, kv head, token); box 64 x 1 x block
+        cuuint64_t dims[3] = {cuuint64_t(kD), cuuint64_t(a.n2), cuuint64_t(a.t2)};
+        cuuint64_t strides[2] = {cuuint64_t(kD * 2), cuuint64_t(a.n2 * kD * 2)};
+        cuuint32_t box[3] = {64, 1, cuuint32_t(kBS)};
+        if (!encode(&prm.tm_k, dt, 3, a.k, dims, strides, box) || !encode(&prm.tm_v, dt, 3, a.v, dims, strides, box))
+            return cudaErrorInvalidValue;
+    }
+    {   // fp32 dQ accumulator: rows (token, head) x d; box 32 x G
+        cuuint64_t dims[2] = {cuuint64_t(kD), cuuint64_t(a.t1 * a.n1)};
+        cuuint64_t strides[1] = {cuuint64_t(kD * 4)};
+        cuuint32_t box[2] = {32, cuuint32_t(G)};
+        if (!encode(&prm.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dqacc, dims, strides, box))
+            return cudaErrorInvalidValue;
+    }
+    auto k = a.dtype == ATTN_F16 ? nsa_bwd_tc_kernel<__half> : nsa_bwd_tc_kernel<__nv_bfloat16>;
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, NsaCfg::SMEM_ALLOC)) != cudaSuccess)
+        return e;
+    k<<<unsigned(nsa_sm_count()), 320, NsaCfg::SMEM_ALLOC, s>>>(prm, g);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

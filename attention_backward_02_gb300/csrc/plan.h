@@ -49,12 +49,13 @@ struct Workspace {
 
 // NSA workspace (all offsets 256-byte aligned):
 //   status   uint32[64]
-//   lse2     f32 [n1][t1_pad]       (max + ln sum) * log2(e)
-//   dvec     f32 [n1][t1_pad]
+//   lse2     f32 [t1_pad][n1]       (max + ln sum) * log2(e), token-major
+//   dvec     f32 [t1_pad][n1]
 //   bitmap   uint32 [nseq][n2][nblk_max][words_max]   token bits per block
 //   counts   int32 [nrows + 1]      then offsets (exclusive scan), in place
+//   pieces   int32 [nrows + 1]      tensor-core work units per row (exclusive scan)
 //   tokens   int32 [t1 * n2 * cnt]  block lists, ascending token ids
-//   dqacc    f32 [n_part][t1_pad][n1][d]
+//   dqacc    f32 [t1_pad][n1][d]
 //   dkacc    f32 [t2][n2][d], dvacc f32 [t2][n2][d]
 struct NsaArgs {
     int dtype;
@@ -70,7 +71,7 @@ struct NsaArgs {
     uint32_t *status;
     float *lse2, *dvec;
     uint32_t *bitmap;
-    int32_t *offsets, *tokens;
+    int32_t *offsets, *tokens, *pieces;
     float *dqacc, *dkacc, *dvacc;
 };
 
@@ -88,5 +89,7 @@ cudaError_t launch_dense_fwd(const DenseArgs &a, const PackedGeo &g, cudaStream_
 cudaError_t launch_nsa_bwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, cudaEvent_t before,
                            cudaEvent_t after);
 cudaError_t launch_nsa_block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s);
+bool nsa_tc_supported(const NsaArgs &a);
+cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s);
 
 }  // namespace attn
