@@ -322,7 +322,7 @@ attn_status_t check_nsa_desc(const attn_nsa_desc_t *d, NsaShape *sh)
 }
 
 struct NsaLayout {
-    size_t status, lse2, dvec, bitmap, offsets, pieces, tokens, dqacc, dkacc, dvacc, total;
+    size_t status, lse2, dvec, bitmap, offsets, pieces, tokens, dqacc, dkacc, dvacc, dqpart, total;
     int64_t t1_pad, nrows;
 };
 
@@ -342,7 +342,10 @@ NsaLayout nsa_layout(const attn_nsa_desc_t *d, const NsaShape &sh)
     L.dqacc = L.tokens + Workspace::align(size_t(sh.t1) * size_t(d->n2 * d->block_count) * sizeof(int32_t) + 4);
     L.dkacc = L.dqacc + Workspace::align(rows * size_t(d->d) * sizeof(float));
     L.dvacc = L.dkacc + Workspace::align(size_t(sh.t2) * size_t(d->n2 * d->d) * sizeof(float));
-    L.total = L.dvacc + Workspace::align(size_t(sh.t2) * size_t(d->n2 * d->d) * sizeof(float));
+    L.dqpart = L.dvacc + Workspace::align(size_t(sh.t2) * size_t(d->n2 * d->d) * sizeof(float));
+    const size_t part_bytes =
+        d->deterministic ? size_t(sh.t1) * size_t(d->n1) * size_t(d->block_count) * size_t(d->d) * sizeof(float) : 0;
+    L.total = L.dqpart + Workspace::align(part_bytes);
     return L;
 }
 
@@ -402,6 +405,9 @@ attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, 
     a.dqacc = reinterpret_cast<float *>(ws + L.dqacc);
     a.dkacc = reinterpret_cast<float *>(ws + L.dkacc);
     a.dvacc = reinterpret_cast<float *>(ws + L.dvacc);
+    a.dqpart = reinterpret_cast<float *>(ws + L.dqpart);
+    // the CUDA-core kernel (head groups other than 8, 16, 32) adds dK / dV atomically from many blocks
+    if (a.deterministic && !nsa_tc_supported(a)) return ATTN_ERR_UNSUPPORTED;
     static thread_local PackedGeo pg;
     pg.nseq = desc->b;
     pg.cu_q[0] = pg.cu_kv[0] = 0;

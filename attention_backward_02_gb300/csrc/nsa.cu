@@ -287,6 +287,38 @@ __global__ void nsa_dq_finalize_kernel(NsaArgs a)
     }
 }
 
+// Deterministic dQ: per (token, query head) the partial rows of the selected
+// slots, summed in slot order; slots whose block was never processed (out of
+// range, a repeat, or fully masked by sparse mode 2) are skipped.
+template <class T>
+__global__ void nsa_dq_finalize_det_kernel(NsaArgs a, PackedGeo geo)
+{
+    const int64_t rows = a.t1 * a.n1;  // (token, head) rows; 32 threads x 4 floats per row
+    const int G = int(a.n1 / a.n2);
+    for (int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32; w < rows;
+         w += int64_t(gridDim.x) * blockDim.x / 32) {
+        const int lane = threadIdx.x % 32;
+        const int64_t t = w / a.n1, h = w % a.n1, g = h / G, hh = h % G;
+        const int64_t b = seq_of_token(geo, t);
+        const int64_t i = t - geo.cu_q[b], lq = geo.q_len(b), lkv = geo.kv_len(b);
+        const int32_t *ids = a.topk + (t * a.n2 + g) * a.cnt;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t c = 0; c < a.cnt; ++c) {
+            const int32_t blk = ids[c];
+            bool use = blk >= 0 && int64_t(blk) < lkv / a.bs;
+            for (int64_t c2 = 0; use && c2 < c; ++c2) use = ids[c2] != blk;
+            if (use && a.sparse_mode == 2) use = visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, int64_t(blk) * a.bs, lq, lkv);
+            if (!use) continue;
+            const float4 v = reinterpret_cast<const float4 *>(a.dqpart + (((t * a.n2 + g) * a.cnt + c) * G + hh) * a.d)[lane];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        uint2 o;
+        o.x = pack2<T>(acc.x * a.scale, acc.y * a.scale);
+        o.y = pack2<T>(acc.z * a.scale, acc.w * a.scale);
+        reinterpret_cast<uint2 *>(static_cast<T *>(a.dq) + w * a.d)[lane] = o;
+    }
+}
+
 template <class T>
 __global__ void nsa_finalize_kernel(NsaArgs a)
 {
@@ -329,11 +361,12 @@ cudaError_t run_nsa(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, cudaEv
     if ((e = block_lists(a, g, s)) != cudaSuccess) return e;
     if (nsa_tc_supported(a)) {
         size_t dq_bytes = size_t(a.t1) * size_t(a.n1 * a.d) * sizeof(float);
-        if (dq_bytes && (e = cudaMemsetAsync(a.dqacc, 0, dq_bytes, s)) != cudaSuccess) return e;
+        if (!a.deterministic && dq_bytes && (e = cudaMemsetAsync(a.dqacc, 0, dq_bytes, s)) != cudaSuccess) return e;
         if (before && (e = cudaEventRecord(before, s)) != cudaSuccess) return e;
         if ((e = launch_nsa_tc(a, g, s)) != cudaSuccess) return e;
         if (after && (e = cudaEventRecord(after, s)) != cudaSuccess) return e;
-        if (a.t1 > 0) nsa_dq_finalize_kernel<T><<<1024, 256, 0, s>>>(a);
+        if (a.t1 > 0 && a.deterministic) nsa_dq_finalize_det_kernel<T><<<1024, 256, 0, s>>>(a, g);
+        else if (a.t1 > 0) nsa_dq_finalize_kernel<T><<<1024, 256, 0, s>>>(a);
     } else if (a.t1 > 0) {
         const int G = int(a.n1 / a.n2), BS = int(a.bs), LD = 129;
         size_t smem = sizeof(float) * (2 * BS * LD + 2 * G * LD + 2 * G * BS + 2 * G);

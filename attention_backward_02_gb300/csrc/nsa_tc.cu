@@ -42,7 +42,7 @@ using namespace tc;
 
 namespace {
 
-constexpr int kD = 128, kBS = 64, kRows = 128, kNst = 2, kMaxSlots = 16;
+constexpr int kD = 128, kBS = 64, kRows = 128, kNst = 2, kMaxSlots = 16, kSlotInts = 4;
 constexpr int kPieceChunks = 32;  // chunks per work unit at most
 
 struct NsaCfg {
@@ -57,8 +57,8 @@ struct NsaCfg {
     static constexpr int OFF_DS = OFF_P + PS_BYTES;
     static constexpr int OFF_LSE = OFF_DS + PS_BYTES;       // kNst x 128 floats
     static constexpr int OFF_DVEC = OFF_LSE + kNst * kRows * 4;
-    static constexpr int OFF_SLOT = OFF_DVEC + kNst * kRows * 4;  // kNst x kMaxSlots x {local index, token}
-    static constexpr int OFF_BAR = OFF_SLOT + kNst * kMaxSlots * 8;
+    static constexpr int OFF_SLOT = OFF_DVEC + kNst * kRows * 4;  // kNst x kMaxSlots x {local index, token, topk slot, -}
+    static constexpr int OFF_BAR = OFF_SLOT + kNst * kMaxSlots * kSlotInts * 4;
     static constexpr int OFF_MISC = OFF_BAR + 16 * 8;
     static constexpr int SMEM = OFF_MISC + 64;
     static constexpr int SMEM_ALLOC = SMEM + 1024;
@@ -70,7 +70,7 @@ struct NsaCfg {
 }  // namespace
 
 struct NsaTcParams {
-    CUtensorMap tm_q, tm_do, tm_k, tm_v, tm_dq;
+    CUtensorMap tm_q, tm_do, tm_k, tm_v, tm_dq, tm_dqpart;
     NsaArgs a;
 };
 
@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
     uint64_t *s_full = bars + 2 + 2 * kNst, *p_ready = s_full + 1, *mma_done = s_full + 2, *drain = s_full + 3;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 8);
-    int32_t *slots = reinterpret_cast<int32_t *>(smem + Cfg::OFF_SLOT);  // [stage][slot][2]
+    int32_t *slots = reinterpret_cast<int32_t *>(smem + Cfg::OFF_SLOT);  // [stage][slot][kSlotInts]
     const NsaArgs &a = p.a;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int G = int(a.n1 / a.n2), tpc = kRows / G;  // query heads per kv head, tokens per chunk
@@ -130,9 +130,9 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
 #define NSA_PIECE_DECODE                                                                         \
     const int64_t row = piece_row(a.pieces, a.nrows, pc);                                       \
     const int64_t lp = pc - a.pieces[row];                                                      \
-    const int64_t tok_begin = a.offsets[row] + lp * kPieceChunks * tpc;                         \
+    const int64_t tok_begin = a.offsets[row] + lp * a.piece_tokens;                            \
     const int64_t tok_end_full = a.offsets[row + 1];                                            \
-    const int64_t tok_end = tok_begin + kPieceChunks * tpc < tok_end_full ? tok_begin + kPieceChunks * tpc : tok_end_full; \
+    const int64_t tok_end = tok_begin + a.piece_tokens < tok_end_full ? tok_begin + a.piece_tokens : tok_end_full; \
     const int nchunks = int((tok_end - tok_begin + tpc - 1) / tpc);                            \
     const int64_t b = row / (a.n2 * a.nblk_max), g = (row / a.nblk_max) % a.n2, blk = row % a.nblk_max; \
     (void)b; (void)g; (void)blk; (void)nchunks;
@@ -161,20 +161,27 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
                     if (use > 0 && ok && !(ok = mbar_wait(&q_empty[st], uint32_t(use - 1) & 1, abort)))
                         flag_abort(abort, a.status);
                     if (!ok) continue;
-                    int32_t *sl = slots + st * kMaxSlots * 2;
+                    int32_t *sl = slots + st * kMaxSlots * kSlotInts;
                     int valid = 0;
                     for (int u = 0; u < tpc; ++u) {
                         const int64_t idx = tok_begin + int64_t(ch) * tpc + u;
                         const int32_t t = idx < tok_end ? a.tokens[idx] : -1;
-                        sl[2 * u] = t >= 0 ? int32_t(t - geo.cu_q[b]) : -1;
-                        sl[2 * u + 1] = t;
+                        int32_t slot = -1;  // deterministic mode: position of this block in the token's topk
+                        if (a.deterministic && t >= 0) {
+                            const int32_t *ids = a.topk + (int64_t(t) * a.n2 + g) * a.cnt;
+                            for (int64_t c = a.cnt - 1; c >= 0; --c)
+                                if (ids[c] == blk) slot = int32_t(c);
+                        }
+                        sl[kSlotInts * u] = t >= 0 ? int32_t(t - geo.cu_q[b]) : -1;
+                        sl[kSlotInts * u + 1] = t;
+                        sl[kSlotInts * u + 2] = slot;
                         valid += t >= 0;
                     }
                     q_armed = ci + 1;
                     uint8_t *sQ = smem + Cfg::OFF_Q + st * Cfg::Q_BYTES, *sdO = smem + Cfg::OFF_DO + st * Cfg::Q_BYTES;
                     mbar_arrive_expect_tx(&q_full[st], 2 * Cfg::Q_BYTES + uint32_t(valid) * G * 8);
                     for (int u = 0; u < tpc; ++u) {
-                        const int32_t t = sl[2 * u + 1];
+                        const int32_t t = sl[kSlotInts * u + 1];
                         const int qrow = t >= 0 ? int(int64_t(t) * a.n1 + g * G) : int(a.t1 * a.n1);  // past the end: zeros
                         for (int c = 0; c < kD / 64; ++c) {
                             tma_load_2d(sQ + c * kRows * 128 + u * G * 128, &p.tm_q, &q_full[st], c * 64, qrow);
@@ -261,11 +268,11 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
                 if (ok && !(ok = mbar_wait(s_full, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
-                const int32_t *sl = slots + st * kMaxSlots * 2;
+                const int32_t *sl = slots + st * kMaxSlots * kSlotInts;
                 if (ok) {
                     // this row's token: empty slot -> everything masked; sparse mode 2 -> keys past
                     // (local index + S2 - S1) masked
-                    const int32_t i_loc = sl[2 * (r / G)];
+                    const int32_t i_loc = sl[kSlotInts * (r / G)];
                     const int64_t cmax64 =
                         i_loc < 0 ? -1 : (a.sparse_mode == 2 ? int64_t(i_loc) + shift - blk * kBS : int64_t(kBS));
                     const int cmax = int(cmax64 < -1 ? -1 : (cmax64 > kBS ? kBS : cmax64));
@@ -333,13 +340,16 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
                 if (leader) {
                     if (ok) {
                         for (int u = 0; u < tpc; ++u) {
-                            const int32_t t = sl[2 * u + 1];
+                            const int32_t t = sl[kSlotInts * u + 1];
                             if (t < 0) continue;
                             const int qrow = int(int64_t(t) * a.n1 + g * G);
+                            // deterministic: its own partial rows, written once (summed in slot order later)
+                            const int prow = int(((int64_t(t) * a.n2 + g) * a.cnt + sl[kSlotInts * u + 2]) * G);
                             for (int box = 0; box < 4; ++box) {
                                 const uint8_t *src = (box < 2 ? stage_q + box * (kRows * 128)
                                                               : stage_do + (box - 2) * (kRows * 128)) + u * G * 128;
-                                tma_reduce_add_2d(&p.tm_dq, src, box * 32, qrow);
+                                if (a.deterministic) tma_store_2d(&p.tm_dqpart, src, box * 32, prow);
+                                else tma_reduce_add_2d(&p.tm_dq, src, box * 32, qrow);
                             }
                         }
                         bulk_commit();
@@ -423,7 +433,7 @@ __global__ void __launch_bounds__(1024) nsa_piece_scan_kernel(NsaArgs a)
     __shared__ int32_t carry;
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
-    const int G = int(a.n1 / a.n2), per_piece = kPieceChunks * (kRows / G);
+    const int per_piece = int(a.piece_tokens);
     const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
     if (threadIdx.x == 0) a.pieces[0] = 0;
     for (int64_t base = 0; base < a.nrows; base += 1024) {
@@ -463,13 +473,15 @@ bool nsa_tc_supported(const NsaArgs &a)
 
 cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
 {
-    nsa_piece_scan_kernel<<<1, 1024, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    if (a.t1 == 0) return cudaSuccess;
     NsaTcParams prm;
     prm.a = a;
     const int G = int(a.n1 / a.n2);
+    // deterministic: a whole block list per work unit, so every dK / dV element has one writer
+    prm.a.piece_tokens = a.deterministic ? (int64_t(1) << 30) : int64_t(kPieceChunks) * (kRows / G);
+    nsa_piece_scan_kernel<<<1, 1024, 0, s>>>(prm.a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (a.t1 == 0) return cudaSuccess;
     const CUtensorMapDataType dt = a.dtype == ATTN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     {   // Q, dO: rows (token, head) x d; box 64 x G (one token's heads of a kv head)
         cuuint64_t dims[2] = {cuuint64_t(kD), cuuint64_t(a.t1 * a.n1)};
@@ -491,6 +503,12 @@ cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
         cuuint32_t box[2] = {32, cuuint32_t(G)};
         if (!encode(&prm.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dqacc, dims, strides, box))
             return cudaErrorInvalidValue;
+        prm.tm_dqpart = prm.tm_dq;
+        if (a.deterministic) {  // fp32 partials: rows (token, kv head, slot, head of group) x d
+            cuuint64_t pdims[2] = {cuuint64_t(kD), cuuint64_t(a.t1 * a.n1 * a.cnt)};
+            if (!encode(&prm.tm_dqpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dqpart, pdims, strides, box))
+                return cudaErrorInvalidValue;
+        }
     }
     auto k = a.dtype == ATTN_F16 ? nsa_bwd_tc_kernel<__half> : nsa_bwd_tc_kernel<__nv_bfloat16>;
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, NsaCfg::SMEM_ALLOC)) != cudaSuccess)

@@ -57,6 +57,7 @@ struct Workspace {
 //   tokens   int32 [t1 * n2 * cnt]  block lists, ascending token ids
 //   dqacc    f32 [t1_pad][n1][d]
 //   dkacc    f32 [t2][n2][d], dvacc f32 [t2][n2][d]
+//   dqpart   f32 [t1][n2][cnt][G][d]   deterministic mode: dQ per (token, selected slot)
 struct NsaArgs {
     int dtype;
     int64_t nseq, n1, n2, d, bs, cnt;
@@ -72,7 +73,8 @@ struct NsaArgs {
     float *lse2, *dvec;
     uint32_t *bitmap;
     int32_t *offsets, *tokens, *pieces;
-    float *dqacc, *dkacc, *dvacc;
+    float *dqacc, *dkacc, *dvacc, *dqpart;
+    int64_t piece_tokens;       // tokens per work unit of the tensor-core kernel (whole lists when deterministic)
 };
 
 // ------------------------------------------------------------ launchers

@@ -102,3 +102,49 @@ def test_ascend_example_shape_is_dense():
 def test_workload4_full():
     """NSA bf16, 4 x 4096 tokens, 16 query heads / 1 kv head, d128, 16 blocks of 64, sparse mode 2."""
     _parity(synth.workload(4))
+
+
+@pytest.mark.parametrize("sparse_mode", [0, 2])
+@pytest.mark.parametrize("n1,n2", [(16, 2), (16, 1), (32, 1)])
+def test_deterministic_parity_and_bitwise(sparse_mode, n1, n2):
+    """Deterministic mode: dQ from per-slot partials summed in slot order, one
+    writer per dK / dV element; two calls give the same bits."""
+    p = _small(sparse_mode, seed=11 + sparse_mode, n1=n1, n2=n2)
+    first = _parity(p, deterministic=True)
+    o_bits, mx, sm = H.nsa_oracle_inputs(p)
+    second = H.run_gpu_nsa(p, o_bits, mx, sm, deterministic=True)
+    for a, b in zip(first, second):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_deterministic_bad_indices_flagged():
+    import attention_backward_02_gb300 as ab
+    p = _small(2, seed=4)
+    bad = p.topk.copy()
+    bad[5, 0, 1] = 1000
+    bad[7, 1, 2] = bad[7, 1, 0]
+    o_bits, mx, sm = H.nsa_oracle_inputs(p)
+    H.run_gpu_nsa(p, o_bits, mx, sm, deterministic=True, topk=bad,
+                  expect_flags=ab._lib.ATTN_DEV_INDEX_RANGE | ab._lib.ATTN_DEV_INDEX_DUP)
+    _parity(p, deterministic=True)
+
+
+def test_deterministic_unsupported_group():
+    """Head groups the tensor-core kernel does not take run on CUDA cores,
+    which add dK / dV atomically: deterministic mode is refused there."""
+    import attention_backward_02_gb300 as ab
+    p = _small(0, seed=12, n1=8, n2=2)
+    o_bits, mx, sm = H.nsa_oracle_inputs(p)
+    with pytest.raises(ab.AttnError) as e:
+        H.run_gpu_nsa(p, o_bits, mx, sm, deterministic=True)
+    assert e.value.status == ab._lib.ATTN_ERR_UNSUPPORTED
+    _parity(p)  # the non-deterministic CUDA-core path still serves this shape
+
+
+def test_workload4_deterministic_bitwise():
+    p = synth.workload(4)
+    first = _parity(p, deterministic=True)
+    o_bits, mx, sm = H.nsa_oracle_inputs(p)
+    second = H.run_gpu_nsa(p, o_bits, mx, sm, deterministic=True)
+    for a, b in zip(first, second):
+        np.testing.assert_array_equal(a, b)
