@@ -62,18 +62,27 @@ template <int D>
 struct TcCfg {
     static constexpr int BN = 128;                  // key rows per CTA tile
     static constexpr int BM = D == 64 ? 128 : 64;   // query rows per iteration
+    static constexpr int NG = D == 64 ? 2 : 1;      // column groups of 32 per softmax thread
+#ifndef ATTN_SDP_RELEASE_GROUPS
+    static constexpr int NH = NG;                   // groups of S^T / dP^T columns released one by one
+#else
+    static constexpr int NH = ATTN_SDP_RELEASE_GROUPS;
+#endif
     static constexpr int NST = 3;                   // Q / dO ring stages
+    static constexpr int THREADS = 448;             // 14 warps
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int DS_BYTES = BN * BM * 2;
-    static constexpr int DQ_BYTES = BM * D * 4;
-    static constexpr int X_BYTES = DS_BYTES > DQ_BYTES ? DS_BYTES : DQ_BYTES;  // dS / dQ buffer
+    static constexpr int X_BYTES = DS_BYTES;
+    static constexpr int DQS_BYTES = BM * D * 2;             // fp32 dQ, half of the columns
+    static constexpr int DQ_BOX_ROWS = D == 64 ? BM : 32;    // rows of one dQ reduce box (32 fp32 wide)
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + KV_BYTES;
     static constexpr int OFF_Q = OFF_V + KV_BYTES;            // NST stages
     static constexpr int OFF_DO = OFF_Q + NST * Q_BYTES;      // NST stages
-    static constexpr int OFF_X = OFF_DO + NST * Q_BYTES;      // 2 dS / dQ buffers
-    static constexpr int OFF_LSE = OFF_X + 2 * X_BYTES;       // NST x BM floats
+    static constexpr int OFF_X = OFF_DO + NST * Q_BYTES;      // 2 dS buffers
+    static constexpr int OFF_DQS = OFF_X + 2 * X_BYTES;       // dQ staging, half a tile
+    static constexpr int OFF_LSE = OFF_DQS + DQS_BYTES;       // NST x BM floats
     static constexpr int OFF_DVEC = OFF_LSE + NST * BM * 4;   // NST x BM floats
     static constexpr int OFF_BAR = OFF_DVEC + NST * BM * 4;
     static constexpr int OFF_MISC = OFF_BAR + 24 * 8;
@@ -84,10 +93,12 @@ struct TcCfg {
     static constexpr int T_COLS = 512;
     static_assert(T_DQ + 64 <= T_COLS, "TMEM budget");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+    static_assert(BM / 2 / NG == 32, "each softmax thread takes 32 columns per group");
+    static_assert(NH == 1 || NH == NG, "release groups");
 };
 
 struct TcParams {
-    CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq, tm_dk, tm_dv;
+    CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq;
     DenseArgs a;
 };
 
@@ -115,11 +126,12 @@ template <> struct IsPacked<PackedGeo> : std::true_type {};
 }  // namespace
 
 template <class T, int D, class Geo>
-__global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_constant__ TcParams p, const Geo geo)
+__global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_constant__ TcParams p, const Geo geo)
 {
     using Cfg = TcCfg<D>;
-    constexpr int BM = Cfg::BM, BN = Cfg::BN, NST = Cfg::NST;
-    constexpr int HC = BM / 2;  // query columns per softmax thread
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, NST = Cfg::NST, NH = Cfg::NH, NG = Cfg::NG;
+    constexpr int HC = BM / 2;       // query columns per softmax thread
+    constexpr int GW = HC / NG;      // of which per column group
     constexpr bool kPacked = IsPacked<Geo>::value;
     constexpr int kType = std::is_same<T, __half>::value ? 0 : 1;
 
@@ -127,8 +139,15 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
     uint64_t *kv_full = bars + 0, *kv_empty = bars + 1, *q_full = bars + 2, *q_empty = bars + 2 + NST;
-    uint64_t *s_full = bars + 2 + 2 * NST, *s_free = s_full + 1, *p_ready = s_full + 2, *mma_done = s_full + 3;
-    uint64_t *drain = s_full + 4;
+    uint64_t *s_full = bars + 2 + 2 * NST;   // [NH] S^T / dP^T column group written
+    uint64_t *s_free = s_full + 2;           // [NH] column group read out by the softmax warps
+    uint64_t *p_ready = s_full + 4;          // P^T in TMEM and dS^T in shared memory
+    uint64_t *p_free = s_full + 5;           // the dV GEMM has read P^T
+    uint64_t *mma_done = s_full + 6;         // all GEMMs of a query tile have completed
+    uint64_t *dq_free = s_full + 7;          // the dQ accumulator has been read out
+    uint64_t *ds_free = s_full + 8;          // [2] dS buffer: the GEMMs that read it have completed
+    uint64_t *acc_free = s_full + 10;        // the dK / dV accumulators have been read out
+    uint64_t *drain = s_full + 11;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 8);
     const DenseArgs &a = p.a;
@@ -142,10 +161,17 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
             mbar_init(&q_full[s], 1);
             mbar_init(&q_empty[s], 1);
         }
-        mbar_init(s_full, 1);
-        mbar_init(s_free, 8);
+        for (int q = 0; q < NH; ++q) {
+            mbar_init(&s_full[q], 1);
+            mbar_init(&s_free[q], 8);
+        }
         mbar_init(p_ready, 8);
+        mbar_init(p_free, 1);
         mbar_init(mma_done, 1);
+        mbar_init(dq_free, 4);
+        mbar_init(&ds_free[0], 1);
+        mbar_init(&ds_free[1], 1);
+        mbar_init(acc_free, 4);
         mbar_init(drain, 1);
         fence_mbar_init();
     }
@@ -216,6 +242,31 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                 };
                 // the first query tile does not need the key tile: load it before waiting for K / V
                 load_q(0, qi);
+                // warm L2 with the K / V tile this CTA takes next, so its load does not stall the next unit
+                {
+                    int64_t nb = b, ng = g, njt = jt + tile_step, nrow0 = kv_row0;
+                    int nkv_b = kv_b;
+                    bool has = njt < ntiles;
+                    if (!has) {
+                        const int64_t r2 = round_ + 1;
+                        const int64_t u2 = r2 * gridDim.x +
+                                           ((r2 & 1) ? int64_t(gridDim.x) - 1 - blockIdx.x : int64_t(blockIdx.x));
+                        if (u2 < a.tc_units) {
+                            const int64_t bg2 = u2 % nheads;
+                            nb = bg2 / a.h_kv;
+                            ng = bg2 % a.h_kv;
+                            njt = u2 / nheads;
+                            nrow0 = kPacked ? geo.kv_start(nb) : 0;
+                            nkv_b = kPacked ? 0 : int(nb);
+                            has = njt * BN < geo.kv_len(nb);
+                        }
+                    }
+                    if (has)
+                        for (int c = 0; c < D / 64; ++c) {
+                            tma_prefetch_4d(&p.tm_k, c * 64, int(nrow0 + njt * BN), int(ng), nkv_b);
+                            tma_prefetch_4d(&p.tm_v, c * 64, int(nrow0 + njt * BN), int(ng), nkv_b);
+                        }
+                }
                 if (kt > 0 && ok && !(ok = mbar_wait(kv_empty, uint32_t(kt - 1) & 1, abort))) flag_abort(abort, a.status);
                 if (ok) {
                     kv_armed = kt + 1;
@@ -241,30 +292,52 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
     } else if (warp == 1) {
         // ================================================= MMA issuer
         if (elect_one()) {
-            constexpr uint32_t idS = idesc_f16(128, BM, kType, 0, 0);
+            constexpr uint32_t idS = idesc_f16(128, BM / NH, kType, 0, 0);
             constexpr uint32_t idDV = idesc_f16(128, D, kType, 0, 1);
             constexpr uint32_t idDQ = idesc_f16(128, 64, kType, 1, 1);
             const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
             bool ok = true;
-            int64_t kt = 0, qi = 0;
+            int64_t kt = 0;
+            uint32_t qi = 0, st_par = 0;
+            int st = 0;
+            auto wait = [&](uint64_t *bar, uint32_t parity) {
+                if (ok && !(ok = mbar_wait(bar, parity, abort))) flag_abort(abort, a.status);
+                tc_fence_after();
+            };
+            // step-0 descriptors of the K / V tile (K-major for S / dP, MN-major for dQ)
+            const uint64_t kK = desc_kmaj(aK, BN, 0), kV = desc_kmaj(aV, BN, 0), mK = desc_mn(aK, BN, 0);
             // dV, dK, dQ of query tile x (global index) whose P / dS are ready
-            auto grads = [&](int64_t x, bool first) {
-                const int st = int(x % NST);
+            // x: global index of the query tile, xs: its ring stage
+            auto grads = [&](uint32_t x, int xs, bool first) {
+                const int st = xs;
                 const uint32_t adS = smem_u32(sX + (x & 1) * Cfg::X_BYTES);
-                const uint32_t aQ = smem_u32(smem + Cfg::OFF_Q + st * Cfg::Q_BYTES);
-                const uint32_t adO = smem_u32(smem + Cfg::OFF_DO + st * Cfg::Q_BYTES);
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_f16_ts(tmem + Cfg::T_DV, tmem + Cfg::T_P + kk * 8, desc_mn(adO, BM, kk), idDV, !first || kk > 0);
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_f16_ss(tmem + Cfg::T_DK, desc_kmaj(adS, BN, kk), desc_mn(aQ, BM, kk), idDV, !first || kk > 0);
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    if (D == 64)
-                        mma_f16_ss(tmem + Cfg::T_DQ, desc_mn(adS, BN, kk), desc_mn(aK, BN, kk), idDQ, kk > 0);
-                    else
-                        mma_f16_ss(tmem + Cfg::T_DQ, desc_mn(aK, BN, kk), desc_mn(adS, BN, kk), idDQ, kk > 0);
+                const uint64_t mdO = desc_mn(smem_u32(smem + Cfg::OFF_DO + st * Cfg::Q_BYTES), BM, 0);
+                const uint64_t mQ = desc_mn(smem_u32(smem + Cfg::OFF_Q + st * Cfg::Q_BYTES), BM, 0);
+                const uint64_t kdS = desc_kmaj(adS, BN, 0), mdS = desc_mn(adS, BN, 0);
+                // a new key tile overwrites dV / dK: the previous tile's epilogue has read them
+                if (first && kt > 0) wait(acc_free, uint32_t(kt - 1) & 1);
+                if (ok) {
+#pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk)
+                        mma_f16_ts(tmem + Cfg::T_DV, tmem + Cfg::T_P + kk * 8, mn_step(mdO, kk), idDV, !first || kk > 0);
+                    mma_commit(p_free);
+#pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk)
+                        mma_f16_ss(tmem + Cfg::T_DK, kmaj_step(kdS, BN, kk), mn_step(mQ, kk), idDV, !first || kk > 0);
                 }
-                mma_commit(mma_done);
-                mma_commit(&q_empty[st]);
+                if (x > 0) wait(dq_free, (x - 1) & 1);
+                if (ok) {
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        if (D == 64)
+                            mma_f16_ss(tmem + Cfg::T_DQ, mn_step(mdS, kk), mn_step(mK, kk), idDQ, kk > 0);
+                        else
+                            mma_f16_ss(tmem + Cfg::T_DQ, mn_step(mK, kk), mn_step(mdS, kk), idDQ, kk > 0);
+                    }
+                    mma_commit(mma_done);
+                    mma_commit(&q_empty[st]);
+                    mma_commit(&ds_free[x & 1]);
+                }
             };
             ATTN_FOR_EACH_UNIT
             for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
@@ -273,36 +346,42 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
                 query_tiles<BM>(a.mask, j0, lq, lkv, &qt0, &nq);
                 const int n_iter = G * nq;
                 if (n_iter == 0) continue;
-                if (ok && !(ok = mbar_wait(kv_full, uint32_t(kt) & 1, abort))) flag_abort(abort, a.status);
-                tc_fence_after();
+                wait(kv_full, uint32_t(kt) & 1);
+                int prev_st = 0;
                 for (int it = 0; it < n_iter; ++it, ++qi) {
-                    const int st = int(qi % NST);
-                    const uint32_t aQ = smem_u32(smem + Cfg::OFF_Q + st * Cfg::Q_BYTES);
-                    const uint32_t adO = smem_u32(smem + Cfg::OFF_DO + st * Cfg::Q_BYTES);
-                    if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(qi / NST) & 1, abort))) flag_abort(abort, a.status);
-                    // S^T / dP^T of the previous query tile have been read out of TMEM
-                    if (qi > 0 && ok && !(ok = mbar_wait(s_free, uint32_t(qi - 1) & 1, abort)))
-                        flag_abort(abort, a.status);
-                    tc_fence_after();
-                    if (ok) {
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            mma_f16_ss(tmem + Cfg::T_S, desc_kmaj(aK, BN, kk), desc_kmaj(aQ, BM, kk), idS, kk > 0);
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            mma_f16_ss(tmem + Cfg::T_DP, desc_kmaj(aV, BN, kk), desc_kmaj(adO, BM, kk), idS, kk > 0);
-                        mma_commit(s_full);
+                    const uint64_t kQ = desc_kmaj(smem_u32(smem + Cfg::OFF_Q + st * Cfg::Q_BYTES), BM, 0);
+                    const uint64_t kdO = desc_kmaj(smem_u32(smem + Cfg::OFF_DO + st * Cfg::Q_BYTES), BM, 0);
+                    wait(&q_full[st], st_par);
+#pragma unroll
+                    for (int q = 0; q < NH; ++q) {
+                        // this column group of the previous tile has been read out of TMEM
+                        if (qi > 0) wait(&s_free[q], (qi - 1) & 1);
+                        if (ok) {
+                            const uint32_t qoff = uint32_t(q * (BM / NH) * 128 / 16);  // query rows, in 16 B
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                mma_f16_ss(tmem + Cfg::T_S + q * (BM / NH), kmaj_step(kK, BN, kk),
+                                           kmaj_step(kQ + qoff, BM, kk), idS, kk > 0);
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                mma_f16_ss(tmem + Cfg::T_DP + q * (BM / NH), kmaj_step(kV, BN, kk),
+                                           kmaj_step(kdO + qoff, BM, kk), idS, kk > 0);
+                            mma_commit(&s_full[q]);
+                        }
                     }
                     if (it > 0) {
-                        if (ok && !(ok = mbar_wait(p_ready, uint32_t(qi - 1) & 1, abort))) flag_abort(abort, a.status);
-                        tc_fence_after();
-                        if (ok) grads(qi - 1, it == 1);
+                        wait(p_ready, (qi - 1) & 1);
+                        grads(qi - 1, prev_st, it == 1);
+                    }
+                    prev_st = st;
+                    if (++st == NST) {
+                        st = 0;
+                        st_par ^= 1;
                     }
                 }
-                if (ok && !(ok = mbar_wait(p_ready, uint32_t(qi - 1) & 1, abort))) flag_abort(abort, a.status);
-                tc_fence_after();
-                if (ok) {
-                    grads(qi - 1, n_iter == 1);
-                    mma_commit(kv_empty);  // K / V free for the next tile once these GEMMs finish
-                }
+                wait(p_ready, (qi - 1) & 1);
+                grads(qi - 1, prev_st, n_iter == 1);
+                if (ok) mma_commit(kv_empty);  // K / V free for the next tile once these GEMMs finish
                 ++kt;
             }
             ATTN_END_UNITS
@@ -311,55 +390,137 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
             mma_commit(drain);
             mbar_wait(drain, 0, &never, 100000000ull);
         }
-    } else {
-        // ================================================= P / dS, dQ, dK / dV
+    } else if (warp < 10) {
+        // ================================================= P^T / dS^T (warps 2..9)
         const int lg = warp & 3, half = (warp - 2) >> 2;
         const uint32_t lane_addr = uint32_t(lg * 32) << 16;
-        const int r = lg * 32 + lane;  // TMEM lane of this thread
+        const int r = lg * 32 + lane;  // TMEM lane of this thread = key row of the tile
         const float sc = a.scale * kLog2e;
-        const bool leader = warp == 2 && lane == 0;
         const uint32_t aX = smem_u32(sX);
-        T *dK = static_cast<T *>(a.dK.ptr), *dV = static_cast<T *>(a.dV.ptr);
         bool ok = true;
-        int64_t kt = 0, qi = 0;
-
-        // dQ of query tile x (head hq, first row i0), whose GEMMs just completed and released
-        // dS buffer x & 1 -> staged there -> TMA add-reduce into the fp32 accumulator
-        auto stage_dq = [&](int64_t x, int64_t hq, int64_t row_base, int64_t i0) {
-            const uint32_t adQ = aX + uint32_t(x & 1) * Cfg::X_BYTES;
-            uint8_t *sdQ = sX + (x & 1) * Cfg::X_BYTES;
-            ok = bar_and(1, 256, ok);
-            if (ok) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_addr + Cfg::T_DQ + half * 32, v);
-                tmem_ld_wait();
-                if (D == 64) {  // lane = query row r, columns = head dims [32 half, 32 half + 32)
-                    const uint32_t base = adQ + uint32_t(half * BM * 128 + r * 128);
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        st_shared_v4(base + (uint32_t(ch ^ (r & 7)) << 4), v[4 * ch], v[4 * ch + 1], v[4 * ch + 2],
-                                     v[4 * ch + 3]);
-                } else {  // lane = head dim r, columns = query rows [32 half, 32 half + 32)
-                    const uint32_t base = adQ + uint32_t(lg * BM * 128) + uint32_t((lane & 3) << 2);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int c = half * 32 + e;
-                        st_shared_f32(base + uint32_t(c * 128) + (uint32_t((lane >> 2) ^ (c & 7)) << 4), v[e]);
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(1, 256);
-            if (leader && ok) {
-                const int64_t row0 = row_base + hq * a.t_pad + i0;
-                for (int box = 0; box < D / 32; ++box)
-                    tma_reduce_add_2d(&p.tm_dq, sdQ + box * BM * 128, box * 32, int(row0));
-                bulk_commit();
-            }
+        uint32_t qi = 0;            // query tiles done by this CTA
+        int st = 0;                 // their Q / dO ring stage ...
+        uint32_t st_par = 0;        // ... and its phase parity
+        // tc: the wait orders later TMEM accesses (else it only guards shared memory)
+        auto wait = [&](uint64_t *bar, uint32_t parity, bool tc) {
+            if (ok && !(ok = mbar_wait(bar, parity, abort))) flag_abort(abort, a.status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (tc) tc_fence_after();
         };
 
         ATTN_FOR_EACH_UNIT
         const int64_t shift = a.mask == ATTN_CAUSAL_BOTTOM_RIGHT ? lkv - lq : 0;
+        for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
+            const int64_t j0 = jt * BN, j = j0 + r;
+            const bool row_ok = j < lkv;
+            int qt0, nq;
+            query_tiles<BM>(a.mask, j0, lq, lkv, &qt0, &nq);
+            const int n_iter = G * nq;
+            int iq = 0;  // query tile within the head
+            for (int it = 0; it < n_iter; ++it, ++qi) {
+                const int64_t i0 = int64_t(qt0 + iq) * BM;
+                wait(&q_full[st], st_par, false);  // LSE / D of this tile
+                // dS buffer qi & 1 held tile qi - 2, whose GEMMs must have completed
+                if (qi >= 2) wait(&ds_free[qi & 1], ((qi >> 1) - 1) & 1, false);
+                const uint32_t adS = aX + uint32_t(qi & 1) * Cfg::X_BYTES;
+                const uint32_t a_lse = smem_u32(smem + Cfg::OFF_LSE + st * BM * 4);
+                const uint32_t a_dv = smem_u32(smem + Cfg::OFF_DVEC + st * BM * 4);
+                // first visible query column of this key row; everything is masked past the sequence
+                const int64_t cmin64 = !row_ok ? INT64_MAX : (a.mask ? j - shift - i0 : INT64_MIN);
+                const int cmin = int(cmin64 < -1 ? -1 : (cmin64 > BM ? BM : cmin64));
+#pragma unroll
+                for (int q = 0; q < NG; ++q) {
+                    const int rel = NH == NG ? q : 0;  // release group of these columns
+                    if (NH == NG || q == 0) wait(&s_full[rel], qi & 1, true);
+                    const int c0 = q * (BM / NG) + half * GW;
+                    uint32_t pk[GW / 2];  // P^T of this column group, packed
+                    if (ok) {
+                        const bool any_mask = __any_sync(0xffffffffu, cmin > c0);
+                        // chunks of 16 columns; the TMEM loads of chunk cc + 1 are issued before
+                        // chunk cc is computed
+                        constexpr int NCH = GW / 16;
+                        uint32_t sbuf[2][16], dbuf[2][16];
+                        tmem_ld16(tmem + lane_addr + Cfg::T_S + c0, sbuf[0]);
+                        tmem_ld16(tmem + lane_addr + Cfg::T_DP + c0, dbuf[0]);
+#pragma unroll
+                        for (int cc = 0; cc < NCH; ++cc) {
+                            const int col0 = c0 + cc * 16, cur = cc & 1;
+                            tmem_ld_wait_regs(sbuf[cur], dbuf[cur]);
+                            if (cc + 1 < NCH) {
+                                tmem_ld16(tmem + lane_addr + Cfg::T_S + col0 + 16, sbuf[cur ^ 1]);
+                                tmem_ld16(tmem + lane_addr + Cfg::T_DP + col0 + 16, dbuf[cur ^ 1]);
+                            }
+                            uint32_t dk[8];
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const float4 l4 = ld_shared_f4(a_lse + uint32_t(col0 + 4 * q4) * 4);
+                                const float4 d4 = ld_shared_f4(a_dv + uint32_t(col0 + 4 * q4) * 4);
+                                const float lse4[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                                for (int h2 = 0; h2 < 2; ++h2) {
+                                    const int e = 4 * q4 + 2 * h2, c = col0 + e;
+                                    float x0 = fmaf(__uint_as_float(sbuf[cur][e]), sc, -lse4[2 * h2]);
+                                    float x1 = fmaf(__uint_as_float(sbuf[cur][e + 1]), sc, -lse4[2 * h2 + 1]);
+                                    if (any_mask) {
+                                        x0 = c >= cmin ? x0 : -INFINITY;
+                                        x1 = c + 1 >= cmin ? x1 : -INFINITY;
+                                    }
+                                    const float g0 = __uint_as_float(dbuf[cur][e]) - dv4[2 * h2];
+                                    const float g1 = __uint_as_float(dbuf[cur][e + 1]) - dv4[2 * h2 + 1];
+                                    pk[cc * 8 + 2 * q4 + h2] = p_and_ds<T>(x0, x1, g0, g1, &dk[2 * q4 + h2]);
+                                }
+                            }
+#pragma unroll
+                            for (int q2 = 0; q2 < 2; ++q2) {
+                                const uint32_t off = sw128_offset(uint32_t(r), uint32_t(col0 + 8 * q2), BN);
+                                st_shared_v4(adS + off, dk[4 * q2], dk[4 * q2 + 1], dk[4 * q2 + 2], dk[4 * q2 + 3]);
+                            }
+                        }
+                    }
+                    if (NH == NG || q == NG - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&s_free[rel]);  // these columns may be overwritten
+                    }
+                    // P^T into TMEM once the previous tile's dV GEMM has read it
+                    if (q == 0 && qi > 0) wait(p_free, (qi - 1) & 1, true);
+                    if (ok) {
+#pragma unroll
+                        for (int cc = 0; cc < GW / 16; ++cc) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) w[e] = pk[cc * 8 + e];
+                            tmem_st8(tmem + lane_addr + Cfg::T_P + c0 / 2 + cc * 8, w);
+                        }
+                    }
+                }
+                if (ok) tmem_st_wait();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_ready);
+                if (++st == NST) {
+                    st = 0;
+                    st_par ^= 1;
+                }
+                if (++iq == nq) iq = 0;
+            }
+        }
+        ATTN_END_UNITS
+        pdl_trigger();
+    } else {
+        // ================================================= dQ reduce, dK / dV epilogue (warps 10..13)
+        const int lg = warp & 3;
+        const uint32_t lane_addr = uint32_t(lg * 32) << 16;
+        const int r = lg * 32 + lane;  // TMEM lane of this thread
+        const bool leader = warp == 10 && lane == 0;
+        uint8_t *sDQS = smem + Cfg::OFF_DQS;
+        const uint32_t aDQS = smem_u32(sDQS);
+        T *dK = static_cast<T *>(a.dK.ptr), *dV = static_cast<T *>(a.dV.ptr);
+        bool ok = true;
+        uint32_t qi = 0;
+
+        ATTN_FOR_EACH_UNIT
         for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
             const int64_t j0 = jt * BN, j = j0 + r;
             const bool row_ok = j < lkv;
@@ -371,157 +532,98 @@ __global__ void __launch_bounds__(320, 1) dense_bwd_tc_kernel(const __grid_const
             const int n_iter = G * nq;
             if (n_iter == 0) {  // no query sees these keys: dK = dV = 0
                 if (row_ok)
-                    for (int x = half * (D / 2); x < (half + 1) * (D / 2); x += 8) {
+                    for (int x = 0; x < D; x += 8) {
                         *reinterpret_cast<uint4 *>(dK + offk + x) = make_uint4(0, 0, 0, 0);
                         *reinterpret_cast<uint4 *>(dV + offv + x) = make_uint4(0, 0, 0, 0);
                     }
                 continue;
             }
-            int64_t prev_hq = 0, prev_i0 = 0;
+            int iq = 0, hg = 0;  // query tile within the head, head within the group
             for (int it = 0; it < n_iter; ++it, ++qi) {
-                const int st = int(qi % NST);
-                const int64_t hq = g * G + it / nq, i0 = int64_t(qt0 + it % nq) * BM;
-                if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(qi / NST) & 1, abort))) flag_abort(abort, a.status);
-                if (ok && !(ok = mbar_wait(s_full, uint32_t(qi) & 1, abort))) flag_abort(abort, a.status);
+                const int64_t hq = g * G + hg, i0 = int64_t(qt0 + iq) * BM;
+                if (++iq == nq) {
+                    iq = 0;
+                    ++hg;
+                }
+                if (ok && !(ok = mbar_wait(mma_done, qi & 1, abort))) flag_abort(abort, a.status);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
-                // dS buffer qi & 1 last staged dQ of tile qi - 2: that reduce must have read it
-                if (leader) bulk_wait_read0();
-                named_bar_sync(1, 256);
-                const uint32_t adS = aX + uint32_t(qi & 1) * Cfg::X_BYTES;
-                // ---- P^T (kept packed until TMEM frees) and dS^T (to shared memory now)
-                uint32_t pk[HC / 2];
-                if (ok) {
-                    const uint32_t a_lse = smem_u32(smem + Cfg::OFF_LSE + st * BM * 4);
-                    const uint32_t a_dv = smem_u32(smem + Cfg::OFF_DVEC + st * BM * 4);
-                    // first visible query column of this key row; everything is masked past the sequence
-                    const int64_t cmin64 = !row_ok ? INT64_MAX : (a.mask ? j - shift - i0 : INT64_MIN);
-                    const int cmin = int(cmin64 < -1 ? -1 : (cmin64 > BM ? BM : cmin64));
-                    const bool any_mask = __any_sync(0xffffffffu, cmin > half * HC);
-                    // chunks of 16 columns; the TMEM loads of chunk cc + 1 are issued before
-                    // chunk cc is computed
-                    constexpr int NCH = HC / 16;
-                    uint32_t sbuf[2][16], dbuf[2][16];
-                    tmem_ld16(tmem + lane_addr + Cfg::T_S + half * HC, sbuf[0]);
-                    tmem_ld16(tmem + lane_addr + Cfg::T_DP + half * HC, dbuf[0]);
+                // dQ of tile qi, half of its columns at a time, through the staging buffer
+                const int64_t row0 = part * a.h * a.t_pad + geo.ws_start(b) + hq * a.t_pad + i0;
 #pragma unroll
-                    for (int cc = 0; cc < NCH; ++cc) {
-                        const int col0 = half * HC + cc * 16, cur = cc & 1;
-                        tmem_ld_wait_regs(sbuf[cur], dbuf[cur]);
-                        if (cc + 1 < NCH) {
-                            tmem_ld16(tmem + lane_addr + Cfg::T_S + col0 + 16, sbuf[cur ^ 1]);
-                            tmem_ld16(tmem + lane_addr + Cfg::T_DP + col0 + 16, dbuf[cur ^ 1]);
-                        }
-                        uint32_t dk[8];
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t v[32];
+                    if (ok) {
+                        tmem_ld32(tmem + lane_addr + Cfg::T_DQ + hb * 32, v);
+                        tmem_ld_wait_regs(v);
+                    }
+                    if (hb == 1) {  // the accumulator has been read out
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(dq_free);
+                    }
+                    if (leader) bulk_wait_read0();  // the previous reduce has read the staging buffer
+                    named_bar_sync(2, 128);
+                    if (ok) {
+                        if (D == 64) {  // lane = query row r, columns = head dims 32 hb ..
+                            const uint32_t base = aDQS + uint32_t(r * 128);
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const float4 l4 = ld_shared_f4(a_lse + uint32_t(col0 + 4 * q4) * 4);
-                            const float4 d4 = ld_shared_f4(a_dv + uint32_t(col0 + 4 * q4) * 4);
-                            const float lse4[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                            for (int ch = 0; ch < 8; ++ch)
+                                st_shared_v4(base + (uint32_t(ch ^ (r & 7)) << 4), v[4 * ch], v[4 * ch + 1],
+                                             v[4 * ch + 2], v[4 * ch + 3]);
+                        } else {  // lane = head dim r (box lg), columns = query rows 32 hb ..
+                            const uint32_t base = aDQS + uint32_t(lg * 32 * 128) + uint32_t((lane & 3) << 2);
 #pragma unroll
-                            for (int h2 = 0; h2 < 2; ++h2) {
-                                const int e = 4 * q4 + 2 * h2, c = col0 + e;
-                                float x0 = fmaf(__uint_as_float(sbuf[cur][e]), sc, -lse4[2 * h2]);
-                                float x1 = fmaf(__uint_as_float(sbuf[cur][e + 1]), sc, -lse4[2 * h2 + 1]);
-                                if (any_mask) {
-                                    x0 = c >= cmin ? x0 : -INFINITY;
-                                    x1 = c + 1 >= cmin ? x1 : -INFINITY;
-                                }
-                                const float g0 = __uint_as_float(dbuf[cur][e]) - dv4[2 * h2];
-                                const float g1 = __uint_as_float(dbuf[cur][e + 1]) - dv4[2 * h2 + 1];
-                                pk[cc * 8 + 2 * q4 + h2] = p_and_ds<T>(x0, x1, g0, g1, &dk[2 * q4 + h2]);
-                            }
-                        }
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const uint32_t off = sw128_offset(uint32_t(r), uint32_t(col0 + 8 * q), BN);
-                            st_shared_v4(adS + off, dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+                            for (int e = 0; e < 32; ++e)
+                                st_shared_f32(base + uint32_t(e * 128) + (uint32_t((lane >> 2) ^ (e & 7)) << 4), v[e]);
                         }
                     }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_free);  // S^T / dP^T may be overwritten
-                // ---- the previous query tile's GEMMs have released P (TMEM) and dS (smem); its dQ is ready
-                if (it > 0) {
-                    if (ok && !(ok = mbar_wait(mma_done, uint32_t(qi - 1) & 1, abort))) flag_abort(abort, a.status);
-                    ok = __all_sync(0xffffffffu, ok);
-                    tc_fence_after();
-                    stage_dq(qi - 1, prev_hq, part * a.h * a.t_pad + geo.ws_start(b), prev_i0);
-                }
-                if (ok) {
-#pragma unroll
-                    for (int c8 = 0; c8 < HC / 16; ++c8) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) w[e] = pk[c8 * 8 + e];
-                        tmem_st8(tmem + lane_addr + Cfg::T_P + half * (HC / 2) + c8 * 8, w);
+                    fence_proxy_async_smem();
+                    ok = bar_and(2, 128, ok);
+                    if (leader && ok) {
+                        if (D == 64)
+                            tma_reduce_add_2d(&p.tm_dq, sDQS, hb * 32, int(row0));
+                        else
+                            for (int box = 0; box < 4; ++box)
+                                tma_reduce_add_2d(&p.tm_dq, sDQS + box * 32 * 128, box * 32, int(row0 + hb * 32));
+                        bulk_commit();
                     }
-                    tmem_st_wait();
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_ready);
-                prev_hq = hq;
-                prev_i0 = i0;
             }
-            // ---- last query tile of this key tile: its dQ, then dK and dV
-            if (ok && !(ok = mbar_wait(mma_done, uint32_t(qi - 1) & 1, abort))) flag_abort(abort, a.status);
-            ok = __all_sync(0xffffffffu, ok);
-            tc_fence_after();
-            stage_dq(qi - 1, prev_hq, part * a.h * a.t_pad + geo.ws_start(b), prev_i0);
-            // dK, dV tiles: staged in the two dS / dQ buffers (swizzled like the loads) and
-            // written by TMA, unless the tile runs past a packed sequence's end (per-row stores)
-            const bool tma_out = !kPacked || j0 + BN <= lkv;
-            if (tma_out) {
-                if (leader) bulk_wait_read0();  // the last dQ reduce has read its buffer
-                ok = bar_and(1, 256, ok);
-            }
-            if (ok) {
+            // ---- dK (scaled) and dV of this key tile: the last tile's GEMMs have completed
+#pragma unroll 1
+            for (int cc = 0; cc < D / 16; ++cc) {
+                uint32_t vk[2][16];
+                if (ok) {
+                    tmem_ld16(tmem + lane_addr + Cfg::T_DV + cc * 16, vk[0]);
+                    tmem_ld16(tmem + lane_addr + Cfg::T_DK + cc * 16, vk[1]);
+                    tmem_ld_wait_regs(vk[0], vk[1]);
+                }
+                if (cc == D / 16 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_free);
+                }
+                if (ok && row_ok) {
 #pragma unroll
-                for (int cc = 0; cc < D / 64; ++cc) {
-                    const int col0 = half * (D / 2) + cc * 32;
-                    uint32_t vv[32], kk[32];
-                    tmem_ld32(tmem + lane_addr + Cfg::T_DV + col0, vv);
-                    tmem_ld32(tmem + lane_addr + Cfg::T_DK + col0, kk);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 2; ++q) {
                         uint4 ov, ok4;
-                        ov.x = pack2<T>(__uint_as_float(vv[8 * q + 0]), __uint_as_float(vv[8 * q + 1]));
-                        ov.y = pack2<T>(__uint_as_float(vv[8 * q + 2]), __uint_as_float(vv[8 * q + 3]));
-                        ov.z = pack2<T>(__uint_as_float(vv[8 * q + 4]), __uint_as_float(vv[8 * q + 5]));
-                        ov.w = pack2<T>(__uint_as_float(vv[8 * q + 6]), __uint_as_float(vv[8 * q + 7]));
-                        ok4.x = pack2<T>(__uint_as_float(kk[8 * q + 0]) * a.scale, __uint_as_float(kk[8 * q + 1]) * a.scale);
-                        ok4.y = pack2<T>(__uint_as_float(kk[8 * q + 2]) * a.scale, __uint_as_float(kk[8 * q + 3]) * a.scale);
-                        ok4.z = pack2<T>(__uint_as_float(kk[8 * q + 4]) * a.scale, __uint_as_float(kk[8 * q + 5]) * a.scale);
-                        ok4.w = pack2<T>(__uint_as_float(kk[8 * q + 6]) * a.scale, __uint_as_float(kk[8 * q + 7]) * a.scale);
-                        if (tma_out) {
-                            const uint32_t off = sw128_offset(uint32_t(r), uint32_t(col0 + 8 * q), BN);
-                            st_shared_v4(aX + off, ov.x, ov.y, ov.z, ov.w);
-                            st_shared_v4(aX + Cfg::X_BYTES + off, ok4.x, ok4.y, ok4.z, ok4.w);
-                        } else if (row_ok) {
-                            *reinterpret_cast<uint4 *>(dV + offv + col0 + 8 * q) = ov;
-                            *reinterpret_cast<uint4 *>(dK + offk + col0 + 8 * q) = ok4;
-                        }
+                        const uint32_t *w = vk[0] + 8 * q, *u = vk[1] + 8 * q;
+                        ov.x = pack2<T>(__uint_as_float(w[0]), __uint_as_float(w[1]));
+                        ov.y = pack2<T>(__uint_as_float(w[2]), __uint_as_float(w[3]));
+                        ov.z = pack2<T>(__uint_as_float(w[4]), __uint_as_float(w[5]));
+                        ov.w = pack2<T>(__uint_as_float(w[6]), __uint_as_float(w[7]));
+                        ok4.x = pack2<T>(__uint_as_float(u[0]) * a.scale, __uint_as_float(u[1]) * a.scale);
+                        ok4.y = pack2<T>(__uint_as_float(u[2]) * a.scale, __uint_as_float(u[3]) * a.scale);
+                        ok4.z = pack2<T>(__uint_as_float(u[4]) * a.scale, __uint_as_float(u[5]) * a.scale);
+                        ok4.w = pack2<T>(__uint_as_float(u[6]) * a.scale, __uint_as_float(u[7]) * a.scale);
+                        *reinterpret_cast<uint4 *>(dV + offv + cc * 16 + 8 * q) = ov;
+                        *reinterpret_cast<uint4 *>(dK + offk + cc * 16 + 8 * q) = ok4;
                     }
-                }
-            }
-            if (tma_out) {
-                fence_proxy_async_smem();
-                named_bar_sync(1, 256);
-                if (leader && ok) {
-                    for (int c = 0; c < D / 64; ++c) {
-                        tma_store_4d(&p.tm_dv, sX + c * BN * 128, c * 64, int(kv_row0 + j0), int(g), kv_b);
-                        tma_store_4d(&p.tm_dk, sX + Cfg::X_BYTES + c * BN * 128, c * 64, int(kv_row0 + j0), int(g), kv_b);
-                    }
-                    bulk_commit();
                 }
             }
             // deterministic mode: this tile's dQ adds land before the next tile's (fixed order)
             if (leader && a.deterministic) bulk_wait0();
-            ++kt;
         }
         ATTN_END_UNITS
         if (leader) bulk_wait0();
@@ -617,18 +719,17 @@ template <class T, int D, class Geo> cudaError_t run_tc(const DenseArgs &a, cons
                    !map_view(&prm.tm_do, a.dO, a.dtype, D, sq, a.h, nb, Cfg::BM)))
         return cudaErrorInvalidValue;
     if (!map_view(&prm.tm_k, a.k, a.dtype, D, skv, a.h_kv, nb, Cfg::BN) ||
-        !map_view(&prm.tm_v, a.v, a.dtype, D, skv, a.h_kv, nb, Cfg::BN) ||
-        !map_view(&prm.tm_dk, a.dK, a.dtype, D, skv, a.h_kv, nb, Cfg::BN) ||
-        !map_view(&prm.tm_dv, a.dV, a.dtype, D, skv, a.h_kv, nb, Cfg::BN))
+        !map_view(&prm.tm_v, a.v, a.dtype, D, skv, a.h_kv, nb, Cfg::BN))
         return cudaErrorInvalidValue;
-    if (!map_dqacc(&prm.tm_dq, a.dqacc, D, int64_t(a.n_part) * a.h * a.t_pad, Cfg::BM)) return cudaErrorInvalidValue;
+    if (!map_dqacc(&prm.tm_dq, a.dqacc, D, int64_t(a.n_part) * a.h * a.t_pad, Cfg::DQ_BOX_ROWS))
+        return cudaErrorInvalidValue;
     if (sq == 0) prm.tm_q = prm.tm_do = prm.tm_k;  // never read: no query tiles
     auto k = dense_bwd_tc_kernel<T, D, Geo>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     prm.a.tc_units = (a.deterministic ? a.n_part : ntiles) * a.nseq * a.h_kv;
     const int64_t units = prm.a.tc_units < sm_count() ? prm.a.tc_units : sm_count();
-    return launch_kernel(k, dim3(unsigned(units)), dim3(320), Cfg::SMEM_ALLOC, s, true, prm, g);
+    return launch_kernel(k, dim3(unsigned(units)), dim3(Cfg::THREADS), Cfg::SMEM_ALLOC, s, true, prm, g);
 }
 
 template <class Geo> cudaError_t dispatch(const DenseArgs &a, const Geo &g, cudaStream_t s)

@@ -88,6 +88,15 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t base, uint32_t krows, int k
     return smem_desc_sw128(base + uint32_t(kk) * 2048u, krows * 128u, 1024);
 }
 
+// The same descriptors advanced to K step kk from their step-0 value: only
+// the start-address field (address >> 4, 14 bits, no carry for shared
+// memory addresses) changes, so a step is one add.
+__device__ __forceinline__ uint64_t kmaj_step(uint64_t d0, uint32_t rows, int kk)
+{
+    return d0 + uint64_t((uint32_t(kk >> 2) * rows * 128u + uint32_t(kk & 3) * 32u) >> 4);
+}
+__device__ __forceinline__ uint64_t mn_step(uint64_t d0, int kk) { return d0 + uint64_t(uint32_t(kk) * 128u); }
+
 __device__ __forceinline__ void flag_abort(volatile int *abort, uint32_t *status)
 {
     *abort = 1;
