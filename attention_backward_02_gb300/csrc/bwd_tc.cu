@@ -69,7 +69,12 @@ struct TcCfg {
     static constexpr int NH = ATTN_SDP_RELEASE_GROUPS;
 #endif
     static constexpr int NST = 3;                   // Q / dO ring stages
-    static constexpr int THREADS = 448;             // 14 warps
+#ifndef ATTN_SOFTMAX_WARPS
+    static constexpr int NSW = 8;                   // P / dS warps (two or four per TMEM lane quadrant)
+#else
+    static constexpr int NSW = ATTN_SOFTMAX_WARPS;
+#endif
+    static constexpr int THREADS = 32 * (2 + NSW + 4);  // TMA, MMA, P / dS, dQ + dK / dV
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int DS_BYTES = BN * BM * 2;
@@ -93,7 +98,8 @@ struct TcCfg {
     static constexpr int T_COLS = 512;
     static_assert(T_DQ + 64 <= T_COLS, "TMEM budget");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
-    static_assert(BM / 2 / NG == 32, "each softmax thread takes 32 columns per group");
+    static constexpr int GW = BM / NG / (NSW / 4);  // query columns per P / dS thread and column group
+    static_assert(GW % 16 == 0 && (NSW == 8 || NSW == 16), "P / dS work split");
     static_assert(NH == 1 || NH == NG, "release groups");
 };
 
@@ -126,12 +132,11 @@ template <> struct IsPacked<PackedGeo> : std::true_type {};
 }  // namespace
 
 template <class T, int D, class Geo>
-__global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_constant__ TcParams p, const Geo geo)
+__global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(const __grid_constant__ TcParams p, const Geo geo)
 {
     using Cfg = TcCfg<D>;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, NST = Cfg::NST, NH = Cfg::NH, NG = Cfg::NG;
-    constexpr int HC = BM / 2;       // query columns per softmax thread
-    constexpr int GW = HC / NG;      // of which per column group
+    constexpr int GW = Cfg::GW;      // query columns per softmax thread and column group
     constexpr bool kPacked = IsPacked<Geo>::value;
     constexpr int kType = std::is_same<T, __half>::value ? 0 : 1;
 
@@ -163,9 +168,9 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
         }
         for (int q = 0; q < NH; ++q) {
             mbar_init(&s_full[q], 1);
-            mbar_init(&s_free[q], 8);
+            mbar_init(&s_free[q], Cfg::NSW);
         }
-        mbar_init(p_ready, 8);
+        mbar_init(p_ready, Cfg::NSW);
         mbar_init(p_free, 1);
         mbar_init(mma_done, 1);
         mbar_init(dq_free, 4);
@@ -180,7 +185,8 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    pdl_wait();  // the preprocess (LSE, D, zeroed dQ accumulator) has completed
+    // The preprocess (LSE, D, zeroed dQ accumulator) may still be running: only the loads of
+    // LSE / D and the dQ reduce-adds wait for it (pdl_wait below), the Q / K / V / dO loads do not.
 
     // ---- work units: (sequence b, kv head g) and its key tiles; unit
     // index = first tile * (nseq * h_kv) + (b * h_kv + g), so for a causal
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
         // ================================================= TMA producer
         if (elect_one()) {
             prefetch_tmap(&p.tm_q); prefetch_tmap(&p.tm_k); prefetch_tmap(&p.tm_v); prefetch_tmap(&p.tm_do);
-            bool ok = true;
+            bool ok = true, pre_done = false;
             int64_t kt = 0, qi = 0, q_armed = 0, kv_armed = 0;  // loads started (for the drain below)
             ATTN_FOR_EACH_UNIT
             for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
@@ -237,10 +243,28 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
                         tma_load_4d(sdO + c * BM * 128, &p.tm_do, &q_full[st], c * 64, int(q_row0 + i0), int(hq), q_b);
                     }
                     const int64_t wrow = hq * a.t_pad + geo.ws_start(b) + i0;
+                    if (!pre_done) {  // LSE / D come from the preprocess
+                        pdl_wait();
+                        pre_done = true;
+                    }
                     bulk_load(smem + Cfg::OFF_LSE + st * BM * 4, a.lse2 + wrow, BM * 4, &q_full[st]);
                     bulk_load(smem + Cfg::OFF_DVEC + st * BM * 4, a.dvec + wrow, BM * 4, &q_full[st]);
                 };
                 // the first query tile does not need the key tile: load it before waiting for K / V
+                // (except on the very first tile, whose K / V load should start first)
+                auto load_kv = [&]() {
+                    if (kt > 0 && ok && !(ok = mbar_wait(kv_empty, uint32_t(kt - 1) & 1, abort)))
+                        flag_abort(abort, a.status);
+                    if (ok) {
+                        kv_armed = kt + 1;
+                        mbar_arrive_expect_tx(kv_full, 2 * Cfg::KV_BYTES);
+                        for (int c = 0; c < D / 64; ++c) {
+                            tma_load_4d(sK + c * BN * 128, &p.tm_k, kv_full, c * 64, int(kv_row0 + j0), int(g), kv_b);
+                            tma_load_4d(sV + c * BN * 128, &p.tm_v, kv_full, c * 64, int(kv_row0 + j0), int(g), kv_b);
+                        }
+                    }
+                };
+                if (kt == 0) load_kv();
                 load_q(0, qi);
                 // warm L2 with the K / V tile this CTA takes next, so its load does not stall the next unit
                 {
@@ -267,15 +291,7 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
                             tma_prefetch_4d(&p.tm_v, c * 64, int(nrow0 + njt * BN), int(ng), nkv_b);
                         }
                 }
-                if (kt > 0 && ok && !(ok = mbar_wait(kv_empty, uint32_t(kt - 1) & 1, abort))) flag_abort(abort, a.status);
-                if (ok) {
-                    kv_armed = kt + 1;
-                    mbar_arrive_expect_tx(kv_full, 2 * Cfg::KV_BYTES);
-                    for (int c = 0; c < D / 64; ++c) {
-                        tma_load_4d(sK + c * BN * 128, &p.tm_k, kv_full, c * 64, int(kv_row0 + j0), int(g), kv_b);
-                        tma_load_4d(sV + c * BN * 128, &p.tm_v, kv_full, c * 64, int(kv_row0 + j0), int(g), kv_b);
-                    }
-                }
+                if (kt > 0) load_kv();
                 ++qi;
                 for (int it = 1; it < n_iter; ++it, ++qi) load_q(it, qi);
                 ++kt;
@@ -390,9 +406,9 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
             mma_commit(drain);
             mbar_wait(drain, 0, &never, 100000000ull);
         }
-    } else if (warp < 10) {
-        // ================================================= P^T / dS^T (warps 2..9)
-        const int lg = warp & 3, half = (warp - 2) >> 2;
+    } else if (warp < 2 + Cfg::NSW) {
+        // ================================================= P^T / dS^T (warps 2 .. 1 + NSW)
+        const int lg = warp & 3, half = (warp - 2) >> 2;  // lane quadrant, column slice
         const uint32_t lane_addr = uint32_t(lg * 32) << 16;
         const int r = lg * 32 + lane;  // TMEM lane of this thread = key row of the tile
         const float sc = a.scale * kLog2e;
@@ -419,9 +435,18 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
             int iq = 0;  // query tile within the head
             for (int it = 0; it < n_iter; ++it, ++qi) {
                 const int64_t i0 = int64_t(qt0 + iq) * BM;
-                wait(&q_full[st], st_par, false);  // LSE / D of this tile
-                // dS buffer qi & 1 held tile qi - 2, whose GEMMs must have completed
-                if (qi >= 2) wait(&ds_free[qi & 1], ((qi >> 1) - 1) & 1, false);
+                // Usually LSE / D of this tile have landed (q_full), the GEMMs of tile qi - 2 that read
+                // dS buffer qi & 1 have completed (ds_free) and the first S^T / dP^T group is written
+                // (s_full): test all three at once and wait one by one only if one is not.
+                const uint32_t t_q = mbar_test_wait(&q_full[st], st_par);
+                const uint32_t t_d = qi >= 2 ? mbar_test_wait(&ds_free[qi & 1], ((qi >> 1) - 1) & 1) : 1u;
+                const uint32_t t_s = mbar_test_wait(&s_full[0], qi & 1);
+                const bool ready0 = __all_sync(0xffffffffu, t_q && t_d && t_s);
+                if (!ready0) {
+                    wait(&q_full[st], st_par, false);
+                    if (qi >= 2) wait(&ds_free[qi & 1], ((qi >> 1) - 1) & 1, false);
+                }
+                bool ready1 = false;  // the previous tile's dV has read P^T and the second group is written
                 const uint32_t adS = aX + uint32_t(qi & 1) * Cfg::X_BYTES;
                 const uint32_t a_lse = smem_u32(smem + Cfg::OFF_LSE + st * BM * 4);
                 const uint32_t a_dv = smem_u32(smem + Cfg::OFF_DVEC + st * BM * 4);
@@ -431,7 +456,8 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
 #pragma unroll
                 for (int q = 0; q < NG; ++q) {
                     const int rel = NH == NG ? q : 0;  // release group of these columns
-                    if (NH == NG || q == 0) wait(&s_full[rel], qi & 1, true);
+                    if (q == 0 ? !ready0 : (NH == NG && !ready1)) wait(&s_full[rel], qi & 1, true);
+                    else if (q == 0) tc_fence_after();
                     const int c0 = q * (BM / NG) + half * GW;
                     uint32_t pk[GW / 2];  // P^T of this column group, packed
                     if (ok) {
@@ -483,7 +509,13 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
                         if (lane == 0) mbar_arrive(&s_free[rel]);  // these columns may be overwritten
                     }
                     // P^T into TMEM once the previous tile's dV GEMM has read it
-                    if (q == 0 && qi > 0) wait(p_free, (qi - 1) & 1, true);
+                    if (q == 0) {
+                        const uint32_t t_p = qi > 0 ? mbar_test_wait(p_free, (qi - 1) & 1) : 1u;
+                        const uint32_t t_s1 = NH == NG && NG > 1 ? mbar_test_wait(&s_full[NG > 1 ? 1 : 0], qi & 1) : 1u;
+                        ready1 = __all_sync(0xffffffffu, t_p && t_s1);
+                        if (!ready1 && qi > 0) wait(p_free, (qi - 1) & 1, true);
+                        else tc_fence_after();
+                    }
                     if (ok) {
 #pragma unroll
                         for (int cc = 0; cc < GW / 16; ++cc) {
@@ -509,16 +541,17 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
         ATTN_END_UNITS
         pdl_trigger();
     } else {
-        // ================================================= dQ reduce, dK / dV epilogue (warps 10..13)
+        // ================================================= dQ reduce, dK / dV epilogue (last 4 warps)
         const int lg = warp & 3;
         const uint32_t lane_addr = uint32_t(lg * 32) << 16;
         const int r = lg * 32 + lane;  // TMEM lane of this thread
-        const bool leader = warp == 10 && lane == 0;
+        const bool leader = warp == 2 + Cfg::NSW && lane == 0;
         uint8_t *sDQS = smem + Cfg::OFF_DQS;
         const uint32_t aDQS = smem_u32(sDQS);
         T *dK = static_cast<T *>(a.dK.ptr), *dV = static_cast<T *>(a.dV.ptr);
         bool ok = true;
         uint32_t qi = 0;
+        pdl_wait();  // the dQ accumulator has been zeroed
 
         ATTN_FOR_EACH_UNIT
         for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
@@ -550,18 +583,20 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
                 tc_fence_after();
                 // dQ of tile qi, half of its columns at a time, through the staging buffer
                 const int64_t row0 = part * a.h * a.t_pad + geo.ws_start(b) + hq * a.t_pad + i0;
+                // read the whole accumulator first, so the next tile's dQ GEMM is not held up by the
+                // reduce (whose rate the L2 sets)
+                uint32_t v[2][32];
+                if (ok) {
+                    tmem_ld32(tmem + lane_addr + Cfg::T_DQ, v[0]);
+                    tmem_ld32(tmem + lane_addr + Cfg::T_DQ + 32, v[1]);
+                    tmem_ld_wait_regs(v[0]);
+                    tmem_ld_wait_regs(v[1]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dq_free);
 #pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    uint32_t v[32];
-                    if (ok) {
-                        tmem_ld32(tmem + lane_addr + Cfg::T_DQ + hb * 32, v);
-                        tmem_ld_wait_regs(v);
-                    }
-                    if (hb == 1) {  // the accumulator has been read out
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(dq_free);
-                    }
+                for (int hb = 0; hb < 2; ++hb) {  // half of the columns at a time through the staging buffer
                     if (leader) bulk_wait_read0();  // the previous reduce has read the staging buffer
                     named_bar_sync(2, 128);
                     if (ok) {
@@ -569,13 +604,13 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
                             const uint32_t base = aDQS + uint32_t(r * 128);
 #pragma unroll
                             for (int ch = 0; ch < 8; ++ch)
-                                st_shared_v4(base + (uint32_t(ch ^ (r & 7)) << 4), v[4 * ch], v[4 * ch + 1],
-                                             v[4 * ch + 2], v[4 * ch + 3]);
+                                st_shared_v4(base + (uint32_t(ch ^ (r & 7)) << 4), v[hb][4 * ch], v[hb][4 * ch + 1],
+                                             v[hb][4 * ch + 2], v[hb][4 * ch + 3]);
                         } else {  // lane = head dim r (box lg), columns = query rows 32 hb ..
                             const uint32_t base = aDQS + uint32_t(lg * 32 * 128) + uint32_t((lane & 3) << 2);
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
-                                st_shared_f32(base + uint32_t(e * 128) + (uint32_t((lane >> 2) ^ (e & 7)) << 4), v[e]);
+                                st_shared_f32(base + uint32_t(e * 128) + (uint32_t((lane >> 2) ^ (e & 7)) << 4), v[hb][e]);
                         }
                     }
                     fence_proxy_async_smem();
@@ -592,34 +627,30 @@ __global__ void __launch_bounds__(448, 1) dense_bwd_tc_kernel(const __grid_const
             }
             // ---- dK (scaled) and dV of this key tile: the last tile's GEMMs have completed
 #pragma unroll 1
-            for (int cc = 0; cc < D / 16; ++cc) {
-                uint32_t vk[2][16];
+            for (int cc = 0; cc < D / 8; ++cc) {
+                uint32_t w[8], u[8];
                 if (ok) {
-                    tmem_ld16(tmem + lane_addr + Cfg::T_DV + cc * 16, vk[0]);
-                    tmem_ld16(tmem + lane_addr + Cfg::T_DK + cc * 16, vk[1]);
-                    tmem_ld_wait_regs(vk[0], vk[1]);
+                    tmem_ld8(tmem + lane_addr + Cfg::T_DV + cc * 8, w);
+                    tmem_ld8(tmem + lane_addr + Cfg::T_DK + cc * 8, u);
+                    tmem_ld_wait_regs(w, u);
                 }
-                if (cc == D / 16 - 1) {
+                if (cc == D / 8 - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(acc_free);
                 }
                 if (ok && row_ok) {
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        uint4 ov, ok4;
-                        const uint32_t *w = vk[0] + 8 * q, *u = vk[1] + 8 * q;
-                        ov.x = pack2<T>(__uint_as_float(w[0]), __uint_as_float(w[1]));
-                        ov.y = pack2<T>(__uint_as_float(w[2]), __uint_as_float(w[3]));
-                        ov.z = pack2<T>(__uint_as_float(w[4]), __uint_as_float(w[5]));
-                        ov.w = pack2<T>(__uint_as_float(w[6]), __uint_as_float(w[7]));
-                        ok4.x = pack2<T>(__uint_as_float(u[0]) * a.scale, __uint_as_float(u[1]) * a.scale);
-                        ok4.y = pack2<T>(__uint_as_float(u[2]) * a.scale, __uint_as_float(u[3]) * a.scale);
-                        ok4.z = pack2<T>(__uint_as_float(u[4]) * a.scale, __uint_as_float(u[5]) * a.scale);
-                        ok4.w = pack2<T>(__uint_as_float(u[6]) * a.scale, __uint_as_float(u[7]) * a.scale);
-                        *reinterpret_cast<uint4 *>(dV + offv + cc * 16 + 8 * q) = ov;
-                        *reinterpret_cast<uint4 *>(dK + offk + cc * 16 + 8 * q) = ok4;
-                    }
+                    uint4 ov, ok4;
+                    ov.x = pack2<T>(__uint_as_float(w[0]), __uint_as_float(w[1]));
+                    ov.y = pack2<T>(__uint_as_float(w[2]), __uint_as_float(w[3]));
+                    ov.z = pack2<T>(__uint_as_float(w[4]), __uint_as_float(w[5]));
+                    ov.w = pack2<T>(__uint_as_float(w[6]), __uint_as_float(w[7]));
+                    ok4.x = pack2<T>(__uint_as_float(u[0]) * a.scale, __uint_as_float(u[1]) * a.scale);
+                    ok4.y = pack2<T>(__uint_as_float(u[2]) * a.scale, __uint_as_float(u[3]) * a.scale);
+                    ok4.z = pack2<T>(__uint_as_float(u[4]) * a.scale, __uint_as_float(u[5]) * a.scale);
+                    ok4.w = pack2<T>(__uint_as_float(u[6]) * a.scale, __uint_as_float(u[7]) * a.scale);
+                    *reinterpret_cast<uint4 *>(dV + offv + cc * 8) = ov;
+                    *reinterpret_cast<uint4 *>(dK + offk + cc * 8) = ok4;
                 }
             }
             // deterministic mode: this tile's dQ adds land before the next tile's (fixed order)

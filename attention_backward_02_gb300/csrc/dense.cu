@@ -43,87 +43,131 @@ __device__ __forceinline__ int64_t lse_index(const DenseArgs &a, const PackedGeo
     return h * a.t_q + t;
 }
 
+// Element offset of position i of sequence b, head h, in a query-side view.
+__device__ __forceinline__ int64_t seq_off(const View &v, const FixedGeo &, int64_t b, int64_t i, int64_t h)
+{
+    return b * v.sb + h * v.sh + i * v.ss;
+}
+__device__ __forceinline__ int64_t seq_off(const View &v, const PackedGeo &g, int64_t b, int64_t i, int64_t h)
+{
+    return h * v.sh + (g.cu_q[b] + i) * v.ss;
+}
+__device__ __forceinline__ int64_t seq_lse(const DenseArgs &a, const FixedGeo &g, int64_t b, int64_t i, int64_t h)
+{
+    return (b * a.h + h) * g.s_q + i;
+}
+__device__ __forceinline__ int64_t seq_lse(const DenseArgs &a, const PackedGeo &g, int64_t b, int64_t i, int64_t h)
+{
+    return h * a.t_q + g.cu_q[b] + i;
+}
+
 // ------------------------------------------------------------- preprocess
-// One workspace row per group of d/8 threads (8 elements each), 256 threads
-// per block, grid (ceil(t_pad / rows per block), h).  Covers every workspace
-// row: padding rows get LSE2 = +inf (so P = 0) and D = 0, and every partial
-// dQ buffer is zeroed.  Launched normally (it overwrites what the previous
-// call's last kernel reads); lets the main kernel launch behind it.
-template <class T, class Geo>
+// Work unit = (head, 128-row workspace tile); a tile lies within one
+// sequence, so it is located once.  d/8 threads per row (8 elements each),
+// 256-thread blocks striding over the units in one resident wave.  Covers
+// every workspace row: padding rows get LSE2 = +inf (so P = 0) and D = 0.
+// Then zeroes every partial dQ buffer.  Launched normally (it overwrites what
+// the previous call's last kernel reads); lets the main kernel launch behind it.
+template <class T, class Geo, int D>
 __global__ void __launch_bounds__(256) dense_preprocess_kernel(DenseArgs a, Geo geo)
 {
+    constexpr int TPR = D / 8, RPP = 256 / TPR, RPT = int(kWsRowAlign) / RPP;  // rows per pass / per thread
     pdl_trigger();
-    const int64_t h = blockIdx.y;
-    const int tpr = int(a.d / 8);  // threads per row
-    const int lane_in_row = threadIdx.x % tpr;
-    const int64_t wr = int64_t(blockIdx.x) * (256 / tpr) + threadIdx.x / tpr;  // workspace row
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.status = 0u;
-    const bool live = wr < a.t_pad;  // no early exit: the row's threads shuffle below
-    int64_t b = 0, i = 0;
-    const bool real = live && geo.ws_locate(wr, &b, &i);
-    const int64_t t = geo.q_start(b) + i;
-    const int64_t row = h * a.t_pad + wr;
-    float dsum = 0.f, lse = 0.f;
-    if (real) {
-        const uint4 ov = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.o.ptr) + tok_off(a.o, geo, t, h) +
-                                                          lane_in_row * 8);
-        const uint4 dv = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.dO.ptr) +
-                                                          tok_off(a.dO, geo, t, h) + lane_in_row * 8);
-        if (lane_in_row == 0) lse = a.lse[lse_index(a, geo, t, h)];
-        const uint32_t *op = &ov.x, *dp = &dv.x;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
+    const int lane_in_row = threadIdx.x % TPR, k0 = threadIdx.x / TPR;
+    const int ntile = int(a.t_pad / kWsRowAlign);
+    const int nunit = int(a.h) * ntile;
+    for (int u = blockIdx.x; u < nunit; u += gridDim.x) {
+        const int h = u / ntile, wt = u - h * ntile;
+        int64_t b = 0, i0 = 0;
+        geo.ws_locate(int64_t(wt) * kWsRowAlign, &b, &i0);
+        const int64_t lq = geo.q_len(b);
+        const int64_t row0 = int64_t(h) * a.t_pad + int64_t(wt) * kWsRowAlign;
+        uint4 ov[RPT], dv[RPT];  // all loads of this thread first
+        float lse[RPT];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float2 of = unpack2<T>(op[e]), df = unpack2<T>(dp[e]);
-            dsum += of.x * df.x + of.y * df.y;
+        for (int r = 0; r < RPT; ++r) {
+            const int64_t i = i0 + k0 + r * RPP;
+            ov[r] = dv[r] = make_uint4(0, 0, 0, 0);
+            lse[r] = 0.f;
+            if (i < lq) {
+                ov[r] = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.o.ptr) + seq_off(a.o, geo, b, i, h) +
+                                                         lane_in_row * 8);
+                dv[r] = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.dO.ptr) + seq_off(a.dO, geo, b, i, h) +
+                                                         lane_in_row * 8);
+                if (lane_in_row == 0) lse[r] = a.lse[seq_lse(a, geo, b, i, h)];
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int k = k0 + r * RPP;
+            const bool real = i0 + k < lq;
+            const uint32_t *op = &ov[r].x, *dp = &dv[r].x;
+            float dsum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float2 of = unpack2<T>(op[e]), df = unpack2<T>(dp[e]);
+                dsum += of.x * df.x + of.y * df.y;
+            }
+#pragma unroll
+            for (int off = TPR / 2; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+            if (lane_in_row == 0) {
+                a.dvec[row0 + k] = real ? dsum : 0.f;
+                a.lse2[row0 + k] = real ? lse[r] * kLog2e : INFINITY;
+            }
         }
     }
-    for (int off = tpr / 2; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
-    if (!live) return;
-    if (lane_in_row == 0) {
-        a.dvec[row] = real ? dsum : 0.f;
-        a.lse2[row] = real ? lse * kLog2e : INFINITY;
-    }
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p = 0; p < a.n_part; ++p) {
-        float4 *dst =
-            reinterpret_cast<float4 *>(a.dqacc + ((int64_t(p) * a.h * a.t_pad + row) * a.d)) + lane_in_row * 2;
-        dst[0] = z;
-        dst[1] = z;
-    }
+    float4 *acc = reinterpret_cast<float4 *>(a.dqacc);
+    const int64_t n4 = int64_t(a.n_part) * a.h * a.t_pad * D / 4;
+    for (int64_t k = int64_t(blockIdx.x) * 256 + threadIdx.x; k < n4; k += int64_t(gridDim.x) * 256) acc[k] = z;
 }
 
 // ------------------------------------------------------------ dq finalize
-// dQ = cast(scale * sum over the partial buffers, in index order).  Same row
-// mapping as the preprocess; launched behind the main kernel and waits for it.
-template <class T, class Geo>
+// dQ = cast(scale * sum over the partial buffers, in index order).  Same
+// units as the preprocess; launched behind the main kernel and waits for it.
+template <class T, class Geo, int D>
 __global__ void __launch_bounds__(256) dq_finalize_kernel(DenseArgs a, Geo geo)
 {
-    const int64_t h = blockIdx.y;
-    const int tpr = int(a.d / 8);
-    const int lane_in_row = threadIdx.x % tpr;
-    const int64_t wr = int64_t(blockIdx.x) * (256 / tpr) + threadIdx.x / tpr;
-    int64_t b = 0, i = 0;
-    const bool real = wr < a.t_pad && geo.ws_locate(wr, &b, &i);
+    constexpr int TPR = D / 8, RPP = 256 / TPR, RPT = int(kWsRowAlign) / RPP;
+    const int lane_in_row = threadIdx.x % TPR, k0 = threadIdx.x / TPR;
+    const int ntile = int(a.t_pad / kWsRowAlign);
+    const int nunit = int(a.h) * ntile;
+    const int64_t part_stride = a.h * a.t_pad * D;
     pdl_wait();
-    if (!real) return;
-    const int64_t t = geo.q_start(b) + i;
-    const int64_t row = h * a.t_pad + wr;
-    float acc[8];
+    for (int u = blockIdx.x; u < nunit; u += gridDim.x) {
+        const int h = u / ntile, wt = u - h * ntile;
+        int64_t b = 0, i0 = 0;
+        geo.ws_locate(int64_t(wt) * kWsRowAlign, &b, &i0);
+        const int64_t lq = geo.q_len(b);
+        const int64_t row0 = int64_t(h) * a.t_pad + int64_t(wt) * kWsRowAlign;
+        float acc[RPT][8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    for (int p = 0; p < a.n_part; ++p) {  // fixed order: bitwise reproducible
-        const float4 *src =
-            reinterpret_cast<const float4 *>(a.dqacc + ((int64_t(p) * a.h * a.t_pad + row) * a.d)) + lane_in_row * 2;
-        float4 x0 = src[0], x1 = src[1];
-        acc[0] += x0.x; acc[1] += x0.y; acc[2] += x0.z; acc[3] += x0.w;
-        acc[4] += x1.x; acc[5] += x1.y; acc[6] += x1.z; acc[7] += x1.w;
+        for (int r = 0; r < RPT; ++r)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[r][e] = 0.f;
+        for (int p = 0; p < a.n_part; ++p) {  // fixed order: bitwise reproducible
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const float4 *src = reinterpret_cast<const float4 *>(a.dqacc + p * part_stride +
+                                                                     (row0 + k0 + r * RPP) * D + lane_in_row * 8);
+                const float4 x0 = src[0], x1 = src[1];
+                acc[r][0] += x0.x; acc[r][1] += x0.y; acc[r][2] += x0.z; acc[r][3] += x0.w;
+                acc[r][4] += x1.x; acc[r][5] += x1.y; acc[r][6] += x1.z; acc[r][7] += x1.w;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int64_t i = i0 + k0 + r * RPP;
+            if (i >= lq) continue;
+            uint4 out;
+            out.x = pack2<T>(acc[r][0] * a.scale, acc[r][1] * a.scale);
+            out.y = pack2<T>(acc[r][2] * a.scale, acc[r][3] * a.scale);
+            out.z = pack2<T>(acc[r][4] * a.scale, acc[r][5] * a.scale);
+            out.w = pack2<T>(acc[r][6] * a.scale, acc[r][7] * a.scale);
+            *reinterpret_cast<uint4 *>(static_cast<T *>(a.dQ.ptr) + seq_off(a.dQ, geo, b, i, h) + lane_in_row * 8) = out;
+        }
     }
-    uint4 out;
-    out.x = pack2<T>(acc[0] * a.scale, acc[1] * a.scale);
-    out.y = pack2<T>(acc[2] * a.scale, acc[3] * a.scale);
-    out.z = pack2<T>(acc[4] * a.scale, acc[5] * a.scale);
-    out.w = pack2<T>(acc[6] * a.scale, acc[7] * a.scale);
-    *reinterpret_cast<uint4 *>(static_cast<T *>(a.dQ.ptr) + tok_off(a.dQ, geo, t, h) + lane_in_row * 8) = out;
 }
 
 // ------------------------------------------------------------- forward
@@ -233,21 +277,41 @@ template <> int64_t max_len_q(const DenseArgs &, const PackedGeo &g)
     return m;
 }
 
+// One wave of 256-thread blocks (8 per SM), or fewer when there are fewer rows.
+unsigned row_grid(const DenseArgs &a)
+{
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0)
+            sms = 1;
+    }
+    const int64_t need = a.h * (a.t_pad / kWsRowAlign);  // (head, 128-row tile) units
+    const int64_t wave = int64_t(sms) * 8;
+    return unsigned(need < 1 ? 1 : (need < wave ? need : wave));
+}
+
 template <class Geo> cudaError_t preprocess(const DenseArgs &a, const Geo &g, cudaStream_t s)
 {
-    const int64_t rows_per_block = 256 / (a.d / 8);
-    dim3 grid(unsigned((a.t_pad + rows_per_block - 1) / rows_per_block), unsigned(a.h));
-    if (a.dtype == ATTN_F16) return launch_kernel(dense_preprocess_kernel<__half, Geo>, grid, 256, 0, s, false, a, g);
-    return launch_kernel(dense_preprocess_kernel<__nv_bfloat16, Geo>, grid, 256, 0, s, false, a, g);
+    const dim3 grid(row_grid(a));
+    if (a.d == 64)
+        return a.dtype == ATTN_F16
+                   ? launch_kernel(dense_preprocess_kernel<__half, Geo, 64>, grid, 256, 0, s, false, a, g)
+                   : launch_kernel(dense_preprocess_kernel<__nv_bfloat16, Geo, 64>, grid, 256, 0, s, false, a, g);
+    return a.dtype == ATTN_F16 ? launch_kernel(dense_preprocess_kernel<__half, Geo, 128>, grid, 256, 0, s, false, a, g)
+                               : launch_kernel(dense_preprocess_kernel<__nv_bfloat16, Geo, 128>, grid, 256, 0, s, false, a, g);
 }
 
 template <class Geo> cudaError_t finalize(const DenseArgs &a, const Geo &g, cudaStream_t s)
 {
     if (a.t_q == 0) return cudaSuccess;
-    const int64_t rows_per_block = 256 / (a.d / 8);
-    dim3 grid(unsigned((a.t_pad + rows_per_block - 1) / rows_per_block), unsigned(a.h));
-    if (a.dtype == ATTN_F16) return launch_kernel(dq_finalize_kernel<__half, Geo>, grid, 256, 0, s, true, a, g);
-    return launch_kernel(dq_finalize_kernel<__nv_bfloat16, Geo>, grid, 256, 0, s, true, a, g);
+    const dim3 grid(row_grid(a));
+    if (a.d == 64)
+        return a.dtype == ATTN_F16 ? launch_kernel(dq_finalize_kernel<__half, Geo, 64>, grid, 256, 0, s, true, a, g)
+                                   : launch_kernel(dq_finalize_kernel<__nv_bfloat16, Geo, 64>, grid, 256, 0, s, true, a, g);
+    return a.dtype == ATTN_F16 ? launch_kernel(dq_finalize_kernel<__half, Geo, 128>, grid, 256, 0, s, true, a, g)
+                               : launch_kernel(dq_finalize_kernel<__nv_bfloat16, Geo, 128>, grid, 256, 0, s, true, a, g);
 }
 
 template <class T, class Geo, int D> cudaError_t fwd_run(const DenseArgs &a, const Geo &g, dim3 grid, cudaStream_t s)
