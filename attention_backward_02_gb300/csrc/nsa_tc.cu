@@ -19,14 +19,18 @@
 //   dK^T += Q^T dS         M=128 (d)   N=64      K=128  A=Q (MN-major)  B=dS (MN-major)
 //   dQ   = dS K_blk        M=128 rows  N=128 (d) K=64   A=dS (K-major)  B=K (MN-major)
 // dQ of each token is added into an fp32 accumulator with TMA reduce-adds
-// (one box of G rows per token), staged in the chunk's own Q / dO ring stage
-// once its GEMMs are done; dK^T / dV^T stay in TMEM for the piece and are
-// added into fp32 accumulators with coalesced reductions at its end.
+// (one box of G rows per token), staged 64 head dims at a time in a buffer of
+// its own, so a Q / dO stage is free as soon as the chunk's GEMMs are done;
+// dK^T / dV^T stay in TMEM for the piece and are added into fp32
+// accumulators at its end.  The chunk's token list travels through a 4-deep
+// ring in shared memory with its own barriers.
 // TMEM: S 64 + dP 64 + dV^T 64 + dK^T 64 + dQ 128 = 384 columns.
 //
-// Roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2..9
+// Roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2..9
 // element-wise work (warp w reads TMEM lanes 32 (w % 4) .. + 31; two warps
-// per lane group split the columns).  Bounded waits as in the dense kernel.
+// per lane group split the columns) and the piece's dK / dV, warps 10..13 the
+// dQ of each chunk (TMEM -> its stage -> reduce), so the element-wise warps go
+// straight on to the next chunk.  Bounded waits as in the dense kernel.
 #include <cudaTypedefs.h>
 
 #include <climits>
@@ -42,24 +46,25 @@ using namespace tc;
 
 namespace {
 
-constexpr int kD = 128, kBS = 64, kRows = 128, kNst = 2, kMaxSlots = 16, kSlotInts = 4;
+constexpr int kD = 128, kBS = 64, kRows = 128, kNst = 2, kMaxSlots = 16, kSlotInts = 4, kSlotRing = 4;
 constexpr int kPieceChunks = 32;  // chunks per work unit at most
 
 struct NsaCfg {
     static constexpr int KV_BYTES = kBS * kD * 2;       // 16 KB
     static constexpr int Q_BYTES = kRows * kD * 2;      // 32 KB
     static constexpr int PS_BYTES = kRows * kBS * 2;    // 16 KB
+    static constexpr int DQS_BYTES = kRows * 64 * 4;    // fp32 dQ, 64 of the 128 head dims (two 32-wide boxes)
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + KV_BYTES;
     static constexpr int OFF_Q = OFF_V + KV_BYTES;          // kNst stages
     static constexpr int OFF_DO = OFF_Q + kNst * Q_BYTES;   // kNst stages
     static constexpr int OFF_P = OFF_DO + kNst * Q_BYTES;
     static constexpr int OFF_DS = OFF_P + PS_BYTES;
-    static constexpr int OFF_LSE = OFF_DS + PS_BYTES;       // kNst x 128 floats
-    static constexpr int OFF_DVEC = OFF_LSE + kNst * kRows * 4;
-    static constexpr int OFF_SLOT = OFF_DVEC + kNst * kRows * 4;  // kNst x kMaxSlots x {local index, token, topk slot, -}
-    static constexpr int OFF_BAR = OFF_SLOT + kNst * kMaxSlots * kSlotInts * 4;
-    static constexpr int OFF_MISC = OFF_BAR + 16 * 8;
+    static constexpr int OFF_DQS = OFF_DS + PS_BYTES;
+    static constexpr int OFF_SLOT = OFF_DQS + DQS_BYTES;    // kSlotRing x kMaxSlots x {local index, token, topk slot, -}
+    static constexpr int OFF_BAR = OFF_SLOT + kSlotRing * kMaxSlots * kSlotInts * 4;
+    static constexpr int OFF_MISC = OFF_BAR + 24 * 8;
+    static constexpr int THREADS = 448;
     static constexpr int SMEM = OFF_MISC + 64;
     static constexpr int SMEM_ALLOC = SMEM + 1024;
     static constexpr int T_S = 0, T_DP = 64, T_DV = 128, T_DK = 192, T_DQ = 256;
@@ -87,7 +92,7 @@ __device__ __forceinline__ int64_t piece_row(const int32_t *piece_off, int64_t n
 }
 
 template <class T>
-__global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constant__ NsaTcParams p, const PackedGeo geo)
+__global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constant__ NsaTcParams p, const PackedGeo geo)
 {
     using Cfg = NsaCfg;
     constexpr int kType = std::is_same<T, __half>::value ? 0 : 1;
@@ -96,9 +101,11 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
     uint64_t *kv_full = bars + 0, *kv_empty = bars + 1, *q_full = bars + 2, *q_empty = bars + 2 + kNst;
     uint64_t *s_full = bars + 2 + 2 * kNst, *p_ready = s_full + 1, *mma_done = s_full + 2, *drain = s_full + 3;
+    uint64_t *dq_free = s_full + 4;  // the dQ warps have read the dQ accumulator
+    uint64_t *slot_full = s_full + 5, *slot_empty = s_full + 5 + kSlotRing;  // [kSlotRing] token lists
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 8);
-    int32_t *slots = reinterpret_cast<int32_t *>(smem + Cfg::OFF_SLOT);  // [stage][slot][kSlotInts]
+    int32_t *slots = reinterpret_cast<int32_t *>(smem + Cfg::OFF_SLOT);  // [ring][slot][kSlotInts]
     const NsaArgs &a = p.a;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int G = int(a.n1 / a.n2), tpc = kRows / G;  // query heads per kv head, tokens per chunk
@@ -116,6 +123,11 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
         mbar_init(p_ready, 8);
         mbar_init(mma_done, 1);
         mbar_init(drain, 1);
+        mbar_init(dq_free, 4);
+        for (int k = 0; k < kSlotRing; ++k) {
+            mbar_init(&slot_full[k], 1);
+            mbar_init(&slot_empty[k], 8 + 4);  // P / dS warps, dQ warps
+        }
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, Cfg::T_COLS);
@@ -138,15 +150,19 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
     (void)b; (void)g; (void)blk; (void)nchunks;
 
     if (warp == 0) {
-        // ================================================= TMA producer
-        if (elect_one()) {
-            prefetch_tmap(&p.tm_q); prefetch_tmap(&p.tm_do); prefetch_tmap(&p.tm_k); prefetch_tmap(&p.tm_v);
+        // ================================================= TMA producer (the whole warp: lane u
+        // takes token u of a chunk, so the chunk's many small copies are issued in parallel)
+        {
+            if (lane == 0) {
+                prefetch_tmap(&p.tm_q); prefetch_tmap(&p.tm_do); prefetch_tmap(&p.tm_k); prefetch_tmap(&p.tm_v);
+            }
             bool ok = true;
             int64_t kt = 0, ci = 0, q_armed = 0, kv_armed = 0;
             for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
                 NSA_PIECE_DECODE
                 if (kt > 0 && ok && !(ok = mbar_wait(kv_empty, uint32_t(kt - 1) & 1, abort))) flag_abort(abort, a.status);
-                if (ok) {
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok && lane == 0) {
                     kv_armed = kt + 1;
                     const int krow = int(geo.cu_kv[b] + blk * kBS);
                     mbar_arrive_expect_tx(kv_full, 2 * Cfg::KV_BYTES);
@@ -155,47 +171,56 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
                         tma_load_3d(sV + c * kBS * 128, &p.tm_v, kv_full, c * 64, int(g), krow);
                     }
                 }
+                // lane u's token of the next chunk, loaded one chunk ahead
+                int32_t t_next = -1;
+                if (lane < tpc) {
+                    const int64_t idx = tok_begin + lane;
+                    t_next = idx < tok_end ? a.tokens[idx] : -1;
+                }
                 for (int ch = 0; ch < nchunks; ++ch, ++ci) {
-                    const int st = int(ci % kNst);
-                    const int64_t use = ci / kNst;
+                    const int st = int(ci % kNst), rs = int(ci % kSlotRing);
+                    const int64_t use = ci / kNst, ruse = ci / kSlotRing;
                     if (use > 0 && ok && !(ok = mbar_wait(&q_empty[st], uint32_t(use - 1) & 1, abort)))
                         flag_abort(abort, a.status);
+                    if (ruse > 0 && ok && !(ok = mbar_wait(&slot_empty[rs], uint32_t(ruse - 1) & 1, abort)))
+                        flag_abort(abort, a.status);
+                    ok = __all_sync(0xffffffffu, ok);
                     if (!ok) continue;
-                    int32_t *sl = slots + st * kMaxSlots * kSlotInts;
-                    int valid = 0;
-                    for (int u = 0; u < tpc; ++u) {
-                        const int64_t idx = tok_begin + int64_t(ch) * tpc + u;
-                        const int32_t t = idx < tok_end ? a.tokens[idx] : -1;
+                    const int u = lane;  // this lane's token slot
+                    const int32_t t = t_next;
+                    if (u < tpc) {
                         int32_t slot = -1;  // deterministic mode: position of this block in the token's topk
                         if (a.deterministic && t >= 0) {
                             const int32_t *ids = a.topk + (int64_t(t) * a.n2 + g) * a.cnt;
                             for (int64_t c = a.cnt - 1; c >= 0; --c)
                                 if (ids[c] == blk) slot = int32_t(c);
                         }
-                        sl[kSlotInts * u] = t >= 0 ? int32_t(t - geo.cu_q[b]) : -1;
-                        sl[kSlotInts * u + 1] = t;
-                        sl[kSlotInts * u + 2] = slot;
-                        valid += t >= 0;
+                        int32_t *sl = slots + (rs * kMaxSlots + u) * kSlotInts;
+                        sl[0] = t >= 0 ? int32_t(t - geo.cu_q[b]) : -1;
+                        sl[1] = t;
+                        sl[2] = slot;
+                        const int64_t idx = tok_begin + int64_t(ch + 1) * tpc + u;
+                        t_next = idx < tok_end ? a.tokens[idx] : -1;
                     }
-                    q_armed = ci + 1;
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&slot_full[rs]);  // the token list is written
+                        q_armed = ci + 1;
+                        mbar_arrive_expect_tx(&q_full[st], 2 * Cfg::Q_BYTES);
+                    }
+                    __syncwarp();  // the expected bytes are registered before any copy lands
                     uint8_t *sQ = smem + Cfg::OFF_Q + st * Cfg::Q_BYTES, *sdO = smem + Cfg::OFF_DO + st * Cfg::Q_BYTES;
-                    mbar_arrive_expect_tx(&q_full[st], 2 * Cfg::Q_BYTES + uint32_t(valid) * G * 8);
-                    for (int u = 0; u < tpc; ++u) {
-                        const int32_t t = sl[kSlotInts * u + 1];
+                    if (u < tpc) {
                         const int qrow = t >= 0 ? int(int64_t(t) * a.n1 + g * G) : int(a.t1 * a.n1);  // past the end: zeros
                         for (int c = 0; c < kD / 64; ++c) {
                             tma_load_2d(sQ + c * kRows * 128 + u * G * 128, &p.tm_q, &q_full[st], c * 64, qrow);
                             tma_load_2d(sdO + c * kRows * 128 + u * G * 128, &p.tm_do, &q_full[st], c * 64, qrow);
                         }
-                        if (t >= 0) {
-                            bulk_load(smem + Cfg::OFF_LSE + st * kRows * 4 + u * G * 4, a.lse2 + qrow, G * 4, &q_full[st]);
-                            bulk_load(smem + Cfg::OFF_DVEC + st * kRows * 4 + u * G * 4, a.dvec + qrow, G * 4, &q_full[st]);
-                        }
                     }
                 }
                 ++kt;
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 volatile int never = 0;
                 for (int64_t x = q_armed - kNst; x < q_armed; ++x)
                     if (x >= 0) mbar_wait(&q_full[x % kNst], uint32_t(x / kNst) & 1, &never, 100000000ull);
@@ -208,7 +233,11 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
             constexpr uint32_t idS = idesc_f16(128, kBS, kType, 0, 0);     // S, dP
             constexpr uint32_t idT = idesc_f16(128, kBS, kType, 1, 1);     // dV^T, dK^T
             constexpr uint32_t idQ = idesc_f16(128, kD, kType, 0, 1);      // dQ
-            const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP), adS = smem_u32(sdS);
+            // step-0 descriptors (a K step adds a constant to the start address field)
+            const uint64_t kK = desc_kmaj(smem_u32(sK), kBS, 0), kV = desc_kmaj(smem_u32(sV), kBS, 0);
+            const uint64_t mK = desc_mn(smem_u32(sK), kBS, 0);
+            const uint64_t mP = desc_mn(smem_u32(sP), kRows, 0), mdS = desc_mn(smem_u32(sdS), kRows, 0);
+            const uint64_t kdS = desc_kmaj(smem_u32(sdS), kRows, 0);
             bool ok = true;
             int64_t kt = 0, ci = 0;
             for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
@@ -219,27 +248,38 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
                     const int st = int(ci % kNst);
                     const uint32_t aQ = smem_u32(smem + Cfg::OFF_Q + st * Cfg::Q_BYTES);
                     const uint32_t adO = smem_u32(smem + Cfg::OFF_DO + st * Cfg::Q_BYTES);
+                    const uint64_t kQ = desc_kmaj(aQ, kRows, 0), kdO = desc_kmaj(adO, kRows, 0);
+                    const uint64_t mQ = desc_mn(aQ, kRows, 0), mdO = desc_mn(adO, kRows, 0);
                     if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(ci / kNst) & 1, abort))) flag_abort(abort, a.status);
                     tc_fence_after();
                     if (ok) {
+#pragma unroll
                         for (int kk = 0; kk < kD / 16; ++kk)
-                            mma_f16_ss(tmem + Cfg::T_S, desc_kmaj(aQ, kRows, kk), desc_kmaj(aK, kBS, kk), idS, kk > 0);
+                            mma_f16_ss(tmem + Cfg::T_S, kmaj_step(kQ, kRows, kk), kmaj_step(kK, kBS, kk), idS, kk > 0);
+#pragma unroll
                         for (int kk = 0; kk < kD / 16; ++kk)
-                            mma_f16_ss(tmem + Cfg::T_DP, desc_kmaj(adO, kRows, kk), desc_kmaj(aV, kBS, kk), idS, kk > 0);
+                            mma_f16_ss(tmem + Cfg::T_DP, kmaj_step(kdO, kRows, kk), kmaj_step(kV, kBS, kk), idS, kk > 0);
                         mma_commit(s_full);
                     }
                     if (ok && !(ok = mbar_wait(p_ready, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
                     tc_fence_after();
                     if (ok) {
+#pragma unroll
                         for (int kk = 0; kk < kRows / 16; ++kk)
-                            mma_f16_ss(tmem + Cfg::T_DV, desc_mn(adO, kRows, kk), desc_mn(aP, kRows, kk), idT,
-                                       ch > 0 || kk > 0);
+                            mma_f16_ss(tmem + Cfg::T_DV, mn_step(mdO, kk), mn_step(mP, kk), idT, ch > 0 || kk > 0);
+#pragma unroll
                         for (int kk = 0; kk < kRows / 16; ++kk)
-                            mma_f16_ss(tmem + Cfg::T_DK, desc_mn(aQ, kRows, kk), desc_mn(adS, kRows, kk), idT,
-                                       ch > 0 || kk > 0);
+                            mma_f16_ss(tmem + Cfg::T_DK, mn_step(mQ, kk), mn_step(mdS, kk), idT, ch > 0 || kk > 0);
+                    }
+                    // the dQ warps have read the previous chunk's dQ
+                    if (ci > 0 && ok && !(ok = mbar_wait(dq_free, uint32_t(ci - 1) & 1, abort))) flag_abort(abort, a.status);
+                    tc_fence_after();
+                    if (ok) {
+#pragma unroll
                         for (int kk = 0; kk < kBS / 16; ++kk)
-                            mma_f16_ss(tmem + Cfg::T_DQ, desc_kmaj(adS, kRows, kk), desc_mn(aK, kBS, kk), idQ, kk > 0);
+                            mma_f16_ss(tmem + Cfg::T_DQ, kmaj_step(kdS, kRows, kk), mn_step(mK, kk), idQ, kk > 0);
                         mma_commit(mma_done);
+                        mma_commit(&q_empty[st]);  // this Q / dO stage may be refilled
                         if (ch == nchunks - 1) mma_commit(kv_empty);
                     }
                 }
@@ -249,13 +289,12 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
             mma_commit(drain);
             mbar_wait(drain, 0, &never, 100000000ull);
         }
-    } else {
-        // ================================================= P / dS, dQ, dK / dV
+    } else if (warp < 10) {
+        // ================================================= P / dS, and dK / dV at the end of a piece
         const int lg = warp & 3, half = (warp - 2) >> 2;
         const uint32_t lane_addr = uint32_t(lg * 32) << 16;
         const int r = lg * 32 + lane;  // TMEM lane: chunk row (S, dP, dQ) or head dim (dV^T, dK^T)
         const float sc = a.scale * kLog2e;
-        const bool leader = warp == 2 && lane == 0;
         const uint32_t aP = smem_u32(sP), adS = smem_u32(sdS);
         bool ok = true;
         int64_t kt = 0, ci = 0;
@@ -263,25 +302,26 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
             NSA_PIECE_DECODE
             const int64_t shift = geo.kv_len(b) - geo.q_len(b);
             for (int ch = 0; ch < nchunks; ++ch, ++ci) {
-                const int st = int(ci % kNst);
-                if (ok && !(ok = mbar_wait(&q_full[st], uint32_t(ci / kNst) & 1, abort))) flag_abort(abort, a.status);
+                const int rs = int(ci % kSlotRing);
+                // this row's token (empty slot: -1), then its LSE and D straight from the workspace
+                if (ok && !(ok = mbar_wait(&slot_full[rs], uint32_t(ci / kSlotRing) & 1, abort)))
+                    flag_abort(abort, a.status);
+                const int32_t *sl = slots + (rs * kMaxSlots + r / G) * kSlotInts;
+                const int32_t i_loc = ok ? sl[0] : -1, tok = ok ? sl[1] : -1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&slot_empty[rs]);
+                const int64_t qrow = int64_t(tok) * a.n1 + g * G + r % G;
+                const float lse = i_loc < 0 ? INFINITY : a.lse2[qrow];
+                const float dvv = i_loc < 0 ? 0.f : a.dvec[qrow];
                 if (ok && !(ok = mbar_wait(s_full, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
-                const int32_t *sl = slots + st * kMaxSlots * kSlotInts;
                 if (ok) {
-                    // this row's token: empty slot -> everything masked; sparse mode 2 -> keys past
-                    // (local index + S2 - S1) masked
-                    const int32_t i_loc = sl[kSlotInts * (r / G)];
+                    // empty slot -> everything masked; sparse mode 2 -> keys past (local index + S2 - S1) masked
                     const int64_t cmax64 =
                         i_loc < 0 ? -1 : (a.sparse_mode == 2 ? int64_t(i_loc) + shift - blk * kBS : int64_t(kBS));
                     const int cmax = int(cmax64 < -1 ? -1 : (cmax64 > kBS ? kBS : cmax64));
                     const bool any_mask = __any_sync(0xffffffffu, cmax < (half + 1) * 32 - 1);
-                    // an empty slot's stats were never loaded: P = 0 and dS = 0 there by construction
-                    const float lse =
-                        i_loc < 0 ? INFINITY : reinterpret_cast<const float *>(smem + Cfg::OFF_LSE + st * kRows * 4)[r];
-                    const float dvv =
-                        i_loc < 0 ? 0.f : reinterpret_cast<const float *>(smem + Cfg::OFF_DVEC + st * kRows * 4)[r];
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc) {
                         const int col0 = half * 32 + cc * 16;
@@ -314,52 +354,12 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_ready);
-                // ---- dQ of this chunk -> its own (now free) Q / dO stage -> TMA add-reduce per token
-                if (ok && !(ok = mbar_wait(mma_done, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
-                ok = bar_and(1, 256, ok);
-                tc_fence_after();
-                uint8_t *stage_q = smem + Cfg::OFF_Q + st * Cfg::Q_BYTES, *stage_do = smem + Cfg::OFF_DO + st * Cfg::Q_BYTES;
-                if (ok) {
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int box = half * 2 + cc;  // head dims [32 box, 32 box + 32)
-                        uint32_t v[32];
-                        tmem_ld32(tmem + lane_addr + Cfg::T_DQ + box * 32, v);
-                        tmem_ld_wait();
-                        const uint32_t base =
-                            smem_u32(box < 2 ? stage_q + box * (kRows * 128) : stage_do + (box - 2) * (kRows * 128)) +
-                            uint32_t(r * 128);
-#pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4)
-                            st_shared_v4(base + (uint32_t(c4 ^ (r & 7)) << 4), v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
-                                         v[4 * c4 + 3]);
-                    }
-                }
-                fence_proxy_async_smem();
-                named_bar_sync(1, 256);
-                if (leader) {
-                    if (ok) {
-                        for (int u = 0; u < tpc; ++u) {
-                            const int32_t t = sl[kSlotInts * u + 1];
-                            if (t < 0) continue;
-                            const int qrow = int(int64_t(t) * a.n1 + g * G);
-                            // deterministic: its own partial rows, written once (summed in slot order later)
-                            const int prow = int(((int64_t(t) * a.n2 + g) * a.cnt + sl[kSlotInts * u + 2]) * G);
-                            for (int box = 0; box < 4; ++box) {
-                                const uint8_t *src = (box < 2 ? stage_q + box * (kRows * 128)
-                                                              : stage_do + (box - 2) * (kRows * 128)) + u * G * 128;
-                                if (a.deterministic) tma_store_2d(&p.tm_dqpart, src, box * 32, prow);
-                                else tma_reduce_add_2d(&p.tm_dq, src, box * 32, qrow);
-                            }
-                        }
-                        bulk_commit();
-                        bulk_wait_read0();
-                    }
-                    mbar_arrive(&q_empty[st]);  // the stage may be refilled
-                }
             }
-            // ---- dV^T, dK^T of this piece (this thread: head dim r, 32 of the 64 keys)
+            // ---- dV^T, dK^T of this piece (this thread: head dim r, 32 of the 64 keys), once its
+            // last chunk's GEMMs have completed
+            if (ok && !(ok = mbar_wait(mma_done, uint32_t(ci - 1) & 1, abort))) flag_abort(abort, a.status);
             ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
             if (ok) {
                 uint32_t vv[32], kk[32];
                 tmem_ld32(tmem + lane_addr + Cfg::T_DV + half * 32, vv);
@@ -376,7 +376,77 @@ __global__ void __launch_bounds__(320, 1) nsa_bwd_tc_kernel(const __grid_constan
             tc_fence_before();
             ++kt;
         }
-        if (leader) bulk_wait0();
+    } else {
+        // ================================================= dQ of each chunk (warps 10..13)
+        const int lg = warp & 3;
+        const uint32_t lane_addr = uint32_t(lg * 32) << 16;
+        const int r = lg * 32 + lane;        // TMEM lane = chunk row
+        const bool issuer = warp == 10;      // lane u of this warp adds token u's rows
+        uint8_t *sDQS = smem + Cfg::OFF_DQS;
+        const uint32_t aDQS = smem_u32(sDQS);
+        bool ok = true;
+        int64_t ci = 0;
+        for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
+            NSA_PIECE_DECODE
+            for (int ch = 0; ch < nchunks; ++ch, ++ci) {
+                const int rs = int(ci % kSlotRing);
+                if (ok && !(ok = mbar_wait(&slot_full[rs], uint32_t(ci / kSlotRing) & 1, abort)))
+                    flag_abort(abort, a.status);
+                int32_t t = -1, slot = -1;  // this lane's token and its topk position
+                if (ok && issuer && lane < tpc) {
+                    const int32_t *sl = slots + (rs * kMaxSlots + lane) * kSlotInts;
+                    t = sl[1];
+                    slot = sl[2];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&slot_empty[rs]);
+                if (ok && !(ok = mbar_wait(mma_done, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {  // head dims 64 hr .. + 63: two 32-wide boxes
+                    uint32_t v[2][32];
+                    if (ok) {
+                        tmem_ld32(tmem + lane_addr + Cfg::T_DQ + hr * 64, v[0]);
+                        tmem_ld32(tmem + lane_addr + Cfg::T_DQ + hr * 64 + 32, v[1]);
+                        tmem_ld_wait_regs(v[0]);
+                        tmem_ld_wait_regs(v[1]);
+                    }
+                    if (hr == 1) {  // the accumulator has been read out
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(dq_free);
+                    }
+                    if (issuer) bulk_wait_read0();  // this lane's previous adds have read the staging buffer
+                    named_bar_sync(2, 128);
+                    if (ok) {
+#pragma unroll
+                        for (int bx = 0; bx < 2; ++bx) {
+                            const uint32_t base = aDQS + uint32_t(bx * kRows * 128 + r * 128);
+#pragma unroll
+                            for (int c4 = 0; c4 < 8; ++c4)
+                                st_shared_v4(base + (uint32_t(c4 ^ (r & 7)) << 4), v[bx][4 * c4], v[bx][4 * c4 + 1],
+                                             v[bx][4 * c4 + 2], v[bx][4 * c4 + 3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    ok = bar_and(2, 128, ok);
+                    if (ok && issuer && t >= 0) {
+                        const int qrow = int(int64_t(t) * a.n1 + g * G);
+                        // deterministic: its own partial rows, written once (summed in slot order later)
+                        const int prow = int(((int64_t(t) * a.n2 + g) * a.cnt + slot) * G);
+                        for (int bx = 0; bx < 2; ++bx) {
+                            const uint8_t *src = sDQS + bx * (kRows * 128) + lane * G * 128;
+                            const int box = hr * 2 + bx;
+                            if (a.deterministic) tma_store_2d(&p.tm_dqpart, src, box * 32, prow);
+                            else tma_reduce_add_2d(&p.tm_dq, src, box * 32, qrow);
+                        }
+                        bulk_commit();
+                    }
+                }
+            }
+        }
+        if (issuer) bulk_wait0();
     }
 #undef NSA_PIECE_DECODE
 
@@ -513,7 +583,7 @@ cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
     auto k = a.dtype == ATTN_F16 ? nsa_bwd_tc_kernel<__half> : nsa_bwd_tc_kernel<__nv_bfloat16>;
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, NsaCfg::SMEM_ALLOC)) != cudaSuccess)
         return e;
-    k<<<unsigned(nsa_sm_count()), 320, NsaCfg::SMEM_ALLOC, s>>>(prm, g);
+    k<<<unsigned(nsa_sm_count()), NsaCfg::THREADS, NsaCfg::SMEM_ALLOC, s>>>(prm, g);
     return cudaGetLastError();
 }
 
