@@ -53,7 +53,7 @@ struct NsaCfg {
     static constexpr int KV_BYTES = kBS * kD * 2;       // 16 KB
     static constexpr int Q_BYTES = kRows * kD * 2;      // 32 KB
     static constexpr int PS_BYTES = kRows * kBS * 2;    // 16 KB
-    static constexpr int DQS_BYTES = kRows * 64 * 4;    // fp32 dQ, 64 of the 128 head dims (two 32-wide boxes)
+    static constexpr int DQS_BYTES = kRows * 64 * 4;    // fp32 dQ: two buffers of one 32-wide box each
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + KV_BYTES;
     static constexpr int OFF_Q = OFF_V + KV_BYTES;          // kNst stages
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
 #pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {  // head dims 64 hr .. + 63: two 32-wide boxes
+                for (int hr = 0; hr < 2; ++hr) {  // head dims 64 hr .. + 63
                     uint32_t v[2][32];
                     if (ok) {
                         tmem_ld32(tmem + lane_addr + Cfg::T_DQ + hr * 64, v[0]);
@@ -417,31 +417,33 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                         __syncwarp();
                         if (lane == 0) mbar_arrive(dq_free);
                     }
-                    if (issuer) bulk_wait_read0();  // this lane's previous adds have read the staging buffer
-                    named_bar_sync(2, 128);
-                    if (ok) {
 #pragma unroll
-                        for (int bx = 0; bx < 2; ++bx) {
+                    for (int bx = 0; bx < 2; ++bx) {  // one 32-wide box per round, alternating buffers
+                        // the adds issued two rounds ago (same buffer) have read it
+                        if (issuer) bulk_wait_read1();
+                        named_bar_sync(2, 128);
+                        if (ok) {
                             const uint32_t base = aDQS + uint32_t(bx * kRows * 128 + r * 128);
 #pragma unroll
                             for (int c4 = 0; c4 < 8; ++c4)
                                 st_shared_v4(base + (uint32_t(c4 ^ (r & 7)) << 4), v[bx][4 * c4], v[bx][4 * c4 + 1],
                                              v[bx][4 * c4 + 2], v[bx][4 * c4 + 3]);
                         }
-                    }
-                    fence_proxy_async_smem();
-                    ok = bar_and(2, 128, ok);
-                    if (ok && issuer && t >= 0) {
-                        const int qrow = int(int64_t(t) * a.n1 + g * G);
-                        // deterministic: its own partial rows, written once (summed in slot order later)
-                        const int prow = int(((int64_t(t) * a.n2 + g) * a.cnt + slot) * G);
-                        for (int bx = 0; bx < 2; ++bx) {
-                            const uint8_t *src = sDQS + bx * (kRows * 128) + lane * G * 128;
-                            const int box = hr * 2 + bx;
-                            if (a.deterministic) tma_store_2d(&p.tm_dqpart, src, box * 32, prow);
-                            else tma_reduce_add_2d(&p.tm_dq, src, box * 32, qrow);
+                        fence_proxy_async_smem();
+                        ok = bar_and(2, 128, ok);
+                        if (issuer) {
+                            if (ok && t >= 0) {
+                                const int box = hr * 2 + bx;
+                                const uint8_t *src = sDQS + bx * (kRows * 128) + lane * G * 128;
+                                if (a.deterministic) {  // its own partial rows, written once (summed in slot order later)
+                                    const int prow = int(((int64_t(t) * a.n2 + g) * a.cnt + slot) * G);
+                                    tma_store_2d(&p.tm_dqpart, src, box * 32, prow);
+                                } else {
+                                    tma_reduce_add_2d(&p.tm_dq, src, box * 32, int(int64_t(t) * a.n1 + g * G));
+                                }
+                            }
+                            bulk_commit();  // one group per round and lane, possibly empty
                         }
-                        bulk_commit();
                     }
                 }
             }
