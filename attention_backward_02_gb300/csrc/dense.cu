@@ -61,9 +61,13 @@ __device__ __forceinline__ int64_t seq_lse(const DenseArgs &a, const PackedGeo &
     return h * a.t_q + g.cu_q[b] + i;
 }
 
+// Rows of a preprocess / finalize work unit: a quarter of the workspace row
+// alignment, so a unit lies within one sequence and the grid has enough blocks.
+constexpr int kUnitRows = int(kWsRowAlign) / 4;
+
 // ------------------------------------------------------------- preprocess
-// Work unit = (head, 128-row workspace tile); a tile lies within one
-// sequence, so it is located once.  d/8 threads per row (8 elements each),
+// Work unit = (head, 32 workspace rows); a unit lies within one sequence, so
+// it is located once.  d/8 threads per row (8 elements each),
 // 256-thread blocks striding over the units in one resident wave.  Covers
 // every workspace row: padding rows get LSE2 = +inf (so P = 0) and D = 0.
 // Then zeroes every partial dQ buffer.  Launched normally (it overwrites what
@@ -71,18 +75,19 @@ __device__ __forceinline__ int64_t seq_lse(const DenseArgs &a, const PackedGeo &
 template <class T, class Geo, int D>
 __global__ void __launch_bounds__(256) dense_preprocess_kernel(DenseArgs a, Geo geo)
 {
-    constexpr int TPR = D / 8, RPP = 256 / TPR, RPT = int(kWsRowAlign) / RPP;  // rows per pass / per thread
+    constexpr int TPR = D / 8, RPP = 256 / TPR, RPT = kUnitRows / RPP;  // rows per pass / per thread
     pdl_trigger();
     if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
     const int lane_in_row = threadIdx.x % TPR, k0 = threadIdx.x / TPR;
-    const int ntile = int(a.t_pad / kWsRowAlign);
+    const int ntile = int(a.t_pad / kUnitRows);
     const int nunit = int(a.h) * ntile;
     for (int u = blockIdx.x; u < nunit; u += gridDim.x) {
-        const int h = u / ntile, wt = u - h * ntile;
+        // heads fastest: blocks running together read the same tokens' rows (one DRAM page run)
+        const int wt = u / int(a.h), h = u - wt * int(a.h);
         int64_t b = 0, i0 = 0;
-        geo.ws_locate(int64_t(wt) * kWsRowAlign, &b, &i0);
+        geo.ws_locate(int64_t(wt) * kUnitRows, &b, &i0);
         const int64_t lq = geo.q_len(b);
-        const int64_t row0 = int64_t(h) * a.t_pad + int64_t(wt) * kWsRowAlign;
+        const int64_t row0 = int64_t(h) * a.t_pad + int64_t(wt) * kUnitRows;
         uint4 ov[RPT], dv[RPT];  // all loads of this thread first
         float lse[RPT];
 #pragma unroll
@@ -129,18 +134,19 @@ __global__ void __launch_bounds__(256) dense_preprocess_kernel(DenseArgs a, Geo 
 template <class T, class Geo, int D>
 __global__ void __launch_bounds__(256) dq_finalize_kernel(DenseArgs a, Geo geo)
 {
-    constexpr int TPR = D / 8, RPP = 256 / TPR, RPT = int(kWsRowAlign) / RPP;
+    constexpr int TPR = D / 8, RPP = 256 / TPR, RPT = kUnitRows / RPP;
     const int lane_in_row = threadIdx.x % TPR, k0 = threadIdx.x / TPR;
-    const int ntile = int(a.t_pad / kWsRowAlign);
+    const int ntile = int(a.t_pad / kUnitRows);
     const int nunit = int(a.h) * ntile;
     const int64_t part_stride = a.h * a.t_pad * D;
     pdl_wait();
     for (int u = blockIdx.x; u < nunit; u += gridDim.x) {
-        const int h = u / ntile, wt = u - h * ntile;
+        // heads fastest: blocks running together read the same tokens' rows (one DRAM page run)
+        const int wt = u / int(a.h), h = u - wt * int(a.h);
         int64_t b = 0, i0 = 0;
-        geo.ws_locate(int64_t(wt) * kWsRowAlign, &b, &i0);
+        geo.ws_locate(int64_t(wt) * kUnitRows, &b, &i0);
         const int64_t lq = geo.q_len(b);
-        const int64_t row0 = int64_t(h) * a.t_pad + int64_t(wt) * kWsRowAlign;
+        const int64_t row0 = int64_t(h) * a.t_pad + int64_t(wt) * kUnitRows;
         float acc[RPT][8];
 #pragma unroll
         for (int r = 0; r < RPT; ++r)
@@ -287,7 +293,7 @@ unsigned row_grid(const DenseArgs &a)
             sms <= 0)
             sms = 1;
     }
-    const int64_t need = a.h * (a.t_pad / kWsRowAlign);  // (head, 128-row tile) units
+    const int64_t need = a.h * (a.t_pad / kUnitRows);  // (head, 32-row) units
     const int64_t wave = int64_t(sms) * 8;
     return unsigned(need < 1 ? 1 : (need < wave ? need : wave));
 }
