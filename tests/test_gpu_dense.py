@@ -51,6 +51,15 @@ def test_edge_lengths(s_q, s_kv):
     _parity(p)
 
 
+@pytest.mark.parametrize("s_q,s_kv", [(300, 10), (129, 1), (256, 300)])
+def test_edge_lengths_d64(s_q, s_kv):
+    """fp16, d = 64 (128-row query tiles): whole query tiles that no key reaches get dQ = 0 without
+    any contribution being added for them."""
+    p = synth.dense_problem("edge64", dtype=F16, b=2, h=2, h_kv=2, d=64, s_q=s_q, s_kv=s_kv, mask=BR,
+                            seed=s_q * 5 + s_kv)
+    _parity(p)
+
+
 def test_varlen_gqa_small():
     lens = np.array([1, 130, 77, 256, 5, 300])
     p = synth.dense_problem("varlen", dtype=BF16, b=len(lens), h=8, h_kv=2, d=128, lens_q=lens, lens_kv=lens,
