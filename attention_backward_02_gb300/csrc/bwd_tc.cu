@@ -31,10 +31,10 @@
 // i-1's dV GEMM has released the P columns of TMEM.  Q, dO and the LSE / D
 // vectors stream through a 3-stage ring.
 //
-// Roles (320 threads): warp 0 issues TMA loads, warp 1 issues the MMAs,
-// warps 2..9 do the element-wise work (warp w reads TMEM lanes
-// 32 (w % 4) .. + 31; the two warps on the same lanes split the columns), the
-// dQ staging and the dK / dV epilogue.
+// Roles (14 warps): warp 0 issues TMA loads, warp 1 the MMAs, warps 2..9 do
+// the element-wise work (warp w reads TMEM lanes 32 (w % 4) .. + 31; the two
+// warps on the same lanes split the columns), warps 10..13 the dQ staging and
+// the dK / dV epilogue.
 //
 // Causal masking: query tiles entirely before the first query that sees the
 // key tile are skipped; the rest are masked per element when needed.  Key
@@ -571,6 +571,38 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                     }
                 continue;
             }
+            // dK (scaled) and dV of this key tile, once its last GEMMs have completed: read out of TMEM
+            // first (the accumulators are released right after the last read, so the next key tile's
+            // first GEMMs need not wait for the dQ reduce), then stored
+            auto epilogue = [&]() {
+#pragma unroll 1
+                for (int cc = 0; cc < D / 8; ++cc) {
+                    uint32_t w[8], u[8];
+                    if (ok) {
+                        tmem_ld8(tmem + lane_addr + Cfg::T_DV + cc * 8, w);
+                        tmem_ld8(tmem + lane_addr + Cfg::T_DK + cc * 8, u);
+                        tmem_ld_wait_regs(w, u);
+                    }
+                    if (cc == D / 8 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_free);
+                    }
+                    if (ok && row_ok) {
+                        uint4 ov, ok4;
+                        ov.x = pack2<T>(__uint_as_float(w[0]), __uint_as_float(w[1]));
+                        ov.y = pack2<T>(__uint_as_float(w[2]), __uint_as_float(w[3]));
+                        ov.z = pack2<T>(__uint_as_float(w[4]), __uint_as_float(w[5]));
+                        ov.w = pack2<T>(__uint_as_float(w[6]), __uint_as_float(w[7]));
+                        ok4.x = pack2<T>(__uint_as_float(u[0]) * a.scale, __uint_as_float(u[1]) * a.scale);
+                        ok4.y = pack2<T>(__uint_as_float(u[2]) * a.scale, __uint_as_float(u[3]) * a.scale);
+                        ok4.z = pack2<T>(__uint_as_float(u[4]) * a.scale, __uint_as_float(u[5]) * a.scale);
+                        ok4.w = pack2<T>(__uint_as_float(u[6]) * a.scale, __uint_as_float(u[7]) * a.scale);
+                        *reinterpret_cast<uint4 *>(dV + offv + cc * 8) = ov;
+                        *reinterpret_cast<uint4 *>(dK + offk + cc * 8) = ok4;
+                    }
+                }
+            };
             int iq = 0, hg = 0;  // query tile within the head, head within the group
             for (int it = 0; it < n_iter; ++it, ++qi) {
                 const int64_t hq = g * G + hg, i0 = int64_t(qt0 + iq) * BM;
@@ -581,6 +613,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                 if (ok && !(ok = mbar_wait(mma_done, qi & 1, abort))) flag_abort(abort, a.status);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
+                if (it == n_iter - 1) epilogue();
                 // dQ of tile qi, half of its columns at a time, through the staging buffer
                 const int64_t row0 = part * a.h * a.t_pad + geo.ws_start(b) + hq * a.t_pad + i0;
                 // read the whole accumulator first, so the next tile's dQ GEMM is not held up by the
@@ -623,34 +656,6 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                                 tma_reduce_add_2d(&p.tm_dq, sDQS + box * 32 * 128, box * 32, int(row0 + hb * 32));
                         bulk_commit();
                     }
-                }
-            }
-            // ---- dK (scaled) and dV of this key tile: the last tile's GEMMs have completed
-#pragma unroll 1
-            for (int cc = 0; cc < D / 8; ++cc) {
-                uint32_t w[8], u[8];
-                if (ok) {
-                    tmem_ld8(tmem + lane_addr + Cfg::T_DV + cc * 8, w);
-                    tmem_ld8(tmem + lane_addr + Cfg::T_DK + cc * 8, u);
-                    tmem_ld_wait_regs(w, u);
-                }
-                if (cc == D / 8 - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(acc_free);
-                }
-                if (ok && row_ok) {
-                    uint4 ov, ok4;
-                    ov.x = pack2<T>(__uint_as_float(w[0]), __uint_as_float(w[1]));
-                    ov.y = pack2<T>(__uint_as_float(w[2]), __uint_as_float(w[3]));
-                    ov.z = pack2<T>(__uint_as_float(w[4]), __uint_as_float(w[5]));
-                    ov.w = pack2<T>(__uint_as_float(w[6]), __uint_as_float(w[7]));
-                    ok4.x = pack2<T>(__uint_as_float(u[0]) * a.scale, __uint_as_float(u[1]) * a.scale);
-                    ok4.y = pack2<T>(__uint_as_float(u[2]) * a.scale, __uint_as_float(u[3]) * a.scale);
-                    ok4.z = pack2<T>(__uint_as_float(u[4]) * a.scale, __uint_as_float(u[5]) * a.scale);
-                    ok4.w = pack2<T>(__uint_as_float(u[6]) * a.scale, __uint_as_float(u[7]) * a.scale);
-                    *reinterpret_cast<uint4 *>(dV + offv + cc * 8) = ov;
-                    *reinterpret_cast<uint4 *>(dK + offk + cc * 8) = ok4;
                 }
             }
             // deterministic mode: this tile's dQ adds land before the next tile's (fixed order)
