@@ -19,7 +19,9 @@
 //   dQ^T = K^T dS^T (D=128) M=D=128     N=BM=64 K=128 A=K^T (MN-major)     B=dS^T (MN-major)
 // dV, dK stay in TMEM for the whole tile and are written once; each dQ tile
 // is staged in shared memory and added into the fp32 accumulator with a TMA
-// reduce-add.  TMEM: S^T BM + dP^T BM + P^T BM/2 + dV D + dK D + dQ 64 columns
+// reduce-add.  With a single accumulator, each CTA counts itself in a global
+// word once its adds have landed, and when all have, every CTA converts a
+// share of the accumulator into dQ (no separate finalize kernel).  TMEM: S^T BM + dP^T BM + P^T BM/2 + dV D + dK D + dQ 64 columns
 // (512 at D = 64, 480 at D = 128).
 //
 // Pipeline.  The MMA warp issues S/dP of query tile i and then dV/dK/dQ of
@@ -103,9 +105,20 @@ struct TcCfg {
     static_assert(NH == 1 || NH == NG, "release groups");
 };
 
+// Work units of each CTA, chosen on the host (see plan_units).  on = 0: the CTAs
+// take the units in snake order instead.
+constexpr int kSchedCtas = 160;
+constexpr int kSchedUnits = 4096;
+struct TcSched {
+    int32_t on;
+    uint16_t off[kSchedCtas + 1];  // CTA c takes unit[off[c]] .. unit[off[c + 1] - 1], in this order
+    uint16_t unit[kSchedUnits];
+};
+
 struct TcParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq;
     DenseArgs a;
+    TcSched sched;
 };
 
 using namespace tc;
@@ -126,10 +139,86 @@ __device__ __forceinline__ void query_tiles(int mask, int64_t j0, int64_t lq, in
     *nq = int((lq + BM - 1) / BM) - *qt0;
 }
 
+// Unit this CTA takes in its round r, or -1 once it has none left.
+__device__ __forceinline__ int64_t cta_unit(const TcParams &p, int64_t r)
+{
+    if (p.sched.on) {
+        const int k = int(p.sched.off[blockIdx.x]) + int(r);
+        return k < int(p.sched.off[blockIdx.x + 1]) ? int64_t(p.sched.unit[k]) : -1;
+    }
+    const int64_t u = r * gridDim.x + ((r & 1) ? int64_t(gridDim.x) - 1 - blockIdx.x : int64_t(blockIdx.x));
+    return u < p.a.tc_units ? u : -1;
+}
+
 template <class Geo> struct IsPacked : std::false_type {};
 template <> struct IsPacked<PackedGeo> : std::true_type {};
 
 }  // namespace
+
+// dQ = cast(scale * dQacc), run by every CTA of the main kernel once all of
+// them have counted their dQ reduce-adds as landed (the grid is one CTA per
+// SM, all resident, so the wait ends; it is bounded all the same).  A warp
+// converts one (head, 32-row) block of the accumulator at a time, heads
+// fastest, with all its loads in flight before the first store.
+template <class T, int D, int NT, class Geo>
+__device__ __forceinline__ void convert_dq(const DenseArgs &a, const Geo &geo, volatile int *go)
+{
+    constexpr int TPR = D / 8;              // 8-column chunks per row
+    constexpr int RPK = 32 / TPR;           // rows per warp-wide step
+    constexpr int KS = 8;                   // steps in flight per pass
+    constexpr int PASSES = 32 / (RPK * KS); // passes per 32-row block
+    static_assert(PASSES >= 1 && PASSES * RPK * KS == 32, "conversion split");
+    if (threadIdx.x == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        bool ok = true;
+        while (ld_acquire_gpu(a.sync) < gridDim.x) {
+            if (globaltimer_ns() - t0 > 1000000000ull) {
+                ok = false;
+                break;
+            }
+            __nanosleep(200);
+        }
+        if (!ok) raise_flag(a.status, ATTN_DEV_TIMEOUT);
+        *go = ok;
+    }
+    __syncthreads();
+    if (!*go) return;
+    const int lane = threadIdx.x % 32;
+    const uint32_t nw = NT / 32, h = uint32_t(a.h);
+    const uint32_t nunit = h * uint32_t(a.t_pad / 32);
+    const int r_in = lane / TPR, c = lane % TPR;
+    T *dQ = static_cast<T *>(a.dQ.ptr);
+    for (uint32_t u = blockIdx.x * nw + threadIdx.x / 32; u < nunit; u += gridDim.x * nw) {
+        const uint32_t wt = u / h, hh = u - wt * h;
+        int64_t b = 0, i0 = 0;
+        geo.ws_locate(int64_t(wt) * 32, &b, &i0);
+        const int64_t lq = geo.q_len(b);
+        const float *src = a.dqacc + (int64_t(hh) * a.t_pad + int64_t(wt) * 32) * D + c * 8;
+        const int64_t qrow0 = IsPacked<Geo>::value ? geo.q_start(b) : 0;
+        T *dst = dQ + (IsPacked<Geo>::value ? 0 : b * a.dQ.sb) + int64_t(hh) * a.dQ.sh + c * 8;
+#pragma unroll
+        for (int ps = 0; ps < PASSES; ++ps) {
+            float4 v[KS][2];
+#pragma unroll
+            for (int k = 0; k < KS; ++k) {
+                const int r = (ps * KS + k) * RPK + r_in;
+                v[k][0] = __ldcg(reinterpret_cast<const float4 *>(src + int64_t(r) * D));
+                v[k][1] = __ldcg(reinterpret_cast<const float4 *>(src + int64_t(r) * D) + 1);
+            }
+#pragma unroll
+            for (int k = 0; k < KS; ++k) {
+                const int r = (ps * KS + k) * RPK + r_in;
+                if (i0 + r >= lq) continue;
+                uint4 o;
+                o.x = pack2<T>(v[k][0].x * a.scale, v[k][0].y * a.scale);
+                o.y = pack2<T>(v[k][0].z * a.scale, v[k][0].w * a.scale);
+                o.z = pack2<T>(v[k][1].x * a.scale, v[k][1].y * a.scale);
+                o.w = pack2<T>(v[k][1].z * a.scale, v[k][1].w * a.scale);
+                *reinterpret_cast<uint4 *>(dst + (qrow0 + i0 + r) * a.dQ.ss) = o;
+            }
+        }
+    }
+}
 
 template <class T, int D, class Geo>
 __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(const __grid_constant__ TcParams p, const Geo geo)
@@ -189,25 +278,29 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
     // LSE / D and the dQ reduce-adds wait for it (pdl_wait below), the Q / K / V / dO loads do not.
 
     // ---- work units: (sequence b, kv head g) and its key tiles; unit
-    // index = first tile * (nseq * h_kv) + (b * h_kv + g), so for a causal
-    // fixed-length batch the units come heaviest first.  The CTA takes units
-    // c, 2C-1-c, 2C+c, ... (C CTAs), which evens out their total work.
+    // index = first tile * (nseq * h_kv) + (b * h_kv + g).  Each CTA takes
+    // the units the host planned for it (cta_unit).
     const int64_t nheads = a.nseq * a.h_kv;
     const int64_t tile_step = a.deterministic ? a.n_part : INT64_MAX / 2;
     const int G = int(a.h / a.h_kv);
 #define ATTN_FOR_EACH_UNIT                                                                                    \
     for (int64_t round_ = 0;; ++round_) {                                                                     \
-        const int64_t unit = round_ * gridDim.x +                                                             \
-                             ((round_ & 1) ? int64_t(gridDim.x) - 1 - blockIdx.x : int64_t(blockIdx.x));      \
-        if (unit >= a.tc_units) break;                                                                        \
-        const int64_t bg = unit % nheads, first_tile = unit / nheads;                                         \
-        const int64_t b = bg / a.h_kv, g = bg % a.h_kv;                                                       \
+        const int64_t unit = cta_unit(p, round_);                                                             \
+        if (unit < 0) break;                                                                                  \
+        /* 32-bit divisions: the unit count fits (checked at launch) */                                       \
+        const uint32_t ft_ = uint32_t(unit) / uint32_t(nheads), bg_ = uint32_t(unit) - ft_ * uint32_t(nheads);  \
+        const uint32_t b_ = bg_ / uint32_t(a.h_kv);                                                           \
+        const int64_t bg = bg_, first_tile = ft_;                                                             \
+        const int64_t b = b_, g = int64_t(bg_ - b_ * uint32_t(a.h_kv));                                       \
         const int64_t part = a.deterministic ? first_tile : 0;                                                \
         const int64_t lq = geo.q_len(b), lkv = geo.kv_len(b);                                                 \
         const int64_t ntiles = (lkv + BN - 1) / BN;                                                           \
         const int q_b = kPacked ? 0 : int(b), kv_b = q_b;                                                     \
         const int64_t q_row0 = kPacked ? geo.q_start(b) : 0, kv_row0 = kPacked ? geo.kv_start(b) : 0;         \
         (void)part;                                                                                           \
+        (void)bg;                                                                                             \
+        (void)g;                                                                                              \
+        (void)kv_b;                                                                                           \
         (void)q_row0;                                                                                         \
         (void)kv_row0;
 #define ATTN_END_UNITS }
@@ -272,14 +365,13 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                     int nkv_b = kv_b;
                     bool has = njt < ntiles;
                     if (!has) {
-                        const int64_t r2 = round_ + 1;
-                        const int64_t u2 = r2 * gridDim.x +
-                                           ((r2 & 1) ? int64_t(gridDim.x) - 1 - blockIdx.x : int64_t(blockIdx.x));
-                        if (u2 < a.tc_units) {
-                            const int64_t bg2 = u2 % nheads;
-                            nb = bg2 / a.h_kv;
-                            ng = bg2 % a.h_kv;
-                            njt = u2 / nheads;
+                        const int64_t u2 = cta_unit(p, round_ + 1);
+                        if (u2 >= 0) {
+                            const uint32_t njt_ = uint32_t(u2) / uint32_t(nheads);
+                            const uint32_t bg2 = uint32_t(u2) - njt_ * uint32_t(nheads);
+                            nb = bg2 / uint32_t(a.h_kv);
+                            ng = int64_t(bg2) - nb * a.h_kv;
+                            njt = njt_;
                             nrow0 = kPacked ? geo.kv_start(nb) : 0;
                             nkv_b = kPacked ? 0 : int(nb);
                             has = njt * BN < geo.kv_len(nb);
@@ -551,7 +643,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
         T *dK = static_cast<T *>(a.dK.ptr), *dV = static_cast<T *>(a.dV.ptr);
         bool ok = true;
         uint32_t qi = 0;
-        pdl_wait();  // the dQ accumulator has been zeroed
+        pdl_wait();  // the dQ accumulator (and the done count) have been zeroed
 
         ATTN_FOR_EACH_UNIT
         for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
@@ -662,8 +754,15 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
             if (leader && a.deterministic) bulk_wait0();
         }
         ATTN_END_UNITS
-        if (leader) bulk_wait0();
-        pdl_trigger();  // the dQ finalize may start launching; it waits for this grid
+        if (leader) {
+            bulk_wait0();
+            if (a.fuse_fin) {  // publish: this CTA's dQ adds have all landed
+                fence_proxy_async_global();
+                __threadfence();
+                atomicAdd(a.sync, 1u);
+            }
+        }
+        pdl_trigger();  // the dQ finalize (when there is one) may start launching; it waits for this grid
     }
 
 #undef ATTN_FOR_EACH_UNIT
@@ -674,6 +773,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::T_COLS);
     }
+    if (a.fuse_fin) convert_dq<T, D, Cfg::THREADS>(a, geo, reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 16));
 }
 
 // ===================================================================== host
@@ -740,6 +840,57 @@ template <class Geo> int64_t max_kv_len(const Geo &g)
     return m;
 }
 
+// Assigns the work units of a fixed-length batch to `ctas` CTAs, longest first, each to the CTA
+// with the least planned work (a greedy longest-processing-time schedule).  Unit index order is
+// already longest first there.  A unit's cost is its query tiles plus one and a half for its start
+// (loading K / V, filling the pipeline, the dK / dV epilogue), in half tiles.  Leaves on = 0 (snake
+// order) in deterministic mode, for varlen batches (sorted by length, the units running together
+// would be one long sequence's, adding into the same dQ rows) or when the plan does not fit.
+template <int BM, int BN, class Geo>
+void plan_units(TcSched &S, const DenseArgs &a, const Geo &g, int64_t units, int64_t ctas)
+{
+    S.on = 0;
+    if (IsPacked<Geo>::value || a.deterministic || units > kSchedUnits || ctas > kSchedCtas || ctas < 1) return;
+    const int64_t nheads = a.nseq * a.h_kv, G = a.h / a.h_kv;
+    static thread_local uint16_t cta_of[kSchedUnits];
+    uint64_t heap[kSchedCtas];  // min-heap of (planned work << 16 | CTA)
+    uint16_t cnt[kSchedCtas];
+    const int n = int(ctas);
+    for (int c = 0; c < n; ++c) {
+        heap[c] = uint64_t(c);
+        cnt[c] = 0;
+    }
+    for (int64_t u = 0; u < units; ++u) {
+        const int64_t jt = u / nheads, b = (u % nheads) / a.h_kv;
+        const int64_t lq = g.q_len(b), lkv = g.kv_len(b);
+        cta_of[u] = 0xffff;
+        if (jt * BN >= lkv) continue;  // past the keys: nothing to do
+        const int64_t i_lo = first_query_seeing(a.mask, jt * BN, lq, lkv);
+        const int64_t nq = lq <= 0 || i_lo >= lq ? 0 : (lq + BM - 1) / BM - i_lo / BM;
+        const int c = int(heap[0] & 0xffff);
+        cta_of[u] = uint16_t(c);
+        ++cnt[c];
+        heap[0] += uint64_t(2 * G * nq + 3) << 16;
+        for (int i = 0;;) {  // sift the root down
+            const int l = 2 * i + 1, r = l + 1;
+            int m = i;
+            if (l < n && heap[l] < heap[m]) m = l;
+            if (r < n && heap[r] < heap[m]) m = r;
+            if (m == i) break;
+            const uint64_t t = heap[i];
+            heap[i] = heap[m];
+            heap[m] = t;
+            i = m;
+        }
+    }
+    S.off[0] = 0;
+    for (int c = 0; c < n; ++c) S.off[c + 1] = uint16_t(S.off[c] + cnt[c]);
+    for (int c = 0; c < n; ++c) cnt[c] = S.off[c];
+    for (int64_t u = 0; u < units; ++u)
+        if (cta_of[u] != 0xffff) S.unit[cnt[cta_of[u]]++] = uint16_t(u);
+    S.on = 1;
+}
+
 template <class T, int D, class Geo> cudaError_t run_tc(const DenseArgs &a, const Geo &g, cudaStream_t s)
 {
     using Cfg = TcCfg<D>;
@@ -764,7 +915,9 @@ template <class T, int D, class Geo> cudaError_t run_tc(const DenseArgs &a, cons
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     prm.a.tc_units = (a.deterministic ? a.n_part : ntiles) * a.nseq * a.h_kv;
+    if (prm.a.tc_units > INT32_MAX) return cudaErrorInvalidValue;  // the kernel splits units in 32 bits
     const int64_t units = prm.a.tc_units < sm_count() ? prm.a.tc_units : sm_count();
+    plan_units<Cfg::BM, Cfg::BN>(prm.sched, prm.a, g, prm.a.tc_units, units);
     return launch_kernel(k, dim3(unsigned(units)), dim3(Cfg::THREADS), Cfg::SMEM_ALLOC, s, true, prm, g);
 }
 

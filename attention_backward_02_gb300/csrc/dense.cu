@@ -77,7 +77,10 @@ __global__ void __launch_bounds__(256) dense_preprocess_kernel(DenseArgs a, Geo 
 {
     constexpr int TPR = D / 8, RPP = 256 / TPR, RPT = kUnitRows / RPP;  // rows per pass / per thread
     pdl_trigger();
-    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        *a.status = 0u;
+        if (a.sync) *a.sync = 0u;
+    }
     const int lane_in_row = threadIdx.x % TPR, k0 = threadIdx.x / TPR;
     const int ntile = int(a.t_pad / kUnitRows);
     const int nunit = int(a.h) * ntile;

@@ -124,6 +124,18 @@ template <uint32_t N> __device__ __forceinline__ void regs_decrease()
 }
 
 // ------------------------------------------------------------- fences
+// Orders this thread's completed bulk-async (TMA) global writes before its
+// later generic-proxy accesses, e.g. the release that publishes them.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// 32-bit load with acquire semantics at GPU scope.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

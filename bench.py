@@ -296,7 +296,7 @@ def run_ours(args, info):
         ws = torch.empty(ab.sdpa_workspace_size(desc)[1], dtype=torch.uint8, device="cuda")
         inputs = [q, k, v, o, do, lse]
         outputs = [dq, dk, dv]
-        launches_per_step = 3
+        launches_per_step = 2  # preprocess, main kernel (which also converts dQ)
 
         def step():
             ab.sdpa_bwd(desc, vq, vk, vv, vo, vdo, lse, vdq, vdk, vdv, workspace=ws, stream=stream)
