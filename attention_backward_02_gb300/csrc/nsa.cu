@@ -6,7 +6,10 @@
 //
 // Kernels:
 //   nsa_preprocess   LSE2 = (softmaxMax + ln softmaxSum) * log2 e (lane 0 of the
-//                    8-wide stats), D = rowsum(dO * O), zeroed dK/dV accumulators
+//                    8-wide stats), D = rowsum(dO * O); zeroes the block bitmap, the
+//                    dK/dV accumulators and (tensor-core path) the dQ accumulator
+// The kernels after the preprocess are chained with programmatic dependent
+// launch: each waits for its predecessor on entry.
 //   block lists      per (sequence, kv head, block): ascending list of the
 //                    tokens that selected the block and see at least one of
 //                    its keys (bitmap -> count -> scan -> ordered emit), with
@@ -32,9 +35,27 @@ __device__ __forceinline__ int64_t seq_of_token(const PackedGeo &g, int64_t t)
 
 // ------------------------------------------------------------- preprocess
 // grid (ceil(t1_pad / 128), n1), 256 threads, 16 threads per 128-wide row.
+__device__ __forceinline__ void zero_words(uint32_t *p, int64_t n, int64_t tid, int64_t nthr)
+{
+    // 16-byte stores over the 256-byte aligned region, then the tail
+    uint4 *p4 = reinterpret_cast<uint4 *>(p);
+    const int64_t n4 = n / 4;
+    for (int64_t k = tid; k < n4; k += nthr) p4[k] = make_uint4(0, 0, 0, 0);
+    for (int64_t k = n4 * 4 + tid; k < n; k += nthr) p[k] = 0u;
+}
+
 template <class T>
 __global__ void __launch_bounds__(256) nsa_preprocess_kernel(NsaArgs a)
 {
+    pdl_trigger();  // the block lists may start launching; they wait for this grid
+    {   // buffers the later kernels add into
+        const int64_t nthr = int64_t(gridDim.x) * gridDim.y * blockDim.x;
+        const int64_t tid = (int64_t(blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+        zero_words(a.bitmap, a.nrows * a.words_max, tid, nthr);
+        zero_words(reinterpret_cast<uint32_t *>(a.dkacc), a.t2 * a.n2 * a.d, tid, nthr);
+        zero_words(reinterpret_cast<uint32_t *>(a.dvacc), a.t2 * a.n2 * a.d, tid, nthr);
+        if (a.zero_dq) zero_words(reinterpret_cast<uint32_t *>(a.dqacc), a.t1 * a.n1 * a.d, tid, nthr);
+    }
     const int64_t h = blockIdx.y;
     const int lane = threadIdx.x % 16;
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.status = 0u;
@@ -72,6 +93,8 @@ __global__ void __launch_bounds__(256) nsa_preprocess_kernel(NsaArgs a)
 // Mark: one thread per (token, kv head).
 __global__ void nsa_mark_kernel(NsaArgs a, PackedGeo geo)
 {
+    pdl_wait();  // the bitmap has been zeroed
+    pdl_trigger();
     const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= a.t1 * a.n2) return;
     const int64_t t = idx / a.n2, g = idx % a.n2;
@@ -101,6 +124,8 @@ __global__ void nsa_mark_kernel(NsaArgs a, PackedGeo geo)
 // Count: one warp per row; counts land in offsets[row + 1].
 __global__ void nsa_count_kernel(NsaArgs a)
 {
+    pdl_wait();
+    pdl_trigger();
     const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
     const int lane = threadIdx.x % 32;
     if (row >= a.nrows) return;
@@ -116,6 +141,8 @@ __global__ void __launch_bounds__(1024) nsa_scan_kernel(NsaArgs a)
 {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
+    pdl_wait();
+    pdl_trigger();
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
     const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
@@ -148,6 +175,8 @@ __global__ void __launch_bounds__(1024) nsa_scan_kernel(NsaArgs a)
 // Emit: one warp per row walks its bitmap words in order (stable by token).
 __global__ void nsa_emit_kernel(NsaArgs a, PackedGeo geo)
 {
+    pdl_wait();
+    pdl_trigger();
     const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
     const int lane = threadIdx.x % 32;
     if (row >= a.nrows) return;
@@ -177,6 +206,8 @@ __global__ void nsa_emit_kernel(NsaArgs a, PackedGeo geo)
 template <class T>
 __global__ void __launch_bounds__(256) nsa_bwd_simt_kernel(NsaArgs a, PackedGeo geo)
 {
+    pdl_wait();
+    pdl_trigger();
     constexpr int D = 128, LD = D + 1;
     extern __shared__ float smem[];
     const int G = int(a.n1 / a.n2), BS = int(a.bs);
@@ -276,6 +307,8 @@ __global__ void __launch_bounds__(256) nsa_bwd_simt_kernel(NsaArgs a, PackedGeo 
 template <class T>
 __global__ void nsa_dq_finalize_kernel(NsaArgs a)
 {
+    pdl_wait();
+    pdl_trigger();
     const int64_t n = a.t1 * a.n1 * a.d;
     T *dQ = static_cast<T *>(a.dq);
     for (int64_t e = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 4; e < n; e += int64_t(gridDim.x) * blockDim.x * 4) {
@@ -293,6 +326,8 @@ __global__ void nsa_dq_finalize_kernel(NsaArgs a)
 template <class T>
 __global__ void nsa_dq_finalize_det_kernel(NsaArgs a, PackedGeo geo)
 {
+    pdl_wait();
+    pdl_trigger();
     const int64_t rows = a.t1 * a.n1;  // (token, head) rows; 32 threads x 4 floats per row
     const int G = int(a.n1 / a.n2);
     for (int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32; w < rows;
@@ -322,6 +357,7 @@ __global__ void nsa_dq_finalize_det_kernel(NsaArgs a, PackedGeo geo)
 template <class T>
 __global__ void nsa_finalize_kernel(NsaArgs a)
 {
+    pdl_wait();
     const int64_t n = a.t2 * a.n2 * a.d;
     T *dK = static_cast<T *>(a.dk), *dV = static_cast<T *>(a.dv);
     for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += int64_t(gridDim.x) * blockDim.x) {
@@ -331,42 +367,46 @@ __global__ void nsa_finalize_kernel(NsaArgs a)
 }
 
 namespace {
-// bitmap must be zero on entry
-cudaError_t block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
+// bitmap must be zero on entry.  pdl: chained behind a kernel (else behind a memset, ordinarily).
+cudaError_t block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, bool pdl)
 {
-    if (a.t1 > 0) nsa_mark_kernel<<<unsigned((a.t1 * a.n2 + 255) / 256), 256, 0, s>>>(a, g);
+    cudaError_t e = cudaSuccess;
+    if (a.t1 > 0 && (e = launch_kernel(nsa_mark_kernel, dim3(unsigned((a.t1 * a.n2 + 255) / 256)), dim3(256), 0, s,
+                                       pdl, a, g)) != cudaSuccess)
+        return e;
     if (a.nrows > 0) {
-        nsa_count_kernel<<<unsigned((a.nrows * 32 + 255) / 256), 256, 0, s>>>(a);
-        nsa_scan_kernel<<<1, 1024, 0, s>>>(a);
-        nsa_emit_kernel<<<unsigned((a.nrows * 32 + 255) / 256), 256, 0, s>>>(a, g);
+        const dim3 grid(unsigned((a.nrows * 32 + 255) / 256));
+        if ((e = launch_kernel(nsa_count_kernel, grid, dim3(256), 0, s, pdl || a.t1 > 0, a)) != cudaSuccess) return e;
+        if ((e = launch_kernel(nsa_scan_kernel, dim3(1), dim3(1024), 0, s, true, a)) != cudaSuccess) return e;
+        if ((e = launch_kernel(nsa_emit_kernel, grid, dim3(256), 0, s, true, a, g)) != cudaSuccess) return e;
     }
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 template <class T>
-cudaError_t run_nsa(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, cudaEvent_t before, cudaEvent_t after)
+cudaError_t run_nsa(const NsaArgs &a0, const PackedGeo &g, cudaStream_t s, cudaEvent_t before, cudaEvent_t after)
 {
     cudaError_t e;
-    if (a.t1 > 0) {
-        dim3 grid(unsigned((a.t1_pad + 127) / 128), unsigned(a.n1));
+    const bool tc = nsa_tc_supported(a0);
+    NsaArgs a = a0;
+    a.zero_dq = tc && !a.deterministic ? 1 : 0;
+    // the preprocess zeroes the bitmap and the accumulators, so it always runs; the kernels after it
+    // are chained to it with programmatic dependent launch
+    {
+        dim3 grid(unsigned(a.t1 > 0 ? (a.t1_pad + 127) / 128 : 1), unsigned(a.n1));
         nsa_preprocess_kernel<T><<<grid, 256, 0, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    size_t bitmap_bytes = size_t(a.nrows) * size_t(a.words_max) * sizeof(uint32_t);
-    if (bitmap_bytes && (e = cudaMemsetAsync(a.bitmap, 0, bitmap_bytes, s)) != cudaSuccess) return e;
-    size_t acc_bytes = size_t(a.t2) * size_t(a.n2 * a.d) * sizeof(float);
-    if (acc_bytes) {
-        if ((e = cudaMemsetAsync(a.dkacc, 0, acc_bytes, s)) != cudaSuccess) return e;
-        if ((e = cudaMemsetAsync(a.dvacc, 0, acc_bytes, s)) != cudaSuccess) return e;
-    }
-    if ((e = block_lists(a, g, s)) != cudaSuccess) return e;
-    if (nsa_tc_supported(a)) {
-        size_t dq_bytes = size_t(a.t1) * size_t(a.n1 * a.d) * sizeof(float);
-        if (!a.deterministic && dq_bytes && (e = cudaMemsetAsync(a.dqacc, 0, dq_bytes, s)) != cudaSuccess) return e;
+    if ((e = block_lists(a, g, s, true)) != cudaSuccess) return e;
+    if (tc) {
         if (before && (e = cudaEventRecord(before, s)) != cudaSuccess) return e;
         if ((e = launch_nsa_tc(a, g, s)) != cudaSuccess) return e;
         if (after && (e = cudaEventRecord(after, s)) != cudaSuccess) return e;
-        if (a.t1 > 0 && a.deterministic) nsa_dq_finalize_det_kernel<T><<<1024, 256, 0, s>>>(a, g);
-        else if (a.t1 > 0) nsa_dq_finalize_kernel<T><<<1024, 256, 0, s>>>(a);
+        if (a.t1 > 0 && a.deterministic)
+            e = launch_kernel(nsa_dq_finalize_det_kernel<T>, dim3(1024), dim3(256), 0, s, true, a, g);
+        else if (a.t1 > 0)
+            e = launch_kernel(nsa_dq_finalize_kernel<T>, dim3(1024), dim3(256), 0, s, true, a);
+        if (e != cudaSuccess) return e;
     } else if (a.t1 > 0) {
         const int G = int(a.n1 / a.n2), BS = int(a.bs), LD = 129;
         size_t smem = sizeof(float) * (2 * BS * LD + 2 * G * LD + 2 * G * BS + 2 * G);
@@ -374,11 +414,13 @@ cudaError_t run_nsa(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, cudaEv
         if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) != cudaSuccess)
             return e;
         if (before && (e = cudaEventRecord(before, s)) != cudaSuccess) return e;
-        k<<<dim3(unsigned(a.t1), unsigned(a.n2)), 256, smem, s>>>(a, g);
+        if ((e = launch_kernel(k, dim3(unsigned(a.t1), unsigned(a.n2)), dim3(256), smem, s, true, a, g)) != cudaSuccess)
+            return e;
         if (after && (e = cudaEventRecord(after, s)) != cudaSuccess) return e;
     }
-    if (a.t2 > 0) nsa_finalize_kernel<T><<<1024, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    if (a.t2 > 0 && (e = launch_kernel(nsa_finalize_kernel<T>, dim3(1024), dim3(256), 0, s, true, a)) != cudaSuccess)
+        return e;
+    return cudaSuccess;
 }
 }  // namespace
 
@@ -388,7 +430,7 @@ cudaError_t launch_nsa_block_lists(const NsaArgs &a, const PackedGeo &g, cudaStr
     if ((e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s)) != cudaSuccess) return e;
     size_t bitmap_bytes = size_t(a.nrows) * size_t(a.words_max) * sizeof(uint32_t);
     if (bitmap_bytes && (e = cudaMemsetAsync(a.bitmap, 0, bitmap_bytes, s)) != cudaSuccess) return e;
-    return block_lists(a, g, s);
+    return block_lists(a, g, s, false);
 }
 
 cudaError_t launch_nsa_bwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, cudaEvent_t before,

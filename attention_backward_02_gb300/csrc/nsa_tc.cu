@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
     const NsaArgs &a = p.a;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int G = int(a.n1 / a.n2), tpc = kRows / G;  // query heads per kv head, tokens per chunk
+    pdl_wait();     // statistics, block lists, pieces and the zeroed accumulators are ready
+    pdl_trigger();  // the finalize kernels may start launching; they wait for this grid
     const int64_t n_pieces = a.pieces[a.nrows];
 
     if (threadIdx.x == 0) {
@@ -503,6 +505,8 @@ __global__ void __launch_bounds__(1024) nsa_piece_scan_kernel(NsaArgs a)
 {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
+    pdl_wait();  // the block lists are complete
+    pdl_trigger();
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
     const int per_piece = int(a.piece_tokens);
@@ -550,8 +554,7 @@ cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
     const int G = int(a.n1 / a.n2);
     // deterministic: a whole block list per work unit, so every dK / dV element has one writer
     prm.a.piece_tokens = a.deterministic ? (int64_t(1) << 30) : int64_t(kPieceChunks) * (kRows / G);
-    nsa_piece_scan_kernel<<<1, 1024, 0, s>>>(prm.a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_kernel(nsa_piece_scan_kernel, dim3(1), dim3(1024), 0, s, true, prm.a);
     if (e != cudaSuccess) return e;
     if (a.t1 == 0) return cudaSuccess;
     const CUtensorMapDataType dt = a.dtype == ATTN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -585,8 +588,7 @@ cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
     auto k = a.dtype == ATTN_F16 ? nsa_bwd_tc_kernel<__half> : nsa_bwd_tc_kernel<__nv_bfloat16>;
     if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, NsaCfg::SMEM_ALLOC)) != cudaSuccess)
         return e;
-    k<<<unsigned(nsa_sm_count()), NsaCfg::THREADS, NsaCfg::SMEM_ALLOC, s>>>(prm, g);
-    return cudaGetLastError();
+    return launch_kernel(k, dim3(unsigned(nsa_sm_count())), dim3(NsaCfg::THREADS), NsaCfg::SMEM_ALLOC, s, true, prm, g);
 }
 
 }  // namespace attn

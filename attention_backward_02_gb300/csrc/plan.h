@@ -79,6 +79,7 @@ struct NsaArgs {
     int32_t *offsets, *tokens, *pieces;
     float *dqacc, *dkacc, *dvacc, *dqpart;
     int64_t piece_tokens;       // tokens per work unit of the tensor-core kernel (whole lists when deterministic)
+    int zero_dq;                // the preprocess also zeroes dqacc (tensor-core path, atomic dQ)
 };
 
 // ------------------------------------------------------------ launchers

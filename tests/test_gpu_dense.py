@@ -80,6 +80,24 @@ def test_empty_sequence_in_batch():
     _parity(p)
 
 
+@pytest.mark.parametrize("d,mask", [(64, NONE), (64, BR), (128, BR)])
+def test_sequence_without_keys(d, mask):
+    """Varlen batch where one sequence has queries but no keys: its dQ rows are 0 (converted by the
+    main kernel from the accumulator nothing was added to) and the other sequences are unaffected."""
+    lq = np.array([64, 50, 100]); lkv = np.array([64, 0, 100])
+    p = synth.dense_problem("nokeys", dtype=F16, b=3, h=2, h_kv=2, d=d, lens_q=lq, lens_kv=lkv, mask=mask,
+                            seed=13 + d + mask)
+    dq, _, _ = _parity(p)
+    assert not np.any(dq[64:114])
+
+
+def test_no_keys_at_all():
+    """s_kv = 0: the main kernel has no work and does not run; the finalize writes dQ = 0."""
+    p = synth.dense_problem("nokv", dtype=BF16, b=2, h=2, h_kv=1, d=64, s_q=70, s_kv=0, mask=NONE, seed=14)
+    dq, dk, dv = _parity(p)
+    assert not np.any(dq) and dk.size == 0 and dv.size == 0
+
+
 @pytest.mark.parametrize("dq_splits", [0, 3])
 def test_deterministic_mode_bitwise(dq_splits):
     p = synth.dense_problem("det", dtype=BF16, b=2, h=4, h_kv=2, d=128, s_q=520, s_kv=520, mask=TL, seed=11)
