@@ -90,35 +90,35 @@ __global__ void __launch_bounds__(256) nsa_preprocess_kernel(NsaArgs a)
 }
 
 // ------------------------------------------------------------ block lists
-// Mark: one thread per (token, kv head).
+// Mark: one thread per (token, kv head, slot).  A slot that repeats an earlier
+// slot's block is flagged and skipped; the earlier one is kept.
 __global__ void nsa_mark_kernel(NsaArgs a, PackedGeo geo)
 {
     pdl_wait();  // the bitmap has been zeroed
     pdl_trigger();
-    const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (idx >= a.t1 * a.n2) return;
+    const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (gid >= a.t1 * a.n2 * a.cnt) return;
+    const int64_t idx = gid / a.cnt, c = gid - idx * a.cnt;  // (token, kv head), slot
     const int64_t t = idx / a.n2, g = idx % a.n2;
     const int64_t b = seq_of_token(geo, t);
     const int64_t i = t - geo.cu_q[b], lq = geo.q_len(b), lkv = geo.kv_len(b);
     const int64_t nblk = lkv / a.bs;
     const int32_t *ids = a.topk + idx * a.cnt;
-    for (int64_t c = 0; c < a.cnt; ++c) {
-        const int32_t blk = ids[c];
-        if (blk < 0 || blk >= nblk) {
-            raise_flag(a.status, ATTN_DEV_INDEX_RANGE);
-            continue;
-        }
-        bool dup = false;
-        for (int64_t c2 = 0; c2 < c; ++c2) dup |= ids[c2] == blk;
-        if (dup) {
-            raise_flag(a.status, ATTN_DEV_INDEX_DUP);
-            continue;
-        }
-        // the block's first key is the one most likely to be visible
-        if (a.sparse_mode == 2 && !visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, int64_t(blk) * a.bs, lq, lkv)) continue;
-        const int64_t row = (b * a.n2 + g) * a.nblk_max + blk;
-        atomicOr(a.bitmap + row * a.words_max + i / 32, 1u << (i % 32));
+    const int32_t blk = ids[c];
+    if (blk < 0 || blk >= nblk) {
+        raise_flag(a.status, ATTN_DEV_INDEX_RANGE);
+        return;
     }
+    bool dup = false;
+    for (int64_t c2 = 0; c2 < c; ++c2) dup |= ids[c2] == blk;
+    if (dup) {
+        raise_flag(a.status, ATTN_DEV_INDEX_DUP);
+        return;
+    }
+    // the block's first key is the one most likely to be visible
+    if (a.sparse_mode == 2 && !visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, int64_t(blk) * a.bs, lq, lkv)) return;
+    const int64_t row = (b * a.n2 + g) * a.nblk_max + blk;
+    atomicOr(a.bitmap + row * a.words_max + i / 32, 1u << (i % 32));
 }
 
 // Count: one warp per row; counts land in offsets[row + 1].
@@ -172,31 +172,34 @@ __global__ void __launch_bounds__(1024) nsa_scan_kernel(NsaArgs a)
     }
 }
 
-// Emit: one warp per row walks its bitmap words in order (stable by token).
+// Emit: one warp per (row, 32-word segment of its bitmap), in token order
+// within the row; a segment starts after the tokens of the row's earlier words.
 __global__ void nsa_emit_kernel(NsaArgs a, PackedGeo geo)
 {
     pdl_wait();
     pdl_trigger();
-    const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+    const int64_t nseg = (a.words_max + 31) / 32;
+    const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
     const int lane = threadIdx.x % 32;
-    if (row >= a.nrows) return;
+    if (wid >= a.nrows * nseg) return;
+    const int64_t row = wid / nseg, w0 = (wid - row * nseg) * 32;
     const int64_t b = row / (a.n2 * a.nblk_max);
-    int32_t pos = a.offsets[row];
-    for (int64_t w0 = 0; w0 < a.words_max; w0 += 32) {
-        const int64_t w = w0 + lane;
-        uint32_t bits = w < a.words_max ? a.bitmap[row * a.words_max + w] : 0u;
-        int n = __popc(bits), incl = n;
-        for (int off = 1; off < 32; off <<= 1) {
-            int u = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += u;
-        }
-        int32_t my = pos + incl - n;
-        while (bits) {
-            int bit = __ffs(bits) - 1;
-            bits &= bits - 1;
-            a.tokens[my++] = int32_t(geo.cu_q[b] + w * 32 + bit);
-        }
-        pos += __shfl_sync(0xffffffffu, incl, 31);
+    const uint32_t *bits_row = a.bitmap + row * a.words_max;
+    int before = 0;  // tokens of the row's words before this segment
+    for (int64_t w = lane; w < w0; w += 32) before += __popc(bits_row[w]);
+    for (int off = 16; off > 0; off >>= 1) before += __shfl_xor_sync(0xffffffffu, before, off);
+    const int64_t w = w0 + lane;
+    uint32_t bits = w < a.words_max ? bits_row[w] : 0u;
+    int n = __popc(bits), incl = n;
+    for (int off = 1; off < 32; off <<= 1) {
+        int u = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += u;
+    }
+    int32_t my = a.offsets[row] + before + incl - n;
+    while (bits) {
+        int bit = __ffs(bits) - 1;
+        bits &= bits - 1;
+        a.tokens[my++] = int32_t(geo.cu_q[b] + w * 32 + bit);
     }
 }
 
@@ -371,14 +374,16 @@ namespace {
 cudaError_t block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, bool pdl)
 {
     cudaError_t e = cudaSuccess;
-    if (a.t1 > 0 && (e = launch_kernel(nsa_mark_kernel, dim3(unsigned((a.t1 * a.n2 + 255) / 256)), dim3(256), 0, s,
-                                       pdl, a, g)) != cudaSuccess)
+    if (a.t1 > 0 && (e = launch_kernel(nsa_mark_kernel, dim3(unsigned((a.t1 * a.n2 * a.cnt + 255) / 256)), dim3(256), 0,
+                                       s, pdl, a, g)) != cudaSuccess)
         return e;
     if (a.nrows > 0) {
         const dim3 grid(unsigned((a.nrows * 32 + 255) / 256));
         if ((e = launch_kernel(nsa_count_kernel, grid, dim3(256), 0, s, pdl || a.t1 > 0, a)) != cudaSuccess) return e;
         if ((e = launch_kernel(nsa_scan_kernel, dim3(1), dim3(1024), 0, s, true, a)) != cudaSuccess) return e;
-        if ((e = launch_kernel(nsa_emit_kernel, grid, dim3(256), 0, s, true, a, g)) != cudaSuccess) return e;
+        const int64_t nseg = (a.words_max + 31) / 32;
+        const dim3 egrid(unsigned((a.nrows * nseg * 32 + 255) / 256));
+        if ((e = launch_kernel(nsa_emit_kernel, egrid, dim3(256), 0, s, true, a, g)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
