@@ -126,7 +126,11 @@ attn_status_t sdpa_fwd_stats(const attn_sdpa_desc_t *desc, attn_view_t q, attn_v
 /* Backward.  q, o, dO, dQ: [B,h,s_q,d] views; k, v, dK, dV: [B,h_kv,s_kv,d];
  * lse as sdpa_fwd_stats writes it.  dQ / dK / dV may have any strides that
  * follow the 16-byte rule (the sample allocates them empty_like the inputs).
- * Outputs have the input dtype, rounded to nearest even.                    */
+ * Outputs have the input dtype, rounded to nearest even.  In the default
+ * (non-deterministic) mode the main kernel's blocks, one per SM, wait for one
+ * another before converting dQ: they must be able to run at once, as they do
+ * on a device the call has to itself; if they cannot, the wait runs out after
+ * about a second and ATTN_DEV_TIMEOUT is set.                               */
 attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t k, attn_view_t v,
                        attn_view_t o, attn_view_t dO, const float *lse, attn_view_t dQ, attn_view_t dK,
                        attn_view_t dV, void *workspace, size_t workspace_bytes, void *stream);
