@@ -2,8 +2,9 @@
 //
 // Every check runs on the host before the first launch, so a call that
 // returns an error has launched nothing.  Launch order on the caller's
-// stream: preprocess -> main backward -> dQ finalize (dense), and
-// preprocess -> block lists -> main -> finalize (NSA).
+// stream: preprocess -> main backward, which also converts dQ (dense; with split
+// dQ buffers, deterministic mode, a dQ finalize follows), and
+// preprocess -> block lists -> main -> finalizes (NSA).
 #include <cmath>
 #include <cstring>
 

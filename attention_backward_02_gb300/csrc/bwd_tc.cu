@@ -17,21 +17,22 @@
 //   dK  += dS^T Q          M=128        N=D   K=BM   A=dS^T (smem, K-major) B=Q  (MN-major)
 //   dQ   = dS K     (D=64) M=BM=128     N=64  K=128  A=dS (MN-major)       B=K  (MN-major)
 //   dQ^T = K^T dS^T (D=128) M=D=128     N=BM=64 K=128 A=K^T (MN-major)     B=dS^T (MN-major)
-// dV, dK stay in TMEM for the whole tile and are written once; each dQ tile
-// is staged in shared memory and added into the fp32 accumulator with a TMA
-// reduce-add.  With a single accumulator, each CTA counts itself in a global
-// word once its adds have landed, and when all have, every CTA converts a
-// share of the accumulator into dQ (no separate finalize kernel).  TMEM: S^T BM + dP^T BM + P^T BM/2 + dV D + dK D + dQ 64 columns
-// (512 at D = 64, 480 at D = 128).
+// dV, dK stay in TMEM for the whole key tile and are written once; each dQ
+// tile is read out of TMEM, staged in shared memory half a tile at a time and
+// added into the fp32 accumulator with a TMA reduce-add.  With a single
+// accumulator, each CTA counts itself in a global word once its adds have
+// landed, and when all have, every CTA converts a share of the accumulator
+// into dQ (no separate finalize kernel).  TMEM: S^T BM + dP^T BM + P^T BM/2 +
+// dV D + dK D + dQ 64 columns (512 at D = 64, 480 at D = 128).
 //
 // Pipeline.  The MMA warp issues S/dP of query tile i and then dV/dK/dQ of
 // tile i-1, so the tensor cores run tile i-1's three GEMMs while the softmax
 // warps turn tile i's S/dP into P/dS.  Two 32 KB shared buffers alternate
 // per query tile: tile i writes its dS into one while tile i-1's GEMMs read
-// their dS from the other, which, once they complete, stages tile i-1's dQ
-// for the reduce-add.  P (16-bit, packed) waits in registers until tile
+// their dS from the other.  P (16-bit, packed) waits in registers until tile
 // i-1's dV GEMM has released the P columns of TMEM.  Q, dO and the LSE / D
-// vectors stream through a 3-stage ring.
+// vectors stream through a 3-stage ring.  Fixed-length batches take their
+// work units in a longest-first order planned on the host.
 //
 // Roles (14 warps): warp 0 issues TMA loads, warp 1 the MMAs, warps 2..9 do
 // the element-wise work (warp w reads TMEM lanes 32 (w % 4) .. + 31; the two

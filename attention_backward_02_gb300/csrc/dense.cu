@@ -1,6 +1,8 @@
 // dense.cu -- dense SDPA kernels other than the tensor-core backward:
 //   preprocess  (D = rowsum(dO * O), LSE * log2 e, zeroed fp32 dQ accumulator)
-//   dq_finalize (dQ = cast(scale * sum of the partial dQ buffers))
+//   dq_finalize (dQ = cast(scale * sum of the partial dQ buffers); deterministic
+//                mode and calls without keys only: otherwise the main kernel
+//                converts its single dQ buffer itself)
 //   fwd         (O and LSE; CUDA-core kernel, not on the timed path)
 //
 // Definitions: cuDNN-frontend sample "51_scaled_dot_product_attention_backward"

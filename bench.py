@@ -4,8 +4,8 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--w
 
 Default workload 1: dense SDPA backward, fp16, b4 h12 s1024 d64, scale 1/8,
 causal, BSHD storage viewed as BHSD (the GPT-2 sizes of the cuDNN-frontend
-SDPA-backward sample).  A step is one sdpa_bwd call (preprocess, main
-backward, dQ finalize) on inputs resident in HBM; the L2 is flushed between
+SDPA-backward sample).  A step is one sdpa_bwd call (preprocess, then the
+main backward kernel, which also converts dQ) on inputs resident in HBM; the L2 is flushed between
 steps by writing a 512 MB buffer outside the timed events.  FLOPs are
 counted as 10 b h s_q s_kv d, halved for causal; NSA counts
 10 T1 n1 (count * size) d over the selected slots.
