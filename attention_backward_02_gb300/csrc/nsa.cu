@@ -5,11 +5,14 @@
 //   gathered row added back to the key / value row it came from.
 //
 // Kernels:
-//   nsa_preprocess   LSE2 = (softmaxMax + ln softmaxSum) * log2 e (lane 0 of the
-//                    8-wide stats), D = rowsum(dO * O); zeroes the block bitmap, the
-//                    dK/dV accumulators and (tensor-core path) the dQ accumulator
-// The kernels after the preprocess are chained with programmatic dependent
-// launch: each waits for its predecessor on entry.
+//   nsa_init         zeroes the status word and the block bitmap
+//   preprocess       LSE2 = (softmaxMax + ln softmaxSum) * log2 e (lane 0 of the
+//                    8-wide stats), D = rowsum(dO * O); zeroes the dK/dV and
+//                    (tensor-core path) dQ accumulators.  It runs as extra blocks
+//                    of the emit launch, without waiting, so it overlaps the
+//                    block-list kernels.
+// The kernels after init are chained with programmatic dependent launch: each
+// waits for its predecessor on entry (the preprocess blocks excepted).
 //   block lists      per (sequence, kv head, block): ascending list of the
 //                    tokens that selected the block and see at least one of
 //                    its keys (bitmap -> count -> scan -> ordered emit), with
@@ -44,23 +47,24 @@ __device__ __forceinline__ void zero_words(uint32_t *p, int64_t n, int64_t tid, 
     for (int64_t k = n4 * 4 + tid; k < n; k += nthr) p[k] = 0u;
 }
 
+// Blocks of the preprocess: (ceil(t1_pad / 128) x n1) row blocks, 16 threads
+// per 128-wide row; they also zero the accumulators the main kernel adds into.
+inline int64_t nsa_pre_blocks(const NsaArgs &a) { return (a.t1 > 0 ? (a.t1_pad + 127) / 128 : 1) * a.n1; }
+
+// Preprocess block pb of nblk (256 threads).
 template <class T>
-__global__ void __launch_bounds__(256) nsa_preprocess_kernel(NsaArgs a)
+__device__ __forceinline__ void nsa_preprocess_block(const NsaArgs &a, int64_t pb, int64_t nblk)
 {
-    pdl_trigger();  // the block lists may start launching; they wait for this grid
-    {   // buffers the later kernels add into
-        const int64_t nthr = int64_t(gridDim.x) * gridDim.y * blockDim.x;
-        const int64_t tid = (int64_t(blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
-        zero_words(a.bitmap, a.nrows * a.words_max, tid, nthr);
+    {   // buffers the main kernel adds into
+        const int64_t nthr = nblk * blockDim.x, tid = pb * blockDim.x + threadIdx.x;
         zero_words(reinterpret_cast<uint32_t *>(a.dkacc), a.t2 * a.n2 * a.d, tid, nthr);
         zero_words(reinterpret_cast<uint32_t *>(a.dvacc), a.t2 * a.n2 * a.d, tid, nthr);
         if (a.zero_dq) zero_words(reinterpret_cast<uint32_t *>(a.dqacc), a.t1 * a.n1 * a.d, tid, nthr);
     }
-    const int64_t h = blockIdx.y;
+    const int64_t gx = nblk / a.n1, bx = pb % gx, h = pb / gx;
     const int lane = threadIdx.x % 16;
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.status = 0u;
     for (int r = threadIdx.x / 16; r < 128; r += 16) {
-        const int64_t t = int64_t(blockIdx.x) * 128 + r;
+        const int64_t t = bx * 128 + r;
         const bool live = t < a.t1_pad;  // no early exit: the row's threads shuffle below
         const int64_t row = t * a.n1 + h;  // token-major
         float dsum = 0.f;
@@ -89,13 +93,22 @@ __global__ void __launch_bounds__(256) nsa_preprocess_kernel(NsaArgs a)
     }
 }
 
+// Init: the status word and the block bitmap (launched first, ordinarily).
+__global__ void __launch_bounds__(256) nsa_init_kernel(NsaArgs a)
+{
+    pdl_trigger();  // the block lists may start launching; they wait for this grid
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
+    zero_words(a.bitmap, a.nrows * a.words_max, int64_t(blockIdx.x) * blockDim.x + threadIdx.x,
+               int64_t(gridDim.x) * blockDim.x);
+}
+
 // ------------------------------------------------------------ block lists
 // Mark: one thread per (token, kv head, slot).  A slot that repeats an earlier
 // slot's block is flagged and skipped; the earlier one is kept.
 __global__ void nsa_mark_kernel(NsaArgs a, PackedGeo geo)
 {
-    pdl_wait();  // the bitmap has been zeroed
-    pdl_trigger();
+    pdl_trigger();  // the next kernel may be placed now; it waits for this grid before it reads anything
+    pdl_wait();     // the bitmap has been zeroed
     const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (gid >= a.t1 * a.n2 * a.cnt) return;
     const int64_t idx = gid / a.cnt, c = gid - idx * a.cnt;  // (token, kv head), slot
@@ -124,8 +137,8 @@ __global__ void nsa_mark_kernel(NsaArgs a, PackedGeo geo)
 // Count: one warp per row; counts land in offsets[row + 1].
 __global__ void nsa_count_kernel(NsaArgs a)
 {
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
     const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
     const int lane = threadIdx.x % 32;
     if (row >= a.nrows) return;
@@ -141,8 +154,8 @@ __global__ void __launch_bounds__(1024) nsa_scan_kernel(NsaArgs a)
 {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
     const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
@@ -174,10 +187,19 @@ __global__ void __launch_bounds__(1024) nsa_scan_kernel(NsaArgs a)
 
 // Emit: one warp per (row, 32-word segment of its bitmap), in token order
 // within the row; a segment starts after the tokens of the row's earlier words.
-__global__ void nsa_emit_kernel(NsaArgs a, PackedGeo geo)
+// Blocks from emit_blocks on run the preprocess instead (pre = 1): it needs
+// nothing from the block lists, so they do not wait and run while the
+// earlier block-list kernels do; the kernels after this one wait for both.
+template <class T>
+__global__ void __launch_bounds__(256) nsa_emit_kernel(NsaArgs a, PackedGeo geo, int64_t emit_blocks, int pre)
 {
-    pdl_wait();
+    if (int64_t(blockIdx.x) >= emit_blocks) {
+        pdl_trigger();
+        if (pre) nsa_preprocess_block<T>(a, int64_t(blockIdx.x) - emit_blocks, int64_t(gridDim.x) - emit_blocks);
+        return;
+    }
     pdl_trigger();
+    pdl_wait();
     const int64_t nseg = (a.words_max + 31) / 32;
     const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
     const int lane = threadIdx.x % 32;
@@ -371,20 +393,26 @@ __global__ void nsa_finalize_kernel(NsaArgs a)
 
 namespace {
 // bitmap must be zero on entry.  pdl: chained behind a kernel (else behind a memset, ordinarily).
-cudaError_t block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, bool pdl)
+// pre: the emit kernel also runs the preprocess (its extra blocks).
+template <class T>
+cudaError_t block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, bool pdl, bool pre)
 {
     cudaError_t e = cudaSuccess;
     if (a.t1 > 0 && (e = launch_kernel(nsa_mark_kernel, dim3(unsigned((a.t1 * a.n2 * a.cnt + 255) / 256)), dim3(256), 0,
                                        s, pdl, a, g)) != cudaSuccess)
         return e;
+    int64_t emit_blocks = 0;
     if (a.nrows > 0) {
         const dim3 grid(unsigned((a.nrows * 32 + 255) / 256));
         if ((e = launch_kernel(nsa_count_kernel, grid, dim3(256), 0, s, pdl || a.t1 > 0, a)) != cudaSuccess) return e;
         if ((e = launch_kernel(nsa_scan_kernel, dim3(1), dim3(1024), 0, s, true, a)) != cudaSuccess) return e;
-        const int64_t nseg = (a.words_max + 31) / 32;
-        const dim3 egrid(unsigned((a.nrows * nseg * 32 + 255) / 256));
-        if ((e = launch_kernel(nsa_emit_kernel, egrid, dim3(256), 0, s, true, a, g)) != cudaSuccess) return e;
+        emit_blocks = (a.nrows * ((a.words_max + 31) / 32) * 32 + 255) / 256;
     }
+    const int64_t blocks = emit_blocks + (pre ? nsa_pre_blocks(a) : 0);
+    if (blocks > 0 &&
+        (e = launch_kernel(nsa_emit_kernel<T>, dim3(unsigned(blocks)), dim3(256), 0, s, pdl || a.t1 > 0 || a.nrows > 0,
+                           a, g, emit_blocks, pre ? 1 : 0)) != cudaSuccess)
+        return e;
     return cudaSuccess;
 }
 
@@ -395,14 +423,15 @@ cudaError_t run_nsa(const NsaArgs &a0, const PackedGeo &g, cudaStream_t s, cudaE
     const bool tc = nsa_tc_supported(a0);
     NsaArgs a = a0;
     a.zero_dq = tc && !a.deterministic ? 1 : 0;
-    // the preprocess zeroes the bitmap and the accumulators, so it always runs; the kernels after it
-    // are chained to it with programmatic dependent launch
+    // init (status word, bitmap) first, ordinarily; then the block lists with the preprocess riding in
+    // the emit launch; every kernel after init is chained with programmatic dependent launch
     {
-        dim3 grid(unsigned(a.t1 > 0 ? (a.t1_pad + 127) / 128 : 1), unsigned(a.n1));
-        nsa_preprocess_kernel<T><<<grid, 256, 0, s>>>(a);
+        const int64_t words = a.nrows * a.words_max;
+        const unsigned blocks = unsigned(words > 0 ? (words / 4 + 255) / 256 < 1024 ? (words / 4 + 255) / 256 : 1024 : 1);
+        nsa_init_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if ((e = block_lists(a, g, s, true)) != cudaSuccess) return e;
+    if ((e = block_lists<T>(a, g, s, true, true)) != cudaSuccess) return e;
     if (tc) {
         if (before && (e = cudaEventRecord(before, s)) != cudaSuccess) return e;
         if ((e = launch_nsa_tc(a, g, s)) != cudaSuccess) return e;
@@ -435,7 +464,8 @@ cudaError_t launch_nsa_block_lists(const NsaArgs &a, const PackedGeo &g, cudaStr
     if ((e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s)) != cudaSuccess) return e;
     size_t bitmap_bytes = size_t(a.nrows) * size_t(a.words_max) * sizeof(uint32_t);
     if (bitmap_bytes && (e = cudaMemsetAsync(a.bitmap, 0, bitmap_bytes, s)) != cudaSuccess) return e;
-    return block_lists(a, g, s, false);
+    // no preprocess here: the emit kernel's type argument only names an instantiation
+    return block_lists<__nv_bfloat16>(a, g, s, false, false);
 }
 
 cudaError_t launch_nsa_bwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, cudaEvent_t before,
