@@ -329,8 +329,21 @@ __global__ void __launch_bounds__(256) nsa_bwd_simt_kernel(NsaArgs a, PackedGeo 
 }
 
 // dQ = cast(scale * fp32 accumulator), tensor-core path
+// dK, dV = cast(fp32 accumulators), 4 elements per step (the tensor-core path's d = 128).
 template <class T>
-__global__ void nsa_dq_finalize_kernel(NsaArgs a)
+__device__ __forceinline__ void convert_dkdv4(const NsaArgs &a)
+{
+    const int64_t n = a.t2 * a.n2 * a.d;
+    T *dK = static_cast<T *>(a.dk), *dV = static_cast<T *>(a.dv);
+    for (int64_t e = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 4; e < n; e += int64_t(gridDim.x) * blockDim.x * 4) {
+        const float4 k4 = *reinterpret_cast<const float4 *>(a.dkacc + e), v4 = *reinterpret_cast<const float4 *>(a.dvacc + e);
+        *reinterpret_cast<uint2 *>(dK + e) = make_uint2(pack2<T>(k4.x, k4.y), pack2<T>(k4.z, k4.w));
+        *reinterpret_cast<uint2 *>(dV + e) = make_uint2(pack2<T>(v4.x, v4.y), pack2<T>(v4.z, v4.w));
+    }
+}
+
+template <class T>
+__global__ void nsa_dq_finalize_kernel(NsaArgs a, int with_kv)
 {
     pdl_wait();
     pdl_trigger();
@@ -343,13 +356,14 @@ __global__ void nsa_dq_finalize_kernel(NsaArgs a)
         o.y = pack2<T>(v.z * a.scale, v.w * a.scale);
         *reinterpret_cast<uint2 *>(dQ + e) = o;
     }
+    if (with_kv) convert_dkdv4<T>(a);  // dK / dV in the same launch
 }
 
 // Deterministic dQ: per (token, query head) the partial rows of the selected
 // slots, summed in slot order; slots whose block was never processed (out of
 // range, a repeat, or fully masked by sparse mode 2) are skipped.
 template <class T>
-__global__ void nsa_dq_finalize_det_kernel(NsaArgs a, PackedGeo geo)
+__global__ void nsa_dq_finalize_det_kernel(NsaArgs a, PackedGeo geo, int with_kv)
 {
     pdl_wait();
     pdl_trigger();
@@ -377,6 +391,7 @@ __global__ void nsa_dq_finalize_det_kernel(NsaArgs a, PackedGeo geo)
         o.y = pack2<T>(acc.z * a.scale, acc.w * a.scale);
         reinterpret_cast<uint2 *>(static_cast<T *>(a.dq) + w * a.d)[lane] = o;
     }
+    if (with_kv) convert_dkdv4<T>(a);  // dK / dV in the same launch
 }
 
 template <class T>
@@ -436,10 +451,11 @@ cudaError_t run_nsa(const NsaArgs &a0, const PackedGeo &g, cudaStream_t s, cudaE
         if (before && (e = cudaEventRecord(before, s)) != cudaSuccess) return e;
         if ((e = launch_nsa_tc(a, g, s)) != cudaSuccess) return e;
         if (after && (e = cudaEventRecord(after, s)) != cudaSuccess) return e;
+        // the dQ finalize converts dK / dV too (d = 128 here)
         if (a.t1 > 0 && a.deterministic)
-            e = launch_kernel(nsa_dq_finalize_det_kernel<T>, dim3(1024), dim3(256), 0, s, true, a, g);
+            e = launch_kernel(nsa_dq_finalize_det_kernel<T>, dim3(1024), dim3(256), 0, s, true, a, g, 1);
         else if (a.t1 > 0)
-            e = launch_kernel(nsa_dq_finalize_kernel<T>, dim3(1024), dim3(256), 0, s, true, a);
+            e = launch_kernel(nsa_dq_finalize_kernel<T>, dim3(1024), dim3(256), 0, s, true, a, 1);
         if (e != cudaSuccess) return e;
     } else if (a.t1 > 0) {
         const int G = int(a.n1 / a.n2), BS = int(a.bs), LD = 129;
@@ -452,7 +468,8 @@ cudaError_t run_nsa(const NsaArgs &a0, const PackedGeo &g, cudaStream_t s, cudaE
             return e;
         if (after && (e = cudaEventRecord(after, s)) != cudaSuccess) return e;
     }
-    if (a.t2 > 0 && (e = launch_kernel(nsa_finalize_kernel<T>, dim3(1024), dim3(256), 0, s, true, a)) != cudaSuccess)
+    const bool kv_done = tc && a.t1 > 0;  // converted by the dQ finalize
+    if (a.t2 > 0 && !kv_done && (e = launch_kernel(nsa_finalize_kernel<T>, dim3(1024), dim3(256), 0, s, true, a)) != cudaSuccess)
         return e;
     return cudaSuccess;
 }
