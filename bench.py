@@ -248,6 +248,24 @@ def run_reference(args, info):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ rank arithmetic
+
+def slowest_rank_ms(total_ms, dist=None, device="cpu"):
+    """Max over ranks of a rank's summed step time: the replicas' job ends
+    with its slowest rank.  dist: torch.distributed (initialised) or None."""
+    if dist is None:
+        return float(total_ms)
+    import torch
+    t = torch.tensor([float(total_ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_replica, ms_per_step):
+    """Whole-job throughput: every replica's FLOPs over the slowest rank's time per step."""
+    return world * flops_per_replica / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------- GPU arm
 
 def run_ours(args, info):
@@ -343,14 +361,10 @@ def run_ours(args, info):
     torch.cuda.synchronize()
     call_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps)]
     main_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    total_ms = sum(call_ms)
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(sum(call_ms), dist, "cuda")
     assert ab.attn_query_status(ws) == 0, "device status flagged during the timed steps"
     ms_per_step = total_ms / args.steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(world, flops, ms_per_step)
     main_mean = statistics.mean(main_ms)
 
     # ---- end to end through the C ABI with host buffers ----
@@ -372,7 +386,7 @@ def run_ours(args, info):
         a1.synchronize()
         e2e_ms.append(a0.elapsed_time(a1))
         flush.fill_(1)
-    e2e_val = world * flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+    e2e_val = job_tflops(world, flops, statistics.mean(e2e_ms))
 
     if rank != 0:
         if dist:

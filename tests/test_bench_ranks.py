@@ -1,0 +1,42 @@
+"""The multi-GPU path of bench.py runs independent replicas, one per rank, and
+reports the whole job's throughput over the slowest rank's time.  Its rank
+arithmetic runs here on CPU with two gloo ranks."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local_ms = 10.0 * (rank + 1)  # rank 1 is the slow one
+        out[rank] = bench.slowest_rank_ms(local_ms, dist, "cpu")
+    finally:
+        dist.destroy_process_group()
+
+
+def test_slowest_rank_over_two_gloo_ranks():
+    world = 2
+    out = mp.Manager().dict()
+    mp.spawn(_rank, args=(world, _free_port(), out), nprocs=world, join=True)
+    assert out[0] == out[1] == 20.0
+
+
+def test_single_rank_and_job_throughput():
+    assert bench.slowest_rank_ms(7.5) == 7.5
+    flops = 1.0e12  # per replica and step
+    # two replicas, 2 ms per step on the slowest: 2 * 1e12 / 2e-3 s = 1000 TFLOP/s
+    assert bench.job_tflops(2, flops, 2.0) == pytest.approx(1000.0)
+    assert bench.job_tflops(1, flops, 2.0) == pytest.approx(500.0)
