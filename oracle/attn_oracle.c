@@ -48,6 +48,17 @@
  * is the special case cu = {S, 2S, ...}.
  * Query head hq belongs to kv head hq / (h / h_kv).
  * A row with no visible key has O = 0, LSE = +inf and P = 0.
+ *
+ * Parity unpinned (conventions the Ascend page leaves open; no value on any
+ * page fixes them, so no test can pin them):
+ *   - sparse_mode 2 is read as causal bottom-right on the sequence's key
+ *     positions, sparse_mode 0 as no mask beyond the selection;
+ *   - softmaxMax / softmaxSum hold one value per (token, head), replicated
+ *     over their 8 lanes; lane 0 is read;
+ *   - topk block ids are local to the token's sequence (block c covers keys
+ *     [c*bs, c*bs + bs) of that sequence) and must be distinct.
+ * Everything else is pinned by the tests: finite differences, softmax
+ * invariants, closed forms and a second, masked-dense NSA path.
  */
 #include <math.h>
 #include <pthread.h>
