@@ -382,13 +382,16 @@ typedef struct {
 } nsa_ctx;
 
 /* Key rows (local to the sequence) of the selected blocks of (t, g), in the
- * order of topk; returns how many, or -1 on an index out of range.         */
+ * order of topk; returns how many, or -1 on an index out of range or one
+ * that repeats an earlier slot (the gather would count its keys twice).     */
 static int64_t gather_rows(const ora_nsa_t *pb, const int32_t *topk_tg, int64_t lkv, int64_t *rows)
 {
     int64_t n = 0;
     for (int64_t c = 0; c < pb->block_count; ++c) {
         const int64_t blk = topk_tg[c];
         if (blk < 0 || (blk + 1) * pb->block_size > lkv) return -1;
+        for (int64_t e = 0; e < c; ++e)
+            if (topk_tg[e] == blk) return -1;
         for (int64_t r = 0; r < pb->block_size; ++r) rows[n++] = blk * pb->block_size + r;
     }
     return n;
@@ -570,6 +573,7 @@ static void nsa_dense_unit(void *vctx, int64_t unit)
         for (int64_t cc = 0; cc < pb->block_count; ++cc) {
             const int64_t blk = c->topk[(t * pb->n2 + g) * pb->block_count + cc];
             if (blk < 0 || (blk + 1) * pb->block_size > lkv) { c->status = ORA_ERR; continue; }
+            if (sel[blk * pb->block_size]) { c->status = ORA_ERR; continue; } /* block already selected */
             for (int64_t r = 0; r < pb->block_size; ++r) sel[blk * pb->block_size + r] = 1;
         }
         for (int64_t j = 0; j < lkv; ++j) sel[j] = sel[j] && nsa_visible(pb, i, j, lq, lkv);

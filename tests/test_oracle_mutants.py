@@ -27,6 +27,21 @@ MUTANTS = [
      "c->dk[((k0 + r) * pb->n2 + g) * d + x] += dksel[r * d + x];", "nsa_fd"),
     ("nsa_sum_ignored", "const double p = exp(pb->scale * dot(qi, ksel + r * d, d) - mx) / sm;",
      "const double p = exp(pb->scale * dot(qi, ksel + r * d, d) - mx);", "nsa_fd"),
+    ("dq_no_scale", "dqi[x] += pb->scale * ds * kj[x];", "dqi[x] += ds * kj[x];", "dense_fd"),
+    ("dv_from_q", "dvj[x] += p * doi[x];", "dvj[x] += p * qi[x];", "dense_fd"),
+    ("lse_without_max", "const double lse = mx + log(sum);", "const double lse = log(sum);", "two_keys"),
+    # query heads of a kv head taken interleaved (h_kv apart) instead of contiguous, in the forward only
+    ("gqa_interleaved", "for (int64_t hq = g * G; hq < (g + 1) * G; ++hq) {",
+     "for (int64_t hq = g; hq < pb->h; hq += pb->h_kv) {", "dense_fd_gqa"),
+    ("seq_boundary", "if (t < cu[b]) return b;", "if (t <= cu[b]) return b;", "sampled_rows"),
+    ("nsa_block_offset", "rows[n++] = blk * pb->block_size + r;", "rows[n++] = blk + r;", "nsa_vs_dense"),
+    ("nsa_D_from_dO", "const double mx = c->mx[row], sm = c->sm[row];\n            const double Di = dot(doi, oi, d);",
+     "const double mx = c->mx[row], sm = c->sm[row];\n            const double Di = dot(doi, doi, d);", "nsa_fd"),
+    ("nsa_dk_no_scale", "dksel[r * d + x] += pb->scale * ds * qi[x];", "dksel[r * d + x] += ds * qi[x];",
+     "nsa_fd"),
+    ("block_lists_last_key", "nsa_visible(pb, i, blk * pb->block_size, lq, lkv)",
+     "nsa_visible(pb, i, blk * pb->block_size + pb->block_size - 1, lq, lkv)", "block_lists"),
+    ("repeat_accepted", "            if (topk_tg[e] == blk) return -1;\n", "", "nsa_repeat"),
 ]
 
 
@@ -49,6 +64,18 @@ def _run_pin(pin):
             pins.test_mask_bitmaps(mask, key)
     elif pin == "nsa_fd":
         pins.test_nsa_finite_differences(0)
+    elif pin == "two_keys":
+        pins.test_two_keys_closed_form()
+    elif pin == "dense_fd_gqa":
+        pins.test_dense_finite_differences_varlen_gqa(oracle.MASK_NONE)
+    elif pin == "sampled_rows":
+        pins.test_sampled_rows_equal_full()
+    elif pin == "nsa_vs_dense":
+        pins.test_nsa_gather_equals_masked_dense(0)
+    elif pin == "block_lists":
+        pins.test_nsa_block_lists_definition(2)
+    elif pin == "nsa_repeat":
+        pins.check_nsa_rejects_repeated_index()
     else:
         raise ValueError(pin)
 

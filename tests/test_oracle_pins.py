@@ -230,7 +230,8 @@ def test_sampled_rows_equal_full():
     o, lse = oracle.dense_fwd(q, k, v, cu, cu, 0.4, CAUSAL_TOP_LEFT)
     o = o + 0.01 * rng.standard_normal(o.shape)  # formula mode: O as supplied
     dq, dk, dv = oracle.dense_bwd(q, k, v, o, do, lse, cu, cu, 0.4, CAUSAL_TOP_LEFT)
-    qr = np.array([0, 5, 17, 40, 79]); kr = np.array([0, 3, 20, 39])
+    # rows of both sequences, including the last token of the first (6) and the first of the second (7)
+    qr = np.array([0, 5, 17, 27, 29, 40, 79]); kr = np.array([0, 3, 12, 15, 20, 39])
     sdq, sdk, sdv = oracle.dense_bwd_rows(q, k, v, o, do, lse, cu, cu, 0.4, CAUSAL_TOP_LEFT, qr, kr)
     np.testing.assert_allclose(sdq, dq.reshape(-1, d)[qr], rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(sdk, dk.reshape(-1, d)[kr], rtol=1e-13, atol=1e-15)
@@ -348,6 +349,29 @@ def test_nsa_rejects_out_of_range_index():
     topk = topk.copy(); topk[3, 0, 1] = 4  # blocks of 2 keys: valid ids are 0..3
     with pytest.raises(ValueError):
         oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.8, 2, 0)
+
+
+def check_nsa_rejects_repeated_index():
+    """A block id repeated within one (token, kv head) would count its keys
+    twice under the gather: every NSA entry point refuses it."""
+    cu_q, cu_kv, q, k, v, do, topk = _nsa_random([8], [8], 2, 1, 3, 2, 2, 0, seed=23)
+    topk = topk.copy(); topk[3, 0, 1] = topk[3, 0, 0]
+    o, mx, sm = np.zeros_like(q), np.ones(q.shape[:2]), np.ones(q.shape[:2])
+    calls = {
+        "nsa_fwd": lambda: oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.8, 2, 0),
+        "nsa_bwd": lambda: oracle.nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, 0.8, 2, 0),
+        "nsa_masked_dense": lambda: oracle.nsa_masked_dense(q, k, v, do, topk, cu_q, cu_kv, 0.8, 2, 0),
+    }
+    for name, call in calls.items():
+        try:
+            call()
+        except ValueError:
+            continue
+        raise AssertionError(f"{name} accepted a repeated block id")
+
+
+def test_nsa_rejects_repeated_index():
+    check_nsa_rejects_repeated_index()
 
 
 @pytest.mark.parametrize("sparse_mode", [0, 2])
