@@ -281,7 +281,6 @@ def run_ours(args, info):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    ab._lib.load()
     lib = ab._lib.load()
     stream = torch.cuda.current_stream()
     nsa = isinstance(p, synth.NsaProblem)
