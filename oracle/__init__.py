@@ -12,7 +12,9 @@ float64 in token-major (TND) layout:
     lse, max, sum: [Tq, h]        topk         : [Tq, h_kv, cnt] int32
 
 Sequences are inclusive cumulative lengths without a leading zero (the form
-of the Ascend page's actualSeqQLen / actualSeqKvLen).
+of the Ascend page's actualSeqQLen / actualSeqKvLen).  In the NSA functions
+value, O and dO may have a head dim of their own (the page allows the value
+head dim to differ from the query / key one); it is read off v's shape.
 """
 from __future__ import annotations
 
@@ -53,7 +55,8 @@ class _Dense(C.Structure):
 class _Nsa(C.Structure):
     _fields_ = [("nseq", C.c_int64), ("cu_q", C.POINTER(C.c_int64)), ("cu_kv", C.POINTER(C.c_int64)),
                 ("n1", C.c_int64), ("n2", C.c_int64), ("d", C.c_int64), ("scale", C.c_double),
-                ("block_size", C.c_int64), ("block_count", C.c_int64), ("sparse_mode", C.c_int)]
+                ("block_size", C.c_int64), ("block_count", C.c_int64), ("sparse_mode", C.c_int),
+                ("d_v", C.c_int64)]
 
 
 def _load():
@@ -139,10 +142,17 @@ def dense_bwd_rows(q, k, v, o, do, lse, cu_q, cu_kv, scale, mask, q_rows, kv_row
     return dq, dk, dv
 
 
-def _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, bs, cnt, sparse_mode):
+def _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, bs, cnt, sparse_mode, d_v=0):
     return _Nsa(len(cu_q), cu_q.ctypes.data_as(C.POINTER(C.c_int64)),
                 cu_kv.ctypes.data_as(C.POINTER(C.c_int64)), n1, n2, d, float(scale), bs, cnt,
-                int(sparse_mode))
+                int(sparse_mode), int(d_v))
+
+
+def _nsa_dims(q, k, v):
+    """(d, d_v): query / key head dim and value head dim (the Ascend page lets them differ)."""
+    if k.shape[2] != q.shape[2]:
+        raise ValueError("query and key head dims differ")
+    return q.shape[2], v.shape[2]
 
 
 def _i32(a):
@@ -157,10 +167,11 @@ def nsa_fwd(q, k, v, topk, cu_q, cu_kv, scale, block_size, sparse_mode, threads=
     """Sparse forward: O [T1,n1,d], softmaxMax [T1,n1], softmaxSum [T1,n1]."""
     q, k, v, topk = _f64(q), _f64(k), _f64(v), _i32(topk)
     cu_q, cu_kv = _cu(cu_q), _cu(cu_kv)
-    t1, n1, d = q.shape
+    t1, n1, _ = q.shape
+    d, dv_ = _nsa_dims(q, k, v)
     n2, cnt = k.shape[1], topk.shape[2]
-    o = np.empty_like(q); mx = np.empty((t1, n1)); sm = np.empty((t1, n1))
-    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode)
+    o = np.empty((t1, n1, dv_)); mx = np.empty((t1, n1)); sm = np.empty((t1, n1))
+    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode, dv_)
     rc = _load().ora_nsa_fwd(C.byref(desc), _d(q), _d(k), _d(v), _ip(topk), _d(o), _d(mx), _d(sm),
                              int(threads))
     if rc:
@@ -173,10 +184,13 @@ def nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, scale, block_size, sparse
     q, k, v, o, do, mx, sm = (_f64(x) for x in (q, k, v, o, do, mx, sm))
     topk = _i32(topk)
     cu_q, cu_kv = _cu(cu_q), _cu(cu_kv)
-    _, n1, d = q.shape
+    _, n1, _ = q.shape
+    d, dv_ = _nsa_dims(q, k, v)
+    if o.shape[2] != dv_ or do.shape[2] != dv_:
+        raise ValueError("attentionOut and its gradient must have the value head dim")
     n2, cnt = k.shape[1], topk.shape[2]
     dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
-    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode)
+    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode, dv_)
     rc = _load().ora_nsa_bwd(C.byref(desc), _d(q), _d(k), _d(v), _d(o), _d(do), _d(mx), _d(sm),
                              _ip(topk), _d(dq), _d(dk), _d(dv), int(threads))
     if rc:
@@ -188,10 +202,13 @@ def nsa_masked_dense(q, k, v, do, topk, cu_q, cu_kv, scale, block_size, sparse_m
     """Independent NSA path: masked dense attention, own softmax; returns o, dq, dk, dv."""
     q, k, v, do, topk = _f64(q), _f64(k), _f64(v), _f64(do), _i32(topk)
     cu_q, cu_kv = _cu(cu_q), _cu(cu_kv)
-    _, n1, d = q.shape
+    t1, n1, _ = q.shape
+    d, dv_ = _nsa_dims(q, k, v)
+    if do.shape[2] != dv_:
+        raise ValueError("the gradient of attentionOut must have the value head dim")
     n2, cnt = k.shape[1], topk.shape[2]
-    o, dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(k), np.empty_like(v)
-    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode)
+    o, dq, dk, dv = np.empty((t1, n1, dv_)), np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode, dv_)
     rc = _load().ora_nsa_masked_dense(C.byref(desc), _d(q), _d(k), _d(v), _d(do), _ip(topk),
                                       _d(o), _d(dq), _d(dk), _d(dv), int(threads))
     if rc:

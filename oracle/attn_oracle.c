@@ -42,6 +42,8 @@
  *
  * Layout of every tensor here (fp64): token-major "TND"
  *   q, o, dO, dq : [Tq][h][d]      k, v, dk, dv : [Tkv][h_kv][d]
+ *   (NSA: v, dv, o and dO have the value head dim d_v, which the Ascend
+ *   page's constraints let differ from the query / key head dim d)
  *   lse, max, sum: [Tq][h]         topk         : [Tq][h_kv][cnt] (int32)
  * Sequences are given by inclusive cumulative lengths (no leading zero), as
  * the Ascend page's actualSeqQLen / actualSeqKvLen are.  A fixed-length batch
@@ -93,7 +95,12 @@ typedef struct {
     int64_t block_count;   /* selectedBlockCount                                */
     int sparse_mode;       /* 0: no mask beyond the selection; 2: causal
                               bottom-right on the sequence's key positions      */
+    int64_t d_v;           /* head dim of value, attentionOut and dY (the page
+                              allows it to differ from the query / key head
+                              dim d); 0: equal to d                             */
 } ora_nsa_t;
+
+static int64_t value_dim(const ora_nsa_t *pb) { return pb->d_v > 0 ? pb->d_v : pb->d; }
 
 static int64_t seq_start(const int64_t *cu, int64_t b) { return b == 0 ? 0 : cu[b - 1]; }
 static int64_t seq_len(const int64_t *cu, int64_t b) { return cu[b] - seq_start(cu, b); }
@@ -407,13 +414,13 @@ static void nsa_fwd_unit(void *vctx, int64_t unit)
 {
     nsa_ctx *c = (nsa_ctx *)vctx;
     const ora_nsa_t *pb = c->pb;
-    const int64_t b = unit / pb->n2, g = unit % pb->n2, G = pb->n1 / pb->n2, d = pb->d;
+    const int64_t b = unit / pb->n2, g = unit % pb->n2, G = pb->n1 / pb->n2, d = pb->d, e = value_dim(pb);
     const int64_t q0 = seq_start(pb->cu_q, b), lq = seq_len(pb->cu_q, b);
     const int64_t k0 = seq_start(pb->cu_kv, b), lkv = seq_len(pb->cu_kv, b);
     const int64_t nsel = pb->block_count * pb->block_size;
     int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)nsel);
     double *ksel = (double *)malloc(sizeof(double) * (size_t)(nsel * d));
-    double *vsel = (double *)malloc(sizeof(double) * (size_t)(nsel * d));
+    double *vsel = (double *)malloc(sizeof(double) * (size_t)(nsel * e));
     double *s = (double *)malloc(sizeof(double) * (size_t)nsel);
     for (int64_t i = 0; i < lq; ++i) {
         const int64_t t = q0 + i;
@@ -422,29 +429,28 @@ static void nsa_fwd_unit(void *vctx, int64_t unit)
             continue;
         }
         /* selectedKey = Gather(key, topk), selectedValue = Gather(value, topk) */
-        for (int64_t r = 0; r < nsel; ++r)
-            for (int64_t x = 0; x < d; ++x) {
-                ksel[r * d + x] = c->k[((k0 + rows[r]) * pb->n2 + g) * d + x];
-                vsel[r * d + x] = c->v[((k0 + rows[r]) * pb->n2 + g) * d + x];
-            }
+        for (int64_t r = 0; r < nsel; ++r) {
+            for (int64_t x = 0; x < d; ++x) ksel[r * d + x] = c->k[((k0 + rows[r]) * pb->n2 + g) * d + x];
+            for (int64_t x = 0; x < e; ++x) vsel[r * e + x] = c->v[((k0 + rows[r]) * pb->n2 + g) * e + x];
+        }
         for (int64_t hq = g * G; hq < (g + 1) * G; ++hq) {
             const int64_t row = t * pb->n1 + hq;
             const double *qi = c->q + row * d;
-            double *oi = c->o_out + row * d;
+            double *oi = c->o_out + row * e;
             double mx = -INFINITY, sum = 0.0;
             for (int64_t r = 0; r < nsel; ++r) {
                 if (!nsa_visible(pb, i, rows[r], lq, lkv)) continue;
                 s[r] = pb->scale * dot(qi, ksel + r * d, d);
                 if (s[r] > mx) mx = s[r];
             }
-            for (int64_t x = 0; x < d; ++x) oi[x] = 0.0;
+            for (int64_t x = 0; x < e; ++x) oi[x] = 0.0;
             if (mx != -INFINITY) {
                 for (int64_t r = 0; r < nsel; ++r)
                     if (nsa_visible(pb, i, rows[r], lq, lkv)) sum += exp(s[r] - mx);
                 for (int64_t r = 0; r < nsel; ++r) {
                     if (!nsa_visible(pb, i, rows[r], lq, lkv)) continue;
                     const double p = exp(s[r] - mx) / sum;
-                    for (int64_t x = 0; x < d; ++x) oi[x] += p * vsel[r * d + x];
+                    for (int64_t x = 0; x < e; ++x) oi[x] += p * vsel[r * e + x];
                 }
             }
             c->mx_out[row] = mx;
@@ -460,58 +466,59 @@ static void nsa_bwd_unit(void *vctx, int64_t unit)
 {
     nsa_ctx *c = (nsa_ctx *)vctx;
     const ora_nsa_t *pb = c->pb;
-    const int64_t b = unit / pb->n2, g = unit % pb->n2, G = pb->n1 / pb->n2, d = pb->d;
+    const int64_t b = unit / pb->n2, g = unit % pb->n2, G = pb->n1 / pb->n2, d = pb->d, e = value_dim(pb);
     const int64_t q0 = seq_start(pb->cu_q, b), lq = seq_len(pb->cu_q, b);
     const int64_t k0 = seq_start(pb->cu_kv, b), lkv = seq_len(pb->cu_kv, b);
     const int64_t nsel = pb->block_count * pb->block_size;
     int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)nsel);
     double *ksel = (double *)malloc(sizeof(double) * (size_t)(nsel * d));
-    double *vsel = (double *)malloc(sizeof(double) * (size_t)(nsel * d));
+    double *vsel = (double *)malloc(sizeof(double) * (size_t)(nsel * e));
     double *dksel = (double *)malloc(sizeof(double) * (size_t)(nsel * d));
-    double *dvsel = (double *)malloc(sizeof(double) * (size_t)(nsel * d));
-    for (int64_t j = 0; j < lkv; ++j)
-        for (int64_t x = 0; x < d; ++x) {
-            c->dk[((k0 + j) * pb->n2 + g) * d + x] = 0.0;
-            c->dv[((k0 + j) * pb->n2 + g) * d + x] = 0.0;
-        }
+    double *dvsel = (double *)malloc(sizeof(double) * (size_t)(nsel * e));
+    for (int64_t j = 0; j < lkv; ++j) {
+        for (int64_t x = 0; x < d; ++x) c->dk[((k0 + j) * pb->n2 + g) * d + x] = 0.0;
+        for (int64_t x = 0; x < e; ++x) c->dv[((k0 + j) * pb->n2 + g) * e + x] = 0.0;
+    }
     for (int64_t i = 0; i < lq; ++i) {
         const int64_t t = q0 + i;
         if (gather_rows(pb, c->topk + (t * pb->n2 + g) * pb->block_count, lkv, rows) < 0) {
             c->status = ORA_ERR;
             continue;
         }
-        for (int64_t r = 0; r < nsel; ++r)
+        for (int64_t r = 0; r < nsel; ++r) {
             for (int64_t x = 0; x < d; ++x) {
                 ksel[r * d + x] = c->k[((k0 + rows[r]) * pb->n2 + g) * d + x];
-                vsel[r * d + x] = c->v[((k0 + rows[r]) * pb->n2 + g) * d + x];
                 dksel[r * d + x] = 0.0;
-                dvsel[r * d + x] = 0.0;
             }
+            for (int64_t x = 0; x < e; ++x) {
+                vsel[r * e + x] = c->v[((k0 + rows[r]) * pb->n2 + g) * e + x];
+                dvsel[r * e + x] = 0.0;
+            }
+        }
         for (int64_t hq = g * G; hq < (g + 1) * G; ++hq) {
             const int64_t row = t * pb->n1 + hq;
-            const double *qi = c->q + row * d, *oi = c->o + row * d, *doi = c->dout + row * d;
+            const double *qi = c->q + row * d, *oi = c->o + row * e, *doi = c->dout + row * e;
             double *dqi = c->dq + row * d;
             const double mx = c->mx[row], sm = c->sm[row];
-            const double Di = dot(doi, oi, d);
+            const double Di = dot(doi, oi, e);
             for (int64_t x = 0; x < d; ++x) dqi[x] = 0.0;
             if (mx == -INFINITY || sm == 0.0) continue; /* no visible key */
             for (int64_t r = 0; r < nsel; ++r) {
                 if (!nsa_visible(pb, i, rows[r], lq, lkv)) continue;
                 const double p = exp(pb->scale * dot(qi, ksel + r * d, d) - mx) / sm;
-                const double ds = p * (dot(doi, vsel + r * d, d) - Di);
+                const double ds = p * (dot(doi, vsel + r * e, e) - Di);
                 for (int64_t x = 0; x < d; ++x) {
                     dqi[x] += pb->scale * ds * ksel[r * d + x];
                     dksel[r * d + x] += pb->scale * ds * qi[x];
-                    dvsel[r * d + x] += p * doi[x];
                 }
+                for (int64_t x = 0; x < e; ++x) dvsel[r * e + x] += p * doi[x];
             }
         }
         /* scatter the gathered gradients back through the indices */
-        for (int64_t r = 0; r < nsel; ++r)
-            for (int64_t x = 0; x < d; ++x) {
-                c->dk[((k0 + rows[r]) * pb->n2 + g) * d + x] += dksel[r * d + x];
-                c->dv[((k0 + rows[r]) * pb->n2 + g) * d + x] += dvsel[r * d + x];
-            }
+        for (int64_t r = 0; r < nsel; ++r) {
+            for (int64_t x = 0; x < d; ++x) c->dk[((k0 + rows[r]) * pb->n2 + g) * d + x] += dksel[r * d + x];
+            for (int64_t x = 0; x < e; ++x) c->dv[((k0 + rows[r]) * pb->n2 + g) * e + x] += dvsel[r * e + x];
+        }
     }
     free(rows); free(ksel); free(vsel); free(dksel); free(dvsel);
 }
@@ -519,6 +526,7 @@ static void nsa_bwd_unit(void *vctx, int64_t unit)
 static int nsa_check(const ora_nsa_t *pb)
 {
     if (!pb || pb->n2 <= 0 || pb->n1 % pb->n2 || pb->block_size <= 0 || pb->block_count <= 0) return ORA_ERR;
+    if (pb->d <= 0 || pb->d_v < 0) return ORA_ERR;
     if (pb->sparse_mode != 0 && pb->sparse_mode != 2) return ORA_ERR;
     return ORA_OK;
 }
@@ -557,16 +565,15 @@ static void nsa_dense_unit(void *vctx, int64_t unit)
 {
     nsa_ctx *c = (nsa_ctx *)vctx;
     const ora_nsa_t *pb = c->pb;
-    const int64_t b = unit / pb->n2, g = unit % pb->n2, G = pb->n1 / pb->n2, d = pb->d;
+    const int64_t b = unit / pb->n2, g = unit % pb->n2, G = pb->n1 / pb->n2, d = pb->d, e = value_dim(pb);
     const int64_t q0 = seq_start(pb->cu_q, b), lq = seq_len(pb->cu_q, b);
     const int64_t k0 = seq_start(pb->cu_kv, b), lkv = seq_len(pb->cu_kv, b);
     char *sel = (char *)malloc((size_t)(lkv > 0 ? lkv : 1));
     double *p = (double *)malloc(sizeof(double) * (size_t)(lkv > 0 ? lkv : 1));
-    for (int64_t j = 0; j < lkv; ++j)
-        for (int64_t x = 0; x < d; ++x) {
-            c->dk[((k0 + j) * pb->n2 + g) * d + x] = 0.0;
-            c->dv[((k0 + j) * pb->n2 + g) * d + x] = 0.0;
-        }
+    for (int64_t j = 0; j < lkv; ++j) {
+        for (int64_t x = 0; x < d; ++x) c->dk[((k0 + j) * pb->n2 + g) * d + x] = 0.0;
+        for (int64_t x = 0; x < e; ++x) c->dv[((k0 + j) * pb->n2 + g) * e + x] = 0.0;
+    }
     for (int64_t i = 0; i < lq; ++i) {
         const int64_t t = q0 + i;
         memset(sel, 0, (size_t)lkv);
@@ -579,37 +586,38 @@ static void nsa_dense_unit(void *vctx, int64_t unit)
         for (int64_t j = 0; j < lkv; ++j) sel[j] = sel[j] && nsa_visible(pb, i, j, lq, lkv);
         for (int64_t hq = g * G; hq < (g + 1) * G; ++hq) {
             const int64_t row = t * pb->n1 + hq;
-            const double *qi = c->q + row * d, *doi = c->dout + row * d;
-            double *oi = c->o_out + row * d, *dqi = c->dq + row * d;
+            const double *qi = c->q + row * d, *doi = c->dout + row * e;
+            double *oi = c->o_out + row * e, *dqi = c->dq + row * d;
             double mx = -INFINITY, sum = 0.0;
             for (int64_t j = 0; j < lkv; ++j) {
                 if (!sel[j]) continue;
                 p[j] = pb->scale * dot(qi, c->k + ((k0 + j) * pb->n2 + g) * d, d);
                 if (p[j] > mx) mx = p[j];
             }
-            for (int64_t x = 0; x < d; ++x) oi[x] = dqi[x] = 0.0;
+            for (int64_t x = 0; x < e; ++x) oi[x] = 0.0;
+            for (int64_t x = 0; x < d; ++x) dqi[x] = 0.0;
             if (mx == -INFINITY) continue;
             for (int64_t j = 0; j < lkv; ++j)
                 if (sel[j]) sum += exp(p[j] - mx);
             for (int64_t j = 0; j < lkv; ++j) {
                 if (!sel[j]) continue;
                 p[j] = exp(p[j] - mx) / sum;
-                const double *vj = c->v + ((k0 + j) * pb->n2 + g) * d;
-                for (int64_t x = 0; x < d; ++x) oi[x] += p[j] * vj[x];
+                const double *vj = c->v + ((k0 + j) * pb->n2 + g) * e;
+                for (int64_t x = 0; x < e; ++x) oi[x] += p[j] * vj[x];
             }
-            const double Di = dot(doi, oi, d);
+            const double Di = dot(doi, oi, e);
             for (int64_t j = 0; j < lkv; ++j) {
                 if (!sel[j]) continue;
                 const double *kj = c->k + ((k0 + j) * pb->n2 + g) * d;
-                const double *vj = c->v + ((k0 + j) * pb->n2 + g) * d;
+                const double *vj = c->v + ((k0 + j) * pb->n2 + g) * e;
                 double *dkj = c->dk + ((k0 + j) * pb->n2 + g) * d;
-                double *dvj = c->dv + ((k0 + j) * pb->n2 + g) * d;
-                const double ds = p[j] * (dot(doi, vj, d) - Di);
+                double *dvj = c->dv + ((k0 + j) * pb->n2 + g) * e;
+                const double ds = p[j] * (dot(doi, vj, e) - Di);
                 for (int64_t x = 0; x < d; ++x) {
                     dqi[x] += pb->scale * ds * kj[x];
                     dkj[x] += pb->scale * ds * qi[x];
-                    dvj[x] += p[j] * doi[x];
                 }
+                for (int64_t x = 0; x < e; ++x) dvj[x] += p[j] * doi[x];
             }
         }
     }

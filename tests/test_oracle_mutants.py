@@ -35,13 +35,18 @@ MUTANTS = [
      "for (int64_t hq = g; hq < pb->h; hq += pb->h_kv) {", "dense_fd_gqa"),
     ("seq_boundary", "if (t < cu[b]) return b;", "if (t <= cu[b]) return b;", "sampled_rows"),
     ("nsa_block_offset", "rows[n++] = blk * pb->block_size + r;", "rows[n++] = blk + r;", "nsa_vs_dense"),
-    ("nsa_D_from_dO", "const double mx = c->mx[row], sm = c->sm[row];\n            const double Di = dot(doi, oi, d);",
-     "const double mx = c->mx[row], sm = c->sm[row];\n            const double Di = dot(doi, doi, d);", "nsa_fd"),
+    ("nsa_D_from_dO", "const double mx = c->mx[row], sm = c->sm[row];\n            const double Di = dot(doi, oi, e);",
+     "const double mx = c->mx[row], sm = c->sm[row];\n            const double Di = dot(doi, doi, e);", "nsa_fd"),
+    # the value head dim mistaken for the query / key one (d < d_v in the pin, so reads stay in bounds)
+    ("nsa_D_over_qk_dim", "const double mx = c->mx[row], sm = c->sm[row];\n            const double Di = dot(doi, oi, e);",
+     "const double mx = c->mx[row], sm = c->sm[row];\n            const double Di = dot(doi, oi, d);", "nsa_fd_dims"),
+    ("nsa_dv_scatter_stride", "c->dv[((k0 + rows[r]) * pb->n2 + g) * e + x] += dvsel[r * e + x];",
+     "c->dv[((k0 + rows[r]) * pb->n2 + g) * d + x] += dvsel[r * e + x];", "nsa_fd_dims"),
     ("nsa_dk_no_scale", "dksel[r * d + x] += pb->scale * ds * qi[x];", "dksel[r * d + x] += ds * qi[x];",
      "nsa_fd"),
     ("block_lists_last_key", "nsa_visible(pb, i, blk * pb->block_size, lq, lkv)",
      "nsa_visible(pb, i, blk * pb->block_size + pb->block_size - 1, lq, lkv)", "block_lists"),
-    ("repeat_accepted", "            if (topk_tg[e] == blk) return -1;\n", "", "nsa_repeat"),
+    ("repeat_accepted", "if (topk_tg[e] == blk) return -1;", "if (topk_tg[e] == blk && 0) return -1;", "nsa_repeat"),
 ]
 
 
@@ -76,6 +81,8 @@ def _run_pin(pin):
         pins.test_nsa_block_lists_definition(2)
     elif pin == "nsa_repeat":
         pins.check_nsa_rejects_repeated_index()
+    elif pin == "nsa_fd_dims":
+        pins.test_nsa_finite_differences_unequal_dims(2)
     else:
         raise ValueError(pin)
 

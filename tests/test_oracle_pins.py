@@ -333,6 +333,53 @@ def test_nsa_finite_differences(sparse_mode):
         assert np.abs(fd - g).max() <= 1e-7 * max(1.0, np.abs(fd).max()), name
 
 
+def _nsa_random_dims(lens_q, lens_kv, n1, n2, d, d_v, bs, cnt, sparse_mode, seed):
+    """As _nsa_random, with value / O / dO head dim d_v != d (the Ascend page allows 192 / 128)."""
+    cu_q, cu_kv, q, k, _, _, topk = _nsa_random(lens_q, lens_kv, n1, n2, d, bs, cnt, sparse_mode, seed)
+    rng = _rng(seed + 1000)
+    v = rng.standard_normal((cu_kv[-1], n2, d_v)); do = rng.standard_normal((cu_q[-1], n1, d_v))
+    return cu_q, cu_kv, q, k, v, do, topk
+
+
+@pytest.mark.parametrize("sparse_mode", [0, 2])
+def test_nsa_finite_differences_unequal_dims(sparse_mode):
+    """Query / key head dim 2, value head dim 3: every gradient against central differences."""
+    cu_q, cu_kv, q, k, v, do, topk = _nsa_random_dims([8, 6], [8, 6], 4, 2, 2, 3, 2, 2, sparse_mode, seed=25)
+    o, mx, sm = oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.8, 2, sparse_mode, threads=1)
+    assert o.shape == (cu_q[-1], 4, 3)
+    dq, dk, dv = oracle.nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, 0.8, 2, sparse_mode, threads=1)
+    assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == v.shape
+
+    def loss():
+        oo, _, _ = oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.8, 2, sparse_mode, threads=1)
+        return float((oo * do).sum())
+
+    for name, x, g in (("dq", q, dq), ("dk", k, dk), ("dv", v, dv)):
+        fd = _fd_grad(loss, x)
+        assert np.abs(fd - g).max() <= 1e-7 * max(1.0, np.abs(fd).max()), name
+
+
+@pytest.mark.parametrize("sparse_mode", [0, 2])
+def test_nsa_gather_equals_masked_dense_unequal_dims(sparse_mode):
+    cu_q, cu_kv, q, k, v, do, topk = _nsa_random_dims([64, 40], [64, 48], 8, 2, 24, 16, 8, 3, sparse_mode,
+                                                        seed=26)
+    o, mx, sm = oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.3, 8, sparse_mode)
+    got = oracle.nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, 0.3, 8, sparse_mode)
+    od, *ref = oracle.nsa_masked_dense(q, k, v, do, topk, cu_q, cu_kv, 0.3, 8, sparse_mode)
+    assert _rel(o, od) < 1e-12
+    for a, b in zip(got, ref):
+        assert _rel(a, b) < 1e-12
+
+
+def test_nsa_rejects_mismatched_head_dims():
+    cu_q, cu_kv, q, k, v, do, topk = _nsa_random_dims([8], [8], 2, 1, 4, 3, 2, 2, 0, seed=27)
+    with pytest.raises(ValueError):
+        oracle.nsa_fwd(q, k[..., :3], v, topk, cu_q, cu_kv, 0.8, 2, 0)  # key head dim != query head dim
+    o, mx, sm = oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.8, 2, 0)
+    with pytest.raises(ValueError):
+        oracle.nsa_bwd(q, k, v, o, do[..., :2], mx, sm, topk, cu_q, cu_kv, 0.8, 2, 0)  # dY not value-dim
+
+
 @pytest.mark.parametrize("sparse_mode", [0, 2])
 def test_nsa_gather_equals_masked_dense(sparse_mode):
     cu_q, cu_kv, q, k, v, do, topk = _nsa_random([64, 40], [64, 48], 8, 2, 16, 8, 3, sparse_mode, seed=22)
