@@ -40,3 +40,14 @@ def test_single_rank_and_job_throughput():
     # two replicas, 2 ms per step on the slowest: 2 * 1e12 / 2e-3 s = 1000 TFLOP/s
     assert bench.job_tflops(2, flops, 2.0) == pytest.approx(1000.0)
     assert bench.job_tflops(1, flops, 2.0) == pytest.approx(500.0)
+
+
+def test_time_repeated_reaches_the_minimum():
+    """The CPU-baseline timer repeats a short sample until the minimum time has passed."""
+    import time
+    import bench
+    calls = []
+    n, dt = bench.time_repeated(lambda: (calls.append(1), time.sleep(0.01)), 0.05)
+    assert n == len(calls) and n >= 5 and dt >= 0.05
+    n, dt = bench.time_repeated(lambda: time.sleep(0.02), 0.0)
+    assert n == 1  # always at least once
