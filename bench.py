@@ -223,6 +223,14 @@ def cpu_sample(p, target_s):
     return oracle_dense_sample(p, rows)
 
 
+def affinity_count():
+    """Host cores this process may run on (the oracle's threads use the online count)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 def time_repeated(run, min_s, max_runs=10000):
     """Calls run() until at least min_s seconds have passed (at least once); returns (runs, seconds)."""
     n, t0 = 0, time.perf_counter()
@@ -254,7 +262,7 @@ def run_reference(args, info):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.thread_count(), "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, "affinity": affinity_count()},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -444,7 +452,8 @@ def run_ours(args, info):
         run, cflops, desc_s = cpu_sample(p, 10.0)
         nrun, dt = time_repeated(run, 10.0)  # about 10 s of CPU work, repeating a sample smaller than that
         line["cpu_baseline"] = {"value": cflops * nrun / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.thread_count(),
-                                "kind": "oracle", "sample": f"{desc_s}; run {nrun} time(s)", "seconds": dt}
+                                "kind": "oracle", "sample": f"{desc_s}; run {nrun} time(s)", "seconds": dt,
+                                "affinity": affinity_count()}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
