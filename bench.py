@@ -428,7 +428,8 @@ def run_ours(args, info):
     traffic = profile_traffic(f"{tag}_workload{args.workload}")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": statistics.median(call_ms),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16" if p.dtype == synth.F16 else "bf16", "data": "synthetic",
         "config": dict(cfg, l2="flushed: 512 MB buffer written between timed steps, outside the events",
                        inputs="N(0,1) seeded; O and stats from the library forward" if not nsa else
