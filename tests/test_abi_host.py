@@ -109,6 +109,55 @@ def test_nsa_descriptor_rejections(ab, kw, code):
     assert ab._lib.load().nsa_workspace_size(C.byref(_nsa(ab, **kw)), C.byref(n)) == code
 
 
+def test_fwd_rejects_before_launch(ab):
+    lib = ab._lib.load()
+    d = _desc(ab)
+    v = ab.attn_view_t(0x10000, 8 * 1024 * 12 * 64, 64, 12 * 64)
+    lse = C.cast(C.c_void_p(0x20000), C.POINTER(C.c_float))
+    call = lambda view=v, lse=lse, ws=0x100000, nbytes=256: lib.sdpa_fwd_stats(
+        C.byref(d), view, view, view, view, lse, C.c_void_p(ws), C.c_size_t(nbytes), None)
+    assert call(lse=None) == 1                                               # no stats output
+    assert call(view=ab.attn_view_t(0x10004, v.sb, v.sh, v.ss)) == 5        # misaligned base
+    assert call(nbytes=16) == 4                                              # short workspace
+    assert call(ws=0) == 4                                                   # no workspace
+
+
+def test_nsa_bwd_rejects_before_launch(ab):
+    lib = ab._lib.load()
+    desc = _nsa(ab)
+    n = C.c_size_t()
+    assert lib.nsa_workspace_size(C.byref(desc), C.byref(n)) == 0
+    fp = lambda a: C.cast(C.c_void_p(a), C.POINTER(C.c_float))
+    ip = lambda a: C.cast(C.c_void_p(a), C.POINTER(C.c_int32))
+
+    def call(q=0x10000, dq=0x30000, topk=0x40000, smax=0x50000, ws=0x100000, nbytes=None):
+        t = [C.c_void_p(q)] + [C.c_void_p(0x10000)] * 4
+        return lib.nsa_selected_attn_bwd(C.byref(desc), *t, fp(smax), fp(0x60000), ip(topk), C.c_void_p(dq),
+                                         C.c_void_p(0x70000), C.c_void_p(0x80000), C.c_void_p(ws),
+                                         C.c_size_t(n.value if nbytes is None else nbytes), None)
+    assert call(q=0) == 1                 # NULL query
+    assert call(dq=0x30008) == 5          # misaligned gradient
+    assert call(topk=0x40002) == 5        # topk not 4-byte aligned
+    assert call(smax=0x50004) == 5        # stats not 16-byte aligned
+    assert call(nbytes=n.value - 1) == 4  # short workspace
+    assert call(ws=0) == 4                # no workspace
+
+
+def test_static_scratch_rejects_large_problems(ab):
+    """A problem whose workspace exceeds the static scratch is refused before anything runs."""
+    d = _desc(ab, b=2, h=32, h_kv=32, s_q=4096, s_kv=4096, d=128, dtype=ab.ATTN_BF16)
+    v = ab.attn_view_t(0x10000, 4096 * 32 * 128, 128, 32 * 128)
+    lse = C.cast(C.c_void_p(0x20000), C.POINTER(C.c_float))
+    assert ab._lib.load().sdpa_bwd_static_scratch(C.byref(d), v, v, v, v, v, lse, v, v, v, None) == 4
+
+
+def test_query_status_needs_its_pointers(ab):
+    lib = ab._lib.load()
+    flags = C.c_uint32()
+    assert lib.attn_query_status(None, None, C.byref(flags)) == 1
+    assert lib.attn_query_status(C.c_void_p(0x100000), None, None) == 1
+
+
 def test_status_strings(ab):
     for code in range(8):
         assert ab._lib.load().attn_status_string(code).startswith(b"ATTN_")
