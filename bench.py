@@ -204,6 +204,14 @@ def oracle_nsa_sample(p, tokens=None):
     return run, flops, f"sequence 0, last {t} of {L} tokens, all {p.n1} heads, fp64"
 
 
+def sample_threads(p):
+    """Threads the oracle runs a cpu_sample of p on: it splits its work into (sequence, kv head) units,
+    one thread per unit at most, and a sample covers one sequence."""
+    import oracle
+    units = p.n2 if isinstance(p, synth.NsaProblem) else p.h_kv
+    return max(1, min(oracle.thread_count(), int(units)))
+
+
 def cpu_sample(p, target_s):
     """A sample of the workload whose oracle run takes about target_s."""
     if isinstance(p, synth.NsaProblem):
@@ -261,8 +269,8 @@ def run_reference(args, info):
             "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
             "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.thread_count(), "kind": "oracle",
-                             "sample": desc, "affinity": affinity_count()},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": sample_threads(p), "kind": "oracle",
+                             "sample": desc, "affinity": affinity_count(), "host_threads": oracle.thread_count()},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -452,7 +460,8 @@ def run_ours(args, info):
         import oracle
         run, cflops, desc_s = cpu_sample(p, 10.0)
         nrun, dt = time_repeated(run, 10.0)  # about 10 s of CPU work, repeating a sample smaller than that
-        line["cpu_baseline"] = {"value": cflops * nrun / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.thread_count(),
+        line["cpu_baseline"] = {"value": cflops * nrun / dt / 1e12, "unit": "TFLOP/s", "cores": sample_threads(p),
+                                "host_threads": oracle.thread_count(),
                                 "kind": "oracle", "sample": f"{desc_s}; run {nrun} time(s)", "seconds": dt,
                                 "affinity": affinity_count()}
     print(json.dumps(line), flush=True)

@@ -51,3 +51,11 @@ def test_time_repeated_reaches_the_minimum():
     assert n == len(calls) and n >= 5 and dt >= 0.05
     n, dt = bench.time_repeated(lambda: time.sleep(0.02), 0.0)
     assert n == 1  # always at least once
+
+
+def test_sample_threads_counts_what_the_oracle_uses():
+    """The oracle runs one thread per (sequence, kv head) unit at most; a CPU sample covers one sequence."""
+    import oracle
+    import synth
+    assert bench.sample_threads(synth.workload(1)) == min(oracle.thread_count(), 12)
+    assert bench.sample_threads(synth.workload(4)) == 1
