@@ -164,71 +164,71 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_dense_sample(p, rows_per_head=None, batch=0):
-    """One batch element, every head, query rows [s - r, s) against keys
-    [0, s): causal bottom-right sub-problem of workload p.  Returns the
-    callable and its FLOPs by the same 10 d per visible pair convention."""
+def _last_rows(cu, n):
+    """Indices of the last min(n, length) tokens of every sequence (inclusive cumulative lengths), and
+    how many each sequence gave."""
+    starts = np.concatenate([[0], cu[:-1]])
+    take = np.minimum(cu - starts, n)
+    idx = np.concatenate([np.arange(e - t, e) for e, t in zip(cu, take)]) if len(cu) else np.zeros(0, np.int64)
+    return idx.astype(np.int64), take.astype(np.int64)
+
+
+def oracle_dense_sample(p, rows=None):
+    """The last `rows` query rows of every sequence, every head, against all of that sequence's keys.
+    With bottom-right alignment each of those rows sees exactly the keys it sees in p (whose causal
+    workloads have equal query and key lengths, or are bottom-right already).  Returns the callable,
+    its FLOPs (10 d per visible pair, the metric's convention), a description and its (sequence,
+    kv head) unit count."""
     import oracle
-    s, d = p.s_q, p.d
-    r = s if rows_per_head is None else max(1, min(s, int(rows_per_head)))
-    t0 = batch * s
-    q = p.f64("q")[t0 + s - r: t0 + s]
-    do = p.f64("do")[t0 + s - r: t0 + s]
-    k = p.f64("k")[batch * p.s_kv: batch * p.s_kv + s]
-    v = p.f64("v")[batch * p.s_kv: batch * p.s_kv + s]
+    idx, take = _last_rows(p.cu_q, p.s_q if rows is None else max(1, int(rows)))
+    lkv = p.cu_kv - np.concatenate([[0], p.cu_kv[:-1]])
+    q, do = p.f64("q")[idx], p.f64("do")[idx]
+    k, v = p.f64("k"), p.f64("v")
+    cu_q = np.cumsum(take)
     mask = oracle.CAUSAL_BOTTOM_RIGHT if p.mask else oracle.MASK_NONE
-    o, lse = oracle.dense_fwd(q, k, v, [r], [s], p.scale, mask)
-    pairs = sum(range(s - r + 1, s + 1)) if p.mask else r * s
-    flops = 10.0 * p.h * pairs * d
+    o, lse = oracle.dense_fwd(q, k, v, cu_q, p.cu_kv, p.scale, mask)
+    if p.mask:  # row i of a sequence's sample sees keys 0 .. i + (lkv - rows)
+        pairs = sum(int(np.clip(np.arange(t) + (n - t) + 1, 0, n).sum()) for t, n in zip(take, lkv))
+    else:
+        pairs = int((take * lkv).sum())
+    flops = 10.0 * p.h * pairs * p.d
 
     def run():
-        oracle.dense_bwd(q, k, v, o, do, lse, [r], [s], p.scale, mask)
+        oracle.dense_bwd(q, k, v, o, do, lse, cu_q, p.cu_kv, p.scale, mask)
 
-    return run, flops, f"batch element {batch}, all {p.h} heads, last {r} of {s} query rows, fp64"
+    desc = f"last {int(take.max())} query rows of each of the {len(take)} sequences, all {p.h} heads, fp64"
+    return run, flops, desc, len(take) * p.h_kv
 
 
 def oracle_nsa_sample(p, tokens=None):
+    """The last `tokens` query tokens of every sequence, all heads, against all of that sequence's keys
+    (the selections and the sparse mode's bottom-right alignment as in p)."""
     import oracle
-    t = p.t1 if tokens is None else max(1, min(p.t1, int(tokens)))
-    L = int(p.cu_q[0])
-    t = min(t, L)
-    q, do = p.f64("q")[L - t:L], p.f64("do")[L - t:L]
-    k, v = p.f64("k")[:L], p.f64("v")[:L]
-    topk = p.topk[L - t:L]
-    o, mx, sm = oracle.nsa_fwd(q, k, v, topk, [t], [L], p.scale, p.block_size, p.sparse_mode)
-    flops = 10.0 * t * p.n1 * p.block_count * p.block_size * p.d
+    idx, take = _last_rows(p.cu_q, p.t1 if tokens is None else max(1, int(tokens)))
+    q, do, topk = p.f64("q")[idx], p.f64("do")[idx], p.topk[idx]
+    k, v = p.f64("k"), p.f64("v")
+    cu_q = np.cumsum(take)
+    o, mx, sm = oracle.nsa_fwd(q, k, v, topk, cu_q, p.cu_kv, p.scale, p.block_size, p.sparse_mode)
+    flops = 10.0 * float(take.sum()) * p.n1 * p.block_count * p.block_size * p.d
 
     def run():
-        oracle.nsa_bwd(q, k, v, o, do, mx, sm, topk, [t], [L], p.scale, p.block_size, p.sparse_mode)
+        oracle.nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, p.cu_kv, p.scale, p.block_size, p.sparse_mode)
 
-    return run, flops, f"sequence 0, last {t} of {L} tokens, all {p.n1} heads, fp64"
-
-
-def sample_threads(p):
-    """Threads the oracle runs a cpu_sample of p on: it splits its work into (sequence, kv head) units,
-    one thread per unit at most, and a sample covers one sequence."""
-    import oracle
-    units = p.n2 if isinstance(p, synth.NsaProblem) else p.h_kv
-    return max(1, min(oracle.thread_count(), int(units)))
+    desc = f"last {int(take.max())} tokens of each of the {len(take)} sequences, all {p.n1} heads, fp64"
+    return run, flops, desc, len(take) * p.n2
 
 
 def cpu_sample(p, target_s):
-    """A sample of the workload whose oracle run takes about target_s."""
-    if isinstance(p, synth.NsaProblem):
-        run, flops, _ = oracle_nsa_sample(p, 64)
-        t0 = time.perf_counter(); run(); dt = time.perf_counter() - t0
-        return oracle_nsa_sample(p, 64 * max(1.0, target_s / max(dt, 1e-6)))
-    run, flops, _ = oracle_dense_sample(p, 64)
+    """A sample of the workload whose oracle run takes about target_s (at most the whole workload).
+    Returns (run, flops, description, threads the oracle runs it on: one per (sequence, kv head) unit
+    at most)."""
+    import oracle
+    build = oracle_nsa_sample if isinstance(p, synth.NsaProblem) else oracle_dense_sample
+    full = p.t1 if isinstance(p, synth.NsaProblem) else p.s_q
+    run, _, _, _ = build(p, 64)
     t0 = time.perf_counter(); run(); dt = time.perf_counter() - t0
-    full_pairs = sum(range(1, p.s_q + 1)) if p.mask else p.s_q * p.s_kv
-    want_pairs = (flops / (10.0 * p.h * p.d)) * target_s / max(dt, 1e-6)
-    rows = p.s_q
-    if want_pairs < full_pairs:  # smallest r whose last-r-rows pair count reaches want_pairs
-        rows, acc = 0, 0
-        while acc < want_pairs and rows < p.s_q:
-            acc += p.s_q - rows
-            rows += 1
-    return oracle_dense_sample(p, rows)
+    run, flops, desc, units = build(p, min(full, 64 * max(1.0, target_s / max(dt, 1e-6))))
+    return run, flops, desc, max(1, min(oracle.thread_count(), units))
 
 
 def affinity_count():
@@ -257,7 +257,7 @@ def run_reference(args, info):
     if rank != 0:
         return
     per_step = min(30.0, 120.0 / max(1, args.steps + args.warmup))
-    run, flops, desc = cpu_sample(p, per_step)
+    run, flops, desc, threads = cpu_sample(p, per_step)
     for _ in range(args.warmup):
         run()
     times = []
@@ -269,7 +269,7 @@ def run_reference(args, info):
             "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
             "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": sample_threads(p), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                              "sample": desc, "affinity": affinity_count(), "host_threads": oracle.thread_count()},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -458,9 +458,9 @@ def run_ours(args, info):
     }
     if world == 1 and not args.no_cpu_baseline:
         import oracle
-        run, cflops, desc_s = cpu_sample(p, 10.0)
+        run, cflops, desc_s, threads = cpu_sample(p, 10.0)
         nrun, dt = time_repeated(run, 10.0)  # about 10 s of CPU work, repeating a sample smaller than that
-        line["cpu_baseline"] = {"value": cflops * nrun / dt / 1e12, "unit": "TFLOP/s", "cores": sample_threads(p),
+        line["cpu_baseline"] = {"value": cflops * nrun / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
                                 "host_threads": oracle.thread_count(),
                                 "kind": "oracle", "sample": f"{desc_s}; run {nrun} time(s)", "seconds": dt,
                                 "affinity": affinity_count()}

@@ -53,9 +53,35 @@ def test_time_repeated_reaches_the_minimum():
     assert n == 1  # always at least once
 
 
-def test_sample_threads_counts_what_the_oracle_uses():
-    """The oracle runs one thread per (sequence, kv head) unit at most; a CPU sample covers one sequence."""
+def test_dense_cpu_sample_rows_keep_their_keys():
+    """The CPU sample (the last r query rows of every sequence against all of its keys, bottom-right)
+    gives its rows the same O and dQ as the full problem, and counts 10 d FLOPs per visible pair."""
+    import numpy as np
     import oracle
     import synth
-    assert bench.sample_threads(synth.workload(1)) == min(oracle.thread_count(), 12)
-    assert bench.sample_threads(synth.workload(4)) == 1
+    p = synth.dense_problem("s", dtype=synth.F16, b=2, h=2, h_kv=1, d=8, s_q=40, s_kv=40, mask=1, seed=3)
+    q, k, v, do = (p.f64(x) for x in ("q", "k", "v", "do"))
+    o, lse = oracle.dense_fwd(q, k, v, p.cu_q, p.cu_kv, p.scale, p.mask)
+    dq, _, _ = oracle.dense_bwd(q, k, v, o, do, lse, p.cu_q, p.cu_kv, p.scale, p.mask)
+    idx, take = bench._last_rows(p.cu_q, 7)
+    assert take.tolist() == [7, 7] and idx.tolist() == list(range(33, 40)) + list(range(73, 80))
+    cu = np.cumsum(take)
+    so, slse = oracle.dense_fwd(q[idx], k, v, cu, p.cu_kv, p.scale, oracle.CAUSAL_BOTTOM_RIGHT)
+    np.testing.assert_allclose(so, o[idx], rtol=1e-12, atol=1e-14)
+    sdq, _, _ = oracle.dense_bwd(q[idx], k, v, so, do[idx], slse, cu, p.cu_kv, p.scale, oracle.CAUSAL_BOTTOM_RIGHT)
+    np.testing.assert_allclose(sdq, dq[idx], rtol=1e-11, atol=1e-13)
+    _, flops, _, units = bench.oracle_dense_sample(p, 7)
+    pairs = 2 * sum(i + 1 for i in range(33, 40))  # top-left causal, equal lengths: row i sees keys 0 .. i
+    assert flops == 10.0 * p.h * pairs * p.d and units == 2
+
+
+def test_cpu_sample_sizes():
+    """A full non-causal sample has the workload's FLOPs; units are (sequence, kv head) pairs."""
+    import synth
+    p = synth.workload(0)
+    _, flops, _, units = bench.oracle_dense_sample(p)
+    assert flops == bench.workload_info(0)[1] and units == p.b * p.h_kv
+    q = synth.nsa_problem("n", dtype=synth.BF16, lens_q=[100, 50], lens_kv=[256, 256], n1=4, n2=2, d=128,
+                          block_size=64, block_count=2, sparse_mode=2, seed=5)
+    _, flops, _, units = bench.oracle_nsa_sample(q, 30)
+    assert flops == 10.0 * 60 * 4 * 2 * 64 * 128 and units == 4
