@@ -57,6 +57,11 @@ def _cu_array(keep, cu):
 
 def sdpa_desc(*, dtype, b, h, h_kv, s_q, s_kv, d, scale, mask=ATTN_MASK_NONE, cu_seqlens_q=None,
               cu_seqlens_kv=None, deterministic=False, dq_splits=0, _keep=None):
+    """An attn_sdpa_desc_t.  Fixed-length mode: b sequences of s_q queries and s_kv keys.  Packed
+    (varlen) mode: cu_seqlens_q / cu_seqlens_kv, b inclusive cumulative lengths each (s_q, s_kv then
+    ignored).  scale multiplies q.k; mask is ATTN_MASK_NONE, ATTN_CAUSAL_TOP_LEFT or
+    ATTN_CAUSAL_BOTTOM_RIGHT; deterministic with dq_splits partial buffers (0: a default) makes dQ
+    bitwise reproducible.  The host arrays live as long as the descriptor."""
     keep = _keep if _keep is not None else _Keep()
     desc = attn_sdpa_desc_t(int(dtype), int(b), int(h), int(h_kv), int(s_q), int(s_kv), int(d), float(scale),
                             int(mask), _cu_array(keep, cu_seqlens_q), _cu_array(keep, cu_seqlens_kv),
@@ -67,6 +72,10 @@ def sdpa_desc(*, dtype, b, h, h_kv, s_q, s_kv, d, scale, mask=ATTN_MASK_NONE, cu
 
 def nsa_desc(*, dtype, cu_seqlens_q, cu_seqlens_kv, n1, n2, d, scale, block_size, block_count, sparse_mode,
              deterministic=False):
+    """An attn_nsa_desc_t: TND layout, b = len(cu_seqlens_q) sequences with inclusive cumulative query /
+    key lengths, n1 query and n2 kv heads, head dim d, scaleValue, selectedBlockSize / Count,
+    sparseMode 0 (selection only) or 2 (also causal, bottom-right per sequence); deterministic makes
+    dq, dk, dv bitwise reproducible (tensor-core head groups only)."""
     keep = _Keep()
     desc = attn_nsa_desc_t(int(dtype), len(cu_seqlens_q), _cu_array(keep, cu_seqlens_q),
                            _cu_array(keep, cu_seqlens_kv), int(n1), int(n2), int(d), float(scale),
@@ -92,6 +101,7 @@ def view_tnd(t) -> attn_view_t:
 
 
 def sdpa_workspace_size(desc):
+    """(forward bytes, backward bytes) of device workspace for this descriptor (host only)."""
     fwd, bwd = C.c_size_t(), C.c_size_t()
     check(_lib.load().sdpa_workspace_size(C.byref(desc), C.byref(fwd), C.byref(bwd)), "sdpa_workspace_size")
     return fwd.value, bwd.value
@@ -117,6 +127,10 @@ def sdpa_fwd_stats(desc, q, k, v, o, lse, *, workspace=None, stream=None):
 
 
 def sdpa_bwd(desc, q, k, v, o, dO, lse, dQ, dK, dV, *, workspace=None, stream=None):
+    """dQ, dK, dV of scaled dot-product attention from O, dO and the fp32 stats lse (as sdpa_fwd_stats
+    writes them).  Tensors are attn_view_t views or [B, H, S, D] CUDA tensors (view_bhsd); the call is
+    asynchronous on `stream` (default: the current stream).  A workspace of the size
+    sdpa_workspace_size gives is allocated when none is passed; it is returned, for attn_query_status."""
     _, bwd = sdpa_workspace_size(desc)
     ws = _workspace(bwd, lse.device, workspace)
     views = [x if isinstance(x, attn_view_t) else view_bhsd(x) for x in (q, k, v, o, dO, dQ, dK, dV)]
@@ -128,6 +142,7 @@ def sdpa_bwd(desc, q, k, v, o, dO, lse, dQ, dK, dV, *, workspace=None, stream=No
 
 
 def nsa_workspace_size(desc):
+    """Bytes of device workspace nsa_selected_attn_bwd needs for this descriptor (host only)."""
     n = C.c_size_t()
     check(_lib.load().nsa_workspace_size(C.byref(desc), C.byref(n)), "nsa_workspace_size")
     return n.value
@@ -135,6 +150,10 @@ def nsa_workspace_size(desc):
 
 def nsa_selected_attn_bwd(desc, q, k, v, o, dO, softmax_max, softmax_sum, topk, dq, dk, dv, *, workspace=None,
                           stream=None):
+    """NSA selected-attention backward on contiguous TND CUDA tensors: q, o, dO, dq [T1, n1, d]; k, v,
+    dk, dv [T2, n2, d]; softmax_max / softmax_sum [T1, n1, 8] fp32; topk [T1, n2, block_count] int32.
+    Asynchronous on `stream`; returns the workspace (allocated when none is passed) for
+    attn_query_status, which reports indices that were out of range or repeated."""
     ws = _workspace(nsa_workspace_size(desc), q.device, workspace)
     fp = lambda t: C.cast(C.c_void_p(t.data_ptr()), C.POINTER(C.c_float))
     st = _lib.load().nsa_selected_attn_bwd(
