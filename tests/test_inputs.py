@@ -66,3 +66,18 @@ def test_nsa_workload_shapes_and_topk():
     np.testing.assert_array_equal(np.diff(np.concatenate([[0], p.cu_q])), [4096] * 4)
     assert abs(p.scale - 128 ** -0.5) < 1e-12
     _check_topk(p.topk[:4096], p.cu_q[:1], p.cu_kv[:1], 1, 64, 16, True)
+
+
+def test_dense_workload_shapes():
+    """Workloads 0-3 as stated: sizes, dtype, scale, mask; workload 3's lengths are seeded draws from
+    [256, 4096] (listed with the input recipe)."""
+    w = {i: synth.workload(i) for i in range(4)}
+    assert (w[0].dtype, w[0].b, w[0].h, w[0].h_kv, w[0].s_q, w[0].d, w[0].mask) == (synth.F16, 1, 2, 2, 128, 64, 0)
+    assert (w[1].dtype, w[1].b, w[1].h, w[1].s_q, w[1].s_kv, w[1].d, w[1].mask) == (synth.F16, 4, 12, 1024, 1024, 64, 1)
+    assert w[0].scale == w[1].scale == 0.125
+    assert (w[2].dtype, w[2].b, w[2].h, w[2].s_q, w[2].d, w[2].mask) == (synth.BF16, 2, 32, 4096, 128, 1)
+    assert abs(w[2].scale - 128 ** -0.5) < 1e-12
+    lens = np.diff(np.concatenate([[0], w[3].cu_q])).tolist()
+    assert lens == [3807, 2457, 3066, 2285, 2298, 3189, 2967, 3373]
+    assert np.array_equal(w[3].cu_q, w[3].cu_kv) and (w[3].h, w[3].h_kv, w[3].d) == (32, 8, 128)
+    assert w[3].varlen and w[3].mask == 2
