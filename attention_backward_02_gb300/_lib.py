@@ -22,7 +22,8 @@ ATTN_MASK_NONE, ATTN_CAUSAL_TOP_LEFT, ATTN_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
 # every exported symbol of include/attnbwd.h
 EXPORTS = ("sdpa_workspace_size", "sdpa_fwd_stats", "sdpa_bwd", "nsa_workspace_size",
            "nsa_selected_attn_bwd", "nsa_block_lists", "attn_query_status", "attn_status_string",
-           "attn_set_main_kernel_events", "sdpa_bwd_static_scratch", "attn_last_error")
+           "attn_set_main_kernel_events", "sdpa_bwd_static_scratch", "attn_static_scratch_status",
+           "attn_selftest_wait_timeout", "attn_last_error")
 
 
 class attn_view_t(C.Structure):
@@ -69,6 +70,8 @@ def load() -> C.CDLL:
         "attn_last_error": [],
         "attn_set_main_kernel_events": [V, V],
         "sdpa_bwd_static_scratch": [D, view, view, view, view, view, P(C.c_float), view, view, view, V],
+        "attn_static_scratch_status": [V, P(C.c_uint32)],
+        "attn_selftest_wait_timeout": [V, S, C.c_double, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)

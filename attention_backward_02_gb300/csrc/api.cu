@@ -161,6 +161,8 @@ cudaError_t mark(cudaEvent_t ev, cudaStream_t s) { return ev ? cudaEventRecord(e
 
 }  // namespace
 
+attn_status_t attn::record_cuda_error(cudaError_t e) { return cuda_status(e); }
+
 extern "C" {
 
 const char *attn_last_error(void) { return g_last_error; }

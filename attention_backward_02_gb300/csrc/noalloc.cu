@@ -7,10 +7,8 @@
 // into this library (a file-scope __device__ array), so the call itself
 // allocates nothing.  It runs exactly the same kernels as sdpa_bwd, with the
 // static array as their workspace.
-#include <mutex>
-
 #include "attnbwd.h"
-#include "common.cuh"
+#include "plan.h"
 
 namespace {
 
@@ -18,23 +16,20 @@ namespace {
 // bytes until the process exits.
 static __device__ __align__(256) unsigned char g_static_scratch[ATTN_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 256;
-std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};  // device address of g_static_scratch, per device
-
-// Once per device, with that device current: look up the device address of
-// the array (host code only holds a host-side stand-in for the symbol).
-attn_status_t scratch_for_current_device(void **out)
+// Device address of the array in the current context.  In host code the
+// array's name is only a host-side stand-in for the symbol, never a device
+// address, so it is looked up on every call (a host-side table lookup once
+// the module is loaded).  Nothing is cached: after cudaDeviceReset, or with
+// another context current, the address may differ.  The first call in a
+// context loads the module, which is why that call must come before any
+// stream capture.
+attn_status_t scratch_for_current_context(void **out)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return ATTN_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return attn::record_cuda_error(e);
+    if (!p) return attn::record_cuda_error(cudaErrorInvalidSymbol);
+    *out = p;
     return ATTN_OK;
 }
 
@@ -49,9 +44,18 @@ extern "C" attn_status_t sdpa_bwd_static_scratch(const attn_sdpa_desc_t *desc, a
     if (st) return st;
     if (need > size_t(ATTN_STATIC_SCRATCH_BYTES)) return ATTN_ERR_WORKSPACE;
     void *scratch = nullptr;
-    if ((st = scratch_for_current_device(&scratch))) return st;
+    if ((st = scratch_for_current_context(&scratch))) return st;
     // sdpa_bwd's first kernel rewrites every scratch byte the later kernels
     // read (status word, D, LSE * log2 e, the zeroed dQ accumulator), so what
     // an earlier call left in the array does not matter.
     return sdpa_bwd(desc, q, k, v, o, dO, lse, dQ, dK, dV, scratch, size_t(ATTN_STATIC_SCRATCH_BYTES), stream);
+}
+
+extern "C" attn_status_t attn_static_scratch_status(void *stream, uint32_t *device_flags)
+{
+    if (!device_flags) return ATTN_ERR_NULLPTR;
+    void *scratch = nullptr;
+    attn_status_t st = scratch_for_current_context(&scratch);
+    if (st) return st;
+    return attn_query_status(scratch, stream, device_flags);
 }

@@ -82,6 +82,10 @@ struct NsaArgs {
     int zero_dq;                // the preprocess also zeroes dqacc (tensor-core path, atomic dQ)
 };
 
+// Maps a CUDA error to ATTN_ERR_CUDA and keeps its text for attn_last_error
+// (this host thread); cudaSuccess maps to ATTN_OK.
+attn_status_t record_cuda_error(cudaError_t e);
+
 // ------------------------------------------------------------ launchers
 // Each returns cudaGetLastError() of its launches.
 cudaError_t launch_dense_preprocess(const DenseArgs &a, const FixedGeo &g, cudaStream_t s);

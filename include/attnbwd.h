@@ -16,16 +16,11 @@
  *   LSE_i = log sum_j exp(s_ij),  P_ij = exp(s_ij - LSE_i),  O_i = sum_j P_ij v_j,
  *   D_i = rowsum(dO_i * O_i),  dP = dO V^T,  dS = P * (dP - D),
  *   dV = P^T dO,  dQ = scale dS K,  dK = scale dS^T Q.
- * Sources: the cuDNN-frontend sample "51_scaled_dot_product_attention_backward"
- * (training forward emitting a (B,H,S,1) float32 stats tensor, backward from
- * those stats by FlashAttention-2, multiplicative attn_scale, causal mask,
- * half-precision I/O with float intermediates and compute, BSHD physical /
- * BHSD logical strides) and the Ascend CANN page "aclnnNsaSelectedAttentionGrad"
- * (Function / Formula: gather of the selected key / value blocks, dV = P^T dY,
- * dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d); Constraints: TND layout,
- * cumulative actual sequence lengths, G = N1/N2 <= 32, block size <= 128 and a
- * multiple of 16, block count in [1,128], deterministic mode opt-in; the
- * two-phase workspace-size-then-run API and its status codes).
+ * Pages cited below by title and section:
+ *   [cuDNN]  cuDNN-frontend sample "51_scaled_dot_product_attention_backward"
+ *   [Ascend] Ascend CANN page "aclnnNsaSelectedAttentionGrad"
+ *   [PR]     PyTorch PR #94729 (matmul -> scale -> softmax -> matmul pattern)
+ * Each call below names the passage that defines it.
  *
  * Conventions shared by every call.
  *  - Tensors are caller-owned device memory.  The library allocates nothing,
@@ -55,6 +50,13 @@
 extern "C" {
 #endif
 
+/* Status codes.  [Ascend] "Return Value" table: a call returns a code; the
+ * page's parameter-check failures map to NULLPTR / INVALID here, and its
+ * run-time failure code to ATTN_ERR_CUDA.  Deviation from a single
+ * "timeout" code: device-side failures (a wait that ran out, a bad index)
+ * cannot be returned by an asynchronous call, so they set bits of a device
+ * status word (ATTN_DEV_*), and attn_query_status returns ATTN_ERR_DEVICE
+ * with those bits in *device_flags.                                          */
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_NULLPTR = 1,     /* a required pointer is NULL                    */
@@ -113,17 +115,27 @@ typedef struct {
 } attn_sdpa_desc_t;
 
 /* Workspace bytes for sdpa_fwd_stats and for sdpa_bwd with this descriptor.
- * Either output pointer may be NULL.  Host only; no CUDA call.              */
+ * Either output pointer may be NULL.  Host only; no CUDA call.
+ * [cuDNN] workspace cell (the caller queries the graph's workspace size and
+ * allocates it); [Ascend] "Function Prototype" (first phase of the two-phase
+ * API returns workspaceSize).                                               */
 attn_status_t sdpa_workspace_size(const attn_sdpa_desc_t *desc, size_t *fwd_bytes, size_t *bwd_bytes);
 
-/* Forward in training mode.  q, o: [B,h,s_q,d] views; k, v: [B,h_kv,s_kv,d].
+/* Forward in training mode.  [cuDNN] forward-graph cell (sdpa with
+ * is_inference=False, attn_scale, causal mask, emitting O and the (B,H,S,1)
+ * float32 stats); [PR] the attention formula (softmax of scaled scores times
+ * V).  q, o: [B,h,s_q,d] views; k, v: [B,h_kv,s_kv,d].
  * lse (fp32, natural log, contiguous): [B][h][s_q] in fixed-length mode,
  * [h][T_q] in packed mode (T_q = total query tokens).                        */
 attn_status_t sdpa_fwd_stats(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t k, attn_view_t v,
                              attn_view_t o, float *lse, void *workspace, size_t workspace_bytes,
                              void *stream);
 
-/* Backward.  q, o, dO, dQ: [B,h,s_q,d] views; k, v, dK, dV: [B,h_kv,s_kv,d];
+/* Backward.  [cuDNN] backward-graph cell (sdpa_backward from Q, K, V, O, dO
+ * and the stats, FlashAttention-2, attn_scale, causal mask; dQ, dK, dV
+ * allocated like the inputs); [Ascend] "Function / Formula" for the
+ * gradient formulas; [Ascend] "Constraints" for opt-in deterministic
+ * computation.  q, o, dO, dQ: [B,h,s_q,d] views; k, v, dK, dV: [B,h_kv,s_kv,d];
  * lse as sdpa_fwd_stats writes it.  dQ / dK / dV may have any strides that
  * follow the 16-byte rule (the sample allocates them empty_like the inputs).
  * Outputs have the input dtype, rounded to nearest even.  In the default
@@ -135,7 +147,7 @@ attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t 
                        attn_view_t o, attn_view_t dO, const float *lse, attn_view_t dQ, attn_view_t dK,
                        attn_view_t dV, void *workspace, size_t workspace_bytes, void *stream);
 
-/* Allocation-free variant of sdpa_bwd.  The papers this library follows
+/* Allocation-free variant of sdpa_bwd.  The pages this library follows
  * have no counterpart to it; it exists for callers that cannot allocate
  * device memory when they run the backward (an engine or plugin that owns
  * all device memory and forbids side allocations, a loop that must not
@@ -152,11 +164,21 @@ attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t 
  *    streams, other host threads) race and corrupt each other's results;
  *    serialise them.  Each call re-initialises the scratch it reads, so what
  *    an earlier call left there does not matter.
- *  - Device status flags land in the static array and cannot be read back. */
+ *  - Device status flags land in the static array; attn_static_scratch_status
+ *    reads them back (and clears them) like attn_query_status.
+ *  - The array's device address is looked up on every call (nothing is
+ *    cached across contexts or cudaDeviceReset); errors of that lookup return
+ *    ATTN_ERR_CUDA with the text in attn_last_error.                         */
 #define ATTN_STATIC_SCRATCH_BYTES (16u << 20)
 attn_status_t sdpa_bwd_static_scratch(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t k, attn_view_t v,
                                       attn_view_t o, attn_view_t dO, const float *lse, attn_view_t dQ,
                                       attn_view_t dK, attn_view_t dV, void *stream);
+
+/* Waits for the stream, then reads and clears the device status word that
+ * the static scratch of sdpa_bwd_static_scratch holds (bits ATTN_DEV_*).
+ * Returns ATTN_ERR_DEVICE when any bit was set.  No counterpart on the
+ * pages.                                                                    */
+attn_status_t attn_static_scratch_status(void *stream, uint32_t *device_flags);
 
 typedef struct {
     attn_dtype_t dtype;
@@ -174,10 +196,16 @@ typedef struct {
     int deterministic;      /* 1: bitwise reproducible dQ                     */
 } attn_nsa_desc_t;
 
-/* Workspace bytes for nsa_selected_attn_bwd.  Host only; no CUDA call.       */
+/* Workspace bytes for nsa_selected_attn_bwd.  Host only; no CUDA call.
+ * [Ascend] "Function Prototype": aclnnNsaSelectedAttentionGradGetWorkspaceSize. */
 attn_status_t nsa_workspace_size(const attn_nsa_desc_t *desc, size_t *bytes);
 
-/* NSA selected-attention backward, TND layout, all contiguous:
+/* NSA selected-attention backward.  [Ascend] "Function / Formula" (gather of
+ * the selected blocks, then the attention backward; dK / dV scattered back
+ * through the indices), parameter table (TND layout, actualSeqQLen /
+ * actualSeqKvLen, softmaxMax / softmaxSum, topkIndices, scaleValue,
+ * selectedBlockSize / Count, sparseMode) and "Constraints".  Layout, all
+ * contiguous:
  *   q, o, dO, dq : [T1][n1][d]      k, v, dk, dv : [T2][n2][d]
  *   softmax_max, softmax_sum : [T1][n1][8] fp32 (the 8 lanes hold one value;
  *       lane 0 is read): P = exp(scale q.k - max) / sum over the selection.
@@ -191,7 +219,9 @@ attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, 
                                     const int32_t *topk, void *dq, void *dk, void *dv,
                                     void *workspace, size_t workspace_bytes, void *stream);
 
-/* The inverted index the NSA backward builds internally, exposed so callers
+/* [Ascend] "Function / Formula" (Gather(key, topkIndices)), read in the
+ * backward direction: which tokens selected each block.
+ * The inverted index the NSA backward builds internally, exposed so callers
  * (and tests) can use or check it: for every (sequence b, kv head g, block k)
  * in that order, row r = (b * n2 + g) * nblk_max + k with
  * nblk_max = max_b S2_b / block_size, tokens[offsets[r] .. offsets[r+1]) are
@@ -206,8 +236,18 @@ attn_status_t nsa_block_lists(const attn_nsa_desc_t *desc, const int32_t *topk, 
 
 /* Waits for the stream, then reads the device status word of a workspace a
  * previous call used (bits ATTN_DEV_*; 0 when clean) and clears it.
- * Returns ATTN_ERR_DEVICE when any bit was set.                              */
+ * Returns ATTN_ERR_DEVICE when any bit was set.  [Ascend] "Return Value"
+ * (failures reported as codes); see the deviation note above the enum.     */
 attn_status_t attn_query_status(void *workspace, void *stream, uint32_t *device_flags);
+
+/* Self-test of the device failure path: launches one block whose bounded
+ * mbarrier wait (the same wait every tensor-core kernel uses) can never
+ * complete, so after about limit_s seconds (0 < limit_s <= 2) it gives up,
+ * sets ATTN_DEV_TIMEOUT in the status word at `workspace` (at least 4 bytes,
+ * 4-byte aligned) and returns; the context stays usable.  Read the flag with
+ * attn_query_status.  [Ascend] "Return Value" (failures as codes, never a
+ * crash).                                                                   */
+attn_status_t attn_selftest_wait_timeout(void *workspace, size_t workspace_bytes, double limit_s, void *stream);
 
 /* Optional instrumentation for benchmarks.  While set, every sdpa_bwd and
  * nsa_selected_attn_bwd call made from this host thread records the CUDA

@@ -158,6 +158,24 @@ def test_query_status_needs_its_pointers(ab):
     assert lib.attn_query_status(C.c_void_p(0x100000), None, None) == 1
 
 
+def test_selftest_rejects_before_launch(ab):
+    """The wait-timeout self-test checks its arguments on the host: no workspace, a short or
+    misaligned one, and limits outside (0, 2] seconds launch nothing."""
+    lib = ab._lib.load()
+    call = lambda ws=0x100000, n=256, lim=0.02: lib.attn_selftest_wait_timeout(C.c_void_p(ws), C.c_size_t(n),
+                                                                                 C.c_double(lim), None)
+    assert call(ws=0) == 1
+    assert call(n=2) == 4
+    assert call(ws=0x100002) == 4
+    assert call(lim=0.0) == 2
+    assert call(lim=5.0) == 2
+    assert call(lim=float("nan")) == 2
+
+
+def test_static_scratch_status_needs_its_pointer(ab):
+    assert ab._lib.load().attn_static_scratch_status(None, None) == 1
+
+
 def test_status_strings(ab):
     for code in range(8):
         assert ab._lib.load().attn_status_string(code).startswith(b"ATTN_")

@@ -109,29 +109,57 @@ def test_deterministic_mode_bitwise(dq_splits):
     _parity(p, deterministic=True, dq_splits=dq_splits)
 
 
+@pytest.mark.parametrize("dq_splits", [0, 2])
+def test_deterministic_mode_bitwise_d64(dq_splits):
+    """Deterministic mode at d = 64 (128-row query tiles, fp16), causal with ragged tails."""
+    p = synth.dense_problem("det64", dtype=F16, b=2, h=4, h_kv=2, d=64, s_q=520, s_kv=520, mask=TL, scale=0.125,
+                            seed=21)
+    o_bits, lse = H.oracle_forward(p)
+    a = H.run_gpu_bwd(p, o_bits, lse, deterministic=True, dq_splits=dq_splits)
+    b = H.run_gpu_bwd(p, o_bits, lse, deterministic=True, dq_splits=dq_splits)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    _parity(p, deterministic=True, dq_splits=dq_splits)
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_varlen_gqa_d64(dtype):
+    """d = 64 with packed sequences and grouped-query heads (8 query heads on 2 kv heads), unequal
+    query / key lengths per sequence, causal bottom-right."""
+    lq = np.array([1, 200, 77, 129, 300]); lkv = np.array([5, 150, 260, 129, 310])
+    p = synth.dense_problem("varlen_gqa64", dtype=dtype, b=len(lq), h=8, h_kv=2, d=64, lens_q=lq, lens_kv=lkv,
+                            mask=BR, seed=22 + dtype)
+    _parity(p)
+
+
 def test_workload1_full():
     """fp16 b4 h12 s1024 d64 causal, BSHD viewed as BHSD: every output element."""
     _parity(synth.workload(1))
 
 
-def _sampled_parity(p, deterministic=False, nsample=96, seed=0):
-    o_bits, lse = H.oracle_forward(p)
+_ORACLE_CACHE = {}
+
+
+def _oracle_full(idx):
+    """Oracle forward (O rounded to 16 bits, LSE) and backward of workload idx, computed once per
+    session: the atomic and deterministic tests of one workload share them."""
+    if idx not in _ORACLE_CACHE:
+        p = synth.workload(idx)
+        o_bits, lse = H.oracle_forward(p)
+        ref = oracle.dense_bwd(p.f64("q"), p.f64("k"), p.f64("v"), synth.bits_to_f64(o_bits, p.dtype),
+                               p.f64("do"), lse, p.cu_q, p.cu_kv, p.scale, p.mask)
+        _ORACLE_CACHE[idx] = (p, o_bits, lse, ref)
+    return _ORACLE_CACHE[idx]
+
+
+def _full_parity(idx, deterministic=False):
+    """Every element of dQ, dK, dV against the oracle, plus the invariant
+    sum_j dV_j = sum_i dO_i per (sequence, kv head group), which holds at any size."""
+    p, o_bits, lse, (rq, rk, rv) = _oracle_full(idx)
     dq, dk, dv = H.run_gpu_bwd(p, o_bits, lse, deterministic)
-    rng = np.random.default_rng(seed)
-    q_rows = rng.choice(p.t_q * p.h, nsample, replace=False)
-    kv_rows = rng.choice(p.t_kv * p.h_kv, nsample, replace=False)
-    # always include the first and last rows of every sequence
-    starts = np.concatenate([[0], p.cu_q[:-1]])
-    edge_t = np.unique(np.concatenate([starts, p.cu_q - 1]))
-    q_rows = np.unique(np.concatenate([q_rows, edge_t * p.h, edge_t * p.h + p.h - 1]))
-    kv_rows = np.unique(np.concatenate([kv_rows, edge_t * p.h_kv]))
-    rq, rk, rv = oracle.dense_bwd_rows(p.f64("q"), p.f64("k"), p.f64("v"), synth.bits_to_f64(o_bits, p.dtype),
-                                       p.f64("do"), lse, p.cu_q, p.cu_kv, p.scale, p.mask, q_rows, kv_rows)
-    H.assert_close(dq.reshape(-1, p.d)[q_rows], rq, "dQ rows")
-    H.assert_close(dk.reshape(-1, p.d)[kv_rows], rk, "dK rows")
-    H.assert_close(dv.reshape(-1, p.d)[kv_rows], rv, "dV rows")
-    # properties that hold at any size: sum_j dK_j = 0 per (sequence, kv head)
-    # up to the rounding of O to 16 bits, and sum_j dV_j = sum_i dO_i per group
+    H.assert_close(dq, rq, "dQ")
+    H.assert_close(dk, rk, "dK")
+    H.assert_close(dv, rv, "dV")
     G = p.h // p.h_kv
     do = p.f64("do")
     for b in range(len(p.cu_kv)):
@@ -141,16 +169,18 @@ def _sampled_parity(p, deterministic=False, nsample=96, seed=0):
             want = do[q0:q1, g * G:(g + 1) * G].sum((0, 1))
             got = dv[s0:s1, g].sum(0)
             assert np.abs(got - want).max() <= 0.05 * np.abs(want).max() + 0.5
+    return dq, dk, dv
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("deterministic", [False, True])
-def test_workload2_sampled(deterministic):
-    """bf16 b2 h32 s4096 d128 causal: sampled rows, both dQ modes."""
-    _sampled_parity(synth.workload(2), deterministic)
+def test_workload2_full(deterministic):
+    """bf16 b2 h32 s4096 d128 causal: every output element, both dQ modes."""
+    _full_parity(2, deterministic)
 
 
 @pytest.mark.slow
-def test_workload3_sampled():
-    """varlen GQA bf16, h 32 / h_kv 8, d128, 8 lengths in [256, 4096], causal bottom-right."""
-    _sampled_parity(synth.workload(3))
+def test_workload3_full():
+    """varlen GQA bf16, h 32 / h_kv 8, d128, 8 lengths in [256, 4096], causal bottom-right: every
+    output element."""
+    _full_parity(3)

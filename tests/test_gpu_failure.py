@@ -1,0 +1,38 @@
+"""The device failure path on a GPU, without faulting it: a bounded mbarrier
+wait that nothing completes runs out after a short limit, the kernel sets
+ATTN_DEV_TIMEOUT in the workspace status word and returns, the host reads the
+flag back, and the context stays usable for the next call."""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+def test_wait_timeout_sets_flag_and_context_survives():
+    import torch
+    import attention_backward_02_gb300 as ab
+    lib = ab._lib.load()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    st = lib.attn_selftest_wait_timeout(C.c_void_p(ws.data_ptr()), C.c_size_t(256), C.c_double(0.02),
+                                        C.c_void_p(stream))
+    ab.check(st, "attn_selftest_wait_timeout")
+    assert ab.attn_query_status(ws) == ab._lib.ATTN_DEV_TIMEOUT
+    assert ab.attn_query_status(ws) == 0  # read and cleared
+    # the context still runs the backward correctly
+    p = synth.dense_problem("after_timeout", dtype=synth.F16, b=1, h=2, h_kv=2, d=64, s_q=200, s_kv=200,
+                            mask=oracle.CAUSAL_TOP_LEFT, seed=41)
+    o_bits, lse = H.oracle_forward(p)
+    dq, dk, dv = H.run_gpu_bwd(p, o_bits, lse)
+    rq, rk, rv = oracle.dense_bwd(p.f64("q"), p.f64("k"), p.f64("v"), synth.bits_to_f64(o_bits, p.dtype),
+                                  p.f64("do"), lse, p.cu_q, p.cu_kv, p.scale, p.mask)
+    H.assert_close(dq, rq, "dQ")
+    H.assert_close(dk, rk, "dK")
+    H.assert_close(dv, rv, "dV")
+    assert np.all(np.isfinite(dq))

@@ -141,6 +141,14 @@ def test_deterministic_unsupported_group():
     _parity(p)  # the non-deterministic CUDA-core path still serves this shape
 
 
+@pytest.mark.parametrize("n1,n2", [(4, 1), (2, 2), (4, 2), (6, 3)])
+@pytest.mark.parametrize("sparse_mode", [0, 2])
+def test_cuda_core_kernel_groups(n1, n2, sparse_mode):
+    """Head groups G = n1 / n2 of 4, 1, 2 and 2 run on the CUDA-core kernel (the tensor-core one takes
+    G in {8, 16, 32}); both sparse modes."""
+    _parity(_small(sparse_mode, seed=31 + n1 + n2 + sparse_mode, n1=n1, n2=n2))
+
+
 def test_workload4_deterministic_bitwise():
     p = synth.workload(4)
     first = _parity(p, deterministic=True)
