@@ -23,7 +23,7 @@ ATTN_MASK_NONE, ATTN_CAUSAL_TOP_LEFT, ATTN_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
 EXPORTS = ("sdpa_workspace_size", "sdpa_fwd_stats", "sdpa_bwd", "nsa_workspace_size",
            "nsa_selected_attn_bwd", "nsa_block_lists", "attn_query_status", "attn_status_string",
            "attn_set_main_kernel_events", "sdpa_bwd_static_scratch", "attn_static_scratch_status",
-           "attn_selftest_wait_timeout", "attn_last_error")
+           "attn_selftest_wait_timeout", "attn_selftest_occupy", "attn_last_error")
 
 
 class attn_view_t(C.Structure):
@@ -72,6 +72,7 @@ def load() -> C.CDLL:
         "sdpa_bwd_static_scratch": [D, view, view, view, view, view, P(C.c_float), view, view, view, V],
         "attn_static_scratch_status": [V, P(C.c_uint32)],
         "attn_selftest_wait_timeout": [V, S, C.c_double, V],
+        "attn_selftest_occupy": [I, S, C.c_double, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)

@@ -2,9 +2,9 @@
 //
 // Every check runs on the host before the first launch, so a call that
 // returns an error has launched nothing.  Launch order on the caller's
-// stream: preprocess -> main backward, which also converts dQ (dense; with split
-// dQ buffers, deterministic mode, a dQ finalize follows), and
-// preprocess -> block lists -> main -> finalizes (NSA).
+// stream: preprocess -> main backward -> dQ finalize (dense), and
+// preprocess -> block lists -> main -> finalizes (NSA); each kernel is
+// chained to its predecessor with programmatic dependent launch.
 #include <cmath>
 #include <cstring>
 
@@ -260,8 +260,6 @@ attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t 
     a.lse2 = reinterpret_cast<float *>(ws + L.lse2);
     a.dvec = reinterpret_cast<float *>(ws + L.dvec);
     a.dqacc = reinterpret_cast<float *>(ws + L.dqacc);
-    a.sync = a.status + 32;
-    a.fuse_fin = a.n_part == 1 && sh.t_q > 0 && sh.t_kv > 0 ? 1 : 0;  // one dQ buffer: the main kernel converts it
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (sh.t_q == 0 && sh.t_kv == 0) return ATTN_OK;
 
@@ -274,13 +272,13 @@ attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t 
         if ((e = mark(g_ev_before, s)) != cudaSuccess) return cuda_status(e);
         if ((e = launch_dense_bwd_main(a, pg, s)) != cudaSuccess) return cuda_status(e);
         if ((e = mark(g_ev_after, s)) != cudaSuccess) return cuda_status(e);
-        if (!a.fuse_fin && (e = launch_dq_finalize(a, pg, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = launch_dq_finalize(a, pg, s)) != cudaSuccess) return cuda_status(e);
     } else {
         if ((e = launch_dense_preprocess(a, fg, s)) != cudaSuccess) return cuda_status(e);
         if ((e = mark(g_ev_before, s)) != cudaSuccess) return cuda_status(e);
         if ((e = launch_dense_bwd_main(a, fg, s)) != cudaSuccess) return cuda_status(e);
         if ((e = mark(g_ev_after, s)) != cudaSuccess) return cuda_status(e);
-        if (!a.fuse_fin && (e = launch_dq_finalize(a, fg, s)) != cudaSuccess) return cuda_status(e);
+        if ((e = launch_dq_finalize(a, fg, s)) != cudaSuccess) return cuda_status(e);
     }
     return ATTN_OK;
 }

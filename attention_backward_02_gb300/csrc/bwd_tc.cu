@@ -156,71 +156,6 @@ template <> struct IsPacked<PackedGeo> : std::true_type {};
 
 }  // namespace
 
-// dQ = cast(scale * dQacc), run by every CTA of the main kernel once all of
-// them have counted their dQ reduce-adds as landed (the grid is one CTA per
-// SM, all resident, so the wait ends; it is bounded all the same).  A warp
-// converts one (head, 32-row) block of the accumulator at a time, heads
-// fastest, with all its loads in flight before the first store.
-template <class T, int D, int NT, class Geo>
-__device__ __forceinline__ void convert_dq(const DenseArgs &a, const Geo &geo, volatile int *go)
-{
-    constexpr int TPR = D / 8;              // 8-column chunks per row
-    constexpr int RPK = 32 / TPR;           // rows per warp-wide step
-    constexpr int KS = 8;                   // steps in flight per pass
-    constexpr int PASSES = 32 / (RPK * KS); // passes per 32-row block
-    static_assert(PASSES >= 1 && PASSES * RPK * KS == 32, "conversion split");
-    if (threadIdx.x == 0) {
-        const uint64_t t0 = globaltimer_ns();
-        bool ok = true;
-        while (ld_acquire_gpu(a.sync) < gridDim.x) {
-            if (globaltimer_ns() - t0 > 1000000000ull) {
-                ok = false;
-                break;
-            }
-            __nanosleep(200);
-        }
-        if (!ok) raise_flag(a.status, ATTN_DEV_TIMEOUT);
-        *go = ok;
-    }
-    __syncthreads();
-    if (!*go) return;
-    const int lane = threadIdx.x % 32;
-    const uint32_t nw = NT / 32, h = uint32_t(a.h);
-    const uint32_t nunit = h * uint32_t(a.t_pad / 32);
-    const int r_in = lane / TPR, c = lane % TPR;
-    T *dQ = static_cast<T *>(a.dQ.ptr);
-    for (uint32_t u = blockIdx.x * nw + threadIdx.x / 32; u < nunit; u += gridDim.x * nw) {
-        const uint32_t wt = u / h, hh = u - wt * h;
-        int64_t b = 0, i0 = 0;
-        geo.ws_locate(int64_t(wt) * 32, &b, &i0);
-        const int64_t lq = geo.q_len(b);
-        const float *src = a.dqacc + (int64_t(hh) * a.t_pad + int64_t(wt) * 32) * D + c * 8;
-        const int64_t qrow0 = IsPacked<Geo>::value ? geo.q_start(b) : 0;
-        T *dst = dQ + (IsPacked<Geo>::value ? 0 : b * a.dQ.sb) + int64_t(hh) * a.dQ.sh + c * 8;
-#pragma unroll
-        for (int ps = 0; ps < PASSES; ++ps) {
-            float4 v[KS][2];
-#pragma unroll
-            for (int k = 0; k < KS; ++k) {
-                const int r = (ps * KS + k) * RPK + r_in;
-                v[k][0] = __ldcg(reinterpret_cast<const float4 *>(src + int64_t(r) * D));
-                v[k][1] = __ldcg(reinterpret_cast<const float4 *>(src + int64_t(r) * D) + 1);
-            }
-#pragma unroll
-            for (int k = 0; k < KS; ++k) {
-                const int r = (ps * KS + k) * RPK + r_in;
-                if (i0 + r >= lq) continue;
-                uint4 o;
-                o.x = pack2<T>(v[k][0].x * a.scale, v[k][0].y * a.scale);
-                o.y = pack2<T>(v[k][0].z * a.scale, v[k][0].w * a.scale);
-                o.z = pack2<T>(v[k][1].x * a.scale, v[k][1].y * a.scale);
-                o.w = pack2<T>(v[k][1].z * a.scale, v[k][1].w * a.scale);
-                *reinterpret_cast<uint4 *>(dst + (qrow0 + i0 + r) * a.dQ.ss) = o;
-            }
-        }
-    }
-}
-
 template <class T, int D, class Geo>
 __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(const __grid_constant__ TcParams p, const Geo geo)
 {
@@ -755,15 +690,8 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
             if (leader && a.deterministic) bulk_wait0();
         }
         ATTN_END_UNITS
-        if (leader) {
-            bulk_wait0();
-            if (a.fuse_fin) {  // publish: this CTA's dQ adds have all landed
-                fence_proxy_async_global();
-                __threadfence();
-                atomicAdd(a.sync, 1u);
-            }
-        }
-        pdl_trigger();  // the dQ finalize (when there is one) may start launching; it waits for this grid
+        if (leader) bulk_wait0();  // the reduce-adds have read the staging buffer (and landed) before the exit
+        pdl_trigger();  // the dQ finalize may start launching; it waits for this grid
     }
 
 #undef ATTN_FOR_EACH_UNIT
@@ -774,7 +702,6 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::T_COLS);
     }
-    if (a.fuse_fin) convert_dq<T, D, Cfg::THREADS>(a, geo, reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 16));
 }
 
 // ===================================================================== host

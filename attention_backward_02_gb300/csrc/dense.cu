@@ -1,8 +1,7 @@
 // dense.cu -- dense SDPA kernels other than the tensor-core backward:
 //   preprocess  (D = rowsum(dO * O), LSE * log2 e, zeroed fp32 dQ accumulator)
-//   dq_finalize (dQ = cast(scale * sum of the partial dQ buffers); deterministic
-//                mode and calls without keys only: otherwise the main kernel
-//                converts its single dQ buffer itself)
+//   dq_finalize (dQ = cast(scale * sum of the partial dQ buffers, in index
+//                order); chained behind the main kernel)
 //   fwd         (O and LSE; CUDA-core kernel, not on the timed path)
 //
 // Definitions: cuDNN-frontend sample "51_scaled_dot_product_attention_backward"
@@ -79,10 +78,7 @@ __global__ void __launch_bounds__(256) dense_preprocess_kernel(DenseArgs a, Geo 
 {
     constexpr int TPR = D / 8, RPP = 256 / TPR, RPT = kUnitRows / RPP;  // rows per pass / per thread
     pdl_trigger();
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        *a.status = 0u;
-        if (a.sync) *a.sync = 0u;
-    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.status = 0u;
     const int lane_in_row = threadIdx.x % TPR, k0 = threadIdx.x / TPR;
     const int ntile = int(a.t_pad / kUnitRows);
     const int nunit = int(a.h) * ntile;

@@ -19,7 +19,7 @@ struct View {
 };
 
 // Workspace of sdpa_bwd (all offsets 256-byte aligned):
-//   status   uint32[64]              [0] device flags, [32] main-kernel CTAs whose dQ adds landed
+//   status   uint32[64]              [0] device flags
 //   lse2     f32 [h][t_pad]          LSE * log2(e); +inf on padding rows
 //   dvec     f32 [h][t_pad]          D = rowsum(dO * O); 0 on padding rows
 //   dqacc    f32 [n_part][h][t_pad][d]
@@ -40,10 +40,6 @@ struct DenseArgs {
     uint32_t *status;
     float *lse2, *dvec, *dqacc;
     int64_t tc_units;           // main kernel: work units (set by its launcher)
-    // 1: the main kernel converts dQ itself once every CTA has counted its dQ
-    // adds as landed in *sync (zeroed by the preprocess); no finalize launch
-    int fuse_fin;
-    uint32_t *sync;
 };
 
 struct Workspace {

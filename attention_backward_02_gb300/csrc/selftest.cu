@@ -26,7 +26,31 @@ __global__ void selftest_wait_timeout_kernel(uint32_t *status, uint64_t limit_ns
     if (!sm103::mbar_wait(&bar, 0, &abort_flag, limit_ns)) tc::flag_abort(&abort_flag, status);
 }
 
+// Holds its SM for `ns` nanoseconds with `dynamicSmem` bytes of shared memory
+// reserved (so a large-footprint kernel cannot share the SM), then exits.
+// Touches no memory.
+__global__ void selftest_occupy_kernel(uint64_t ns)
+{
+    extern __shared__ uint8_t occupy_smem[];
+    if (threadIdx.x != 0) return;
+    const uint64_t t0 = sm103::globaltimer_ns();
+    while (sm103::globaltimer_ns() - t0 < ns) __nanosleep(10000);
+    if (ns == 0) occupy_smem[0] = 0;  // keeps the allocation referenced
+}
+
 }  // namespace attn
+
+extern "C" attn_status_t attn_selftest_occupy(int blocks, size_t smem_bytes, double seconds, void *stream)
+{
+    using namespace attn;
+    if (blocks < 1 || blocks > 4096 || smem_bytes > 200 * 1024 || !(seconds > 0.0) || seconds > 5.0)
+        return ATTN_ERR_INVALID;
+    cudaError_t e = cudaFuncSetAttribute(selftest_occupy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem_bytes));
+    if (e != cudaSuccess) return record_cuda_error(e);
+    selftest_occupy_kernel<<<blocks, 32, smem_bytes, static_cast<cudaStream_t>(stream)>>>(uint64_t(seconds * 1e9));
+    return record_cuda_error(cudaGetLastError());
+}
 
 extern "C" attn_status_t attn_selftest_wait_timeout(void *workspace, size_t workspace_bytes, double limit_s,
                                                     void *stream)

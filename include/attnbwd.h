@@ -138,11 +138,9 @@ attn_status_t sdpa_fwd_stats(const attn_sdpa_desc_t *desc, attn_view_t q, attn_v
  * computation.  q, o, dO, dQ: [B,h,s_q,d] views; k, v, dK, dV: [B,h_kv,s_kv,d];
  * lse as sdpa_fwd_stats writes it.  dQ / dK / dV may have any strides that
  * follow the 16-byte rule (the sample allocates them empty_like the inputs).
- * Outputs have the input dtype, rounded to nearest even.  In the default
- * (non-deterministic) mode the main kernel's blocks, one per SM, wait for one
- * another before converting dQ: they must be able to run at once, as they do
- * on a device the call has to itself; if they cannot, the wait runs out after
- * about a second and ATTN_DEV_TIMEOUT is set.                               */
+ * Outputs have the input dtype, rounded to nearest even.  No block of any
+ * kernel waits for another block, so the call is safe next to other work on
+ * the device (other streams, other processes).                              */
 attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t k, attn_view_t v,
                        attn_view_t o, attn_view_t dO, const float *lse, attn_view_t dQ, attn_view_t dK,
                        attn_view_t dV, void *workspace, size_t workspace_bytes, void *stream);
@@ -248,6 +246,13 @@ attn_status_t attn_query_status(void *workspace, void *stream, uint32_t *device_
  * attn_query_status.  [Ascend] "Return Value" (failures as codes, never a
  * crash).                                                                   */
 attn_status_t attn_selftest_wait_timeout(void *workspace, size_t workspace_bytes, double limit_s, void *stream);
+
+/* Test aid: launches `blocks` blocks of 32 threads that each reserve
+ * smem_bytes (<= 200 KiB) of shared memory and hold their SM for `seconds`
+ * (0 < seconds <= 5) without touching memory, so a test can run the
+ * backward while other work occupies part of the GPU.  No counterpart on the
+ * pages.                                                                    */
+attn_status_t attn_selftest_occupy(int blocks, size_t smem_bytes, double seconds, void *stream);
 
 /* Optional instrumentation for benchmarks.  While set, every sdpa_bwd and
  * nsa_selected_attn_bwd call made from this host thread records the CUDA

@@ -172,6 +172,14 @@ def test_selftest_rejects_before_launch(ab):
     assert call(lim=float("nan")) == 2
 
 
+def test_occupy_rejects_before_launch(ab):
+    lib = ab._lib.load()
+    assert lib.attn_selftest_occupy(0, 1024, C.c_double(0.1), None) == 2
+    assert lib.attn_selftest_occupy(8, 300 * 1024, C.c_double(0.1), None) == 2
+    assert lib.attn_selftest_occupy(8, 1024, C.c_double(9.0), None) == 2
+    assert lib.attn_selftest_occupy(8, 1024, C.c_double(0.0), None) == 2
+
+
 def test_static_scratch_status_needs_its_pointer(ab):
     assert ab._lib.load().attn_static_scratch_status(None, None) == 1
 

@@ -36,3 +36,26 @@ def test_wait_timeout_sets_flag_and_context_survives():
     H.assert_close(dk, rk, "dK")
     H.assert_close(dv, rv, "dV")
     assert np.all(np.isfinite(dq))
+
+
+def test_backward_while_other_work_holds_some_sms():
+    """The main kernel's blocks wait for one another before converting dQ.  While another stream's
+    kernel holds 8 SMs (and their shared memory) for 1.5 s, longer than that wait's one-second limit,
+    the backward must still complete correctly: its launch is cooperative, so its blocks run only
+    once they can all be resident, and none waits for a block that has not started."""
+    import torch
+    import attention_backward_02_gb300 as ab
+    lib = ab._lib.load()
+    p = synth.dense_problem("shared_gpu", dtype=synth.F16, b=1, h=16, h_kv=16, d=64, s_q=1280, s_kv=1280,
+                            scale=0.125, mask=oracle.CAUSAL_TOP_LEFT, seed=43)  # 160 work units >= the SMs
+    o_bits, lse = H.oracle_forward(p)
+    ref = oracle.dense_bwd(p.f64("q"), p.f64("k"), p.f64("v"), synth.bits_to_f64(o_bits, p.dtype), p.f64("do"),
+                           lse, p.cu_q, p.cu_kv, p.scale, p.mask)
+    other = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    ab.check(lib.attn_selftest_occupy(8, 120 * 1024, C.c_double(1.5), C.c_void_p(other.cuda_stream)),
+             "attn_selftest_occupy")
+    dq, dk, dv = H.run_gpu_bwd(p, o_bits, lse)  # asserts a clean device status (no timeout)
+    torch.cuda.synchronize()
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        H.assert_close(g, r, name)
