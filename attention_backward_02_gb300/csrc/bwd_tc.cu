@@ -117,7 +117,7 @@ struct TcSched {
 };
 
 struct TcParams {
-    CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq;
+    CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dq, tm_dk, tm_dv;
     DenseArgs a;
     TcSched sched;
 };
@@ -368,6 +368,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
 #pragma unroll
                     for (int kk = 0; kk < BM / 16; ++kk)
                         mma_f16_ss(tmem + Cfg::T_DK, kmaj_step(kdS, BN, kk), mn_step(mQ, kk), idDV, !first || kk > 0);
+                    mma_commit(&q_empty[st]);  // the Q / dO stage may be refilled once dV / dK have read it
                 }
                 if (x > 0) wait(dq_free, (x - 1) & 1);
                 if (ok) {
@@ -379,7 +380,6 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                             mma_f16_ss(tmem + Cfg::T_DQ, mn_step(mK, kk), mn_step(mdS, kk), idDQ, kk > 0);
                     }
                     mma_commit(mma_done);
-                    mma_commit(&q_empty[st]);
                     mma_commit(&ds_free[x & 1]);
                 }
             };
@@ -585,23 +585,68 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
         for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
             const int64_t j0 = jt * BN, j = j0 + r;
             const bool row_ok = j < lkv;
-            const int64_t kv_tok = kv_row0 + j;
-            const int64_t offk = kv_b * a.dK.sb + g * a.dK.sh + kv_tok * a.dK.ss;
-            const int64_t offv = kv_b * a.dV.sb + g * a.dV.sh + kv_tok * a.dV.ss;
+            // element offsets of this thread's dK / dV row (recomputed where used: fewer live registers)
+            auto offk = [&]() { return kv_b * a.dK.sb + g * a.dK.sh + (kv_row0 + j) * a.dK.ss; };
+            auto offv = [&]() { return kv_b * a.dV.sb + g * a.dV.sh + (kv_row0 + j) * a.dV.ss; };
             int qt0, nq;
             query_tiles<BM>(a.mask, j0, lq, lkv, &qt0, &nq);
             const int n_iter = G * nq;
             if (n_iter == 0) {  // no query sees these keys: dK = dV = 0
                 if (row_ok)
                     for (int x = 0; x < D; x += 8) {
-                        *reinterpret_cast<uint4 *>(dK + offk + x) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(dV + offv + x) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(dK + offk() + x) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(dV + offv() + x) = make_uint4(0, 0, 0, 0);
                     }
                 continue;
             }
-            // dK (scaled) and dV of this key tile, once its last GEMMs have completed: read out of TMEM
-            // first (the accumulators are released right after the last read, so the next key tile's
-            // first GEMMs need not wait for the dQ reduce), then stored
+            // dK (scaled) and dV of this key tile, once its last GEMMs have completed.  When TMA may
+            // store the tile whole (fixed-length layout, whose extent clips the last tile; or a packed
+            // tile inside its sequence), each 64-column box of dV, then of dK, is staged as 16-bit rows
+            // in the dQ staging buffer and written by a TMA store.
+            const bool tma_epi = !kPacked || j0 + BN <= lkv;
+            auto epilogue_tma = [&]() {
+                constexpr int NBOX = D / 64;
+#pragma unroll 1
+                for (int t = 0; t < 2 * NBOX; ++t) {
+                    const bool isk = t >= NBOX;
+                    const int cb = t % NBOX;
+                    const uint32_t tcol = (isk ? Cfg::T_DK : Cfg::T_DV) + cb * 64;
+                    const float mul = isk ? a.scale : 1.f;
+                    if (leader) bulk_wait_read0();  // the buffer's previous reader (reduce or store) is done
+                    named_bar_sync(2, 128);
+                    if (ok) {
+#pragma unroll
+                        for (int c16 = 0; c16 < 4; ++c16) {  // 16 columns at a time, two 16-byte chunks
+                            uint32_t w[16];
+                            tmem_ld16(tmem + lane_addr + tcol + c16 * 16, w);
+                            tmem_ld_wait_regs(w);
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const uint32_t off = sw128_offset(uint32_t(r), uint32_t(c16 * 16 + h2 * 8), BN);
+                                st_shared_v4(aDQS + off,
+                                             pack2<T>(__uint_as_float(w[8 * h2 + 0]) * mul, __uint_as_float(w[8 * h2 + 1]) * mul),
+                                             pack2<T>(__uint_as_float(w[8 * h2 + 2]) * mul, __uint_as_float(w[8 * h2 + 3]) * mul),
+                                             pack2<T>(__uint_as_float(w[8 * h2 + 4]) * mul, __uint_as_float(w[8 * h2 + 5]) * mul),
+                                             pack2<T>(__uint_as_float(w[8 * h2 + 6]) * mul, __uint_as_float(w[8 * h2 + 7]) * mul));
+                            }
+                        }
+                    }
+                    if (t == 2 * NBOX - 1) {  // every accumulator column has been read
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_free);
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(2, 128);
+                    if (leader && ok) {
+                        tma_store_4d(isk ? &p.tm_dk : &p.tm_dv, sDQS, cb * 64, int(kv_row0 + j0), int(g), kv_b);
+                        bulk_commit();
+                    }
+                }
+            };
+            // otherwise: read out of TMEM first (the accumulators are released right after the last
+            // read, so the next key tile's first GEMMs need not wait for the dQ reduce), then stored
+            // row by row
             auto epilogue = [&]() {
 #pragma unroll 1
                 for (int cc = 0; cc < D / 8; ++cc) {
@@ -626,8 +671,8 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                         ok4.y = pack2<T>(__uint_as_float(u[2]) * a.scale, __uint_as_float(u[3]) * a.scale);
                         ok4.z = pack2<T>(__uint_as_float(u[4]) * a.scale, __uint_as_float(u[5]) * a.scale);
                         ok4.w = pack2<T>(__uint_as_float(u[6]) * a.scale, __uint_as_float(u[7]) * a.scale);
-                        *reinterpret_cast<uint4 *>(dV + offv + cc * 8) = ov;
-                        *reinterpret_cast<uint4 *>(dK + offk + cc * 8) = ok4;
+                        *reinterpret_cast<uint4 *>(dV + offv() + cc * 8) = ov;
+                        *reinterpret_cast<uint4 *>(dK + offk() + cc * 8) = ok4;
                     }
                 }
             };
@@ -641,7 +686,10 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                 if (ok && !(ok = mbar_wait(mma_done, qi & 1, abort))) flag_abort(abort, a.status);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
-                if (it == n_iter - 1) epilogue();
+                if (it == n_iter - 1) {
+                    if (tma_epi) epilogue_tma();
+                    else epilogue();
+                }
                 // dQ of tile qi, half of its columns at a time, through the staging buffer
                 const int64_t row0 = part * a.h * a.t_pad + geo.ws_start(b) + hq * a.t_pad + i0;
                 // read the whole accumulator first, so the next tile's dQ GEMM is not held up by the
@@ -834,7 +882,9 @@ template <class T, int D, class Geo> cudaError_t run_tc(const DenseArgs &a, cons
                    !map_view(&prm.tm_do, a.dO, a.dtype, D, sq, a.h, nb, Cfg::BM)))
         return cudaErrorInvalidValue;
     if (!map_view(&prm.tm_k, a.k, a.dtype, D, skv, a.h_kv, nb, Cfg::BN) ||
-        !map_view(&prm.tm_v, a.v, a.dtype, D, skv, a.h_kv, nb, Cfg::BN))
+        !map_view(&prm.tm_v, a.v, a.dtype, D, skv, a.h_kv, nb, Cfg::BN) ||
+        !map_view(&prm.tm_dk, a.dK, a.dtype, D, skv, a.h_kv, nb, Cfg::BN) ||
+        !map_view(&prm.tm_dv, a.dV, a.dtype, D, skv, a.h_kv, nb, Cfg::BN))
         return cudaErrorInvalidValue;
     if (!map_dqacc(&prm.tm_dq, a.dqacc, D, int64_t(a.n_part) * a.h * a.t_pad, Cfg::DQ_BOX_ROWS))
         return cudaErrorInvalidValue;
