@@ -51,6 +51,7 @@
 // the CTA drains its in-flight copies and MMAs, frees its TMEM and exits.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <climits>
 #include <type_traits>
 
@@ -262,6 +263,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                     const int64_t use = x / NST;
                     if (use > 0 && ok && !(ok = mbar_wait(&q_empty[st], uint32_t(use - 1) & 1, abort)))
                         flag_abort(abort, a.status);
+                    // the CTA's first tile gets its inputs before the rest of the ring is filled: every
+                    // CTA starts by loading at once, and the later stages would compete for the memory
+                    if (x == 1 && ok && !(ok = mbar_wait(&q_full[0], 0, abort))) flag_abort(abort, a.status);
                     if (!ok) return;
                     const int64_t hq = g * G + it / nq, i0 = int64_t(qt0 + it % nq) * BM;
                     uint8_t *sQ = smem + Cfg::OFF_Q + st * Cfg::Q_BYTES, *sdO = smem + Cfg::OFF_DO + st * Cfg::Q_BYTES;
@@ -296,7 +300,9 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                 if (kt == 0) load_kv();
                 load_q(0, qi);
                 // warm L2 with the K / V tile this CTA takes next, so its load does not stall the next unit
-                {
+                // (on the CTA's first tile only after its second query tile: the first tile's own loads
+                // go first)
+                auto prefetch_next = [&]() {
                     int64_t nb = b, ng = g, njt = jt + tile_step, nrow0 = kv_row0;
                     int nkv_b = kv_b;
                     bool has = njt < ntiles;
@@ -318,10 +324,14 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                             tma_prefetch_4d(&p.tm_k, c * 64, int(nrow0 + njt * BN), int(ng), nkv_b);
                             tma_prefetch_4d(&p.tm_v, c * 64, int(nrow0 + njt * BN), int(ng), nkv_b);
                         }
-                }
+                };
+                if (kt > 0 || n_iter == 1) prefetch_next();
                 if (kt > 0) load_kv();
                 ++qi;
-                for (int it = 1; it < n_iter; ++it, ++qi) load_q(it, qi);
+                for (int it = 1; it < n_iter; ++it, ++qi) {
+                    load_q(it, qi);
+                    if (kt == 0 && it == 1) prefetch_next();
+                }
                 ++kt;
             }
             ATTN_END_UNITS
@@ -352,12 +362,28 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
             const uint64_t kK = desc_kmaj(aK, BN, 0), kV = desc_kmaj(aV, BN, 0), mK = desc_mn(aK, BN, 0);
             // dV, dK, dQ of query tile x (global index) whose P / dS are ready
             // x: global index of the query tile, xs: its ring stage
-            auto grads = [&](uint32_t x, int xs, bool first) {
+            // last: the key tile's last query tile; its dQ GEMM, the only one of the three that reads K,
+            // goes first, so the K / V reload for the next key tile can start as early as possible
+            auto grads = [&](uint32_t x, int xs, bool first, bool last) {
                 const int st = xs;
                 const uint32_t adS = smem_u32(sX + (x & 1) * Cfg::X_BYTES);
                 const uint64_t mdO = desc_mn(smem_u32(smem + Cfg::OFF_DO + st * Cfg::Q_BYTES), BM, 0);
                 const uint64_t mQ = desc_mn(smem_u32(smem + Cfg::OFF_Q + st * Cfg::Q_BYTES), BM, 0);
                 const uint64_t kdS = desc_kmaj(adS, BN, 0), mdS = desc_mn(adS, BN, 0);
+                auto dq_gemm = [&]() {
+                    if (x > 0) wait(dq_free, (x - 1) & 1);
+                    if (ok) {
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            if (D == 64)
+                                mma_f16_ss(tmem + Cfg::T_DQ, mn_step(mdS, kk), mn_step(mK, kk), idDQ, kk > 0);
+                            else
+                                mma_f16_ss(tmem + Cfg::T_DQ, mn_step(mK, kk), mn_step(mdS, kk), idDQ, kk > 0);
+                        }
+                        if (last) mma_commit(kv_empty);  // K / V are no longer read once these GEMMs finish
+                    }
+                };
+                if (last) dq_gemm();
                 // a new key tile overwrites dV / dK: the previous tile's epilogue has read them
                 if (first && kt > 0) wait(acc_free, uint32_t(kt - 1) & 1);
                 if (ok) {
@@ -370,15 +396,8 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                         mma_f16_ss(tmem + Cfg::T_DK, kmaj_step(kdS, BN, kk), mn_step(mQ, kk), idDV, !first || kk > 0);
                     mma_commit(&q_empty[st]);  // the Q / dO stage may be refilled once dV / dK have read it
                 }
-                if (x > 0) wait(dq_free, (x - 1) & 1);
+                if (!last) dq_gemm();
                 if (ok) {
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        if (D == 64)
-                            mma_f16_ss(tmem + Cfg::T_DQ, mn_step(mdS, kk), mn_step(mK, kk), idDQ, kk > 0);
-                        else
-                            mma_f16_ss(tmem + Cfg::T_DQ, mn_step(mK, kk), mn_step(mdS, kk), idDQ, kk > 0);
-                    }
                     mma_commit(mma_done);
                     mma_commit(&ds_free[x & 1]);
                 }
@@ -415,7 +434,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                     }
                     if (it > 0) {
                         wait(p_ready, (qi - 1) & 1);
-                        grads(qi - 1, prev_st, it == 1);
+                        grads(qi - 1, prev_st, it == 1, false);
                     }
                     prev_st = st;
                     if (++st == NST) {
@@ -424,8 +443,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                     }
                 }
                 wait(p_ready, (qi - 1) & 1);
-                grads(qi - 1, prev_st, n_iter == 1);
-                if (ok) mma_commit(kv_empty);  // K / V free for the next tile once these GEMMs finish
+                grads(qi - 1, prev_st, n_iter == 1, true);
                 ++kt;
             }
             ATTN_END_UNITS
@@ -601,9 +619,11 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
             }
             // dK (scaled) and dV of this key tile, once its last GEMMs have completed.  When TMA may
             // store the tile whole (fixed-length layout, whose extent clips the last tile; or a packed
-            // tile inside its sequence), each 64-column box of dV, then of dK, is staged as 16-bit rows
-            // in the dQ staging buffer and written by a TMA store.
-            const bool tma_epi = !kPacked || j0 + BN <= lkv;
+            // tile inside its sequence), dV, then dK, is staged as 16-bit rows in the dQ staging buffer
+            // and written by a TMA store
+            // (d = 64 only: at d = 128 the 64 KB of dK / dV would pass through the 16 KB buffer in four
+            // serial rounds, slower than the row stores)
+            const bool tma_epi = D == 64 && (!kPacked || j0 + BN <= lkv);
             auto epilogue_tma = [&]() {
                 constexpr int NBOX = D / 64;
 #pragma unroll 1
@@ -816,55 +836,116 @@ template <class Geo> int64_t max_kv_len(const Geo &g)
     return m;
 }
 
-// Assigns the work units of a fixed-length batch to `ctas` CTAs, longest first, each to the CTA
-// with the least planned work (a greedy longest-processing-time schedule).  Unit index order is
-// already longest first there.  A unit's cost is its query tiles plus one and a half for its start
-// (loading K / V, filling the pipeline, the dK / dV epilogue), in half tiles.  Leaves on = 0 (snake
-// order) in deterministic mode, for varlen batches (sorted by length, the units running together
-// would be one long sequence's, adding into the same dQ rows) or when the plan does not fit.
+// Assigns the work units of a fixed-length batch to `ctas` CTAs.  A unit's cost is its query tiles
+// plus one for its start (loading K / V, the pipeline refill, the dK / dV epilogue), in half tiles;
+// units without work cost one (they write zero dK / dV rows).  Two plans: greedy (each unit,
+// longest first, to the least loaded CTA) and bin packing, first fit decreasing (with a capacity
+// starting at the mean load per CTA, at least the largest unit, units longest first go to the
+// first CTA they fit in; the capacity grows until ctas CTAs suffice).  The packing finds the
+// balanced groupings of the causal workloads' regular unit sizes that greedy misses by up to a
+// tile; it is used when its makespan is at least 3 % shorter.  Each CTA takes its units longest
+// first.  The plan of the last shape is kept
+// (planning is host work on every call).  Leaves on = 0 (snake order) in deterministic mode, for
+// varlen batches (sorted by length, the units running together would be one long sequence's,
+// adding into the same dQ rows) or when the plan does not fit.
 template <int BM, int BN, class Geo>
 void plan_units(TcSched &S, const DenseArgs &a, const Geo &g, int64_t units, int64_t ctas)
 {
     S.on = 0;
     if (IsPacked<Geo>::value || a.deterministic || units > kSchedUnits || ctas > kSchedCtas || ctas < 1) return;
-    const int64_t nheads = a.nseq * a.h_kv, G = a.h / a.h_kv;
-    static thread_local uint16_t cta_of[kSchedUnits];
-    uint64_t heap[kSchedCtas];  // min-heap of (planned work << 16 | CTA)
-    uint16_t cnt[kSchedCtas];
-    const int n = int(ctas);
-    for (int c = 0; c < n; ++c) {
-        heap[c] = uint64_t(c);
-        cnt[c] = 0;
+    struct Key {
+        int64_t nseq, h, h_kv, s_q, s_kv, units, ctas;
+        int mask;
+        bool operator==(const Key &o) const
+        {
+            return nseq == o.nseq && h == o.h && h_kv == o.h_kv && s_q == o.s_q && s_kv == o.s_kv && units == o.units &&
+                   ctas == o.ctas && mask == o.mask;
+        }
+    };
+    static thread_local Key last_key = {-1, 0, 0, 0, 0, 0, 0, 0};
+    static thread_local TcSched last_plan;
+    const Key key = {a.nseq, a.h, a.h_kv, g.q_len(0), g.kv_len(0), units, ctas, a.mask};
+    if (key == last_key) {
+        S = last_plan;
+        return;
     }
-    for (int64_t u = 0; u < units; ++u) {
+    const int64_t nheads = a.nseq * a.h_kv, G = a.h / a.h_kv;
+    const int n = int(ctas), nu = int(units);
+    static thread_local int32_t cost[kSchedUnits], order[kSchedUnits], cta_of[kSchedUnits];
+    int64_t load[kSchedCtas];
+    int64_t total = 0, biggest = 0;
+    for (int u = 0; u < nu; ++u) {
         const int64_t jt = u / nheads, b = (u % nheads) / a.h_kv;
         const int64_t lq = g.q_len(b), lkv = g.kv_len(b);
-        cta_of[u] = 0xffff;
-        if (jt * BN >= lkv) continue;  // past the keys: nothing to do
-        const int64_t i_lo = first_query_seeing(a.mask, jt * BN, lq, lkv);
-        const int64_t nq = lq <= 0 || i_lo >= lq ? 0 : (lq + BM - 1) / BM - i_lo / BM;
-        const int c = int(heap[0] & 0xffff);
-        cta_of[u] = uint16_t(c);
-        ++cnt[c];
-        heap[0] += uint64_t(2 * G * nq + 3) << 16;
-        for (int i = 0;;) {  // sift the root down
-            const int l = 2 * i + 1, r = l + 1;
-            int m = i;
-            if (l < n && heap[l] < heap[m]) m = l;
-            if (r < n && heap[r] < heap[m]) m = r;
-            if (m == i) break;
-            const uint64_t t = heap[i];
-            heap[i] = heap[m];
-            heap[m] = t;
-            i = m;
+        int64_t nq = 0;
+        if (jt * BN < lkv) {
+            const int64_t i_lo = first_query_seeing(a.mask, jt * BN, lq, lkv);
+            nq = lq <= 0 || i_lo >= lq ? 0 : (lq + BM - 1) / BM - i_lo / BM;
+        }
+        cost[u] = jt * BN >= lkv ? 0 : nq > 0 ? int32_t(2 * G * nq + 2) : 1;
+        order[u] = u;
+        total += cost[u];
+        biggest = cost[u] > biggest ? cost[u] : biggest;
+    }
+    std::stable_sort(order, order + nu, [&](int32_t x, int32_t y) { return cost[x] > cost[y]; });
+    // greedy: each unit, longest first, to the least loaded CTA
+    static thread_local int32_t greedy_of[kSchedUnits];
+    int64_t greedy_max = 0;
+    {
+        for (int c = 0; c < n; ++c) load[c] = 0;
+        for (int k = 0; k < nu; ++k) {
+            const int u = order[k];
+            greedy_of[u] = -1;
+            if (cost[u] == 0) continue;
+            int c = 0;
+            for (int d = 1; d < n; ++d)
+                if (load[d] < load[c]) c = d;
+            greedy_of[u] = c;
+            load[c] += cost[u];
+            greedy_max = load[c] > greedy_max ? load[c] : greedy_max;
         }
     }
+    int64_t cap = (total + n - 1) / n;
+    cap = cap > biggest ? cap : biggest;
+    for (;; ++cap) {
+        int used = 0;
+        bool fits = true;
+        for (int k = 0; k < nu && fits; ++k) {
+            const int u = order[k];
+            cta_of[u] = -1;
+            if (cost[u] == 0) continue;  // past the keys: nothing to do
+            int c = 0;
+            while (c < used && load[c] + cost[u] > cap) ++c;
+            if (c == used) {
+                if (used == n) {
+                    fits = false;
+                    break;
+                }
+                load[used++] = 0;
+            }
+            cta_of[u] = c;
+            load[c] += cost[u];
+        }
+        if (fits) break;
+    }
+    // the packing is kept only where it shortens the planned makespan clearly: the greedy plan
+    // starts the heads' units interleaved, which long sequences need for L2 reuse of Q / dO
+    if (100 * cap > 97 * greedy_max)
+        for (int u = 0; u < nu; ++u) cta_of[u] = greedy_of[u];
+    int cnt[kSchedCtas];
+    for (int c = 0; c < n; ++c) cnt[c] = 0;
+    for (int u = 0; u < nu; ++u)
+        if (cta_of[u] >= 0) ++cnt[cta_of[u]];
     S.off[0] = 0;
     for (int c = 0; c < n; ++c) S.off[c + 1] = uint16_t(S.off[c] + cnt[c]);
     for (int c = 0; c < n; ++c) cnt[c] = S.off[c];
-    for (int64_t u = 0; u < units; ++u)
-        if (cta_of[u] != 0xffff) S.unit[cnt[cta_of[u]]++] = uint16_t(u);
+    for (int k = 0; k < nu; ++k) {  // each CTA's units longest first
+        const int u = order[k];
+        if (cta_of[u] >= 0) S.unit[cnt[cta_of[u]]++] = uint16_t(u);
+    }
     S.on = 1;
+    last_plan = S;
+    last_key = key;
 }
 
 template <class T, int D, class Geo> cudaError_t run_tc(const DenseArgs &a, const Geo &g, cudaStream_t s)
