@@ -5,8 +5,9 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--w
 Default workload 1: dense SDPA backward, fp16, b4 h12 s1024 d64, scale 1/8,
 causal, BSHD storage viewed as BHSD (the GPT-2 sizes of the cuDNN-frontend
 SDPA-backward sample).  A step is one sdpa_bwd call (preprocess, then the
-main backward kernel, which also converts dQ) on inputs resident in HBM; the L2 is flushed between
-steps by writing a 512 MB buffer outside the timed events.  FLOPs are
+main backward kernel, dQ finalize) on inputs resident in HBM; the L2 is flushed between
+steps by writing a 512 MB buffer outside the timed events.  The line also carries the other
+workloads (2-4, both dQ modes) under "workloads".  FLOPs are
 counted as 10 b h s_q s_kv d, halved for causal; NSA counts
 10 T1 n1 (count * size) d over the selected slots.
 
@@ -295,10 +296,149 @@ def job_tflops(world, flops_per_replica, ms_per_step):
 
 # ------------------------------------------------------------------- GPU arm
 
+def nsa_useful_flops(p):
+    """FLOPs of the selected slots whose block has at least one key the token sees under the sparse
+    mode (10 d per visible-block key, n1 heads): the slot count less the fully masked filler blocks."""
+    starts_q = np.concatenate([[0], p.cu_q[:-1]])
+    lq = p.cu_q - starts_q
+    lkv = p.cu_kv - np.concatenate([[0], p.cu_kv[:-1]])
+    seq = np.repeat(np.arange(len(lq)), lq)
+    pos = np.arange(p.t1) - starts_q[seq]
+    if p.sparse_mode == 2:
+        last = pos + (lkv - lq)[seq]                       # last visible key of each token
+        first_key = p.topk.astype(np.int64) * p.block_size  # [T1, n2, cnt]
+        useful = (first_key <= last[:, None, None]).sum()
+    else:
+        useful = p.topk.size
+    return 10.0 * float(useful) * (p.n1 // p.n2) * p.block_size * p.d
+
+
+class Problem:
+    """One workload's inputs resident in HBM, its outputs and workspace, and step(set, stream): one
+    backward call on buffer set `set` (two sets, for the pipelined end-to-end measurement)."""
+
+    def __init__(self, p, deterministic, sets=1):
+        import torch
+        import attention_backward_02_gb300 as ab
+        from tests import harness as H
+        self.p, self.ab = p, ab
+        self.nsa = isinstance(p, synth.NsaProblem)
+        self.sets = []
+        if self.nsa:
+            o_bits, mx, sm = H.nsa_oracle_inputs(p)
+            self.desc = H.nsa_desc(p, deterministic)
+            self.launches = 7
+            nbytes = ab.nsa_workspace_size(self.desc)
+            for _ in range(sets):
+                q, k, v, do, o = (H.bits_to_gpu(x, p.dtype) for x in (p.q, p.k, p.v, p.do, o_bits))
+                mx8 = torch.from_numpy(np.repeat(mx[..., None], 8, -1)).cuda()
+                sm8 = torch.from_numpy(np.repeat(sm[..., None], 8, -1)).cuda()
+                topk = torch.from_numpy(p.topk).cuda()
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+                ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+                self.sets.append(dict(inputs=[q, k, v, o, do, mx8, sm8, topk], outputs=[dq, dk, dv], ws=ws))
+        else:
+            self.desc = H.dense_desc(p, deterministic)
+            self.launches = 3  # preprocess, main kernel, dQ finalize
+            nbytes = ab.sdpa_workspace_size(self.desc)[1]
+            for si in range(sets):
+                q, k, v, do = (H.bits_to_gpu(x, p.dtype) for x in (p.q, p.k, p.v, p.do))
+                if si == 0:
+                    o = torch.empty_like(q)
+                    lse = torch.empty(p.t_q * p.h, dtype=torch.float32, device="cuda")
+                    vq, vk, vv, vo = H.dense_views(p, (q, k, v, o))
+                    ab.sdpa_fwd_stats(H.dense_desc(p), vq, vk, vv, vo, lse)  # O and LSE from the library forward
+                else:
+                    o, lse = self.sets[0]["inputs"][3].clone(), self.sets[0]["inputs"][5].clone()
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+                ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+                views = H.dense_views(p, (q, k, v, o, do, dq, dk, dv))
+                self.sets.append(dict(inputs=[q, k, v, o, do, lse], outputs=[dq, dk, dv], ws=ws, views=views))
+
+    def step(self, si=0, stream=None):
+        t = self.sets[si]
+        if self.nsa:
+            q, k, v, o, do, mx8, sm8, topk = t["inputs"]
+            dq, dk, dv = t["outputs"]
+            self.ab.nsa_selected_attn_bwd(self.desc, q, k, v, o, do, mx8, sm8, topk, dq, dk, dv, workspace=t["ws"],
+                                          stream=stream)
+        else:
+            vq, vk, vv, vo, vdo, vdq, vdk, vdv = t["views"]
+            self.ab.sdpa_bwd(self.desc, vq, vk, vv, vo, vdo, t["inputs"][5], vdq, vdk, vdv, workspace=t["ws"],
+                             stream=stream)
+
+    def status(self, si=0):
+        return self.ab.attn_query_status(self.sets[si]["ws"])
+
+
+def time_calls(prob, steps, flush, stream, lib):
+    """Per step: CUDA events around the whole call (L2 flushed between steps, outside the events), then
+    a second pass with events around the main kernel alone.  Returns (call_ms list, main_ms list)."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in ev:  # instantiate the events before the timed region
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        e_call0, _, _, e_call1 = ev[i]
+        e_call0.record(stream)
+        prob.step(0, stream)
+        e_call1.record(stream)
+        flush.fill_(1)
+    torch.cuda.synchronize()
+    # events inside the call break the launch overlap, so this pass does not feed the headline number
+    for i in range(steps):
+        _, e_main0, e_main1, _ = ev[i]
+        lib.attn_set_main_kernel_events(C.c_void_p(e_main0.cuda_event), C.c_void_p(e_main1.cuda_event))
+        prob.step(0, stream)
+        lib.attn_set_main_kernel_events(None, None)
+        flush.fill_(1)
+    torch.cuda.synchronize()
+    return [ev[i][0].elapsed_time(ev[i][3]) for i in range(steps)], [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
+
+
+def e2e_pipelined(prob, steps, flush_unused=None):
+    """End to end through the C ABI with host buffers, steps pipelined over two device buffer sets and
+    three streams: the host-to-device copy of step i+1 and the device-to-host copy of step i-1 overlap
+    the call of step i.  Returns ms per step (first copy in to last copy out, over steps)."""
+    import torch
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    host_in = [[torch.empty(x.shape, dtype=x.dtype, pin_memory=True).copy_(x) for x in t["inputs"]]
+               for t in prob.sets]
+    host_out = [[torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in t["outputs"]] for t in prob.sets]
+    ev_in = [torch.cuda.Event() for _ in prob.sets]
+    ev_cmp = [torch.cuda.Event() for _ in prob.sets]
+    ev_out = [torch.cuda.Event() for _ in prob.sets]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(s_in)
+    for i in range(steps):
+        si = i % len(prob.sets)
+        t = prob.sets[si]
+        if i >= len(prob.sets):  # the set's previous step has been computed and copied out
+            s_in.wait_event(ev_cmp[si])
+            s_in.wait_event(ev_out[si])
+        with torch.cuda.stream(s_in):
+            for dst, src in zip(t["inputs"], host_in[si]):
+                dst.copy_(src, non_blocking=True)
+        ev_in[si].record(s_in)
+        s_cmp.wait_event(ev_in[si])
+        prob.step(si, s_cmp)
+        ev_cmp[si].record(s_cmp)
+        s_out.wait_event(ev_cmp[si])
+        with torch.cuda.stream(s_out):
+            for dst, src in zip(host_out[si], t["outputs"]):
+                dst.copy_(src, non_blocking=True)
+        ev_out[si].record(s_out)
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
 def run_ours(args, info):
     import torch
     import attention_backward_02_gb300 as ab
-    from tests import harness as H
 
     p, flops, cfg = info
     rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
@@ -311,50 +451,15 @@ def run_ours(args, info):
     lib = ab._lib.load()
     stream = torch.cuda.current_stream()
     nsa = isinstance(p, synth.NsaProblem)
-
-    # ---- inputs resident in HBM (O and the stats from the forward) ----
-    if nsa:
-        o_bits, mx, sm = H.nsa_oracle_inputs(p)
-        q, k, v, do, o = (H.bits_to_gpu(x, p.dtype) for x in (p.q, p.k, p.v, p.do, o_bits))
-        mx8 = torch.from_numpy(np.repeat(mx[..., None], 8, -1)).cuda()
-        sm8 = torch.from_numpy(np.repeat(sm[..., None], 8, -1)).cuda()
-        topk = torch.from_numpy(p.topk).cuda()
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        desc = H.nsa_desc(p)
-        ws = torch.empty(ab.nsa_workspace_size(desc), dtype=torch.uint8, device="cuda")
-        inputs = [q, k, v, o, do, mx8, sm8, topk]
-        outputs = [dq, dk, dv]
-        launches_per_step = 7
-
-        def step():
-            ab.nsa_selected_attn_bwd(desc, q, k, v, o, do, mx8, sm8, topk, dq, dk, dv, workspace=ws, stream=stream)
-    else:
-        q, k, v, do = (H.bits_to_gpu(x, p.dtype) for x in (p.q, p.k, p.v, p.do))
-        o = torch.empty_like(q)
-        lse = torch.empty(p.t_q * p.h, dtype=torch.float32, device="cuda")
-        desc = H.dense_desc(p)
-        vq, vk, vv, vo = H.dense_views(p, (q, k, v, o))
-        ab.sdpa_fwd_stats(desc, vq, vk, vv, vo, lse)  # O and LSE from the library's forward
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        vdo, vdq, vdk, vdv = H.dense_views(p, (do, dq, dk, dv))
-        ws = torch.empty(ab.sdpa_workspace_size(desc)[1], dtype=torch.uint8, device="cuda")
-        inputs = [q, k, v, o, do, lse]
-        outputs = [dq, dk, dv]
-        launches_per_step = 2  # preprocess, main kernel (which also converts dQ)
-
-        def step():
-            ab.sdpa_bwd(desc, vq, vk, vv, vo, vdo, lse, vdq, vdk, vdv, workspace=ws, stream=stream)
+    prob = Problem(p, False, sets=2)
+    launches_per_step = prob.launches
+    inputs, outputs = prob.sets[0]["inputs"], prob.sets[0]["outputs"]
 
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     for _ in range(args.warmup):
-        step()
+        prob.step(0, stream)
         flush.fill_(1)
-    assert ab.attn_query_status(ws) == 0, "device status flagged during warm-up"
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    for e in ev:  # instantiate the events before the timed region
-        for x in e:
-            x.record(stream)
+    assert prob.status() == 0, "device status flagged during warm-up"
     torch.cuda.synchronize()
     props = torch.cuda.get_device_properties(local)
     bus = getattr(props, "pci_bus_id", None)
@@ -365,30 +470,12 @@ def run_ours(args, info):
     torch.cuda.synchronize()
     with ClockSampler(pci) as clocks:
         t_wall = time.perf_counter()
-        for i in range(args.steps):
-            e_call0, _, _, e_call1 = ev[i]
-            e_call0.record(stream)
-            step()
-            e_call1.record(stream)
-            flush.fill_(1)  # L2 flush outside the timed events
-        torch.cuda.synchronize()
+        call_ms, main_ms = time_calls(prob, args.steps, flush, stream, lib)
         t_wall = time.perf_counter() - t_wall
     if dist:
         dist.barrier()
-    # second pass, same steps: events around the main kernel alone (for the
-    # roofline); events inside the call break the launch overlap, so this pass
-    # does not feed the headline number
-    for i in range(args.steps):
-        _, e_main0, e_main1, _ = ev[i]
-        lib.attn_set_main_kernel_events(C.c_void_p(e_main0.cuda_event), C.c_void_p(e_main1.cuda_event))
-        step()
-        lib.attn_set_main_kernel_events(None, None)
-        flush.fill_(1)
-    torch.cuda.synchronize()
-    call_ms = [ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps)]
-    main_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     total_ms = slowest_rank_ms(sum(call_ms), dist, "cuda")
-    assert ab.attn_query_status(ws) == 0, "device status flagged during the timed steps"
+    assert prob.status() == 0, "device status flagged during the timed steps"
     ms_per_step = total_ms / args.steps
     value = job_tflops(world, flops, ms_per_step)
     main_mean = statistics.mean(main_ms)
@@ -396,10 +483,10 @@ def run_ours(args, info):
     # ---- warm L2: the same call back to back, no flush in between (context beside the flushed figure) ----
     warm_steps = max(1, min(args.steps, 50))
     w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step()
+    prob.step(0, stream)
     w0.record(stream)
     for _ in range(warm_steps):
-        step()
+        prob.step(0, stream)
     w1.record(stream)
     torch.cuda.synchronize()
     warm_ms = w0.elapsed_time(w1) / warm_steps
@@ -416,7 +503,7 @@ def run_ours(args, info):
         a0.record(stream)
         for dst, src in zip(inputs, host_in):
             dst.copy_(src, non_blocking=True)
-        step()
+        prob.step(0, stream)
         for dst, src in zip(host_out, outputs):
             dst.copy_(src, non_blocking=True)
         a1.record(stream)
@@ -424,6 +511,10 @@ def run_ours(args, info):
         e2e_ms.append(a0.elapsed_time(a1))
         flush.fill_(1)
     e2e_val = job_tflops(world, flops, statistics.mean(e2e_ms))
+    pipe_ms = e2e_pipelined(prob, max(4, e2e_steps))
+    assert prob.status(0) == 0 and prob.status(1) == 0, "device status flagged during the end-to-end steps"
+    del prob
+    torch.cuda.empty_cache()
 
     if rank != 0:
         if dist:
@@ -449,13 +540,19 @@ def run_ours(args, info):
                      "peak_source": f"{pk_src} bf16_tflops (burst; fp16 has the same dense rate)",
                      "whole_call_frac": value / world / peak},
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": statistics.mean(e2e_ms)},
+                "ms_per_step": statistics.mean(e2e_ms),
+                "pipelined": {"value": job_tflops(world, flops, pipe_ms), "unit": "TFLOP/s", "ms_per_step": pipe_ms,
+                              "how": "two device buffer sets; copy in, call, copy out on three streams, overlapped"}},
         "warm_l2": {"value": job_tflops(world, flops, warm_ms), "unit": "TFLOP/s", "ms_per_step": warm_ms,
                     "steps": warm_steps},
-        "gpu_launches": launches_per_step * args.steps,  # of the timed pass
+        "gpu_launches": launches_per_step * args.steps,  # of the timed (whole-call) pass
         "clocks": clocks.summary(),
         "wall_s_timed_region": t_wall,
     }
+    if nsa:
+        line["roofline"]["useful_flops_frac"] = achieved * nsa_useful_flops(p) / flops / peak
+    if world == 1 and not args.no_extra_workloads:
+        line["workloads"] = extra_workloads(args, flush, stream, lib, peak)
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         run, cflops, desc_s, threads = cpu_sample(p, 10.0)
@@ -469,6 +566,37 @@ def run_ours(args, info):
         dist.destroy_process_group()
 
 
+def extra_workloads(args, flush, stream, lib, peak, steps=10, warmup=3):
+    """The other workloads beside the headline one: per workload and dQ mode, the whole call and the
+    main kernel (mean ms over `steps` flushed steps) and their fractions of the tensor peak."""
+    import torch
+    out = {}
+    for idx, det in ((2, False), (2, True), (3, False), (4, False), (4, True)):
+        if idx == args.workload and not det:
+            continue
+        p, flops, cfg = workload_info(idx)
+        prob = Problem(p, det)
+        for _ in range(warmup):
+            prob.step(0, stream)
+            flush.fill_(1)
+        call_ms, main_ms = time_calls(prob, steps, flush, stream, lib)
+        ok = prob.status() == 0
+        call, main = statistics.mean(call_ms), statistics.mean(main_ms)
+        entry = {"workload": cfg["workload"], "deterministic": det, "call_ms": call, "main_kernel_ms": main,
+                 "tflops": flops / (call * 1e-3) / 1e12, "main_kernel_tflops": flops / (main * 1e-3) / 1e12,
+                 "whole_call_frac": flops / (call * 1e-3) / 1e12 / peak,
+                 "main_kernel_frac": flops / (main * 1e-3) / 1e12 / peak, "steps": steps, "device_status_clean": ok}
+        if isinstance(p, synth.NsaProblem):
+            uf = nsa_useful_flops(p)
+            entry["useful_flops"] = uf
+            entry["slot_flops"] = flops
+            entry["main_kernel_useful_frac"] = uf / (main * 1e-3) / 1e12 / peak
+        out[f"w{idx}{'_det' if det else ''}"] = entry
+        del prob
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,6 +605,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=1, choices=[1, 2, 3, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="time only the chosen workload (default: also workloads 2-4 in both dQ modes)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
