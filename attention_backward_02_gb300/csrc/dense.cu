@@ -2,7 +2,6 @@
 //   preprocess  (D = rowsum(dO * O), LSE * log2 e, zeroed fp32 dQ accumulator)
 //   dq_finalize (dQ = cast(scale * sum of the partial dQ buffers, in index
 //                order); chained behind the main kernel)
-//   fwd         (O and LSE; CUDA-core kernel, not on the timed path)
 //
 // Definitions: cuDNN-frontend sample "51_scaled_dot_product_attention_backward"
 // (FlashAttention-2 backward from the (B,H,S,1) fp32 stats; D, P, dP, dS are
@@ -13,36 +12,6 @@
 #include "plan.h"
 
 namespace attn {
-
-// Element offset of token t (packed index space) of head h in a view.
-__device__ __forceinline__ int64_t tok_off(const View &v, const FixedGeo &g, int64_t t, int64_t h)
-{
-    int64_t b = t / g.s_q, i = t - b * g.s_q;
-    return b * v.sb + h * v.sh + i * v.ss;
-}
-__device__ __forceinline__ int64_t tok_off(const View &v, const PackedGeo &, int64_t t, int64_t h)
-{
-    return h * v.sh + t * v.ss;
-}
-__device__ __forceinline__ int64_t kv_off(const View &v, const FixedGeo &g, int64_t t, int64_t h)
-{
-    int64_t b = t / g.s_kv, i = t - b * g.s_kv;
-    return b * v.sb + h * v.sh + i * v.ss;
-}
-__device__ __forceinline__ int64_t kv_off(const View &v, const PackedGeo &, int64_t t, int64_t h)
-{
-    return h * v.sh + t * v.ss;
-}
-// Caller's stats layout: [B][h][s_q] (fixed) or [h][T_q] (packed).
-__device__ __forceinline__ int64_t lse_index(const DenseArgs &a, const FixedGeo &g, int64_t t, int64_t h)
-{
-    int64_t b = t / g.s_q, i = t - b * g.s_q;
-    return (b * a.h + h) * g.s_q + i;
-}
-__device__ __forceinline__ int64_t lse_index(const DenseArgs &a, const PackedGeo &, int64_t t, int64_t h)
-{
-    return h * a.t_q + t;
-}
 
 // Element offset of position i of sequence b, head h, in a query-side view.
 __device__ __forceinline__ int64_t seq_off(const View &v, const FixedGeo &, int64_t b, int64_t i, int64_t h)
@@ -177,112 +146,8 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(DenseArgs a, Geo geo)
     }
 }
 
-// ------------------------------------------------------------- forward
-// CUDA-core forward, two passes over the keys: (1) row max and sum of
-// exp2, (2) O = sum P V with the final LSE.  One CTA per (32-row query
-// tile, query head, sequence), 256 threads.
-template <class T, class Geo, int D>
-__global__ void __launch_bounds__(256) dense_fwd_kernel(DenseArgs a, Geo geo)
-{
-    constexpr int BM = 32, BN = 32, LD = D + 1;
-    extern __shared__ float fwd_smem[];
-    float(*Qs)[LD] = reinterpret_cast<float(*)[LD]>(fwd_smem);
-    float(*Ks)[LD] = reinterpret_cast<float(*)[LD]>(fwd_smem + BM * LD);
-    float(*Vs)[LD] = reinterpret_cast<float(*)[LD]>(fwd_smem + (BM + BN) * LD);
-    float(*Ss)[BN + 1] = reinterpret_cast<float(*)[BN + 1]>(fwd_smem + (BM + 2 * BN) * LD);
-    float *row_m = fwd_smem + (BM + 2 * BN) * LD + BM * (BN + 1);
-    float *row_l = row_m + BM;
-    const int64_t b = blockIdx.z, hq = blockIdx.y, g = hq / (a.h / a.h_kv);
-    const int64_t lq = geo.q_len(b), lkv = geo.kv_len(b);
-    const int64_t i0 = int64_t(blockIdx.x) * BM;
-    if (i0 >= lq) return;
-    const int64_t q0 = geo.q_start(b), k0 = geo.kv_start(b);
-    const int tid = threadIdx.x;
-    const float c = a.scale * kLog2e;
-    const T *Q = static_cast<const T *>(a.q.ptr);
-    const T *K = static_cast<const T *>(a.k.ptr);
-    const T *V = static_cast<const T *>(a.v.ptr);
-
-    for (int e = tid; e < BM * D; e += 256) {
-        int r = e / D, x = e % D;
-        Qs[r][x] = (i0 + r < lq) ? to_f32(Q[tok_off(a.q, geo, q0 + i0 + r, hq) + x]) : 0.f;
-    }
-    if (tid < BM) { row_m[tid] = -INFINITY; row_l[tid] = 0.f; }
-    const int64_t i_last = (i0 + BM - 1 < lq - 1) ? i0 + BM - 1 : lq - 1;
-    const int64_t j_end = last_visible_key(a.mask, i_last, lq, lkv) + 1;  // keys beyond are masked for all rows
-
-    const int r = tid / 8, part = tid % 8;  // row r, 4 columns / (D/8) features per thread
-    float o_acc[D / 8];
-    for (int pass = 0; pass < 2; ++pass) {
-#pragma unroll
-        for (int e = 0; e < D / 8; ++e) o_acc[e] = 0.f;
-        for (int64_t j0 = 0; j0 < j_end; j0 += BN) {
-            __syncthreads();
-            for (int e = tid; e < BN * D; e += 256) {
-                int rr = e / D, x = e % D;
-                bool in = j0 + rr < lkv;
-                Ks[rr][x] = in ? to_f32(K[kv_off(a.k, geo, k0 + j0 + rr, g) + x]) : 0.f;
-                Vs[rr][x] = in ? to_f32(V[kv_off(a.v, geo, k0 + j0 + rr, g) + x]) : 0.f;
-            }
-            __syncthreads();
-            for (int cc = part; cc < BN; cc += 8) {
-                float s = 0.f;
-#pragma unroll 8
-                for (int x = 0; x < D; ++x) s += Qs[r][x] * Ks[cc][x];
-                bool vis = (i0 + r < lq) && (j0 + cc < lkv) && visible(a.mask, i0 + r, j0 + cc, lq, lkv);
-                Ss[r][cc] = vis ? s * c : -INFINITY;
-            }
-            __syncthreads();
-            if (pass == 0) {
-                float m = -INFINITY;
-                for (int cc = part; cc < BN; cc += 8) m = fmaxf(m, Ss[r][cc]);
-                for (int off = 4; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                float m_new = fmaxf(row_m[r], m);
-                float l = 0.f;
-                if (m_new != -INFINITY)
-                    for (int cc = part; cc < BN; cc += 8) l += exp2f(Ss[r][cc] - m_new);
-                for (int off = 4; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-                __syncwarp();
-                if (part == 0) {
-                    float l_old = row_m[r] == -INFINITY ? 0.f : row_l[r] * exp2f(row_m[r] - m_new);
-                    row_l[r] = l_old + l;
-                    row_m[r] = m_new;
-                }
-            } else {
-                const float lse2 = row_m[r] == -INFINITY ? INFINITY : row_m[r] + log2f(row_l[r]);
-                for (int cc = 0; cc < BN; ++cc) {
-                    float p = (lse2 == INFINITY) ? 0.f : exp2f(Ss[r][cc] - lse2);
-#pragma unroll
-                    for (int e = 0; e < D / 8; ++e) o_acc[e] += p * Vs[cc][part * (D / 8) + e];
-                }
-            }
-        }
-        __syncthreads();
-    }
-    if (i0 + r < lq) {
-        T *O = static_cast<T *>(a.o.ptr);
-        int64_t off = tok_off(a.o, geo, q0 + i0 + r, hq) + part * (D / 8);
-#pragma unroll
-        for (int e = 0; e < D / 8; ++e) O[off + e] = from_f32<T>(o_acc[e]);
-        if (part == 0) {
-            float lse = row_m[r] == -INFINITY ? INFINITY : (row_m[r] + log2f(row_l[r])) / kLog2e;
-            int64_t idx = a.packed ? hq * a.t_q + (q0 + i0 + r) : (b * a.h + hq) * lq + (i0 + r);
-            a.lse_out[idx] = lse;
-        }
-    }
-}
-
 // ------------------------------------------------------------- launchers
 namespace {
-
-template <class Geo> int64_t max_len_q(const DenseArgs &a, const Geo &g);
-template <> int64_t max_len_q(const DenseArgs &, const FixedGeo &g) { return g.s_q; }
-template <> int64_t max_len_q(const DenseArgs &, const PackedGeo &g)
-{
-    int64_t m = 0;
-    for (int64_t b = 0; b < g.nseq; ++b) m = g.q_len(b) > m ? g.q_len(b) : m;
-    return m;
-}
 
 // One wave of 256-thread blocks (8 per SM), or fewer when there are fewer rows.
 unsigned row_grid(const DenseArgs &a)
@@ -321,34 +186,11 @@ template <class Geo> cudaError_t finalize(const DenseArgs &a, const Geo &g, cuda
                                : launch_kernel(dq_finalize_kernel<__nv_bfloat16, Geo, 128>, grid, 256, 0, s, true, a, g);
 }
 
-template <class T, class Geo, int D> cudaError_t fwd_run(const DenseArgs &a, const Geo &g, dim3 grid, cudaStream_t s)
-{
-    constexpr int BM = 32, BN = 32, LD = D + 1;
-    const size_t smem = sizeof(float) * ((BM + 2 * BN) * LD + BM * (BN + 1) + 2 * BM);
-    auto k = dense_fwd_kernel<T, Geo, D>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    k<<<grid, 256, smem, s>>>(a, g);
-    return cudaGetLastError();
-}
-
-template <class Geo> cudaError_t fwd(const DenseArgs &a, const Geo &g, cudaStream_t s)
-{
-    int64_t ml = max_len_q(a, g);
-    if (ml == 0) return cudaSuccess;
-    dim3 grid(unsigned((ml + 31) / 32), unsigned(a.h), unsigned(g.nseq));
-    if (a.d == 64)
-        return a.dtype == ATTN_F16 ? fwd_run<__half, Geo, 64>(a, g, grid, s) : fwd_run<__nv_bfloat16, Geo, 64>(a, g, grid, s);
-    return a.dtype == ATTN_F16 ? fwd_run<__half, Geo, 128>(a, g, grid, s) : fwd_run<__nv_bfloat16, Geo, 128>(a, g, grid, s);
-}
-
 }  // namespace
 
 cudaError_t launch_dense_preprocess(const DenseArgs &a, const FixedGeo &g, cudaStream_t s) { return preprocess(a, g, s); }
 cudaError_t launch_dense_preprocess(const DenseArgs &a, const PackedGeo &g, cudaStream_t s) { return preprocess(a, g, s); }
 cudaError_t launch_dq_finalize(const DenseArgs &a, const FixedGeo &g, cudaStream_t s) { return finalize(a, g, s); }
 cudaError_t launch_dq_finalize(const DenseArgs &a, const PackedGeo &g, cudaStream_t s) { return finalize(a, g, s); }
-cudaError_t launch_dense_fwd(const DenseArgs &a, const FixedGeo &g, cudaStream_t s) { return fwd(a, g, s); }
-cudaError_t launch_dense_fwd(const DenseArgs &a, const PackedGeo &g, cudaStream_t s) { return fwd(a, g, s); }
 
 }  // namespace attn
