@@ -16,6 +16,7 @@ from ._lib import (ATTN_BF16, ATTN_CAUSAL_BOTTOM_RIGHT, ATTN_CAUSAL_TOP_LEFT, AT
 
 __all__ = ["sdpa_desc", "nsa_desc", "view_bhsd", "view_tnd", "sdpa_workspace_size", "sdpa_fwd_stats",
            "sdpa_bwd", "nsa_workspace_size", "nsa_selected_attn_bwd", "nsa_block_lists",
+           "nsa_fwd_workspace_size", "nsa_selected_attn_fwd",
            "attn_query_status", "AttnError", "ATTN_F16", "ATTN_BF16", "ATTN_MASK_NONE",
            "ATTN_CAUSAL_TOP_LEFT", "ATTN_CAUSAL_BOTTOM_RIGHT"]
 
@@ -71,15 +72,17 @@ def sdpa_desc(*, dtype, b, h, h_kv, s_q, s_kv, d, scale, mask=ATTN_MASK_NONE, cu
 
 
 def nsa_desc(*, dtype, cu_seqlens_q, cu_seqlens_kv, n1, n2, d, scale, block_size, block_count, sparse_mode,
-             deterministic=False):
+             deterministic=False, d_v=0, grad_fp32=False):
     """An attn_nsa_desc_t: TND layout, b = len(cu_seqlens_q) sequences with inclusive cumulative query /
-    key lengths, n1 query and n2 kv heads, head dim d, scaleValue, selectedBlockSize / Count,
-    sparseMode 0 (selection only) or 2 (also causal, bottom-right per sequence); deterministic makes
-    dq, dk, dv bitwise reproducible (tensor-core head groups only)."""
+    key lengths, n1 query and n2 kv heads, query / key head dim d and value head dim d_v (0: d),
+    scaleValue, selectedBlockSize / Count, sparseMode 0 (selection only) or 2 (also causal,
+    bottom-right per sequence); deterministic makes dq, dk, dv bitwise reproducible (tensor-core head
+    groups only); grad_fp32 makes dq, dk, dv fp32."""
     keep = _Keep()
     desc = attn_nsa_desc_t(int(dtype), len(cu_seqlens_q), _cu_array(keep, cu_seqlens_q),
                            _cu_array(keep, cu_seqlens_kv), int(n1), int(n2), int(d), float(scale),
-                           int(block_size), int(block_count), int(sparse_mode), int(bool(deterministic)))
+                           int(block_size), int(block_count), int(sparse_mode), int(bool(deterministic)),
+                           int(d_v), int(bool(grad_fp32)))
     desc._keep = keep
     return desc
 
@@ -162,6 +165,27 @@ def nsa_selected_attn_bwd(desc, q, k, v, o, dO, softmax_max, softmax_sum, topk, 
         *(C.c_void_p(t.data_ptr()) for t in (dq, dk, dv)), C.c_void_p(ws.data_ptr()), C.c_size_t(ws.numel()),
         C.c_void_p(_stream_ptr(stream)))
     check(st, "nsa_selected_attn_bwd")
+    return ws
+
+
+def nsa_fwd_workspace_size(desc):
+    """Bytes of device workspace nsa_selected_attn_fwd needs (host only)."""
+    n = C.c_size_t()
+    check(_lib.load().nsa_fwd_workspace_size(C.byref(desc), C.byref(n)), "nsa_fwd_workspace_size")
+    return n.value
+
+
+def nsa_selected_attn_fwd(desc, q, k, v, topk, o, softmax_max, softmax_sum, *, workspace=None, stream=None):
+    """NSA selected-attention forward on contiguous TND CUDA tensors: q [T1, n1, d], k [T2, n2, d],
+    v [T2, n2, d_v], topk [T1, n2, block_count] int32 -> o [T1, n1, d_v] (input dtype), softmax_max /
+    softmax_sum [T1, n1, 8] fp32.  Asynchronous on `stream`; returns the workspace (status word)."""
+    ws = _workspace(nsa_fwd_workspace_size(desc), q.device, workspace)
+    fp = lambda t: C.cast(C.c_void_p(t.data_ptr()), C.POINTER(C.c_float))
+    st = _lib.load().nsa_selected_attn_fwd(
+        C.byref(desc), *(C.c_void_p(t.data_ptr()) for t in (q, k, v)),
+        C.cast(C.c_void_p(topk.data_ptr()), C.POINTER(C.c_int32)), C.c_void_p(o.data_ptr()), fp(softmax_max),
+        fp(softmax_sum), C.c_void_p(ws.data_ptr()), C.c_size_t(ws.numel()), C.c_void_p(_stream_ptr(stream)))
+    check(st, "nsa_selected_attn_fwd")
     return ws
 
 

@@ -23,7 +23,8 @@ ATTN_MASK_NONE, ATTN_CAUSAL_TOP_LEFT, ATTN_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
 EXPORTS = ("sdpa_workspace_size", "sdpa_fwd_stats", "sdpa_bwd", "nsa_workspace_size",
            "nsa_selected_attn_bwd", "nsa_block_lists", "attn_query_status", "attn_status_string",
            "attn_set_main_kernel_events", "sdpa_bwd_static_scratch", "attn_static_scratch_status",
-           "attn_selftest_wait_timeout", "attn_selftest_occupy", "attn_last_error")
+           "attn_selftest_wait_timeout", "attn_selftest_occupy", "attn_last_error",
+           "nsa_fwd_workspace_size", "nsa_selected_attn_fwd")
 
 
 class attn_view_t(C.Structure):
@@ -41,7 +42,8 @@ class attn_nsa_desc_t(C.Structure):
     _fields_ = [("dtype", C.c_int), ("b", C.c_int64), ("cu_seqlens_q", C.POINTER(C.c_int64)),
                 ("cu_seqlens_kv", C.POINTER(C.c_int64)), ("n1", C.c_int64), ("n2", C.c_int64),
                 ("d", C.c_int64), ("scale", C.c_double), ("block_size", C.c_int64),
-                ("block_count", C.c_int64), ("sparse_mode", C.c_int), ("deterministic", C.c_int)]
+                ("block_count", C.c_int64), ("sparse_mode", C.c_int), ("deterministic", C.c_int),
+                ("d_v", C.c_int64), ("grad_fp32", C.c_int)]
 
 
 _lib = None
@@ -63,6 +65,8 @@ def load() -> C.CDLL:
         "sdpa_fwd_stats": [D, view, view, view, view, P(C.c_float), V, S, V],
         "sdpa_bwd": [D, view, view, view, view, view, P(C.c_float), view, view, view, V, S, V],
         "nsa_workspace_size": [N, P(S)],
+        "nsa_fwd_workspace_size": [N, P(S)],
+        "nsa_selected_attn_fwd": [N, V, V, V, P(C.c_int32), V, P(C.c_float), P(C.c_float), V, S, V],
         "nsa_selected_attn_bwd": [N, V, V, V, V, V, P(C.c_float), P(C.c_float), P(C.c_int32), V, V, V, V, S, V],
         "nsa_block_lists": [N, P(C.c_int32), P(C.c_int32), P(C.c_int32), P(C.c_int64), V, S, V],
         "attn_query_status": [V, V, P(C.c_uint32)],

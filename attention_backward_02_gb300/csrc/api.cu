@@ -288,7 +288,7 @@ attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t 
 namespace {
 
 struct NsaShape {
-    int64_t t1, t2, nblk_max, words_max, maxlen_q;
+    int64_t t1, t2, nblk_max, words_max, maxlen_q, dv;
 };
 
 attn_status_t check_nsa_desc(const attn_nsa_desc_t *d, NsaShape *sh)
@@ -307,6 +307,8 @@ attn_status_t check_nsa_desc(const attn_nsa_desc_t *d, NsaShape *sh)
     if (d->sparse_mode != 0 && d->sparse_mode != 2) return ATTN_ERR_INVALID;
     if (d->deterministic != 0 && d->deterministic != 1) return ATTN_ERR_INVALID;
     if (d->d != 128 && d->d != 192) return ATTN_ERR_INVALID;
+    if (d->d_v != 0 && d->d_v != 128 && d->d_v != 192) return ATTN_ERR_INVALID;
+    if (d->grad_fp32 != 0 && d->grad_fp32 != 1) return ATTN_ERR_INVALID;
     if (check_cu(d->cu_seqlens_q, d->b, &sh->t1) || check_cu(d->cu_seqlens_kv, d->b, &sh->t2))
         return ATTN_ERR_INVALID;
     sh->nblk_max = 0;
@@ -319,7 +321,7 @@ attn_status_t check_nsa_desc(const attn_nsa_desc_t *d, NsaShape *sh)
         if (lq > sh->maxlen_q) sh->maxlen_q = lq;
     }
     sh->words_max = (sh->maxlen_q + 31) / 32;
-    if (d->d != 128) return ATTN_ERR_UNSUPPORTED;
+    sh->dv = d->d_v ? d->d_v : d->d;
     if (sh->t1 * d->n1 >= (int64_t(1) << 31) || sh->t2 * d->n2 >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
@@ -345,7 +347,7 @@ NsaLayout nsa_layout(const attn_nsa_desc_t *d, const NsaShape &sh)
     L.dqacc = L.tokens + Workspace::align(size_t(sh.t1) * size_t(d->n2 * d->block_count) * sizeof(int32_t) + 4);
     L.dkacc = L.dqacc + Workspace::align(rows * size_t(d->d) * sizeof(float));
     L.dvacc = L.dkacc + Workspace::align(size_t(sh.t2) * size_t(d->n2 * d->d) * sizeof(float));
-    L.dqpart = L.dvacc + Workspace::align(size_t(sh.t2) * size_t(d->n2 * d->d) * sizeof(float));
+    L.dqpart = L.dvacc + Workspace::align(size_t(sh.t2) * size_t(d->n2 * sh.dv) * sizeof(float));
     const size_t part_bytes =
         d->deterministic ? size_t(sh.t1) * size_t(d->n1) * size_t(d->block_count) * size_t(d->d) * sizeof(float) : 0;
     L.total = L.dqpart + Workspace::align(part_bytes);
@@ -386,7 +388,8 @@ attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, 
     NsaArgs a;
     std::memset(&a, 0, sizeof a);
     a.dtype = desc->dtype;
-    a.nseq = desc->b; a.n1 = desc->n1; a.n2 = desc->n2; a.d = desc->d;
+    a.nseq = desc->b; a.n1 = desc->n1; a.n2 = desc->n2; a.d = desc->d; a.dv = sh.dv;
+    a.grad_fp32 = desc->grad_fp32;
     a.bs = desc->block_size; a.cnt = desc->block_count;
     a.t1 = sh.t1; a.t2 = sh.t2; a.t1_pad = L.t1_pad;
     a.nblk_max = sh.nblk_max; a.words_max = sh.words_max; a.nrows = L.nrows;
@@ -396,7 +399,7 @@ attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, 
     a.n_part = 1;
     a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO;
     a.smax = softmax_max; a.ssum = softmax_sum; a.topk = topk;
-    a.dq = dq; a.dk = dk; a.dv = dv;
+    a.dq = dq; a.dk = dk; a.dvp = dv;
     char *ws = static_cast<char *>(workspace);
     a.status = reinterpret_cast<uint32_t *>(ws + L.status);
     a.lse2 = reinterpret_cast<float *>(ws + L.lse2);
@@ -421,6 +424,53 @@ attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, 
     return cuda_status(launch_nsa_bwd(a, pg, static_cast<cudaStream_t>(stream), g_ev_before, g_ev_after));
 }
 
+attn_status_t nsa_fwd_workspace_size(const attn_nsa_desc_t *desc, size_t *bytes)
+{
+    NsaShape sh;
+    attn_status_t st = check_nsa_desc(desc, &sh);
+    if (st) return st;
+    if (!bytes) return ATTN_ERR_NULLPTR;
+    *bytes = Workspace::align(64 * sizeof(uint32_t));
+    return ATTN_OK;
+}
+
+attn_status_t nsa_selected_attn_fwd(const attn_nsa_desc_t *desc, const void *q, const void *k, const void *v,
+                                    const int32_t *topk, void *o, float *softmax_max, float *softmax_sum,
+                                    void *workspace, size_t workspace_bytes, void *stream)
+{
+    NsaShape sh;
+    attn_status_t st = check_nsa_desc(desc, &sh);
+    if (st) return st;
+    if (sh.t1 > 0 && (!q || !o || !softmax_max || !softmax_sum || !topk)) return ATTN_ERR_NULLPTR;
+    if (sh.t2 > 0 && (!k || !v)) return ATTN_ERR_NULLPTR;
+    for (const void *p : {q, k, v, (const void *)o})
+        if (p && !aligned16(p)) return ATTN_ERR_ALIGN;
+    if ((topk && (reinterpret_cast<uintptr_t>(topk) & 3)) || (softmax_max && !aligned16(softmax_max)) ||
+        (softmax_sum && !aligned16(softmax_sum)))
+        return ATTN_ERR_ALIGN;
+    if ((st = check_ws(workspace, workspace_bytes, Workspace::align(64 * sizeof(uint32_t))))) return st;
+    if (sh.t1 == 0) return ATTN_OK;
+    NsaArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.dtype = desc->dtype;
+    a.nseq = desc->b; a.n1 = desc->n1; a.n2 = desc->n2; a.d = desc->d; a.dv = sh.dv;
+    a.bs = desc->block_size; a.cnt = desc->block_count;
+    a.t1 = sh.t1; a.t2 = sh.t2;
+    a.scale = float(desc->scale);
+    a.sparse_mode = desc->sparse_mode;
+    a.q = q; a.k = k; a.v = v; a.topk = topk;
+    a.o_out = o; a.smax_out = softmax_max; a.ssum_out = softmax_sum;
+    a.status = static_cast<uint32_t *>(workspace);
+    static thread_local PackedGeo pg;
+    pg.nseq = desc->b;
+    pg.cu_q[0] = pg.cu_kv[0] = 0;
+    for (int64_t b = 0; b < desc->b; ++b) {
+        pg.cu_q[b + 1] = desc->cu_seqlens_q[b];
+        pg.cu_kv[b + 1] = desc->cu_seqlens_kv[b];
+    }
+    return cuda_status(launch_nsa_fwd(a, pg, static_cast<cudaStream_t>(stream)));
+}
+
 attn_status_t nsa_block_lists(const attn_nsa_desc_t *desc, const int32_t *topk, int32_t *offsets, int32_t *tokens,
                               int64_t *nblk_max_out, void *workspace, size_t workspace_bytes, void *stream)
 {
@@ -435,7 +485,8 @@ attn_status_t nsa_block_lists(const attn_nsa_desc_t *desc, const int32_t *topk, 
     NsaArgs a;
     std::memset(&a, 0, sizeof a);
     a.dtype = desc->dtype;
-    a.nseq = desc->b; a.n1 = desc->n1; a.n2 = desc->n2; a.d = desc->d;
+    a.nseq = desc->b; a.n1 = desc->n1; a.n2 = desc->n2; a.d = desc->d; a.dv = sh.dv;
+    a.grad_fp32 = desc->grad_fp32;
     a.bs = desc->block_size; a.cnt = desc->block_count;
     a.t1 = sh.t1; a.t2 = sh.t2; a.t1_pad = L.t1_pad;
     a.nblk_max = sh.nblk_max; a.words_max = sh.words_max; a.nrows = L.nrows;

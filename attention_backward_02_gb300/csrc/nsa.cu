@@ -58,7 +58,7 @@ __device__ __forceinline__ void nsa_preprocess_block(const NsaArgs &a, int64_t p
     {   // buffers the main kernel adds into
         const int64_t nthr = nblk * blockDim.x, tid = pb * blockDim.x + threadIdx.x;
         zero_words(reinterpret_cast<uint32_t *>(a.dkacc), a.t2 * a.n2 * a.d, tid, nthr);
-        zero_words(reinterpret_cast<uint32_t *>(a.dvacc), a.t2 * a.n2 * a.d, tid, nthr);
+        zero_words(reinterpret_cast<uint32_t *>(a.dvacc), a.t2 * a.n2 * a.dv, tid, nthr);
         if (a.zero_dq) zero_words(reinterpret_cast<uint32_t *>(a.dqacc), a.t1 * a.n1 * a.d, tid, nthr);
     }
     const int64_t gx = nblk / a.n1, bx = pb % gx, h = pb / gx;
@@ -68,17 +68,18 @@ __device__ __forceinline__ void nsa_preprocess_block(const NsaArgs &a, int64_t p
         const bool live = t < a.t1_pad;  // no early exit: the row's threads shuffle below
         const int64_t row = t * a.n1 + h;  // token-major
         float dsum = 0.f;
-        if (t < a.t1) {
-            const int64_t off = (t * a.n1 + h) * a.d + lane * 8;
-            uint4 ov = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.o) + off);
-            uint4 dv = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.dO) + off);
-            const uint32_t *op = &ov.x, *dp = &dv.x;
+        if (t < a.t1)  // D = rowsum(dO * O) over the value head dim, 8 elements per chunk
+            for (int64_t ch = lane; ch < a.dv / 8; ch += 16) {
+                const int64_t off = (t * a.n1 + h) * a.dv + ch * 8;
+                uint4 ov = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.o) + off);
+                uint4 dv = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.dO) + off);
+                const uint32_t *op = &ov.x, *dp = &dv.x;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float2 of = unpack2<T>(op[e]), df = unpack2<T>(dp[e]);
-                dsum += of.x * df.x + of.y * df.y;
+                for (int e = 0; e < 4; ++e) {
+                    float2 of = unpack2<T>(op[e]), df = unpack2<T>(dp[e]);
+                    dsum += of.x * df.x + of.y * df.y;
+                }
             }
-        }
         for (int off = 8; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
         if (!live) continue;
         if (lane == 0) {
@@ -226,23 +227,37 @@ __global__ void __launch_bounds__(256) nsa_emit_kernel(NsaArgs a, PackedGeo geo,
 }
 
 // ------------------------------------------------------------ main (CUDA cores)
-// One CTA per (token, kv head); loops over the selected blocks.  dQ rows of
-// the token are owned by the CTA; dK / dV go to fp32 accumulators.
-template <class T>
+// One CTA per (token, kv head); loops over the selected blocks, KB keys at a
+// time.  dQ rows of the token are owned by the CTA; dK / dV go to fp32
+// accumulators.  DQK: query / key head dim, DV: value head dim.
+constexpr int kNsaKB = 32;  // keys per pass of the CUDA-core kernels
+inline size_t nsa_simt_smem(int64_t G, int dqk, int dv)
+{
+    return sizeof(float) * size_t(kNsaKB * (dqk + 1) + kNsaKB * (dv + 1) + G * (dqk + 1) + G * (dv + 1) +
+                                  2 * G * kNsaKB + 2 * G);
+}
+
+template <class OutT> __device__ __forceinline__ OutT out_cast(float x);
+template <> __device__ __forceinline__ float out_cast<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half out_cast<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 out_cast<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+template <class T, class OutT, int DQK, int DV>
 __global__ void __launch_bounds__(256) nsa_bwd_simt_kernel(NsaArgs a, PackedGeo geo)
 {
     pdl_wait();
     pdl_trigger();
-    constexpr int D = 128, LD = D + 1;
+    constexpr int KB = kNsaKB, LDQ = DQK + 1, LDV = DV + 1;
+    constexpr int PER = (32 * DQK + 255) / 256;  // dQ features per thread at G = 32
     extern __shared__ float smem[];
-    const int G = int(a.n1 / a.n2), BS = int(a.bs);
-    float(*Ks)[LD] = reinterpret_cast<float(*)[LD]>(smem);
-    float(*Vs)[LD] = reinterpret_cast<float(*)[LD]>(smem + BS * LD);
-    float(*Qs)[LD] = reinterpret_cast<float(*)[LD]>(smem + 2 * BS * LD);
-    float(*dOs)[LD] = reinterpret_cast<float(*)[LD]>(smem + 2 * BS * LD + G * LD);
-    float *Ps = smem + 2 * BS * LD + 2 * G * LD;  // [G][BS]
-    float *dSs = Ps + G * BS;
-    float *lse_s = dSs + G * BS;
+    const int G = int(a.n1 / a.n2);
+    float(*Ks)[LDQ] = reinterpret_cast<float(*)[LDQ]>(smem);
+    float(*Vs)[LDV] = reinterpret_cast<float(*)[LDV]>(smem + KB * LDQ);
+    float(*Qs)[LDQ] = reinterpret_cast<float(*)[LDQ]>(smem + KB * LDQ + KB * LDV);
+    float(*dOs)[LDV] = reinterpret_cast<float(*)[LDV]>(smem + KB * LDQ + KB * LDV + G * LDQ);
+    float *Ps = smem + KB * LDQ + KB * LDV + G * LDQ + G * LDV;  // [G][KB]
+    float *dSs = Ps + G * KB;
+    float *lse_s = dSs + G * KB;
     float *d_s = lse_s + G;
 
     const int64_t t = blockIdx.x, g = blockIdx.y;
@@ -253,20 +268,21 @@ __global__ void __launch_bounds__(256) nsa_bwd_simt_kernel(NsaArgs a, PackedGeo 
     const T *Q = static_cast<const T *>(a.q), *K = static_cast<const T *>(a.k);
     const T *V = static_cast<const T *>(a.v), *dO = static_cast<const T *>(a.dO);
 
-    for (int e = tid; e < G * D; e += 256) {
-        int hh = e / D, x = e % D;
-        int64_t off = (t * a.n1 + g * G + hh) * D + x;
-        Qs[hh][x] = to_f32(Q[off]);
-        dOs[hh][x] = to_f32(dO[off]);
+    for (int e = tid; e < G * DQK; e += 256) {
+        const int hh = e / DQK, x = e % DQK;
+        Qs[hh][x] = to_f32(Q[(t * a.n1 + g * G + hh) * DQK + x]);
+    }
+    for (int e = tid; e < G * DV; e += 256) {
+        const int hh = e / DV, x = e % DV;
+        dOs[hh][x] = to_f32(dO[(t * a.n1 + g * G + hh) * DV + x]);
     }
     if (tid < G) {
         lse_s[tid] = a.lse2[t * a.n1 + g * G + tid];
         d_s[tid] = a.dvec[t * a.n1 + g * G + tid];
     }
-    // thread owns dQ features of (head hh_q, x range)
-    const int per = (G * D + 255) / 256;
-    float dq[16];
-    for (int e = 0; e < 16; ++e) dq[e] = 0.f;
+    float dq[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) dq[e] = 0.f;
     const int32_t *ids = a.topk + (t * a.n2 + g) * a.cnt;
     const int64_t nblk = lkv / a.bs;
     for (int64_t cc = 0; cc < a.cnt; ++cc) {
@@ -275,99 +291,240 @@ __global__ void __launch_bounds__(256) nsa_bwd_simt_kernel(NsaArgs a, PackedGeo 
         bool dup = false;
         for (int64_t c2 = 0; c2 < cc; ++c2) dup |= ids[c2] == blk;
         if (dup) continue;
-        const int64_t j0 = blk * a.bs;
-        __syncthreads();
-        for (int e = tid; e < BS * D; e += 256) {
-            int r = e / D, x = e % D;
-            Ks[r][x] = to_f32(K[((k0 + j0 + r) * a.n2 + g) * D + x]);
-            Vs[r][x] = to_f32(V[((k0 + j0 + r) * a.n2 + g) * D + x]);
-        }
-        __syncthreads();
-        for (int e = tid; e < G * BS; e += 256) {
-            int hh = e / BS, r = e % BS;
-            bool vis = a.sparse_mode != 2 || visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, j0 + r, lq, lkv);
-            float s = 0.f, dp = 0.f;
-            if (vis) {
+        for (int64_t sub = 0; sub < a.bs; sub += KB) {
+            const int64_t j0 = blk * a.bs + sub;
+            const int nk = int(a.bs - sub < KB ? a.bs - sub : KB);
+            __syncthreads();
+            for (int e = tid; e < nk * DQK; e += 256) {
+                const int r = e / DQK, x = e % DQK;
+                Ks[r][x] = to_f32(K[((k0 + j0 + r) * a.n2 + g) * DQK + x]);
+            }
+            for (int e = tid; e < nk * DV; e += 256) {
+                const int r = e / DV, x = e % DV;
+                Vs[r][x] = to_f32(V[((k0 + j0 + r) * a.n2 + g) * DV + x]);
+            }
+            __syncthreads();
+            for (int e = tid; e < G * nk; e += 256) {
+                const int hh = e / nk, r = e % nk;
+                const bool vis = a.sparse_mode != 2 || visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, j0 + r, lq, lkv);
+                float sv = 0.f, dp = 0.f;
+                if (vis) {
 #pragma unroll 8
-                for (int x = 0; x < D; ++x) {
-                    s += Qs[hh][x] * Ks[r][x];
-                    dp += dOs[hh][x] * Vs[r][x];
+                    for (int x = 0; x < DQK; ++x) sv += Qs[hh][x] * Ks[r][x];
+#pragma unroll 8
+                    for (int x = 0; x < DV; ++x) dp += dOs[hh][x] * Vs[r][x];
+                }
+                const float pv = (vis && lse_s[hh] != INFINITY) ? exp2f(sv * c - lse_s[hh]) : 0.f;
+                Ps[hh * KB + r] = pv;
+                dSs[hh * KB + r] = pv * (dp - d_s[hh]);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < PER; ++e) {
+                const int f = tid + e * 256;
+                if (f >= G * DQK) break;
+                const int hh = f / DQK, x = f % DQK;
+                float acc = 0.f;
+                for (int r = 0; r < nk; ++r) acc += dSs[hh * KB + r] * Ks[r][x];
+                dq[e] += acc;
+            }
+            for (int f = tid; f < nk * DQK; f += 256) {
+                const int r = f / DQK, x = f % DQK;
+                float dk = 0.f;
+                for (int hh = 0; hh < G; ++hh) dk += dSs[hh * KB + r] * Qs[hh][x];
+                atomicAdd(a.dkacc + ((k0 + j0 + r) * a.n2 + g) * DQK + x, dk * a.scale);
+            }
+            for (int f = tid; f < nk * DV; f += 256) {
+                const int r = f / DV, x = f % DV;
+                float dv = 0.f;
+                for (int hh = 0; hh < G; ++hh) dv += Ps[hh * KB + r] * dOs[hh][x];
+                atomicAdd(a.dvacc + ((k0 + j0 + r) * a.n2 + g) * DV + x, dv);
+            }
+        }
+    }
+    OutT *dQ = static_cast<OutT *>(a.dq);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+        const int f = tid + e * 256;
+        if (f >= G * DQK) break;
+        const int hh = f / DQK, x = f % DQK;
+        dQ[(t * a.n1 + g * G + hh) * DQK + x] = out_cast<OutT>(dq[e] * a.scale);
+    }
+}
+
+// ------------------------------------------------------------- forward (CUDA cores)
+// NSA selected-attention forward: one CTA per (token, kv head), KB keys of the
+// selected blocks at a time, online softmax per query head (max in log2 units).
+// O = sum_j exp(s_j - max) v_j / sum; softmaxMax = max_j s_j (natural units),
+// softmaxSum = sum_j exp(s_j - max), both written to all 8 lanes.
+template <class T, int DQK, int DV>
+__global__ void __launch_bounds__(256) nsa_fwd_simt_kernel(NsaArgs a, PackedGeo geo)
+{
+    constexpr int KB = kNsaKB, LDQ = DQK + 1, LDV = DV + 1;
+    constexpr int PER = (32 * DV + 255) / 256;  // O features per thread at G = 32
+    extern __shared__ float smem[];
+    const int G = int(a.n1 / a.n2);
+    float(*Ks)[LDQ] = reinterpret_cast<float(*)[LDQ]>(smem);
+    float(*Vs)[LDV] = reinterpret_cast<float(*)[LDV]>(smem + KB * LDQ);
+    float(*Qs)[LDQ] = reinterpret_cast<float(*)[LDQ]>(smem + KB * LDQ + KB * LDV);
+    float *Ps = smem + KB * LDQ + KB * LDV + G * LDQ;  // [G][KB]
+    float *m_s = Ps + G * KB, *l_s = m_s + G, *al_s = l_s + G;
+
+    const int64_t t = blockIdx.x, g = blockIdx.y;
+    const int64_t b = seq_of_token(geo, t);
+    const int64_t i = t - geo.cu_q[b], lq = geo.q_len(b), lkv = geo.kv_len(b), k0 = geo.cu_kv[b];
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const float c = a.scale * kLog2e;
+    const T *Q = static_cast<const T *>(a.q), *K = static_cast<const T *>(a.k), *V = static_cast<const T *>(a.v);
+
+    for (int e = tid; e < G * DQK; e += 256) {
+        const int hh = e / DQK, x = e % DQK;
+        Qs[hh][x] = to_f32(Q[(t * a.n1 + g * G + hh) * DQK + x]);
+    }
+    if (tid < G) {
+        m_s[tid] = -INFINITY;
+        l_s[tid] = 0.f;
+    }
+    float o[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) o[e] = 0.f;
+    const int32_t *ids = a.topk + (t * a.n2 + g) * a.cnt;
+    const int64_t nblk = lkv / a.bs;
+    for (int64_t cc = 0; cc < a.cnt; ++cc) {
+        const int64_t blk = ids[cc];
+        if (blk < 0 || blk >= nblk) {
+            if (tid == 0) raise_flag(a.status, ATTN_DEV_INDEX_RANGE);
+            continue;
+        }
+        bool dup = false;
+        for (int64_t c2 = 0; c2 < cc; ++c2) dup |= ids[c2] == blk;
+        if (dup) {
+            if (tid == 0) raise_flag(a.status, ATTN_DEV_INDEX_DUP);
+            continue;
+        }
+        for (int64_t sub = 0; sub < a.bs; sub += KB) {
+            const int64_t j0 = blk * a.bs + sub;
+            const int nk = int(a.bs - sub < KB ? a.bs - sub : KB);
+            __syncthreads();
+            for (int e = tid; e < nk * DQK; e += 256) {
+                const int r = e / DQK, x = e % DQK;
+                Ks[r][x] = to_f32(K[((k0 + j0 + r) * a.n2 + g) * DQK + x]);
+            }
+            for (int e = tid; e < nk * DV; e += 256) {
+                const int r = e / DV, x = e % DV;
+                Vs[r][x] = to_f32(V[((k0 + j0 + r) * a.n2 + g) * DV + x]);
+            }
+            __syncthreads();
+            for (int e = tid; e < G * KB; e += 256) {  // scores, log2 units; -inf where masked
+                const int hh = e / KB, r = e % KB;
+                float sv = -INFINITY;
+                if (r < nk && (a.sparse_mode != 2 || visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, j0 + r, lq, lkv))) {
+                    sv = 0.f;
+#pragma unroll 8
+                    for (int x = 0; x < DQK; ++x) sv += Qs[hh][x] * Ks[r][x];
+                    sv *= c;
+                }
+                Ps[hh * KB + r] = sv;
+            }
+            __syncthreads();
+            for (int hh = warp; hh < G; hh += 8) {  // one warp per head: raise the max, P, the sum
+                const float sv = Ps[hh * KB + lane];
+                float mb = sv;
+                for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+                const float m_old = m_s[hh], m_new = fmaxf(m_old, mb);
+                const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_old - m_new);
+                const float pv = sv == -INFINITY ? 0.f : exp2f(sv - m_new);
+                float ps = pv;
+                for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+                Ps[hh * KB + lane] = pv;
+                __syncwarp();
+                if (lane == 0) {
+                    l_s[hh] = l_s[hh] * alpha + ps;
+                    m_s[hh] = m_new;
+                    al_s[hh] = alpha;
                 }
             }
-            float p = (vis && lse_s[hh] != INFINITY) ? exp2f(s * c - lse_s[hh]) : 0.f;
-            Ps[hh * BS + r] = p;
-            dSs[hh * BS + r] = p * (dp - d_s[hh]);
-        }
-        __syncthreads();
-        for (int e = 0; e < per; ++e) {
-            int f = tid + e * 256;
-            if (f >= G * D) break;
-            int hh = f / D, x = f % D;
-            float acc = 0.f;
-            for (int r = 0; r < BS; ++r) acc += dSs[hh * BS + r] * Ks[r][x];
-            dq[e] += acc;
-        }
-        for (int f = tid; f < BS * D; f += 256) {
-            int r = f / D, x = f % D;
-            float dk = 0.f, dv = 0.f;
-            for (int hh = 0; hh < G; ++hh) {
-                dk += dSs[hh * BS + r] * Qs[hh][x];
-                dv += Ps[hh * BS + r] * dOs[hh][x];
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < PER; ++e) {
+                const int f = tid + e * 256;
+                if (f >= G * DV) break;
+                const int hh = f / DV, x = f % DV;
+                float acc = 0.f;
+                for (int r = 0; r < nk; ++r) acc += Ps[hh * KB + r] * Vs[r][x];
+                o[e] = o[e] * al_s[hh] + acc;
             }
-            int64_t off = ((k0 + j0 + r) * a.n2 + g) * D + x;
-            atomicAdd(a.dkacc + off, dk * a.scale);
-            atomicAdd(a.dvacc + off, dv);
         }
     }
-    T *dQ = static_cast<T *>(a.dq);
-    for (int e = 0; e < per; ++e) {
-        int f = tid + e * 256;
-        if (f >= G * D) break;
-        int hh = f / D, x = f % D;
-        dQ[(t * a.n1 + g * G + hh) * D + x] = from_f32<T>(dq[e] * a.scale);
+    __syncthreads();
+    T *O = static_cast<T *>(a.o_out);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+        const int f = tid + e * 256;
+        if (f >= G * DV) break;
+        const int hh = f / DV, x = f % DV;
+        const float l = l_s[hh];
+        O[(t * a.n1 + g * G + hh) * DV + x] = from_f32<T>(l > 0.f ? o[e] / l : 0.f);
     }
+    for (int e = tid; e < G * 8; e += 256) {
+        const int hh = e / 8;
+        const int64_t row = t * a.n1 + g * G + hh;
+        const float m = m_s[hh];
+        a.smax_out[row * 8 + e % 8] = m == -INFINITY ? -INFINITY : m / kLog2e;
+        a.ssum_out[row * 8 + e % 8] = l_s[hh];
+    }
+}
+
+// Four fp32 values to OutT (16-bit: packed, round to nearest even).
+template <class OutT> __device__ __forceinline__ void store4(OutT *p, float4 v);
+template <> __device__ __forceinline__ void store4<float>(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+template <> __device__ __forceinline__ void store4<__half>(__half *p, float4 v)
+{
+    *reinterpret_cast<uint2 *>(p) = make_uint2(pack2<__half>(v.x, v.y), pack2<__half>(v.z, v.w));
+}
+template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *p, float4 v)
+{
+    *reinterpret_cast<uint2 *>(p) = make_uint2(pack2<__nv_bfloat16>(v.x, v.y), pack2<__nv_bfloat16>(v.z, v.w));
+}
+
+// dK, dV = cast(fp32 accumulators), 4 elements per step (head dims are multiples of 8).
+template <class OutT>
+__device__ __forceinline__ void convert_dkdv4(const NsaArgs &a)
+{
+    const int64_t nk = a.t2 * a.n2 * a.d, nv = a.t2 * a.n2 * a.dv;
+    OutT *dK = static_cast<OutT *>(a.dk), *dV = static_cast<OutT *>(a.dv_out());
+    const int64_t step = int64_t(gridDim.x) * blockDim.x * 4;
+    for (int64_t e = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 4; e < nk; e += step)
+        store4<OutT>(dK + e, *reinterpret_cast<const float4 *>(a.dkacc + e));
+    for (int64_t e = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 4; e < nv; e += step)
+        store4<OutT>(dV + e, *reinterpret_cast<const float4 *>(a.dvacc + e));
 }
 
 // dQ = cast(scale * fp32 accumulator), tensor-core path
-// dK, dV = cast(fp32 accumulators), 4 elements per step (the tensor-core path's d = 128).
-template <class T>
-__device__ __forceinline__ void convert_dkdv4(const NsaArgs &a)
-{
-    const int64_t n = a.t2 * a.n2 * a.d;
-    T *dK = static_cast<T *>(a.dk), *dV = static_cast<T *>(a.dv);
-    for (int64_t e = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 4; e < n; e += int64_t(gridDim.x) * blockDim.x * 4) {
-        const float4 k4 = *reinterpret_cast<const float4 *>(a.dkacc + e), v4 = *reinterpret_cast<const float4 *>(a.dvacc + e);
-        *reinterpret_cast<uint2 *>(dK + e) = make_uint2(pack2<T>(k4.x, k4.y), pack2<T>(k4.z, k4.w));
-        *reinterpret_cast<uint2 *>(dV + e) = make_uint2(pack2<T>(v4.x, v4.y), pack2<T>(v4.z, v4.w));
-    }
-}
-
-template <class T>
+template <class OutT>
 __global__ void nsa_dq_finalize_kernel(NsaArgs a, int with_kv)
 {
     pdl_wait();
     pdl_trigger();
     const int64_t n = a.t1 * a.n1 * a.d;
-    T *dQ = static_cast<T *>(a.dq);
+    OutT *dQ = static_cast<OutT *>(a.dq);
     for (int64_t e = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 4; e < n; e += int64_t(gridDim.x) * blockDim.x * 4) {
         const float4 v = *reinterpret_cast<const float4 *>(a.dqacc + e);
-        uint2 o;
-        o.x = pack2<T>(v.x * a.scale, v.y * a.scale);
-        o.y = pack2<T>(v.z * a.scale, v.w * a.scale);
-        *reinterpret_cast<uint2 *>(dQ + e) = o;
+        store4<OutT>(dQ + e, make_float4(v.x * a.scale, v.y * a.scale, v.z * a.scale, v.w * a.scale));
     }
-    if (with_kv) convert_dkdv4<T>(a);  // dK / dV in the same launch
+    if (with_kv) convert_dkdv4<OutT>(a);  // dK / dV in the same launch
 }
 
 // Deterministic dQ: per (token, query head) the partial rows of the selected
 // slots, summed in slot order; slots whose block was never processed (out of
-// range, a repeat, or fully masked by sparse mode 2) are skipped.
-template <class T>
+// range, a repeat, or fully masked by sparse mode 2) are skipped.  (d = 128:
+// 32 threads x 4 floats per row.)
+template <class OutT>
 __global__ void nsa_dq_finalize_det_kernel(NsaArgs a, PackedGeo geo, int with_kv)
 {
     pdl_wait();
     pdl_trigger();
-    const int64_t rows = a.t1 * a.n1;  // (token, head) rows; 32 threads x 4 floats per row
+    const int64_t rows = a.t1 * a.n1;
     const int G = int(a.n1 / a.n2);
     for (int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32; w < rows;
          w += int64_t(gridDim.x) * blockDim.x / 32) {
@@ -386,24 +543,17 @@ __global__ void nsa_dq_finalize_det_kernel(NsaArgs a, PackedGeo geo, int with_kv
             const float4 v = reinterpret_cast<const float4 *>(a.dqpart + (((t * a.n2 + g) * a.cnt + c) * G + hh) * a.d)[lane];
             acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
         }
-        uint2 o;
-        o.x = pack2<T>(acc.x * a.scale, acc.y * a.scale);
-        o.y = pack2<T>(acc.z * a.scale, acc.w * a.scale);
-        reinterpret_cast<uint2 *>(static_cast<T *>(a.dq) + w * a.d)[lane] = o;
+        store4<OutT>(static_cast<OutT *>(a.dq) + w * a.d + lane * 4,
+                     make_float4(acc.x * a.scale, acc.y * a.scale, acc.z * a.scale, acc.w * a.scale));
     }
-    if (with_kv) convert_dkdv4<T>(a);  // dK / dV in the same launch
+    if (with_kv) convert_dkdv4<OutT>(a);  // dK / dV in the same launch
 }
 
-template <class T>
+template <class OutT>
 __global__ void nsa_finalize_kernel(NsaArgs a)
 {
     pdl_wait();
-    const int64_t n = a.t2 * a.n2 * a.d;
-    T *dK = static_cast<T *>(a.dk), *dV = static_cast<T *>(a.dv);
-    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += int64_t(gridDim.x) * blockDim.x) {
-        dK[e] = from_f32<T>(a.dkacc[e]);
-        dV[e] = from_f32<T>(a.dvacc[e]);
-    }
+    convert_dkdv4<OutT>(a);
 }
 
 namespace {
@@ -431,7 +581,22 @@ cudaError_t block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, bo
     return cudaSuccess;
 }
 
-template <class T>
+template <class T, class OutT>
+cudaError_t launch_simt_bwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
+{
+    const int64_t G = a.n1 / a.n2;
+    void (*k)(NsaArgs, PackedGeo) = nullptr;
+    if (a.d == 128 && a.dv == 128) k = nsa_bwd_simt_kernel<T, OutT, 128, 128>;
+    else if (a.d == 192 && a.dv == 128) k = nsa_bwd_simt_kernel<T, OutT, 192, 128>;
+    else if (a.d == 128 && a.dv == 192) k = nsa_bwd_simt_kernel<T, OutT, 128, 192>;
+    else k = nsa_bwd_simt_kernel<T, OutT, 192, 192>;
+    const size_t smem = nsa_simt_smem(G, int(a.d), int(a.dv));
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    return launch_kernel(k, dim3(unsigned(a.t1), unsigned(a.n2)), dim3(256), smem, s, true, a, g);
+}
+
+template <class T, class OutT>
 cudaError_t run_nsa(const NsaArgs &a0, const PackedGeo &g, cudaStream_t s, cudaEvent_t before, cudaEvent_t after)
 {
     cudaError_t e;
@@ -451,27 +616,42 @@ cudaError_t run_nsa(const NsaArgs &a0, const PackedGeo &g, cudaStream_t s, cudaE
         if (before && (e = cudaEventRecord(before, s)) != cudaSuccess) return e;
         if ((e = launch_nsa_tc(a, g, s)) != cudaSuccess) return e;
         if (after && (e = cudaEventRecord(after, s)) != cudaSuccess) return e;
-        // the dQ finalize converts dK / dV too (d = 128 here)
+        // the dQ finalize converts dK / dV too
         if (a.t1 > 0 && a.deterministic)
-            e = launch_kernel(nsa_dq_finalize_det_kernel<T>, dim3(1024), dim3(256), 0, s, true, a, g, 1);
+            e = launch_kernel(nsa_dq_finalize_det_kernel<OutT>, dim3(1024), dim3(256), 0, s, true, a, g, 1);
         else if (a.t1 > 0)
-            e = launch_kernel(nsa_dq_finalize_kernel<T>, dim3(1024), dim3(256), 0, s, true, a, 1);
+            e = launch_kernel(nsa_dq_finalize_kernel<OutT>, dim3(1024), dim3(256), 0, s, true, a, 1);
         if (e != cudaSuccess) return e;
     } else if (a.t1 > 0) {
-        const int G = int(a.n1 / a.n2), BS = int(a.bs), LD = 129;
-        size_t smem = sizeof(float) * (2 * BS * LD + 2 * G * LD + 2 * G * BS + 2 * G);
-        auto k = nsa_bwd_simt_kernel<T>;
-        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) != cudaSuccess)
-            return e;
         if (before && (e = cudaEventRecord(before, s)) != cudaSuccess) return e;
-        if ((e = launch_kernel(k, dim3(unsigned(a.t1), unsigned(a.n2)), dim3(256), smem, s, true, a, g)) != cudaSuccess)
-            return e;
+        if ((e = launch_simt_bwd<T, OutT>(a, g, s)) != cudaSuccess) return e;
         if (after && (e = cudaEventRecord(after, s)) != cudaSuccess) return e;
     }
     const bool kv_done = tc && a.t1 > 0;  // converted by the dQ finalize
-    if (a.t2 > 0 && !kv_done && (e = launch_kernel(nsa_finalize_kernel<T>, dim3(1024), dim3(256), 0, s, true, a)) != cudaSuccess)
+    if (a.t2 > 0 && !kv_done &&
+        (e = launch_kernel(nsa_finalize_kernel<OutT>, dim3(1024), dim3(256), 0, s, true, a)) != cudaSuccess)
         return e;
     return cudaSuccess;
+}
+
+template <class T, int DQK, int DV> cudaError_t run_nsa_fwd_t(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
+{
+    auto k = nsa_fwd_simt_kernel<T, DQK, DV>;
+    const int64_t G = a.n1 / a.n2;
+    const size_t smem = sizeof(float) * size_t(kNsaKB * (DQK + 1) + kNsaKB * (DV + 1) + G * (DQK + 1) + G * kNsaKB + 3 * G);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s)) != cudaSuccess) return e;
+    k<<<dim3(unsigned(a.t1), unsigned(a.n2)), 256, smem, s>>>(a, g);
+    return cudaGetLastError();
+}
+
+template <class T> cudaError_t run_nsa_fwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
+{
+    if (a.d == 128 && a.dv == 128) return run_nsa_fwd_t<T, 128, 128>(a, g, s);
+    if (a.d == 192 && a.dv == 128) return run_nsa_fwd_t<T, 192, 128>(a, g, s);
+    if (a.d == 128 && a.dv == 192) return run_nsa_fwd_t<T, 128, 192>(a, g, s);
+    return run_nsa_fwd_t<T, 192, 192>(a, g, s);
 }
 }  // namespace
 
@@ -488,8 +668,16 @@ cudaError_t launch_nsa_block_lists(const NsaArgs &a, const PackedGeo &g, cudaStr
 cudaError_t launch_nsa_bwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, cudaEvent_t before,
                            cudaEvent_t after)
 {
-    return a.dtype == ATTN_F16 ? run_nsa<__half>(a, g, s, before, after)
-                               : run_nsa<__nv_bfloat16>(a, g, s, before, after);
+    if (a.grad_fp32)
+        return a.dtype == ATTN_F16 ? run_nsa<__half, float>(a, g, s, before, after)
+                                   : run_nsa<__nv_bfloat16, float>(a, g, s, before, after);
+    return a.dtype == ATTN_F16 ? run_nsa<__half, __half>(a, g, s, before, after)
+                               : run_nsa<__nv_bfloat16, __nv_bfloat16>(a, g, s, before, after);
+}
+
+cudaError_t launch_nsa_fwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
+{
+    return a.dtype == ATTN_F16 ? run_nsa_fwd<__half>(a, g, s) : run_nsa_fwd<__nv_bfloat16>(a, g, s);
 }
 
 }  // namespace attn

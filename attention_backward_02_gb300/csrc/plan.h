@@ -56,19 +56,23 @@ struct Workspace {
 //   pieces   int32 [nrows + 1]      tensor-core work units per row (exclusive scan)
 //   tokens   int32 [t1 * n2 * cnt]  block lists, ascending token ids
 //   dqacc    f32 [t1_pad][n1][d]
-//   dkacc    f32 [t2][n2][d], dvacc f32 [t2][n2][d]
+//   dkacc    f32 [t2][n2][d], dvacc f32 [t2][n2][dv]
 //   dqpart   f32 [t1][n2][cnt][G][d]   deterministic mode: dQ per (token, selected slot)
 struct NsaArgs {
     int dtype;
-    int64_t nseq, n1, n2, d, bs, cnt;
+    int grad_fp32;              // dq, dk, dv are fp32 (else the input dtype)
+    int64_t nseq, n1, n2, d, dv, bs, cnt;   // d: query / key head dim, dv: value head dim
     int64_t t1, t2, t1_pad;
     int64_t nblk_max, words_max, nrows;   // nrows = nseq * n2 * nblk_max
     float scale;
     int sparse_mode, deterministic, n_part;
     const void *q, *k, *v, *o, *dO;
+    void *o_out;                // forward: O
+    float *smax_out, *ssum_out; // forward: softmaxMax / softmaxSum [T1][n1][8]
     const float *smax, *ssum;
     const int32_t *topk;
-    void *dq, *dk, *dv;
+    void *dq, *dk, *dvp;         // gradients (dvp: dV)
+    __host__ __device__ void *dv_out() const { return dvp; }
     uint32_t *status;
     float *lse2, *dvec;
     uint32_t *bitmap;
@@ -98,5 +102,7 @@ cudaError_t launch_nsa_bwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s,
 cudaError_t launch_nsa_block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s);
 bool nsa_tc_supported(const NsaArgs &a);
 cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s);
+// NSA forward: a.o, a.smax, a.ssum are written (o is the output here).
+cudaError_t launch_nsa_fwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s);
 
 }  // namespace attn

@@ -185,14 +185,37 @@ typedef struct {
     const int64_t *cu_seqlens_kv;  /* host, b inclusive cumulative lengths   */
     int64_t n1;             /* query heads (headNum)                          */
     int64_t n2;             /* key/value heads; n1 % n2 == 0, n1/n2 <= 32     */
-    int64_t d;              /* head dim: 128                                  */
+    int64_t d;              /* head dim of q and k: 128 or 192                */
     double scale;           /* scaleValue                                     */
     int64_t block_size;     /* selectedBlockSize: 64                          */
     int64_t block_count;    /* selectedBlockCount in [1, 128], count*size < 8192 */
     int sparse_mode;        /* 0: only the selection; 2: also causal,
                                bottom-right aligned per sequence              */
     int deterministic;      /* 1: bitwise reproducible dQ                     */
+    int64_t d_v;            /* head dim of v, O, dO and dv: 128 or 192; 0 means
+                               d ([Ascend] Constraints: D is 192 or 128, and K
+                               and V may differ)                              */
+    int grad_fp32;          /* 1: dq, dk, dv are fp32; 0: the input dtype
+                               ([Ascend] parameter table: FLOAT16, BFLOAT16,
+                               FLOAT32 outputs)                               */
 } attn_nsa_desc_t;
+
+/* NSA selected-attention forward (training mode): O and the softmax stats the
+ * backward reads.  [Ascend] "Function / Formula" (gather of the selected
+ * blocks, then attention over them) and parameter table (softmaxMax /
+ * softmaxSum [T1, N1, 8]).  For query token t, kv head g and query head
+ * h of g, over the keys of the selected blocks that the sparse mode leaves
+ * visible: softmax_max = max_j s_j with s_j = scale q.k_j, softmax_sum =
+ * sum_j exp(s_j - softmax_max), O = sum_j exp(s_j - softmax_max) v_j /
+ * softmax_sum; all 8 lanes of a stats row hold the same value.  A row that
+ * sees no key has O = 0, softmax_max = -inf, softmax_sum = 0.
+ *   q : [T1][n1][d]  k : [T2][n2][d]  v : [T2][n2][d_v]  o : [T1][n1][d_v]
+ *   topk : as for the backward; invalid indices are skipped and flagged.
+ * The workspace holds the device status word: nsa_fwd_workspace_size bytes. */
+attn_status_t nsa_fwd_workspace_size(const attn_nsa_desc_t *desc, size_t *bytes);
+attn_status_t nsa_selected_attn_fwd(const attn_nsa_desc_t *desc, const void *q, const void *k, const void *v,
+                                    const int32_t *topk, void *o, float *softmax_max, float *softmax_sum,
+                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /* Workspace bytes for nsa_selected_attn_bwd.  Host only; no CUDA call.
  * [Ascend] "Function Prototype": aclnnNsaSelectedAttentionGradGetWorkspaceSize. */
@@ -203,8 +226,10 @@ attn_status_t nsa_workspace_size(const attn_nsa_desc_t *desc, size_t *bytes);
  * through the indices), parameter table (TND layout, actualSeqQLen /
  * actualSeqKvLen, softmaxMax / softmaxSum, topkIndices, scaleValue,
  * selectedBlockSize / Count, sparseMode) and "Constraints".  Layout, all
- * contiguous:
- *   q, o, dO, dq : [T1][n1][d]      k, v, dk, dv : [T2][n2][d]
+ * contiguous (d_v = value head dim):
+ *   q, dq : [T1][n1][d]    o, dO : [T1][n1][d_v]
+ *   k, dk : [T2][n2][d]    v, dv : [T2][n2][d_v]
+ *   dq, dk, dv are fp32 when grad_fp32 is set, else the input dtype.
  *   softmax_max, softmax_sum : [T1][n1][8] fp32 (the 8 lanes hold one value;
  *       lane 0 is read): P = exp(scale q.k - max) / sum over the selection.
  *   topk : [T1][n2][block_count] int32 block ids local to the token's

@@ -188,7 +188,8 @@ def nsa_topk(rng, cu_q, cu_kv, n2, block_size, block_count, causal):
 
 
 def nsa_problem(name, *, dtype, lens_q, lens_kv=None, n1, n2, d, block_size, block_count,
-                sparse_mode, scale=None, seed=42) -> NsaProblem:
+                sparse_mode, scale=None, seed=42, d_v=None) -> NsaProblem:
+    """d: query / key head dim; d_v: value head dim of v, O and dO (default d)."""
     rng = np.random.default_rng(seed)
     lens_q = np.asarray(lens_q, np.int64)
     lens_kv = np.asarray(lens_kv if lens_kv is not None else lens_q, np.int64)
@@ -198,8 +199,8 @@ def nsa_problem(name, *, dtype, lens_q, lens_kv=None, n1, n2, d, block_size, blo
         scale = 1.0 / np.sqrt(d)
     q = _normal_bits(rng, (t1, n1, d), dtype)
     k = _normal_bits(rng, (t2, n2, d), dtype)
-    v = _normal_bits(rng, (t2, n2, d), dtype)
-    do = _normal_bits(rng, (t1, n1, d), dtype)
+    v = _normal_bits(rng, (t2, n2, d if d_v is None else d_v), dtype)
+    do = _normal_bits(rng, (t1, n1, d if d_v is None else d_v), dtype)
     topk = nsa_topk(rng, cu_q, cu_kv, n2, block_size, block_count, causal=(sparse_mode == 2))
     return NsaProblem(name, dtype, n1, n2, d, float(scale), block_size, block_count, sparse_mode,
                       cu_q, cu_kv, q, k, v, do, topk)

@@ -140,23 +140,45 @@ def nsa_oracle_inputs(p: synth.NsaProblem, threads=0):
     return o_bits, mx.astype(np.float32), sm.astype(np.float32)
 
 
-def nsa_desc(p: synth.NsaProblem, deterministic=False):
+def nsa_desc(p: synth.NsaProblem, deterministic=False, grad_fp32=False):
     import attention_backward_02_gb300 as ab
+    d_v = p.v.shape[-1]
     return ab.nsa_desc(dtype=p.dtype, cu_seqlens_q=list(p.cu_q), cu_seqlens_kv=list(p.cu_kv), n1=p.n1, n2=p.n2,
                        d=p.d, scale=p.scale, block_size=p.block_size, block_count=p.block_count,
-                       sparse_mode=p.sparse_mode, deterministic=deterministic)
+                       sparse_mode=p.sparse_mode, deterministic=deterministic, d_v=0 if d_v == p.d else d_v,
+                       grad_fp32=grad_fp32)
 
 
-def run_gpu_nsa(p: synth.NsaProblem, o_bits, mx, sm, deterministic=False, topk=None, expect_flags=0):
+def run_gpu_nsa_fwd(p: synth.NsaProblem, topk=None, expect_flags=0):
+    """nsa_selected_attn_fwd on the GPU: O (16-bit values as f64), softmax max and sum (lane 0, f64)
+    and the 8-lane stats as returned."""
+    import torch
+    import attention_backward_02_gb300 as ab
+    q, k, v = (bits_to_gpu(x, p.dtype) for x in (p.q, p.k, p.v))
+    o = torch.full((p.t1, p.n1, p.v.shape[-1]), float("nan"), dtype=q.dtype, device="cuda")
+    mx8 = torch.full((p.t1, p.n1, 8), float("nan"), dtype=torch.float32, device="cuda")
+    sm8 = torch.full((p.t1, p.n1, 8), float("nan"), dtype=torch.float32, device="cuda")
+    tk = torch.from_numpy(np.ascontiguousarray(p.topk if topk is None else topk, np.int32)).cuda()
+    ws = ab.nsa_selected_attn_fwd(nsa_desc(p), q, k, v, tk, o, mx8, sm8)
+    flags = ab.attn_query_status(ws)
+    assert flags == expect_flags, f"device status {flags:#x}, expected {expect_flags:#x}"
+    torch.cuda.synchronize()
+    m8, s8 = mx8.cpu().numpy().astype(np.float64), sm8.cpu().numpy().astype(np.float64)
+    return gpu_to_f64(o), m8[..., 0], s8[..., 0], m8, s8
+
+
+def run_gpu_nsa(p: synth.NsaProblem, o_bits, mx, sm, deterministic=False, topk=None, expect_flags=0,
+                grad_fp32=False):
     import torch
     import attention_backward_02_gb300 as ab
     q, k, v, do, o = (bits_to_gpu(x, p.dtype) for x in (p.q, p.k, p.v, p.do, o_bits))
     mx8 = torch.from_numpy(np.repeat(mx[..., None], 8, -1).astype(np.float32)).cuda()
     sm8 = torch.from_numpy(np.repeat(sm[..., None], 8, -1).astype(np.float32)).cuda()
     tk = torch.from_numpy(np.ascontiguousarray(p.topk if topk is None else topk, np.int32)).cuda()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    gdt = torch.float32 if grad_fp32 else q.dtype
+    dq, dk, dv = (torch.empty(x.shape, dtype=gdt, device="cuda") for x in (q, k, v))
     dq.fill_(float("nan")); dk.fill_(float("nan")); dv.fill_(float("nan"))
-    ws = ab.nsa_selected_attn_bwd(nsa_desc(p, deterministic), q, k, v, o, do, mx8, sm8, tk, dq, dk, dv)
+    ws = ab.nsa_selected_attn_bwd(nsa_desc(p, deterministic, grad_fp32), q, k, v, o, do, mx8, sm8, tk, dq, dk, dv)
     flags = ab.attn_query_status(ws)
     assert flags == expect_flags, f"device status {flags:#x}, expected {expect_flags:#x}"
     torch.cuda.synchronize()

@@ -101,12 +101,33 @@ def _nsa(ab, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(), 0), (dict(block_size=48), 2), (dict(block_size=256), 2), (dict(block_count=0), 2),
     (dict(block_count=128, block_size=64), 2), (dict(n1=16, n2=3), 2), (dict(n1=64, n2=1), 2),
-    (dict(sparse_mode=1), 2), (dict(d=64), 2), (dict(d=192), 3),
+    (dict(sparse_mode=1), 2), (dict(d=64), 2), (dict(d=192), 0), (dict(d_v=192), 0), (dict(d=192, d_v=128), 0),
+    (dict(d_v=64), 2), (dict(grad_fp32=True), 0),
     (dict(cu_seqlens_kv=[4000, 8192]), 2), (dict(cu_seqlens_kv=[512, 1024], block_count=16), 2),
 ])
 def test_nsa_descriptor_rejections(ab, kw, code):
     n = C.c_size_t()
     assert ab._lib.load().nsa_workspace_size(C.byref(_nsa(ab, **kw)), C.byref(n)) == code
+
+
+def test_nsa_fwd_rejects_before_launch(ab):
+    lib = ab._lib.load()
+    desc = _nsa(ab)
+    n = C.c_size_t()
+    assert lib.nsa_fwd_workspace_size(C.byref(desc), C.byref(n)) == 0 and n.value >= 4
+    fp = lambda a: C.cast(C.c_void_p(a), C.POINTER(C.c_float))
+    ip = lambda a: C.cast(C.c_void_p(a), C.POINTER(C.c_int32))
+
+    def call(q=0x10000, o=0x30000, topk=0x40000, smax=0x50000, ws=0x100000, nbytes=256):
+        return lib.nsa_selected_attn_fwd(C.byref(desc), C.c_void_p(q), C.c_void_p(0x10000), C.c_void_p(0x10000),
+                                         ip(topk), C.c_void_p(o), fp(smax), fp(0x60000), C.c_void_p(ws),
+                                         C.c_size_t(nbytes), None)
+    assert call(q=0) == 1            # NULL query
+    assert call(o=0x30008) == 5      # misaligned output
+    assert call(topk=0x40002) == 5   # topk not 4-byte aligned
+    assert call(smax=0x50004) == 5   # stats not 16-byte aligned
+    assert call(nbytes=2) == 4       # short workspace
+    assert call(ws=0) == 4           # no workspace
 
 
 def test_fwd_rejects_before_launch(ab):
