@@ -56,7 +56,8 @@ class _Nsa(C.Structure):
     _fields_ = [("nseq", C.c_int64), ("cu_q", C.POINTER(C.c_int64)), ("cu_kv", C.POINTER(C.c_int64)),
                 ("n1", C.c_int64), ("n2", C.c_int64), ("d", C.c_int64), ("scale", C.c_double),
                 ("block_size", C.c_int64), ("block_count", C.c_int64), ("sparse_mode", C.c_int),
-                ("d_v", C.c_int64)]
+                ("d_v", C.c_int64), ("atten_mask", C.POINTER(C.c_uint8)), ("mask_rows", C.c_int64),
+                ("mask_cols", C.c_int64)]
 
 
 def _load():
@@ -142,10 +143,23 @@ def dense_bwd_rows(q, k, v, o, do, lse, cu_q, cu_kv, scale, mask, q_rows, kv_row
     return dq, dk, dv
 
 
-def _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, bs, cnt, sparse_mode, d_v=0):
+def _mask(mask):
+    """attenMaskOptional as a C-contiguous uint8 [rows, cols] array (nonzero: key removed), or None."""
+    if mask is None:
+        return None
+    m = np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+    if m.ndim != 2:
+        raise ValueError("attenMaskOptional is 2-D: [query positions, key positions]")
+    return m
+
+
+def _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, bs, cnt, sparse_mode, d_v=0, mask=None):
+    """mask: the uint8 array from _mask (kept alive by the caller) or None."""
+    mp = mask.ctypes.data_as(C.POINTER(C.c_uint8)) if mask is not None else None
+    rows, cols = (mask.shape if mask is not None else (0, 0))
     return _Nsa(len(cu_q), cu_q.ctypes.data_as(C.POINTER(C.c_int64)),
                 cu_kv.ctypes.data_as(C.POINTER(C.c_int64)), n1, n2, d, float(scale), bs, cnt,
-                int(sparse_mode), int(d_v))
+                int(sparse_mode), int(d_v), mp, int(rows), int(cols))
 
 
 def _nsa_dims(q, k, v):
@@ -163,15 +177,17 @@ def _ip(a):
     return a.ctypes.data_as(C.POINTER(C.c_int32))
 
 
-def nsa_fwd(q, k, v, topk, cu_q, cu_kv, scale, block_size, sparse_mode, threads=0):
-    """Sparse forward: O [T1,n1,d], softmaxMax [T1,n1], softmaxSum [T1,n1]."""
+def nsa_fwd(q, k, v, topk, cu_q, cu_kv, scale, block_size, sparse_mode, threads=0, mask=None):
+    """Sparse forward: O [T1,n1,d], softmaxMax [T1,n1], softmaxSum [T1,n1].  mask: optional 2-D
+    attenMaskOptional over (query, key) positions local to the sequence, nonzero = removed."""
     q, k, v, topk = _f64(q), _f64(k), _f64(v), _i32(topk)
+    mask = _mask(mask)
     cu_q, cu_kv = _cu(cu_q), _cu(cu_kv)
     t1, n1, _ = q.shape
     d, dv_ = _nsa_dims(q, k, v)
     n2, cnt = k.shape[1], topk.shape[2]
     o = np.empty((t1, n1, dv_)); mx = np.empty((t1, n1)); sm = np.empty((t1, n1))
-    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode, dv_)
+    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode, dv_, mask)
     rc = _load().ora_nsa_fwd(C.byref(desc), _d(q), _d(k), _d(v), _ip(topk), _d(o), _d(mx), _d(sm),
                              int(threads))
     if rc:
@@ -179,9 +195,10 @@ def nsa_fwd(q, k, v, topk, cu_q, cu_kv, scale, block_size, sparse_mode, threads=
     return o, mx, sm
 
 
-def nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, scale, block_size, sparse_mode, threads=0):
-    """Gather -> dense backward on the gathered rows -> scatter-add back."""
+def nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, scale, block_size, sparse_mode, threads=0, mask=None):
+    """Gather -> dense backward on the gathered rows -> scatter-add back.  mask as for nsa_fwd."""
     q, k, v, o, do, mx, sm = (_f64(x) for x in (q, k, v, o, do, mx, sm))
+    mask = _mask(mask)
     topk = _i32(topk)
     cu_q, cu_kv = _cu(cu_q), _cu(cu_kv)
     _, n1, _ = q.shape
@@ -190,7 +207,7 @@ def nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, scale, block_size, sparse
         raise ValueError("attentionOut and its gradient must have the value head dim")
     n2, cnt = k.shape[1], topk.shape[2]
     dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
-    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode, dv_)
+    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode, dv_, mask)
     rc = _load().ora_nsa_bwd(C.byref(desc), _d(q), _d(k), _d(v), _d(o), _d(do), _d(mx), _d(sm),
                              _ip(topk), _d(dq), _d(dk), _d(dv), int(threads))
     if rc:
@@ -198,9 +215,10 @@ def nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, scale, block_size, sparse
     return dq, dk, dv
 
 
-def nsa_masked_dense(q, k, v, do, topk, cu_q, cu_kv, scale, block_size, sparse_mode, threads=0):
+def nsa_masked_dense(q, k, v, do, topk, cu_q, cu_kv, scale, block_size, sparse_mode, threads=0, mask=None):
     """Independent NSA path: masked dense attention, own softmax; returns o, dq, dk, dv."""
     q, k, v, do, topk = _f64(q), _f64(k), _f64(v), _f64(do), _i32(topk)
+    mask = _mask(mask)
     cu_q, cu_kv = _cu(cu_q), _cu(cu_kv)
     t1, n1, _ = q.shape
     d, dv_ = _nsa_dims(q, k, v)
@@ -208,7 +226,7 @@ def nsa_masked_dense(q, k, v, do, topk, cu_q, cu_kv, scale, block_size, sparse_m
         raise ValueError("the gradient of attentionOut must have the value head dim")
     n2, cnt = k.shape[1], topk.shape[2]
     o, dq, dk, dv = np.empty((t1, n1, dv_)), np.empty_like(q), np.empty_like(k), np.empty_like(v)
-    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode, dv_)
+    desc = _nsa_desc(cu_q, cu_kv, n1, n2, d, scale, block_size, cnt, sparse_mode, dv_, mask)
     rc = _load().ora_nsa_masked_dense(C.byref(desc), _d(q), _d(k), _d(v), _d(do), _ip(topk),
                                       _d(o), _d(dq), _d(dk), _d(dv), int(threads))
     if rc:

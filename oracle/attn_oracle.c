@@ -38,7 +38,10 @@
  * sequence.  The keys and values are gathered explicitly, the backward above
  * runs on the gathered rows, and the gathered dK / dV rows are added back to
  * the rows they came from.  The softmax stats are the page's softmaxMax and
- * softmaxSum: P = exp(s - max) / sum.
+ * softmaxSum: P = exp(s - max) / sum.  The page's attenMaskOptional (2-D,
+ * BOOL / UINT8, in the signature and the parameter table, used by no formula)
+ * is read as: entry (i, j) nonzero removes key j for query i, positions local
+ * to the sequence, on top of the selection and the sparse mode.
  *
  * Layout of every tensor here (fp64): token-major "TND"
  *   q, o, dO, dq : [Tq][h][d]      k, v, dk, dv : [Tkv][h_kv][d]
@@ -98,6 +101,11 @@ typedef struct {
     int64_t d_v;           /* head dim of value, attentionOut and dY (the page
                               allows it to differ from the query / key head
                               dim d); 0: equal to d                             */
+    const uint8_t *atten_mask; /* attenMaskOptional: NULL, or [mask_rows][mask_cols]
+                              with nonzero = key j removed for query i (local
+                              positions), on top of the selection and the
+                              sparse mode                                       */
+    int64_t mask_rows, mask_cols;
 } ora_nsa_t;
 
 static int64_t value_dim(const ora_nsa_t *pb) { return pb->d_v > 0 ? pb->d_v : pb->d; }
@@ -405,9 +413,17 @@ static int64_t gather_rows(const ora_nsa_t *pb, const int32_t *topk_tg, int64_t 
 }
 
 /* sparseMode 2 masks key j of query i when j > i + (lkv - lq).              */
-static int nsa_visible(const ora_nsa_t *pb, int64_t i, int64_t j, int64_t lq, int64_t lkv)
+static int nsa_mode_visible(const ora_nsa_t *pb, int64_t i, int64_t j, int64_t lq, int64_t lkv)
 {
     return pb->sparse_mode == 2 ? visible(2, i, j, lq, lkv) : 1;
+}
+
+/* The sparse mode, then attenMaskOptional: a nonzero mask entry (i, j) removes
+ * key j for query i.                                                          */
+static int nsa_visible(const ora_nsa_t *pb, int64_t i, int64_t j, int64_t lq, int64_t lkv)
+{
+    if (!nsa_mode_visible(pb, i, j, lq, lkv)) return 0;
+    return !(pb->atten_mask && pb->atten_mask[i * pb->mask_cols + j]);
 }
 
 static void nsa_fwd_unit(void *vctx, int64_t unit)
@@ -528,6 +544,10 @@ static int nsa_check(const ora_nsa_t *pb)
     if (!pb || pb->n2 <= 0 || pb->n1 % pb->n2 || pb->block_size <= 0 || pb->block_count <= 0) return ORA_ERR;
     if (pb->d <= 0 || pb->d_v < 0) return ORA_ERR;
     if (pb->sparse_mode != 0 && pb->sparse_mode != 2) return ORA_ERR;
+    if (pb->atten_mask) {  /* the mask covers every sequence's local positions */
+        for (int64_t b = 0; b < pb->nseq; ++b)
+            if (seq_len(pb->cu_q, b) > pb->mask_rows || seq_len(pb->cu_kv, b) > pb->mask_cols) return ORA_ERR;
+    }
     return ORA_OK;
 }
 
@@ -658,8 +678,9 @@ int ora_nsa_block_lists(const ora_nsa_t *pb, const int32_t *topk, int64_t nblk_m
                     int chosen = 0;
                     for (int64_t cc = 0; cc < pb->block_count; ++cc)
                         if (topk[((q0 + i) * pb->n2 + g) * pb->block_count + cc] == blk) chosen = 1;
-                    /* the block's first key is its most visible one */
-                    if (chosen && nsa_visible(pb, i, blk * pb->block_size, lq, lkv))
+                    /* the block's first key is its most visible one (the sparse mode
+                       alone decides; attenMaskOptional applies per element later) */
+                    if (chosen && nsa_mode_visible(pb, i, blk * pb->block_size, lq, lkv))
                         tokens[n++] = (int32_t)(q0 + i);
                 }
                 offsets[(b * pb->n2 + g) * nblk_max + blk + 1] = n;

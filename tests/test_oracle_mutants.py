@@ -44,8 +44,13 @@ MUTANTS = [
      "c->dv[((k0 + rows[r]) * pb->n2 + g) * d + x] += dvsel[r * e + x];", "nsa_fd_dims"),
     ("nsa_dk_no_scale", "dksel[r * d + x] += pb->scale * ds * qi[x];", "dksel[r * d + x] += ds * qi[x];",
      "nsa_fd"),
-    ("block_lists_last_key", "nsa_visible(pb, i, blk * pb->block_size, lq, lkv)",
-     "nsa_visible(pb, i, blk * pb->block_size + pb->block_size - 1, lq, lkv)", "block_lists"),
+    ("block_lists_last_key", "nsa_mode_visible(pb, i, blk * pb->block_size, lq, lkv)",
+     "nsa_mode_visible(pb, i, blk * pb->block_size + pb->block_size - 1, lq, lkv)", "block_lists"),
+    # attenMaskOptional read as "keep" instead of "remove", and ignored altogether
+    ("mask_inverted", "return !(pb->atten_mask && pb->atten_mask[i * pb->mask_cols + j]);",
+     "return !(pb->atten_mask && !pb->atten_mask[i * pb->mask_cols + j]);", "mask_one_key"),
+    ("mask_ignored", "return !(pb->atten_mask && pb->atten_mask[i * pb->mask_cols + j]);", "return 1;",
+     "mask_causal"),
     ("repeat_accepted", "if (topk_tg[e] == blk) return -1;", "if (topk_tg[e] == blk && 0) return -1;", "nsa_repeat"),
 ]
 
@@ -83,6 +88,10 @@ def _run_pin(pin):
         pins.check_nsa_rejects_repeated_index()
     elif pin == "nsa_fd_dims":
         pins.test_nsa_finite_differences_unequal_dims(2)
+    elif pin == "mask_one_key":
+        pins.test_nsa_mask_keeps_one_key_closed_form()
+    elif pin == "mask_causal":
+        pins.test_nsa_causal_mask_equals_sparse_mode_2()
     else:
         raise ValueError(pin)
 

@@ -439,3 +439,89 @@ def test_nsa_block_lists_definition(sparse_mode):
                 np.testing.assert_array_equal(got, toks + starts_q[b])
                 pos += len(toks)
     assert offsets[-1] == pos
+
+
+# ------------------------------------------------ attenMaskOptional (2-D mask)
+# Reading of the Ascend page's attenMaskOptional (2-D BOOL / UINT8, in the signature and the parameter
+# table, used by no formula): entry (i, j) nonzero removes key j for query i, positions local to the
+# sequence, on top of the selection and the sparse mode.
+
+def test_nsa_zero_mask_is_no_mask():
+    cu_q, cu_kv, q, k, v, do, topk = _nsa_random([64, 40], [64, 48], 8, 2, 16, 8, 3, 2, seed=31)
+    zero = np.zeros((64, 64), np.uint8)
+    o, mx, sm = oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.3, 8, 2)
+    om, mxm, smm = oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.3, 8, 2, mask=zero)
+    np.testing.assert_array_equal(o, om)
+    np.testing.assert_array_equal(mx, mxm)
+    np.testing.assert_array_equal(sm, smm)
+    a = oracle.nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, 0.3, 8, 2)
+    b = oracle.nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, 0.3, 8, 2, mask=zero)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_nsa_causal_mask_equals_sparse_mode_2():
+    """sparseMode 0 with the bottom-right causal pattern as attenMaskOptional is sparseMode 2."""
+    lq, lkv = 24, 40
+    cu_q, cu_kv, q, k, v, do, topk = _nsa_random([lq, lq], [lkv, lkv], 8, 2, 16, 8, 3, 2, seed=32)
+    i, j = np.meshgrid(np.arange(lq), np.arange(lkv), indexing="ij")
+    causal = (j > i + (lkv - lq)).astype(np.uint8)
+    o2, mx2, sm2 = oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.3, 8, 2)
+    o0, mx0, sm0 = oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.3, 8, 0, mask=causal)
+    assert _rel(o0, o2) < 1e-14 and _rel(sm0, sm2) < 1e-14
+    np.testing.assert_array_equal(mx0, mx2)
+    a = oracle.nsa_bwd(q, k, v, o2, do, mx2, sm2, topk, cu_q, cu_kv, 0.3, 8, 2)
+    b = oracle.nsa_bwd(q, k, v, o2, do, mx2, sm2, topk, cu_q, cu_kv, 0.3, 8, 0, mask=causal)
+    for x, y in zip(a, b):
+        assert _rel(y, x) < 1e-14
+
+
+def test_nsa_mask_keeps_one_key_closed_form():
+    """A mask that leaves each query exactly one key of its selection: P = 1 on that key, so O is
+    that key's value row, softmaxSum = 1, softmaxMax = its score (the mask removes, it does not keep)."""
+    rng = _rng(33)
+    lq, lkv, d = 6, 8, 4
+    q = rng.standard_normal((lq, 1, d)); k = rng.standard_normal((lkv, 1, d)); v = rng.standard_normal((lkv, 1, d))
+    topk = np.tile(np.array([0, 1], np.int32), (lq, 1, 1))  # blocks of 4: every key selected
+    keep = np.array([3, 0, 7, 5, 1, 6])
+    mask = np.ones((lq, lkv), np.uint8)
+    mask[np.arange(lq), keep] = 0
+    o, mx, sm = oracle.nsa_fwd(q, k, v, topk, [lq], [lkv], 0.5, 4, 0, mask=mask)
+    np.testing.assert_allclose(o[:, 0], v[keep, 0], rtol=1e-15)
+    np.testing.assert_allclose(sm[:, 0], 1.0, rtol=1e-15)
+    np.testing.assert_allclose(mx[:, 0], 0.5 * np.einsum("id,id->i", q[:, 0], k[keep, 0]), rtol=1e-14)
+
+
+@pytest.mark.parametrize("sparse_mode", [0, 2])
+def test_nsa_mask_finite_differences(sparse_mode):
+    cu_q, cu_kv, q, k, v, do, topk = _nsa_random([8, 6], [8, 6], 4, 2, 3, 2, 2, sparse_mode, seed=34)
+    mask = (_rng(35).random((8, 8)) < 0.3).astype(np.uint8)
+    o, mx, sm = oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.8, 2, sparse_mode, threads=1, mask=mask)
+    dq, dk, dv = oracle.nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, 0.8, 2, sparse_mode, threads=1,
+                                mask=mask)
+
+    def loss():
+        oo, _, _ = oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.8, 2, sparse_mode, threads=1, mask=mask)
+        return float((oo * do).sum())
+
+    for name, x, g in (("dq", q, dq), ("dk", k, dk), ("dv", v, dv)):
+        fd = _fd_grad(loss, x)
+        assert np.abs(fd - g).max() <= 1e-7 * max(1.0, np.abs(fd).max()), name
+
+
+@pytest.mark.parametrize("sparse_mode", [0, 2])
+def test_nsa_mask_gather_equals_masked_dense(sparse_mode):
+    cu_q, cu_kv, q, k, v, do, topk = _nsa_random([64, 40], [64, 48], 8, 2, 16, 8, 3, sparse_mode, seed=36)
+    mask = (_rng(37).random((64, 64)) < 0.25).astype(np.uint8)
+    o, mx, sm = oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.3, 8, sparse_mode, mask=mask)
+    got = oracle.nsa_bwd(q, k, v, o, do, mx, sm, topk, cu_q, cu_kv, 0.3, 8, sparse_mode, mask=mask)
+    od, *ref = oracle.nsa_masked_dense(q, k, v, do, topk, cu_q, cu_kv, 0.3, 8, sparse_mode, mask=mask)
+    assert _rel(o, od) < 1e-12
+    for a, b in zip(got, ref):
+        assert _rel(a, b) < 1e-12
+
+
+def test_nsa_mask_must_cover_the_sequences():
+    cu_q, cu_kv, q, k, v, do, topk = _nsa_random([8], [8], 2, 1, 3, 2, 2, 0, seed=38)
+    with pytest.raises(ValueError):
+        oracle.nsa_fwd(q, k, v, topk, cu_q, cu_kv, 0.8, 2, 0, mask=np.zeros((8, 7), np.uint8))
