@@ -72,17 +72,26 @@ def sdpa_desc(*, dtype, b, h, h_kv, s_q, s_kv, d, scale, mask=ATTN_MASK_NONE, cu
 
 
 def nsa_desc(*, dtype, cu_seqlens_q, cu_seqlens_kv, n1, n2, d, scale, block_size, block_count, sparse_mode,
-             deterministic=False, d_v=0, grad_fp32=False):
+             deterministic=False, d_v=0, grad_fp32=False, atten_mask=None):
     """An attn_nsa_desc_t: TND layout, b = len(cu_seqlens_q) sequences with inclusive cumulative query /
     key lengths, n1 query and n2 kv heads, query / key head dim d and value head dim d_v (0: d),
     scaleValue, selectedBlockSize / Count, sparseMode 0 (selection only) or 2 (also causal,
     bottom-right per sequence); deterministic makes dq, dk, dv bitwise reproducible (tensor-core head
-    groups only); grad_fp32 makes dq, dk, dv fp32."""
+    groups only); grad_fp32 makes dq, dk, dv fp32; atten_mask (attenMaskOptional) is a 2-D uint8 CUDA
+    tensor [rows, cols] over local (query, key) positions, nonzero = key removed, covering every
+    sequence (held by the descriptor)."""
     keep = _Keep()
+    if atten_mask is not None:
+        if atten_mask.dim() != 2 or not atten_mask.is_contiguous() or atten_mask.element_size() != 1:
+            raise ValueError("atten_mask: a contiguous 2-D tensor of 1-byte elements")
+        keep.items.append(atten_mask)
     desc = attn_nsa_desc_t(int(dtype), len(cu_seqlens_q), _cu_array(keep, cu_seqlens_q),
                            _cu_array(keep, cu_seqlens_kv), int(n1), int(n2), int(d), float(scale),
                            int(block_size), int(block_count), int(sparse_mode), int(bool(deterministic)),
-                           int(d_v), int(bool(grad_fp32)))
+                           int(d_v), int(bool(grad_fp32)),
+                           atten_mask.data_ptr() if atten_mask is not None else None,
+                           int(atten_mask.shape[0]) if atten_mask is not None else 0,
+                           int(atten_mask.shape[1]) if atten_mask is not None else 0)
     desc._keep = keep
     return desc
 

@@ -43,7 +43,8 @@ class attn_nsa_desc_t(C.Structure):
                 ("cu_seqlens_kv", C.POINTER(C.c_int64)), ("n1", C.c_int64), ("n2", C.c_int64),
                 ("d", C.c_int64), ("scale", C.c_double), ("block_size", C.c_int64),
                 ("block_count", C.c_int64), ("sparse_mode", C.c_int), ("deterministic", C.c_int),
-                ("d_v", C.c_int64), ("grad_fp32", C.c_int)]
+                ("d_v", C.c_int64), ("grad_fp32", C.c_int), ("atten_mask", C.c_void_p),
+                ("mask_rows", C.c_int64), ("mask_cols", C.c_int64)]
 
 
 _lib = None

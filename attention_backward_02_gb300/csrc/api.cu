@@ -322,6 +322,11 @@ attn_status_t check_nsa_desc(const attn_nsa_desc_t *d, NsaShape *sh)
     }
     sh->words_max = (sh->maxlen_q + 31) / 32;
     sh->dv = d->d_v ? d->d_v : d->d;
+    if (d->atten_mask) {  // the mask covers every sequence's local positions
+        if (d->mask_rows < sh->maxlen_q || d->mask_cols < 0) return ATTN_ERR_INVALID;
+        for (int64_t b = 0; b < d->b; ++b)
+            if (d->cu_seqlens_kv[b] - (b ? d->cu_seqlens_kv[b - 1] : 0) > d->mask_cols) return ATTN_ERR_INVALID;
+    }
     if (sh->t1 * d->n1 >= (int64_t(1) << 31) || sh->t2 * d->n2 >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
@@ -391,6 +396,7 @@ attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, 
     a.nseq = desc->b; a.n1 = desc->n1; a.n2 = desc->n2; a.d = desc->d; a.dv = sh.dv;
     a.grad_fp32 = desc->grad_fp32;
     a.bs = desc->block_size; a.cnt = desc->block_count;
+    a.mask = desc->atten_mask; a.mask_cols = desc->mask_cols;
     a.t1 = sh.t1; a.t2 = sh.t2; a.t1_pad = L.t1_pad;
     a.nblk_max = sh.nblk_max; a.words_max = sh.words_max; a.nrows = L.nrows;
     a.scale = float(desc->scale);
@@ -455,6 +461,7 @@ attn_status_t nsa_selected_attn_fwd(const attn_nsa_desc_t *desc, const void *q, 
     a.dtype = desc->dtype;
     a.nseq = desc->b; a.n1 = desc->n1; a.n2 = desc->n2; a.d = desc->d; a.dv = sh.dv;
     a.bs = desc->block_size; a.cnt = desc->block_count;
+    a.mask = desc->atten_mask; a.mask_cols = desc->mask_cols;
     a.t1 = sh.t1; a.t2 = sh.t2;
     a.scale = float(desc->scale);
     a.sparse_mode = desc->sparse_mode;
@@ -488,6 +495,7 @@ attn_status_t nsa_block_lists(const attn_nsa_desc_t *desc, const int32_t *topk, 
     a.nseq = desc->b; a.n1 = desc->n1; a.n2 = desc->n2; a.d = desc->d; a.dv = sh.dv;
     a.grad_fp32 = desc->grad_fp32;
     a.bs = desc->block_size; a.cnt = desc->block_count;
+    a.mask = desc->atten_mask; a.mask_cols = desc->mask_cols;
     a.t1 = sh.t1; a.t2 = sh.t2; a.t1_pad = L.t1_pad;
     a.nblk_max = sh.nblk_max; a.words_max = sh.words_max; a.nrows = L.nrows;
     a.sparse_mode = desc->sparse_mode;

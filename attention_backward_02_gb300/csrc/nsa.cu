@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(256) nsa_emit_kernel(NsaArgs a, PackedGeo geo,
 
 // ------------------------------------------------------------ main (CUDA cores)
 // One CTA per (token, kv head); loops over the selected blocks, KB keys at a
-// time.  dQ rows of the token are owned by the CTA; dK / dV go to fp32
+// time, masking by the sparse mode and attenMaskOptional (if given).  dQ rows of the token are owned by the CTA; dK / dV go to fp32
 // accumulators.  DQK: query / key head dim, DV: value head dim.
 constexpr int kNsaKB = 32;  // keys per pass of the CUDA-core kernels
 inline size_t nsa_simt_smem(int64_t G, int dqk, int dv)
@@ -306,7 +306,8 @@ __global__ void __launch_bounds__(256) nsa_bwd_simt_kernel(NsaArgs a, PackedGeo 
             __syncthreads();
             for (int e = tid; e < G * nk; e += 256) {
                 const int hh = e / nk, r = e % nk;
-                const bool vis = a.sparse_mode != 2 || visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, j0 + r, lq, lkv);
+                const bool vis = (a.sparse_mode != 2 || visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, j0 + r, lq, lkv)) &&
+                                 !(a.mask && a.mask[i * a.mask_cols + j0 + r]);
                 float sv = 0.f, dp = 0.f;
                 if (vis) {
 #pragma unroll 8
@@ -355,6 +356,7 @@ __global__ void __launch_bounds__(256) nsa_bwd_simt_kernel(NsaArgs a, PackedGeo 
 // ------------------------------------------------------------- forward (CUDA cores)
 // NSA selected-attention forward: one CTA per (token, kv head), KB keys of the
 // selected blocks at a time, online softmax per query head (max in log2 units).
+// A key is used when the sparse mode and attenMaskOptional (if given) keep it.
 // O = sum_j exp(s_j - max) v_j / sum; softmaxMax = max_j s_j (natural units),
 // softmaxSum = sum_j exp(s_j - max), both written to all 8 lanes.
 template <class T, int DQK, int DV>
@@ -418,7 +420,8 @@ __global__ void __launch_bounds__(256) nsa_fwd_simt_kernel(NsaArgs a, PackedGeo 
             for (int e = tid; e < G * KB; e += 256) {  // scores, log2 units; -inf where masked
                 const int hh = e / KB, r = e % KB;
                 float sv = -INFINITY;
-                if (r < nk && (a.sparse_mode != 2 || visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, j0 + r, lq, lkv))) {
+                if (r < nk && (a.sparse_mode != 2 || visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, j0 + r, lq, lkv)) &&
+                    !(a.mask && a.mask[i * a.mask_cols + j0 + r])) {
                     sv = 0.f;
 #pragma unroll 8
                     for (int x = 0; x < DQK; ++x) sv += Qs[hh][x] * Ks[r][x];

@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(1024) nsa_piece_scan_kernel(NsaArgs a)
 bool nsa_tc_supported(const NsaArgs &a)
 {
     const int64_t G = a.n1 / a.n2;
-    return a.d == kD && a.dv == kD && a.bs == kBS && (G == 8 || G == 16 || G == 32);
+    return a.d == kD && a.dv == kD && a.bs == kBS && (G == 8 || G == 16 || G == 32) && !a.mask;
 }
 
 cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)

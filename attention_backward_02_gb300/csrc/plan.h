@@ -67,6 +67,8 @@ struct NsaArgs {
     float scale;
     int sparse_mode, deterministic, n_part;
     const void *q, *k, *v, *o, *dO;
+    const uint8_t *mask;        // attenMaskOptional [..][mask_cols], nonzero = removed (NULL: none)
+    int64_t mask_cols;
     void *o_out;                // forward: O
     float *smax_out, *ssum_out; // forward: softmaxMax / softmaxSum [T1][n1][8]
     const float *smax, *ssum;

@@ -198,6 +198,16 @@ typedef struct {
     int grad_fp32;          /* 1: dq, dk, dv are fp32; 0: the input dtype
                                ([Ascend] parameter table: FLOAT16, BFLOAT16,
                                FLOAT32 outputs)                               */
+    /* attenMaskOptional ([Ascend] function prototype and parameter table: a
+     * 2-D BOOL / UINT8 mask that no formula on the page uses).  Read here as:
+     * device array [mask_rows][mask_cols] of uint8, row-major; entry (i, j)
+     * nonzero removes key j for query i (positions local to the sequence),
+     * on top of the selection and the sparse mode; it must cover every
+     * sequence (mask_rows >= its query length, mask_cols >= its key length).
+     * NULL: no mask.  Masked calls run on the CUDA-core kernels (no
+     * deterministic mode there).                                             */
+    const uint8_t *atten_mask;
+    int64_t mask_rows, mask_cols;
 } attn_nsa_desc_t;
 
 /* NSA selected-attention forward (training mode): O and the softmax stats the

@@ -132,24 +132,27 @@ def run_gpu_fwd(p: synth.DenseProblem):
 
 # ------------------------------------------------------------------------ NSA
 
-def nsa_oracle_inputs(p: synth.NsaProblem, threads=0):
+def nsa_oracle_inputs(p: synth.NsaProblem, threads=0, mask=None):
     """Sparse forward by the oracle: O rounded to 16 bits, fp32 max / sum."""
     o, mx, sm = oracle.nsa_fwd(p.f64("q"), p.f64("k"), p.f64("v"), p.topk, p.cu_q, p.cu_kv, p.scale,
-                               p.block_size, p.sparse_mode, threads=threads)
+                               p.block_size, p.sparse_mode, threads=threads, mask=mask)
     o_bits = synth.to_bits(o.astype(np.float32), p.dtype)
     return o_bits, mx.astype(np.float32), sm.astype(np.float32)
 
 
-def nsa_desc(p: synth.NsaProblem, deterministic=False, grad_fp32=False):
+def nsa_desc(p: synth.NsaProblem, deterministic=False, grad_fp32=False, mask=None):
+    """mask: optional numpy 2-D attenMaskOptional (copied to the GPU; the descriptor holds it)."""
+    import torch
     import attention_backward_02_gb300 as ab
     d_v = p.v.shape[-1]
+    m = None if mask is None else torch.from_numpy(np.ascontiguousarray(mask != 0, dtype=np.uint8)).cuda()
     return ab.nsa_desc(dtype=p.dtype, cu_seqlens_q=list(p.cu_q), cu_seqlens_kv=list(p.cu_kv), n1=p.n1, n2=p.n2,
                        d=p.d, scale=p.scale, block_size=p.block_size, block_count=p.block_count,
                        sparse_mode=p.sparse_mode, deterministic=deterministic, d_v=0 if d_v == p.d else d_v,
-                       grad_fp32=grad_fp32)
+                       grad_fp32=grad_fp32, atten_mask=m)
 
 
-def run_gpu_nsa_fwd(p: synth.NsaProblem, topk=None, expect_flags=0):
+def run_gpu_nsa_fwd(p: synth.NsaProblem, topk=None, expect_flags=0, mask=None):
     """nsa_selected_attn_fwd on the GPU: O (16-bit values as f64), softmax max and sum (lane 0, f64)
     and the 8-lane stats as returned."""
     import torch
@@ -159,7 +162,7 @@ def run_gpu_nsa_fwd(p: synth.NsaProblem, topk=None, expect_flags=0):
     mx8 = torch.full((p.t1, p.n1, 8), float("nan"), dtype=torch.float32, device="cuda")
     sm8 = torch.full((p.t1, p.n1, 8), float("nan"), dtype=torch.float32, device="cuda")
     tk = torch.from_numpy(np.ascontiguousarray(p.topk if topk is None else topk, np.int32)).cuda()
-    ws = ab.nsa_selected_attn_fwd(nsa_desc(p), q, k, v, tk, o, mx8, sm8)
+    ws = ab.nsa_selected_attn_fwd(nsa_desc(p, mask=mask), q, k, v, tk, o, mx8, sm8)
     flags = ab.attn_query_status(ws)
     assert flags == expect_flags, f"device status {flags:#x}, expected {expect_flags:#x}"
     torch.cuda.synchronize()
@@ -168,7 +171,7 @@ def run_gpu_nsa_fwd(p: synth.NsaProblem, topk=None, expect_flags=0):
 
 
 def run_gpu_nsa(p: synth.NsaProblem, o_bits, mx, sm, deterministic=False, topk=None, expect_flags=0,
-                grad_fp32=False):
+                grad_fp32=False, mask=None):
     import torch
     import attention_backward_02_gb300 as ab
     q, k, v, do, o = (bits_to_gpu(x, p.dtype) for x in (p.q, p.k, p.v, p.do, o_bits))
@@ -178,7 +181,8 @@ def run_gpu_nsa(p: synth.NsaProblem, o_bits, mx, sm, deterministic=False, topk=N
     gdt = torch.float32 if grad_fp32 else q.dtype
     dq, dk, dv = (torch.empty(x.shape, dtype=gdt, device="cuda") for x in (q, k, v))
     dq.fill_(float("nan")); dk.fill_(float("nan")); dv.fill_(float("nan"))
-    ws = ab.nsa_selected_attn_bwd(nsa_desc(p, deterministic, grad_fp32), q, k, v, o, do, mx8, sm8, tk, dq, dk, dv)
+    ws = ab.nsa_selected_attn_bwd(nsa_desc(p, deterministic, grad_fp32, mask), q, k, v, o, do, mx8, sm8, tk, dq,
+                                  dk, dv)
     flags = ab.attn_query_status(ws)
     assert flags == expect_flags, f"device status {flags:#x}, expected {expect_flags:#x}"
     torch.cuda.synchronize()

@@ -103,3 +103,49 @@ def test_nsa_unequal_dims_deterministic_refused():
     with pytest.raises(ab.AttnError) as e:
         H.run_gpu_nsa(p, o_bits, mx, sm, deterministic=True)
     assert e.value.status == ab._lib.ATTN_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------ attenMaskOptional (2-D mask)
+
+def _mask(rows, cols, seed, frac=0.3):
+    return (np.random.default_rng(seed).random((rows, cols)) < frac).astype(np.uint8)
+
+
+@pytest.mark.parametrize("sparse_mode", [0, 2])
+@pytest.mark.parametrize("n1,n2", [(16, 2), (4, 1)])
+def test_nsa_forward_with_mask(sparse_mode, n1, n2):
+    p = _problem(sparse_mode, n1=n1, n2=n2, seed=90 + n1 + sparse_mode)
+    mask = _mask(320, 512, 91 + sparse_mode)  # covers both sequences (and more)
+    o, mx, sm, m8, s8 = H.run_gpu_nsa_fwd(p, mask=mask)
+    ro, rmx, rsm = oracle.nsa_fwd(p.f64("q"), p.f64("k"), p.f64("v"), p.topk, p.cu_q, p.cu_kv, p.scale,
+                                  p.block_size, p.sparse_mode, mask=mask)
+    H.assert_close(o, ro, "O")
+    fin = np.isfinite(rmx)
+    assert np.all(np.isneginf(mx[~fin])) and np.all(sm[~fin] == 0)
+    np.testing.assert_allclose(mx[fin], rmx[fin], rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(sm[fin], rsm[fin], rtol=1e-4)
+
+
+@pytest.mark.parametrize("sparse_mode", [0, 2])
+@pytest.mark.parametrize("n1,n2,d,d_v", [(16, 2, 128, 128), (4, 1, 128, 128), (8, 2, 192, 128)])
+def test_nsa_backward_with_mask(sparse_mode, n1, n2, d, d_v):
+    """A mask routes the call to the CUDA-core kernel whatever the head group (16 / 2 would otherwise
+    run on the tensor-core kernel)."""
+    p = _problem(sparse_mode, n1=n1, n2=n2, d=d, d_v=d_v, seed=92 + n1 + d + sparse_mode)
+    mask = _mask(300, 512, 93 + n1 + sparse_mode)
+    o_bits, mx, sm = H.nsa_oracle_inputs(p, mask=mask)
+    dq, dk, dv = H.run_gpu_nsa(p, o_bits, mx, sm, mask=mask)
+    rq, rk, rv = oracle.nsa_bwd(p.f64("q"), p.f64("k"), p.f64("v"), synth.bits_to_f64(o_bits, p.dtype),
+                                p.f64("do"), mx.astype(np.float64), sm.astype(np.float64), p.topk, p.cu_q,
+                                p.cu_kv, p.scale, p.block_size, p.sparse_mode, mask=mask)
+    H.assert_close(dq, rq, "dQ")
+    H.assert_close(dk, rk, "dK")
+    H.assert_close(dv, rv, "dV")
+
+
+def test_nsa_mask_too_small_refused():
+    import attention_backward_02_gb300 as ab
+    p = _problem(0, seed=94)
+    with pytest.raises(ab.AttnError) as e:
+        H.run_gpu_nsa_fwd(p, mask=_mask(300, 100, 95))  # narrower than the 512-key sequence
+    assert e.value.status == ab._lib.ATTN_ERR_INVALID
