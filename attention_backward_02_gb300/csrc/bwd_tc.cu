@@ -928,9 +928,58 @@ void plan_units(TcSched &S, const DenseArgs &a, const Geo &g, int64_t units, int
         }
         if (fits) break;
     }
-    // the packing is kept only where it shortens the planned makespan clearly: the greedy plan
-    // starts the heads' units interleaved, which long sequences need for L2 reuse of Q / dO
-    if (100 * cap > 97 * greedy_max)
+    // the packing is kept only where it shortens the planned makespan clearly
+    bool use_ffd = 100 * cap <= 97 * greedy_max;
+    int64_t best = use_ffd ? cap : greedy_max;
+    // head-local plan, for problems whose inputs and dQ accumulator do not fit in L2: the key tiles of
+    // one (sequence, kv head) are paired (jt, n - 1 - jt), equal in cost under a causal mask; pairs
+    // go out head by head in full rounds of `ctas` (all rounds but the last full one), so the CTAs
+    // running together share a few heads' Q / dO rows and dQ accumulator rows; the remaining units
+    // go greedily, longest first, to the least loaded CTA
+    static thread_local int32_t local_of[kSchedUnits], local_rank[kSchedUnits], tail[kSchedUnits];
+    bool use_local = false;
+    const int64_t ws_bytes = (a.t_q * a.h * a.d * 2 + a.t_kv * a.h_kv * a.d) * 2 + a.h * a.t_pad * a.d * 4;
+    if (ws_bytes > (int64_t(64) << 20)) {
+        const int64_t ntiles = nu / nheads;
+        const int64_t pairs = (ntiles + 1) / 2, njobs = pairs * nheads;
+        const int64_t full = njobs / n > 1 ? njobs / n - 1 : 0;
+        for (int c = 0; c < n; ++c) load[c] = 0;
+        int32_t rank = 0;
+        int ntail = 0;
+        for (int64_t job = 0; job < njobs; ++job) {
+            const int64_t head = job / pairs, pj = job % pairs;
+            const int64_t ua = pj * nheads + head, ub = (ntiles - 1 - pj) * nheads + head;
+            for (int k = 0; k < (ua == ub ? 1 : 2); ++k) {
+                const int64_t u = k == 0 ? ua : ub;
+                local_of[u] = -1;
+                if (cost[u] == 0) continue;
+                if (job < full * n) {
+                    const int c = int(job % n);
+                    local_of[u] = c;
+                    local_rank[u] = rank++;
+                    load[c] += cost[u];
+                } else {
+                    tail[ntail++] = int32_t(u);
+                }
+            }
+        }
+        std::stable_sort(tail, tail + ntail, [&](int32_t x, int32_t y) { return cost[x] > cost[y]; });
+        for (int k = 0; k < ntail; ++k) {
+            const int u = tail[k];
+            int c = 0;
+            for (int d = 1; d < n; ++d)
+                if (load[d] < load[c]) c = d;
+            local_of[u] = c;
+            local_rank[u] = rank++;
+            load[c] += cost[u];
+        }
+        int64_t local_max = 0;
+        for (int c = 0; c < n; ++c) local_max = load[c] > local_max ? load[c] : local_max;
+        use_local = 100 * local_max <= 105 * best;
+    }
+    if (use_local)
+        for (int u = 0; u < nu; ++u) cta_of[u] = local_of[u];
+    else if (!use_ffd)
         for (int u = 0; u < nu; ++u) cta_of[u] = greedy_of[u];
     int cnt[kSchedCtas];
     for (int c = 0; c < n; ++c) cnt[c] = 0;
@@ -939,7 +988,13 @@ void plan_units(TcSched &S, const DenseArgs &a, const Geo &g, int64_t units, int
     S.off[0] = 0;
     for (int c = 0; c < n; ++c) S.off[c + 1] = uint16_t(S.off[c] + cnt[c]);
     for (int c = 0; c < n; ++c) cnt[c] = S.off[c];
-    for (int k = 0; k < nu; ++k) {  // each CTA's units longest first
+    if (use_local) {  // each CTA's units in the order they were dealt
+        std::stable_sort(order, order + nu, [&](int32_t x, int32_t y) {
+            const int32_t rx = cta_of[x] >= 0 ? local_rank[x] : INT32_MAX, ry = cta_of[y] >= 0 ? local_rank[y] : INT32_MAX;
+            return rx < ry;
+        });
+    }
+    for (int k = 0; k < nu; ++k) {  // each CTA's units longest first (head-local plan: as dealt)
         const int u = order[k];
         if (cta_of[u] >= 0) S.unit[cnt[cta_of[u]]++] = uint16_t(u);
     }
