@@ -41,8 +41,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # ------------------------------------------------------------------ workloads
 
-def workload_info(idx):
-    p = synth.workload(idx)
+def workload_info(idx, p=None):
+    """(problem, FLOPs per step, config) of workload idx; p: a shard of it (default: the workload)."""
+    p = synth.workload(idx) if p is None else p
     if isinstance(p, synth.NsaProblem):
         flops = 10.0 * p.t1 * p.n1 * p.block_count * p.block_size * p.d
         name = (f"nsa_bwd_bf16_tnd_{len(p.cu_q)}x{p.t1 // len(p.cu_q)}_n1{p.n1}_n2{p.n2}_d{p.d}"
@@ -278,8 +279,28 @@ def run_reference(args, info):
 
 # ------------------------------------------------------------ rank arithmetic
 
+def shard_seed(idx, rank):
+    """Seed of rank `rank`'s shard of workload idx: rank 0 draws exactly the single-GPU workload."""
+    return 42 + idx + 7919 * rank
+
+
+def shard_units(per_rank_seqs, kv_heads, rank):
+    """The (global sequence, kv head) units of rank `rank`'s shard.  The global problem holds
+    world * per_rank_seqs sequences; rank r owns sequences [r * per_rank_seqs, (r + 1) *
+    per_rank_seqs) with every kv head.  The units are independent (each owns its dQ / dK / dV rows),
+    so the shards need no collective on the data path."""
+    s0 = rank * per_rank_seqs
+    return [(s, g) for s in range(s0, s0 + per_rank_seqs) for g in range(kv_heads)]
+
+
+def shard_workload(idx, rank):
+    """Rank `rank`'s shard of the global problem of workload idx: the workload's sequences, drawn
+    with the rank's own seed (the sequences are the global ones [rank * b, (rank + 1) * b))."""
+    return synth.workload(idx, seed=shard_seed(idx, rank)) if rank else synth.workload(idx)
+
+
 def slowest_rank_ms(total_ms, dist=None, device="cpu"):
-    """Max over ranks of a rank's summed step time: the replicas' job ends
+    """Max over ranks of a rank's summed step time: the sharded job ends
     with its slowest rank.  dist: torch.distributed (initialised) or None."""
     if dist is None:
         return float(total_ms)
@@ -290,7 +311,8 @@ def slowest_rank_ms(total_ms, dist=None, device="cpu"):
 
 
 def job_tflops(world, flops_per_replica, ms_per_step):
-    """Whole-job throughput: every replica's FLOPs over the slowest rank's time per step."""
+    """Whole-job throughput: every rank's shard's FLOPs (equal per rank) over the slowest rank's time
+    per step."""
     return world * flops_per_replica / (ms_per_step * 1e-3) / 1e12
 
 
@@ -445,9 +467,12 @@ def run_ours(args, info):
     import torch
     import attention_backward_02_gb300 as ab
 
-    p, flops, cfg = info
     rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    # this rank's shard of the global problem (rank 0: the workload itself); equal FLOPs on every rank
+    p, flops, cfg = info if rank == 0 else workload_info(args.workload, shard_workload(args.workload, rank))
+    if rank != 0:
+        cfg = info[2]
     torch.cuda.set_device(local)
     dist = None
     if world > 1:
@@ -538,7 +563,9 @@ def run_ours(args, info):
         "config": dict(cfg, l2="flushed: 512 MB buffer written between timed steps, outside the events",
                        inputs="N(0,1) seeded; O and stats from the library forward" if not nsa else
                        "N(0,1) seeded; O and softmax stats from the library sparse forward",
-                       parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+                       parallelism=(f"data-parallel shards x{world}: global problem of {world} x the "
+                                    "workload's sequences, each rank its own (sequence, kv head) units, "
+                                    "no collective on the data path") if world > 1 else "single GPU"),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": tag, "kernel_ms": main_mean,

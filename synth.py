@@ -210,7 +210,7 @@ def nsa_problem(name, *, dtype, lens_q, lens_kv=None, n1, n2, d, block_size, blo
 # the five workloads (seed 42 + index)
 # --------------------------------------------------------------------------
 
-def workload(idx: int, **over):
+def workload(idx: int, seed=None, **over):
     """Workload idx in 0..4, with the sizes of the pages' problems:
 
     0  dense fwd+bwd, fp16, b1 h2 s128 d64, scale 1/8, non-causal
@@ -221,7 +221,7 @@ def workload(idx: int, **over):
     4  NSA selected attention, bf16, 4 x 4096 tokens, n1 16 / n2 1, d128,
        block 64 x 16, sparse mode 2
     """
-    seed = 42 + idx
+    seed = 42 + idx if seed is None else int(seed)  # another seed: another shard of the same shape
     if idx == 0:
         kw = dict(dtype=F16, b=1, h=2, h_kv=2, d=64, s_q=128, s_kv=128, scale=1 / 8, mask=0)
     elif idx == 1:

@@ -85,3 +85,42 @@ def test_cpu_sample_sizes():
                           block_size=64, block_count=2, sparse_mode=2, seed=5)
     _, flops, _, units = bench.oracle_nsa_sample(q, 30)
     assert flops == 10.0 * 60 * 4 * 2 * 64 * 128 and units == 4
+
+
+def _shard_rank(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mine = bench.shard_units(4, 12, rank)  # workload 1's shard: 4 sequences, 12 kv heads per rank
+        gathered = [None] * world
+        dist.all_gather_object(gathered, mine)
+        out[rank] = gathered
+    finally:
+        dist.destroy_process_group()
+
+
+def test_shards_cover_every_unit_once_over_two_gloo_ranks():
+    """Two gloo ranks: the union of their (sequence, kv head) units is the global problem's, with no
+    unit on two ranks (so no collective is needed: every unit owns its dQ / dK / dV rows)."""
+    world = 2
+    out = mp.Manager().dict()
+    mp.spawn(_shard_rank, args=(world, _free_port(), out), nprocs=world, join=True)
+    for rank in range(world):
+        units = [u for shard in out[rank] for u in shard]
+        assert len(units) == len(set(units)) == world * 4 * 12
+        assert set(units) == {(s, g) for s in range(world * 4) for g in range(12)}
+
+
+def test_rank0_shard_is_the_workload():
+    """Rank 0 of a sharded run holds exactly the single-GPU workload; other ranks hold the same shapes
+    with their own draws."""
+    import numpy as np
+    import synth
+    for idx in (1,):
+        w, s0, s1 = synth.workload(idx), bench.shard_workload(idx, 0), bench.shard_workload(idx, 1)
+        np.testing.assert_array_equal(w.q, s0.q)
+        assert s1.q.shape[1:] == w.q.shape[1:] and not np.array_equal(s1.q[:10], w.q[:10])
+        _, f0, _ = bench.workload_info(idx, s0)
+        _, fw, _ = bench.workload_info(idx)
+        assert f0 == fw
