@@ -418,7 +418,7 @@ attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, 
     a.dkacc = reinterpret_cast<float *>(ws + L.dkacc);
     a.dvacc = reinterpret_cast<float *>(ws + L.dvacc);
     a.dqpart = reinterpret_cast<float *>(ws + L.dqpart);
-    // the CUDA-core kernel (head groups other than 8, 16, 32) adds dK / dV atomically from many blocks
+    // the CUDA-core kernel (a head dim of 192) adds dK / dV atomically from many blocks
     if (a.deterministic && !nsa_tc_supported(a)) return ATTN_ERR_UNSUPPORTED;
     static thread_local PackedGeo pg;
     pg.nseq = desc->b;

@@ -8,10 +8,13 @@
 //
 // Block-centric: a work unit ("piece") is one (sequence, kv head, key block)
 // and up to kPieceChunks chunks of the ascending list of tokens that selected
-// the block (built by the block-list kernels).  A chunk is 128 rows: 128 / G
-// tokens x the G query heads of the kv head, which TND stores contiguously,
-// so one TMA box per token brings a token's G rows (empty slots load out of
-// bounds and arrive as zeros).  Per chunk:
+// the block (built by the block-list kernels).  A chunk is 128 rows: 128 / R
+// tokens x R rows, where a token's G query heads of the kv head (contiguous
+// in TND) fill the first G of its R = 8 ceil(G / 8) rows, so one TMA box per
+// token brings its G rows to a 1024-byte aligned start (empty slots load out
+// of bounds and arrive as zeros; the R - G padding rows, and the rows past
+// 128 / R tokens, are zeroed once and masked).  Any G from 1 to 32 runs here;
+// G = 8, 16, 32 fill every row.  Per chunk:
 //   S   = Q K_blk^T        M=128 rows  N=64 keys K=128  A=Q (K-major)   B=K (K-major)
 //   dP  = dO V_blk^T       M=128       N=64      K=128  A=dO (K-major)  B=V (K-major)
 //   P   = exp2(S scale log2 e - LSE log2 e), dS = P (dP - D)     (LSE from max/sum)
@@ -108,7 +111,20 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
     int32_t *slots = reinterpret_cast<int32_t *>(smem + Cfg::OFF_SLOT);  // [ring][slot][kSlotInts]
     const NsaArgs &a = p.a;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int G = int(a.n1 / a.n2), tpc = kRows / G;  // query heads per kv head, tokens per chunk
+    // query heads per kv head, rows per token (a multiple of 8), tokens per chunk
+    const int G = int(a.n1 / a.n2), R = (G + 7) / 8 * 8, tpc = kRows / R;
+    // rows of the Q / dO stages no box writes (padding of each token, and past tpc tokens): zero
+    // once, so the MMAs read finite values there (their P and dS are zero)
+    if (R != G || tpc * R != kRows) {
+        for (int x = threadIdx.x; x < 2 * kNst * 2 * kRows * 8; x += blockDim.x) {
+            const int chunk16 = x % 8, row = (x / 8) % kRows, cb = (x / (8 * kRows)) % 2, buf = x / (16 * kRows);
+            if (row / R < tpc && row % R < G) continue;
+            const int off = (buf < kNst ? Cfg::OFF_Q + buf * Cfg::Q_BYTES : Cfg::OFF_DO + (buf - kNst) * Cfg::Q_BYTES) +
+                            cb * kRows * 128 + row * 128 + chunk16 * 16;
+            *reinterpret_cast<uint4 *>(smem + off) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();  // the tensor cores (async proxy) read these rows
+    }
     pdl_wait();     // statistics, block lists, pieces and the zeroed accumulators are ready
     pdl_trigger();  // the finalize kernels may start launching; they wait for this grid
     const int64_t n_pieces = a.pieces[a.nrows];
@@ -208,15 +224,15 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                     if (lane == 0) {
                         mbar_arrive(&slot_full[rs]);  // the token list is written
                         q_armed = ci + 1;
-                        mbar_arrive_expect_tx(&q_full[st], 2 * Cfg::Q_BYTES);
+                        mbar_arrive_expect_tx(&q_full[st], uint32_t(tpc * G * 512));  // Q and dO, d = 128, 16-bit
                     }
                     __syncwarp();  // the expected bytes are registered before any copy lands
                     uint8_t *sQ = smem + Cfg::OFF_Q + st * Cfg::Q_BYTES, *sdO = smem + Cfg::OFF_DO + st * Cfg::Q_BYTES;
                     if (u < tpc) {
                         const int qrow = t >= 0 ? int(int64_t(t) * a.n1 + g * G) : int(a.t1 * a.n1);  // past the end: zeros
                         for (int c = 0; c < kD / 64; ++c) {
-                            tma_load_2d(sQ + c * kRows * 128 + u * G * 128, &p.tm_q, &q_full[st], c * 64, qrow);
-                            tma_load_2d(sdO + c * kRows * 128 + u * G * 128, &p.tm_do, &q_full[st], c * 64, qrow);
+                            tma_load_2d(sQ + c * kRows * 128 + u * R * 128, &p.tm_q, &q_full[st], c * 64, qrow);
+                            tma_load_2d(sdO + c * kRows * 128 + u * R * 128, &p.tm_do, &q_full[st], c * 64, qrow);
                         }
                     }
                 }
@@ -308,11 +324,12 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                 // this row's token (empty slot: -1), then its LSE and D straight from the workspace
                 if (ok && !(ok = mbar_wait(&slot_full[rs], uint32_t(ci / kSlotRing) & 1, abort)))
                     flag_abort(abort, a.status);
-                const int32_t *sl = slots + (rs * kMaxSlots + r / G) * kSlotInts;
-                const int32_t i_loc = ok ? sl[0] : -1, tok = ok ? sl[1] : -1;
+                const bool row_used = r / R < tpc && r % R < G;  // else a padding row
+                const int32_t *sl = slots + (rs * kMaxSlots + (row_used ? r / R : 0)) * kSlotInts;
+                const int32_t i_loc = ok && row_used ? sl[0] : -1, tok = ok && row_used ? sl[1] : -1;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&slot_empty[rs]);
-                const int64_t qrow = int64_t(tok) * a.n1 + g * G + r % G;
+                const int64_t qrow = int64_t(tok) * a.n1 + g * G + r % R;
                 const float lse = i_loc < 0 ? INFINITY : a.lse2[qrow];
                 const float dvv = i_loc < 0 ? 0.f : a.dvec[qrow];
                 if (ok && !(ok = mbar_wait(s_full, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
@@ -323,7 +340,9 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                     const int64_t cmax64 =
                         i_loc < 0 ? -1 : (a.sparse_mode == 2 ? int64_t(i_loc) + shift - blk * kBS : int64_t(kBS));
                     const int cmax = int(cmax64 < -1 ? -1 : (cmax64 > kBS ? kBS : cmax64));
-                    const bool any_mask = __any_sync(0xffffffffu, cmax < (half + 1) * 32 - 1);
+                    const bool any_mask = a.mask || __any_sync(0xffffffffu, cmax < (half + 1) * 32 - 1);
+                    // attenMaskOptional: this query's row of the mask, from the block's first key
+                    const uint8_t *mrow = a.mask && i_loc >= 0 ? a.mask + int64_t(i_loc) * a.mask_cols + blk * kBS : nullptr;
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc) {
                         const int col0 = half * 32 + cc * 16;
@@ -338,8 +357,8 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                             float x0 = fmaf(__uint_as_float(s[2 * e]), sc, -lse);
                             float x1 = fmaf(__uint_as_float(s[2 * e + 1]), sc, -lse);
                             if (any_mask) {
-                                x0 = c <= cmax ? x0 : -INFINITY;
-                                x1 = c + 1 <= cmax ? x1 : -INFINITY;
+                                x0 = c <= cmax && !(mrow && mrow[c]) ? x0 : -INFINITY;
+                                x1 = c + 1 <= cmax && !(mrow && mrow[c + 1]) ? x1 : -INFINITY;
                             }
                             pk[e] = p_and_ds<T>(x0, x1, __uint_as_float(dp[2 * e]) - dvv,
                                                 __uint_as_float(dp[2 * e + 1]) - dvv, &dk[e]);
@@ -436,7 +455,7 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                         if (issuer) {
                             if (ok && t >= 0) {
                                 const int box = hr * 2 + bx;
-                                const uint8_t *src = sDQS + bx * (kRows * 128) + lane * G * 128;
+                                const uint8_t *src = sDQS + bx * (kRows * 128) + lane * R * 128;
                                 if (a.deterministic) {  // its own partial rows, written once (summed in slot order later)
                                     const int prow = int(((int64_t(t) * a.n2 + g) * a.cnt + slot) * G);
                                     tma_store_2d(&p.tm_dqpart, src, box * 32, prow);
@@ -544,7 +563,7 @@ __global__ void __launch_bounds__(1024) nsa_piece_scan_kernel(NsaArgs a)
 bool nsa_tc_supported(const NsaArgs &a)
 {
     const int64_t G = a.n1 / a.n2;
-    return a.d == kD && a.dv == kD && a.bs == kBS && (G == 8 || G == 16 || G == 32) && !a.mask;
+    return a.d == kD && a.dv == kD && a.bs == kBS && G >= 1 && G <= 32;
 }
 
 cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
@@ -553,7 +572,7 @@ cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
     prm.a = a;
     const int G = int(a.n1 / a.n2);
     // deterministic: a whole block list per work unit, so every dK / dV element has one writer
-    prm.a.piece_tokens = a.deterministic ? (int64_t(1) << 30) : int64_t(kPieceChunks) * (kRows / G);
+    prm.a.piece_tokens = a.deterministic ? (int64_t(1) << 30) : int64_t(kPieceChunks) * (kRows / ((G + 7) / 8 * 8));
     cudaError_t e = launch_kernel(nsa_piece_scan_kernel, dim3(1), dim3(1024), 0, s, true, prm.a);
     if (e != cudaSuccess) return e;
     if (a.t1 == 0) return cudaSuccess;

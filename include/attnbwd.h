@@ -191,7 +191,8 @@ typedef struct {
     int64_t block_count;    /* selectedBlockCount in [1, 128], count*size < 8192 */
     int sparse_mode;        /* 0: only the selection; 2: also causal,
                                bottom-right aligned per sequence              */
-    int deterministic;      /* 1: bitwise reproducible dQ                     */
+    int deterministic;      /* 1: bitwise reproducible dQ, dK, dV; needs
+                               d = d_v = 128 (ATTN_ERR_UNSUPPORTED otherwise) */
     int64_t d_v;            /* head dim of v, O, dO and dv: 128 or 192; 0 means
                                d ([Ascend] Constraints: D is 192 or 128, and K
                                and V may differ)                              */
@@ -204,8 +205,7 @@ typedef struct {
      * nonzero removes key j for query i (positions local to the sequence),
      * on top of the selection and the sparse mode; it must cover every
      * sequence (mask_rows >= its query length, mask_cols >= its key length).
-     * NULL: no mask.  Masked calls run on the CUDA-core kernels (no
-     * deterministic mode there).                                             */
+     * NULL: no mask.                                                       */
     const uint8_t *atten_mask;
     int64_t mask_rows, mask_cols;
 } attn_nsa_desc_t;

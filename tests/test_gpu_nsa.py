@@ -129,23 +129,24 @@ def test_deterministic_bad_indices_flagged():
     _parity(p, deterministic=True)
 
 
-def test_deterministic_unsupported_group():
-    """Head groups the tensor-core kernel does not take run on CUDA cores,
-    which add dK / dV atomically: deterministic mode is refused there."""
-    import attention_backward_02_gb300 as ab
-    p = _small(0, seed=12, n1=8, n2=2)
+@pytest.mark.parametrize("n1,n2", [(8, 2), (3, 1), (12, 1), (20, 2)])
+def test_deterministic_padded_groups(n1, n2):
+    """Deterministic mode for head groups G = 4, 3, 12, 10 (rows padded to a multiple of 8 per token in
+    the tensor-core kernel): oracle parity and the same bits from two calls."""
+    p = _small(0, seed=12 + n1, n1=n1, n2=n2)
+    first = _parity(p, deterministic=True)
     o_bits, mx, sm = H.nsa_oracle_inputs(p)
-    with pytest.raises(ab.AttnError) as e:
-        H.run_gpu_nsa(p, o_bits, mx, sm, deterministic=True)
-    assert e.value.status == ab._lib.ATTN_ERR_UNSUPPORTED
-    _parity(p)  # the non-deterministic CUDA-core path still serves this shape
+    second = H.run_gpu_nsa(p, o_bits, mx, sm, deterministic=True)
+    for x, y in zip(first, second):
+        np.testing.assert_array_equal(x, y)
 
 
-@pytest.mark.parametrize("n1,n2", [(4, 1), (2, 2), (4, 2), (6, 3)])
+@pytest.mark.parametrize("n1,n2", [(4, 1), (2, 2), (4, 2), (6, 3), (1, 1), (3, 1), (5, 1), (7, 1), (12, 1),
+                                   (20, 1), (24, 1), (27, 1), (30, 3)])
 @pytest.mark.parametrize("sparse_mode", [0, 2])
-def test_cuda_core_kernel_groups(n1, n2, sparse_mode):
-    """Head groups G = n1 / n2 of 4, 1, 2 and 2 run on the CUDA-core kernel (the tensor-core one takes
-    G in {8, 16, 32}); both sparse modes."""
+def test_padded_head_groups(n1, n2, sparse_mode):
+    """Head groups G = n1 / n2 that do not fill a 128-row chunk in whole tokens of G rows (1 to 30):
+    each token's rows are padded to a multiple of 8 in the tensor-core kernel; both sparse modes."""
     _parity(_small(sparse_mode, seed=31 + n1 + n2 + sparse_mode, n1=n1, n2=n2))
 
 

@@ -75,10 +75,8 @@ def _bwd_parity(p, grad_fp32=False, deterministic=False):
 @pytest.mark.parametrize("n1,n2", [(16, 2), (4, 1)])
 @pytest.mark.parametrize("deterministic", [False, True])
 def test_nsa_backward_fp32_gradients(n1, n2, deterministic):
-    """fp32 dq / dk / dv: the tensor-core path (16 / 2 heads) and the CUDA-core path (4 / 1)."""
+    """fp32 dq / dk / dv on the tensor-core kernel: a full head group (16 / 2) and a padded one (4 / 1)."""
     p = _problem(2, n1=n1, n2=n2, seed=60 + n1)
-    if deterministic and n1 // n2 not in (8, 16, 32):
-        pytest.skip("deterministic mode runs on the tensor-core head groups only")
     dq, dk, dv = _bwd_parity(p, grad_fp32=True, deterministic=deterministic)
     assert dq.dtype == np.float64  # fp32 values widened by the harness
 
@@ -127,14 +125,16 @@ def test_nsa_forward_with_mask(sparse_mode, n1, n2):
 
 
 @pytest.mark.parametrize("sparse_mode", [0, 2])
-@pytest.mark.parametrize("n1,n2,d,d_v", [(16, 2, 128, 128), (4, 1, 128, 128), (8, 2, 192, 128)])
-def test_nsa_backward_with_mask(sparse_mode, n1, n2, d, d_v):
-    """A mask routes the call to the CUDA-core kernel whatever the head group (16 / 2 would otherwise
-    run on the tensor-core kernel)."""
+@pytest.mark.parametrize("n1,n2,d,d_v,deterministic", [(16, 2, 128, 128, False), (4, 1, 128, 128, False),
+                                                       (16, 2, 128, 128, True), (5, 1, 128, 128, True),
+                                                       (8, 2, 192, 128, False)])
+def test_nsa_backward_with_mask(sparse_mode, n1, n2, d, d_v, deterministic):
+    """The mask per element: on the tensor-core kernel (d = d_v = 128, both dQ modes, head groups of
+    8, 4 and 5) and on the CUDA-core kernel (d = 192)."""
     p = _problem(sparse_mode, n1=n1, n2=n2, d=d, d_v=d_v, seed=92 + n1 + d + sparse_mode)
     mask = _mask(300, 512, 93 + n1 + sparse_mode)
     o_bits, mx, sm = H.nsa_oracle_inputs(p, mask=mask)
-    dq, dk, dv = H.run_gpu_nsa(p, o_bits, mx, sm, mask=mask)
+    dq, dk, dv = H.run_gpu_nsa(p, o_bits, mx, sm, mask=mask, deterministic=deterministic)
     rq, rk, rv = oracle.nsa_bwd(p.f64("q"), p.f64("k"), p.f64("v"), synth.bits_to_f64(o_bits, p.dtype),
                                 p.f64("do"), mx.astype(np.float64), sm.astype(np.float64), p.topk, p.cu_q,
                                 p.cu_kv, p.scale, p.block_size, p.sparse_mode, mask=mask)
