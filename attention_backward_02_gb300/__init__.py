@@ -11,8 +11,8 @@ from __future__ import annotations
 import ctypes as C
 
 from . import _lib
-from ._lib import (ATTN_BF16, ATTN_CAUSAL_BOTTOM_RIGHT, ATTN_CAUSAL_TOP_LEFT, ATTN_F16, ATTN_MASK_NONE,
-                   AttnError, attn_nsa_desc_t, attn_sdpa_desc_t, attn_view_t, check)
+from ._lib import (ATTN_BF16, ATTN_CAUSAL_BOTTOM_RIGHT, ATTN_CAUSAL_TOP_LEFT, ATTN_DQ_ATOMIC, ATTN_DQ_ORDERED,
+                   ATTN_DQ_SPLIT, ATTN_F16, ATTN_MASK_NONE, AttnError, attn_nsa_desc_t, attn_sdpa_desc_t, attn_view_t, check)
 
 __all__ = ["sdpa_desc", "nsa_desc", "view_bhsd", "view_tnd", "sdpa_workspace_size", "sdpa_fwd_stats",
            "sdpa_bwd", "nsa_workspace_size", "nsa_selected_attn_bwd", "nsa_block_lists",
@@ -61,12 +61,14 @@ def sdpa_desc(*, dtype, b, h, h_kv, s_q, s_kv, d, scale, mask=ATTN_MASK_NONE, cu
     """An attn_sdpa_desc_t.  Fixed-length mode: b sequences of s_q queries and s_kv keys.  Packed
     (varlen) mode: cu_seqlens_q / cu_seqlens_kv, b inclusive cumulative lengths each (s_q, s_kv then
     ignored).  scale multiplies q.k; mask is ATTN_MASK_NONE, ATTN_CAUSAL_TOP_LEFT or
-    ATTN_CAUSAL_BOTTOM_RIGHT; deterministic with dq_splits partial buffers (0: a default) makes dQ
-    bitwise reproducible.  The host arrays live as long as the descriptor."""
+    ATTN_CAUSAL_BOTTOM_RIGHT.  deterministic: False / ATTN_DQ_ATOMIC, True / ATTN_DQ_SPLIT (dq_splits
+    partial buffers, 0: a default) or ATTN_DQ_ORDERED (one buffer, adds in a fixed order); the last two
+    make dQ bitwise reproducible.  The host arrays live as long as the descriptor."""
     keep = _keep if _keep is not None else _Keep()
+    mode = int(deterministic) if not isinstance(deterministic, bool) else int(deterministic)
     desc = attn_sdpa_desc_t(int(dtype), int(b), int(h), int(h_kv), int(s_q), int(s_kv), int(d), float(scale),
                             int(mask), _cu_array(keep, cu_seqlens_q), _cu_array(keep, cu_seqlens_kv),
-                            int(bool(deterministic)), int(dq_splits))
+                            mode, int(dq_splits))
     desc._keep = keep
     return desc
 

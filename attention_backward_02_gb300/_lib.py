@@ -18,6 +18,7 @@ ATTN_ERR_WORKSPACE, ATTN_ERR_ALIGN, ATTN_ERR_CUDA, ATTN_ERR_DEVICE = 4, 5, 6, 7
 ATTN_DEV_TIMEOUT, ATTN_DEV_INDEX_RANGE, ATTN_DEV_INDEX_DUP = 0x1, 0x2, 0x4
 ATTN_F16, ATTN_BF16 = 0, 1
 ATTN_MASK_NONE, ATTN_CAUSAL_TOP_LEFT, ATTN_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
+ATTN_DQ_ATOMIC, ATTN_DQ_SPLIT, ATTN_DQ_ORDERED = 0, 1, 2
 
 # every exported symbol of include/attnbwd.h
 EXPORTS = ("sdpa_workspace_size", "sdpa_fwd_stats", "sdpa_bwd", "nsa_workspace_size",

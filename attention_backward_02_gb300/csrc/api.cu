@@ -48,7 +48,7 @@ attn_status_t check_dense_desc(const attn_sdpa_desc_t *d, DenseShape *sh)
     if (d->mask != ATTN_MASK_NONE && d->mask != ATTN_CAUSAL_TOP_LEFT && d->mask != ATTN_CAUSAL_BOTTOM_RIGHT)
         return ATTN_ERR_INVALID;
     if ((d->cu_seqlens_q == nullptr) != (d->cu_seqlens_kv == nullptr)) return ATTN_ERR_NULLPTR;
-    if (d->deterministic != 0 && d->deterministic != 1) return ATTN_ERR_INVALID;
+    if (d->deterministic < 0 || d->deterministic > 2) return ATTN_ERR_INVALID;
     if (d->dq_splits < 0) return ATTN_ERR_INVALID;
     sh->packed = d->cu_seqlens_q != nullptr;
     sh->nseq = d->b;
@@ -73,12 +73,12 @@ attn_status_t check_dense_desc(const attn_sdpa_desc_t *d, DenseShape *sh)
 
 int dense_parts(const attn_sdpa_desc_t *d)
 {
-    if (!d->deterministic) return 1;
+    if (d->deterministic != 1) return 1;
     return d->dq_splits > 0 ? d->dq_splits : kDefaultDqSplits;
 }
 
 struct DenseLayout {
-    size_t status, lse2, dvec, dqacc, total;
+    size_t status, lse2, dvec, dqacc, sem, total;
     int64_t t_pad;
 };
 
@@ -100,7 +100,9 @@ DenseLayout dense_layout(const attn_sdpa_desc_t *d, const DenseShape &sh)
     L.lse2 = Workspace::align(64 * sizeof(uint32_t));
     L.dvec = L.lse2 + Workspace::align(rows * sizeof(float));
     L.dqacc = L.dvec + Workspace::align(rows * sizeof(float));
-    L.total = L.dqacc + Workspace::align(size_t(dense_parts(d)) * rows * size_t(d->d) * sizeof(float));
+    L.sem = L.dqacc + Workspace::align(size_t(dense_parts(d)) * rows * size_t(d->d) * sizeof(float));
+    // ordered dQ mode: one add counter per (head, 64 workspace rows)
+    L.total = L.sem + (d->deterministic == 2 ? Workspace::align(rows / 64 * sizeof(uint32_t)) : 0);
     return L;
 }
 
@@ -239,6 +241,17 @@ attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t 
     DenseLayout L = dense_layout(desc, sh);
     // 32-bit row coordinates of the fp32 dQ accumulator inside the kernels
     if (int64_t(dense_parts(desc)) * desc->h * L.t_pad >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
+    if (desc->deterministic == 2) {  // ordered dQ: every work unit is planned on the host
+        int64_t max_kv = desc->s_kv;
+        if (sh.packed) {
+            max_kv = 0;
+            for (int64_t b = 0; b < desc->b; ++b) {
+                const int64_t l = desc->cu_seqlens_kv[b] - (b ? desc->cu_seqlens_kv[b - 1] : 0);
+                max_kv = l > max_kv ? l : max_kv;
+            }
+        }
+        if ((max_kv + 127) / 128 * desc->b * desc->h_kv > kOrderedMaxUnits) return ATTN_ERR_UNSUPPORTED;
+    }
     if ((st = check_ws(workspace, workspace_bytes, L.total))) return st;
 
     DenseArgs a;
@@ -248,7 +261,8 @@ attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t 
     a.t_q = sh.t_q; a.t_kv = sh.t_kv; a.t_pad = L.t_pad;
     a.scale = float(desc->scale);
     a.mask = desc->mask;
-    a.deterministic = desc->deterministic;
+    a.deterministic = desc->deterministic == 1;
+    a.ordered = desc->deterministic == 2;
     a.n_part = dense_parts(desc);
     a.packed = sh.packed;
     a.q = to_view(q, sh.packed); a.k = to_view(k, sh.packed); a.v = to_view(v, sh.packed);
@@ -260,6 +274,8 @@ attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t 
     a.lse2 = reinterpret_cast<float *>(ws + L.lse2);
     a.dvec = reinterpret_cast<float *>(ws + L.dvec);
     a.dqacc = reinterpret_cast<float *>(ws + L.dqacc);
+    a.sem = reinterpret_cast<uint32_t *>(ws + L.sem);
+    a.sem_stride = L.t_pad / 64;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (sh.t_q == 0 && sh.t_kv == 0) return ATTN_OK;
 

@@ -19,11 +19,13 @@
 //   dQ^T = K^T dS^T (D=128) M=D=128     N=BM=64 K=128 A=K^T (MN-major)     B=dS^T (MN-major)
 // dV, dK stay in TMEM for the whole key tile and are written once; each dQ
 // tile is read out of TMEM, staged in shared memory half a tile at a time and
-// added into the fp32 accumulator with a TMA reduce-add.  With a single
-// accumulator, each CTA counts itself in a global word once its adds have
-// landed, and when all have, every CTA converts a share of the accumulator
-// into dQ (no separate finalize kernel).  TMEM: S^T BM + dP^T BM + P^T BM/2 +
-// dV D + dK D + dQ 64 columns (512 at D = 64, 480 at D = 128).
+// added into the fp32 accumulator with a TMA reduce-add; a kernel chained
+// behind this one converts the accumulator into dQ.  Bitwise reproducible dQ
+// either way: split (n_part partial buffers, each with one chain of key tiles
+// adding in a fixed order) or ordered (one buffer; the adds into a query tile
+// go in decreasing key-tile order, each waiting on a per-tile counter in the
+// workspace).  TMEM: S^T BM + dP^T BM + P^T BM/2 + dV D + dK D + dQ 64 columns
+// (512 at D = 64, 480 at D = 128).
 //
 // Pipeline.  The MMA warp issues S/dP of query tile i and then dV/dK/dQ of
 // tile i-1, so the tensor cores run tile i-1's three GEMMs while the softmax
@@ -53,7 +55,10 @@
 
 #include <algorithm>
 #include <climits>
+#include <queue>
 #include <type_traits>
+#include <utility>
+#include <vector>
 
 #include "plan.h"
 #include "sm103.cuh"
@@ -157,7 +162,9 @@ template <> struct IsPacked<PackedGeo> : std::true_type {};
 
 }  // namespace
 
-template <class T, int D, class Geo>
+// kOrdered: ordered dQ mode (one accumulator, each query tile's adds in a fixed order; needs the planned
+// unit order and a cooperative launch).  A template parameter, so the other modes carry none of its code.
+template <class T, int D, class Geo, bool kOrdered>
 __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(const __grid_constant__ TcParams p, const Geo geo)
 {
     using Cfg = TcCfg<D>;
@@ -597,7 +604,8 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
         T *dK = static_cast<T *>(a.dK.ptr), *dV = static_cast<T *>(a.dV.ptr);
         bool ok = true;
         uint32_t qi = 0;
-        pdl_wait();  // the dQ accumulator (and the done count) have been zeroed
+        uint32_t *pend = nullptr;  // ordered dQ mode: counter of the tile whose adds are still to be counted
+        pdl_wait();  // the dQ accumulator (and the ordered mode's counters) have been zeroed
 
         ATTN_FOR_EACH_UNIT
         for (int64_t jt = first_tile; jt < ntiles; jt += tile_step) {
@@ -712,6 +720,8 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                 }
                 // dQ of tile qi, half of its columns at a time, through the staging buffer
                 const int64_t row0 = part * a.h * a.t_pad + geo.ws_start(b) + hq * a.t_pad + i0;
+                // ordered dQ mode: this query tile's add counter
+                auto sem_of = [&]() { return a.sem + hq * a.sem_stride + (geo.ws_start(b) + i0) / 64; };
                 // read the whole accumulator first, so the next tile's dQ GEMM is not held up by the
                 // reduce (whose rate the L2 sets)
                 uint32_t v[2][32];
@@ -744,6 +754,22 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                     }
                     fence_proxy_async_smem();
                     ok = bar_and(2, 128, ok);
+                    if (kOrdered && leader && ok && hb == 0) {
+                        // the key tiles with work for this query tile are 0 .. J (whether a key tile has
+                        // work for it does not increase with the key tile: J by bisection) and they add
+                        // in the order J, J - 1, .., 0, so this add waits until J - jt adds have landed
+                        const int qtile = int(i0 / BM);
+                        int64_t lo = jt, hi = ntiles - 1;
+                        while (lo < hi) {
+                            const int64_t mid = (lo + hi + 1) / 2;
+                            int q0, n;
+                            query_tiles<BM>(a.mask, mid * BN, lq, lkv, &q0, &n);
+                            if (n > 0 && q0 <= qtile) lo = mid;
+                            else hi = mid - 1;
+                        }
+                        if (!(ok = wait_count(sem_of(), uint32_t(lo - jt), abort))) flag_abort(abort, a.status);
+                        fence_proxy_async_global();
+                    }
                     if (leader && ok) {
                         if (D == 64)
                             tma_reduce_add_2d(&p.tm_dq, sDQS, hb * 32, int(row0));
@@ -751,6 +777,24 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                             for (int box = 0; box < 4; ++box)
                                 tma_reduce_add_2d(&p.tm_dq, sDQS + box * 32 * 128, box * 32, int(row0 + hb * 32));
                         bulk_commit();
+                    }
+                    if (kOrdered && leader && ok && hb == 1) {
+                        // count the previous tile's adds once they have landed (this tile's two groups may
+                        // still be in flight); the key tile's last tile is counted at once, so a unit
+                        // leaves nothing pending behind it
+                        if (pend) {
+                            bulk_wait2();
+                            fence_proxy_async_global();
+                            red_release_gpu_add(pend, 1u);
+                            pend = nullptr;
+                        }
+                        if (it == n_iter - 1) {
+                            bulk_wait0();
+                            fence_proxy_async_global();
+                            red_release_gpu_add(sem_of(), 1u);
+                        } else {
+                            pend = sem_of();
+                        }
                     }
                 }
             }
@@ -836,6 +880,62 @@ template <class Geo> int64_t max_kv_len(const Geo &g)
     return m;
 }
 
+// Ordered dQ mode: the adds into each query tile's dQ go in decreasing key-tile order, each one
+// waiting until the adds of all higher key tiles have landed.  Units are dealt in decreasing key-tile
+// order (longest first among equal ones) to the least loaded CTA, and every CTA takes its units in
+// the order dealt, so the key tiles a CTA works on never increase.  A wait then depends only on
+// units of higher key tiles, which their CTAs take before any lower one; with every CTA resident
+// (cooperative launch) no cycle of waits can form.  Leaves on = 0 when the units do not fit (the API
+// refuses such problems).
+template <int BM, int BN, class Geo>
+void plan_ordered(TcSched &S, const DenseArgs &a, const Geo &g, int64_t units, int64_t ctas)
+{
+    S.on = 0;
+    if (units > kSchedUnits || ctas > kSchedCtas || ctas < 1) return;
+    const int64_t nheads = a.nseq * a.h_kv, G = a.h / a.h_kv;
+    const int n = int(ctas), nu = int(units);
+    static thread_local int32_t cost[kSchedUnits], order[kSchedUnits], cta_of[kSchedUnits];
+    for (int u = 0; u < nu; ++u) {
+        const int64_t jt = u / nheads, b = (u % nheads) / a.h_kv;
+        const int64_t lq = g.q_len(b), lkv = g.kv_len(b);
+        int64_t nq = 0;
+        if (jt * BN < lkv) {
+            const int64_t i_lo = first_query_seeing(a.mask, jt * BN, lq, lkv);
+            nq = lq <= 0 || i_lo >= lq ? 0 : (lq + BM - 1) / BM - i_lo / BM;
+        }
+        cost[u] = jt * BN >= lkv ? 0 : nq > 0 ? int32_t(2 * G * nq + 2) : 1;
+        order[u] = u;
+    }
+    std::stable_sort(order, order + nu, [&](int32_t x, int32_t y) {
+        const int64_t jx = x / nheads, jy = y / nheads;
+        return jx != jy ? jx > jy : cost[x] > cost[y];
+    });
+    // least loaded CTA first (lowest index among equals): a min-heap of (load, cta)
+    std::priority_queue<std::pair<int64_t, int>, std::vector<std::pair<int64_t, int>>,
+                        std::greater<std::pair<int64_t, int>>> heap;
+    for (int c = 0; c < n; ++c) heap.push({0, c});
+    int cnt[kSchedCtas];
+    for (int c = 0; c < n; ++c) cnt[c] = 0;
+    for (int k = 0; k < nu; ++k) {
+        const int u = order[k];
+        cta_of[u] = -1;
+        if (cost[u] == 0) continue;  // past the sequence's keys: nothing to do
+        const auto top = heap.top();
+        heap.pop();
+        cta_of[u] = top.second;
+        ++cnt[top.second];
+        heap.push({top.first + cost[u], top.second});
+    }
+    S.off[0] = 0;
+    for (int c = 0; c < n; ++c) S.off[c + 1] = uint16_t(S.off[c] + cnt[c]);
+    for (int c = 0; c < n; ++c) cnt[c] = S.off[c];
+    for (int k = 0; k < nu; ++k) {
+        const int u = order[k];
+        if (cta_of[u] >= 0) S.unit[cnt[cta_of[u]]++] = uint16_t(u);
+    }
+    S.on = 1;
+}
+
 // Assigns the work units of a fixed-length batch to `ctas` CTAs.  A unit's cost is its query tiles
 // plus one for its start (loading K / V, the pipeline refill, the dK / dV epilogue), in half tiles;
 // units without work cost one (they write zero dK / dV rows).  Two plans: greedy (each unit,
@@ -852,6 +952,10 @@ template <int BM, int BN, class Geo>
 void plan_units(TcSched &S, const DenseArgs &a, const Geo &g, int64_t units, int64_t ctas)
 {
     S.on = 0;
+    if (a.ordered) {
+        plan_ordered<BM, BN>(S, a, g, units, ctas);
+        return;
+    }
     if (IsPacked<Geo>::value || a.deterministic || units > kSchedUnits || ctas > kSchedCtas || ctas < 1) return;
     struct Key {
         int64_t nseq, h, h_kv, s_q, s_kv, units, ctas;
@@ -1025,14 +1129,17 @@ template <class T, int D, class Geo> cudaError_t run_tc(const DenseArgs &a, cons
     if (!map_dqacc(&prm.tm_dq, a.dqacc, D, int64_t(a.n_part) * a.h * a.t_pad, Cfg::DQ_BOX_ROWS))
         return cudaErrorInvalidValue;
     if (sq == 0) prm.tm_q = prm.tm_do = prm.tm_k;  // never read: no query tiles
-    auto k = dense_bwd_tc_kernel<T, D, Geo>;
+    auto k = a.ordered ? dense_bwd_tc_kernel<T, D, Geo, true> : dense_bwd_tc_kernel<T, D, Geo, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     prm.a.tc_units = (a.deterministic ? a.n_part : ntiles) * a.nseq * a.h_kv;
     if (prm.a.tc_units > INT32_MAX) return cudaErrorInvalidValue;  // the kernel splits units in 32 bits
     const int64_t units = prm.a.tc_units < sm_count() ? prm.a.tc_units : sm_count();
     plan_units<Cfg::BM, Cfg::BN>(prm.sched, prm.a, g, prm.a.tc_units, units);
-    return launch_kernel(k, dim3(unsigned(units)), dim3(Cfg::THREADS), Cfg::SMEM_ALLOC, s, true, prm, g);
+    if (a.ordered && !prm.sched.on) return cudaErrorNotSupported;  // the waits need the planned order
+    // ordered dQ mode waits across CTAs: a cooperative launch puts all of them on the GPU at once
+    return launch_kernel_ex(k, dim3(unsigned(units)), dim3(Cfg::THREADS), Cfg::SMEM_ALLOC, s, true, a.ordered != 0,
+                            prm, g);
 }
 
 template <class Geo> cudaError_t dispatch(const DenseArgs &a, const Geo &g, cudaStream_t s)

@@ -140,22 +140,38 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // in pdl_wait until this grid has completed).
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Launches k on stream s, optionally with programmatic stream serialization.
+// Launches k on stream s, optionally with programmatic stream serialization
+// and optionally as a cooperative launch (all blocks resident at once, or
+// the launch fails).
 template <class... KArgs, class... Args>
-inline cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                                 Args &&...args)
+inline cudaError_t launch_kernel_ex(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                                    bool coop, Args &&...args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n++].val.programmaticStreamSerializationAllowed = 1;
+    }
+    if (coop) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n++].val.cooperative = 1;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, k, static_cast<Args &&>(args)...);
+}
+
+template <class... KArgs, class... Args>
+inline cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                                 Args &&...args)
+{
+    return launch_kernel_ex(k, grid, block, smem, s, pdl, false, static_cast<Args &&>(args)...);
 }
 
 // ----------------------------------------------------------- status word

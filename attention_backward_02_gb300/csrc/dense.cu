@@ -40,7 +40,8 @@ constexpr int kUnitRows = int(kWsRowAlign) / 4;
 // it is located once.  d/8 threads per row (8 elements each),
 // 256-thread blocks striding over the units in one resident wave.  Covers
 // every workspace row: padding rows get LSE2 = +inf (so P = 0) and D = 0.
-// Then zeroes every partial dQ buffer.  Launched normally (it overwrites what
+// Then zeroes every partial dQ buffer (and, in ordered dQ mode, the per-tile
+// add counters).  Launched normally (it overwrites what
 // the previous call's last kernel reads); lets the main kernel launch behind it.
 template <class T, class Geo, int D>
 __global__ void __launch_bounds__(256) dense_preprocess_kernel(DenseArgs a, Geo geo)
@@ -96,6 +97,9 @@ __global__ void __launch_bounds__(256) dense_preprocess_kernel(DenseArgs a, Geo 
     float4 *acc = reinterpret_cast<float4 *>(a.dqacc);
     const int64_t n4 = int64_t(a.n_part) * a.h * a.t_pad * D / 4;
     for (int64_t k = int64_t(blockIdx.x) * 256 + threadIdx.x; k < n4; k += int64_t(gridDim.x) * 256) acc[k] = z;
+    if (a.ordered)  // no query tile has received an add yet
+        for (int64_t k = int64_t(blockIdx.x) * 256 + threadIdx.x; k < a.h * a.sem_stride; k += int64_t(gridDim.x) * 256)
+            a.sem[k] = 0u;
 }
 
 // ------------------------------------------------------------ dq finalize

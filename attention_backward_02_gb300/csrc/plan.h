@@ -23,6 +23,7 @@ struct View {
 //   lse2     f32 [h][t_pad]          LSE * log2(e); +inf on padding rows
 //   dvec     f32 [h][t_pad]          D = rowsum(dO * O); 0 on padding rows
 //   dqacc    f32 [n_part][h][t_pad][d]
+//   sem      u32 [h][t_pad / 64]     ordered dQ mode: adds done per query tile
 // t_pad = sum over sequences of their query length rounded up to 128
 // (Geo::ws_start / ws_rows); the row of (head hq, sequence b, position i) is
 // hq * t_pad + ws_start(b) + i.
@@ -33,6 +34,9 @@ struct DenseArgs {
     float scale;
     int mask;
     int deterministic, n_part;  // n_part partial dQ buffers (1 unless deterministic)
+    int ordered;                // one dQ buffer, each query tile's adds in a fixed order (sem)
+    uint32_t *sem;              // ordered: adds done per (head, 64-row workspace tile)
+    int64_t sem_stride;         // sem words per head (t_pad / 64)
     bool packed;
     View q, k, v, o, dO, dQ, dK, dV;
     const float *lse;           // caller's stats ([B][h][s_q] or [h][T_q])
@@ -41,6 +45,9 @@ struct DenseArgs {
     float *lse2, *dvec, *dqacc;
     int64_t tc_units;           // main kernel: work units (set by its launcher)
 };
+
+// Ordered dQ mode: the host plans every work unit (key tile of a sequence and kv head) up front.
+constexpr int64_t kOrderedMaxUnits = 4096;
 
 struct Workspace {
     static constexpr size_t kAlign = 256;

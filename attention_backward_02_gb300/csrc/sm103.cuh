@@ -136,6 +136,26 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
     return v;
 }
 
+// Adds v with release semantics at GPU scope (publishes this thread's earlier writes).
+__device__ __forceinline__ void red_release_gpu_add(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until *p == want (acquire).  Gives up after `limit_ns` or once *abort is non-zero.
+__device__ __forceinline__ bool wait_count(const uint32_t *p, uint32_t want, volatile int *abort,
+                                           uint64_t limit_ns = 1000000000ull)
+{
+    if (ld_acquire_gpu(p) == want) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(p) == want) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -218,6 +238,8 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 // all but this thread's most recent bulk group have read their shared-memory source
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Waits until at most two bulk groups of this thread are pending (the older ones have completed).
+__device__ __forceinline__ void bulk_wait2() { asm volatile("cp.async.bulk.wait_group 2;" ::: "memory"); }
 
 // Brings a tile of a 4-D tensor into L2 ahead of its load (no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3)

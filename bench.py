@@ -603,8 +603,9 @@ def extra_workloads(args, flush, stream, lib, peak, steps=10, warmup=3):
     main kernel (mean ms over `steps` flushed steps) and their fractions of the tensor peak."""
     import torch
     out = {}
-    for idx, det in ((2, False), (2, True), (3, False), (4, False), (4, True)):
-        if idx == args.workload and not det:
+    # dQ modes: False atomic, True split partial buffers (NSA: per-slot partials), 2 ordered single buffer
+    for idx, det in ((2, False), (2, True), (2, 2), (3, False), (3, 2), (4, False), (4, True)):
+        if idx == args.workload and det is False:
             continue
         p, flops, cfg = workload_info(idx)
         prob = Problem(p, det)
@@ -614,7 +615,8 @@ def extra_workloads(args, flush, stream, lib, peak, steps=10, warmup=3):
         call_ms, main_ms = time_calls(prob, steps, flush, stream, lib)
         ok = prob.status() == 0
         call, main = statistics.mean(call_ms), statistics.mean(main_ms)
-        entry = {"workload": cfg["workload"], "deterministic": det, "call_ms": call, "main_kernel_ms": main,
+        mode = {False: "atomic", True: "split", 2: "ordered"}[det]
+        entry = {"workload": cfg["workload"], "dq_mode": mode, "call_ms": call, "main_kernel_ms": main,
                  "tflops": flops / (call * 1e-3) / 1e12, "main_kernel_tflops": flops / (main * 1e-3) / 1e12,
                  "whole_call_frac": flops / (call * 1e-3) / 1e12 / peak,
                  "main_kernel_frac": flops / (main * 1e-3) / 1e12 / peak, "steps": steps, "device_status_clean": ok}
@@ -623,7 +625,7 @@ def extra_workloads(args, flush, stream, lib, peak, steps=10, warmup=3):
             entry["useful_flops"] = uf
             entry["slot_flops"] = flops
             entry["main_kernel_useful_frac"] = uf / (main * 1e-3) / 1e12 / peak
-        out[f"w{idx}{'_det' if det else ''}"] = entry
+        out[f"w{idx}" + {"atomic": "", "split": "_det", "ordered": "_ordered"}[mode]] = entry
         del prob
         torch.cuda.empty_cache()
     return out

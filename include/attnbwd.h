@@ -106,13 +106,22 @@ typedef struct {
      * Both NULL: fixed-length mode.                                          */
     const int64_t *cu_seqlens_q;
     const int64_t *cu_seqlens_kv;
-    /* sdpa_bwd only.  0: dQ accumulated with fp32 reductions whose order
-     * varies from run to run.  1: bitwise reproducible dQ: each of dq_splits
-     * partial fp32 buffers has one writer that adds in a fixed order, and the
-     * buffers are summed in index order (0 picks a default).                */
+    /* sdpa_bwd only: an attn_dq_mode_t.  ATTN_DQ_ATOMIC: dQ accumulated with
+     * fp32 reductions whose order varies from run to run.  ATTN_DQ_SPLIT:
+     * bitwise reproducible dQ; each of dq_splits partial fp32 buffers (0: a
+     * default) has one writer that adds in a fixed order, and the buffers are
+     * summed in index order.  ATTN_DQ_ORDERED: bitwise reproducible dQ with
+     * one fp32 buffer; the key tiles of each query tile add in decreasing
+     * order, each waiting for a per-tile counter in the workspace (bounded
+     * wait: ATTN_DEV_TIMEOUT), under a cooperative launch (every block of the
+     * kernel resident at once); problems of more than 4096 work units (key
+     * tiles of 128 rows x sequences x kv heads) return ATTN_ERR_UNSUPPORTED.
+     * [Ascend] "Constraints": deterministic computation is opt-in.          */
     int deterministic;
     int dq_splits;
 } attn_sdpa_desc_t;
+
+typedef enum { ATTN_DQ_ATOMIC = 0, ATTN_DQ_SPLIT = 1, ATTN_DQ_ORDERED = 2 } attn_dq_mode_t;
 
 /* Workspace bytes for sdpa_fwd_stats and for sdpa_bwd with this descriptor.
  * Either output pointer may be NULL.  Host only; no CUDA call.

@@ -54,9 +54,25 @@ def test_workspace_size(ab):
     assert st == 0 and det >= nbytes + 3 * 12 * t_pad * 64 * 4
 
 
+def test_workspace_size_ordered(ab):
+    """Ordered dQ mode: one accumulator plus one 32-bit counter per (head, 64 workspace rows)."""
+    _, atomic = _status(ab, _desc(ab))
+    st, ordered = _status(ab, _desc(ab, deterministic=ab.ATTN_DQ_ORDERED))
+    assert st == 0 and ordered == atomic + 12 * (4 * 1024 // 64) * 4
+
+
+def test_ordered_mode_unit_budget(ab):
+    """Ordered dQ mode plans every work unit on the host: more than 4096 (key tiles of 128 x sequences
+    x kv heads) is refused before any launch."""
+    d = _desc(ab, b=64, h=32, h_kv=32, s_q=4096, s_kv=4096, d=128, deterministic=ab.ATTN_DQ_ORDERED)
+    assert _bwd_call(ab, d) == 3
+    assert _bwd_call(ab, _desc(ab, deterministic=ab.ATTN_DQ_ORDERED), ws=0) == 4  # within budget: next check
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(dtype=7), 2), (dict(h=12, h_kv=5), 2), (dict(b=0), 2), (dict(d=96), 3), (dict(d=256), 3),
     (dict(mask=5), 2), (dict(scale=float("nan")), 2), (dict(s_q=-1), 2), (dict(dq_splits=-2), 2),
+    (dict(deterministic=3), 2), (dict(deterministic=-1), 2),
 ])
 def test_descriptor_rejections(ab, kw, code):
     assert _status(ab, _desc(ab, **kw))[0] == code

@@ -122,6 +122,40 @@ def test_deterministic_mode_bitwise_d64(dq_splits):
     _parity(p, deterministic=True, dq_splits=dq_splits)
 
 
+ORDERED = 2  # ATTN_DQ_ORDERED
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mask", [NONE, TL, BR])
+def test_ordered_mode_bitwise(d, mask):
+    """Ordered dQ mode (one fp32 buffer; each query tile's key tiles add in decreasing order behind a
+    per-tile counter): oracle parity and the same bits from two calls, with s_q != s_kv, ragged
+    tails, grouped-query heads and each mask."""
+    p = synth.dense_problem("ord", dtype=BF16 if d == 128 else F16, b=2, h=4, h_kv=2, d=d, s_q=530, s_kv=700,
+                            mask=mask, scale=1 / np.sqrt(d), seed=40 + d + mask)
+    o_bits, lse = H.oracle_forward(p)
+    a = H.run_gpu_bwd(p, o_bits, lse, deterministic=ORDERED)
+    b = H.run_gpu_bwd(p, o_bits, lse, deterministic=ORDERED)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    _parity(p, deterministic=ORDERED)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_ordered_mode_varlen_gqa(d):
+    """Ordered dQ mode with packed sequences of unequal lengths (one empty, one without keys),
+    grouped-query heads, causal bottom-right."""
+    lq = np.array([1, 200, 0, 129, 300, 77]); lkv = np.array([5, 150, 0, 0, 610, 400])
+    p = synth.dense_problem("ord_varlen", dtype=BF16, b=len(lq), h=8, h_kv=2, d=d, lens_q=lq, lens_kv=lkv,
+                            mask=BR, seed=50 + d)
+    o_bits, lse = H.oracle_forward(p)
+    a = H.run_gpu_bwd(p, o_bits, lse, deterministic=ORDERED)
+    b = H.run_gpu_bwd(p, o_bits, lse, deterministic=ORDERED)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    _parity(p, deterministic=ORDERED)
+
+
 @pytest.mark.parametrize("dtype", [F16, BF16])
 def test_varlen_gqa_d64(dtype):
     """d = 64 with packed sequences and grouped-query heads (8 query heads on 2 kv heads), unequal
@@ -132,9 +166,10 @@ def test_varlen_gqa_d64(dtype):
     _parity(p)
 
 
-def test_workload1_full():
-    """fp16 b4 h12 s1024 d64 causal, BSHD viewed as BHSD: every output element."""
-    _parity(synth.workload(1))
+@pytest.mark.parametrize("deterministic", [False, 2])
+def test_workload1_full(deterministic):
+    """fp16 b4 h12 s1024 d64 causal, BSHD viewed as BHSD: every output element (atomic and ordered dQ)."""
+    _parity(synth.workload(1), deterministic=deterministic)
 
 
 _ORACLE_CACHE = {}
@@ -173,14 +208,29 @@ def _full_parity(idx, deterministic=False):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("deterministic", [False, True, ORDERED])
 def test_workload2_full(deterministic):
-    """bf16 b2 h32 s4096 d128 causal: every output element, both dQ modes."""
+    """bf16 b2 h32 s4096 d128 causal: every output element, all three dQ modes."""
     _full_parity(2, deterministic)
 
 
 @pytest.mark.slow
-def test_workload3_full():
+@pytest.mark.parametrize("deterministic", [False, ORDERED])
+def test_workload3_full(deterministic):
     """varlen GQA bf16, h 32 / h_kv 8, d128, 8 lengths in [256, 4096], causal bottom-right: every
-    output element."""
-    _full_parity(3)
+    output element (atomic and ordered dQ)."""
+    _full_parity(3, deterministic)
+
+
+@pytest.mark.parametrize("idx", [1, 2])
+def test_ordered_mode_workload_bitwise(idx):
+    """Ordered dQ mode at the full workloads 1 and 2: two calls give the same bits."""
+    if idx == 2:
+        p, o_bits, lse, _ = _oracle_full(2)
+    else:
+        p = synth.workload(1)
+        o_bits, lse = H.oracle_forward(p)
+    a = H.run_gpu_bwd(p, o_bits, lse, ORDERED)
+    b = H.run_gpu_bwd(p, o_bits, lse, ORDERED)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)

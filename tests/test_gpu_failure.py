@@ -38,11 +38,12 @@ def test_wait_timeout_sets_flag_and_context_survives():
     assert np.all(np.isfinite(dq))
 
 
-def test_backward_while_other_work_holds_some_sms():
-    """The main kernel's blocks wait for one another before converting dQ.  While another stream's
-    kernel holds 8 SMs (and their shared memory) for 1.5 s, longer than that wait's one-second limit,
-    the backward must still complete correctly: its launch is cooperative, so its blocks run only
-    once they can all be resident, and none waits for a block that has not started."""
+@pytest.mark.parametrize("mode", [0, 2])
+def test_backward_while_other_work_holds_some_sms(mode):
+    """While another stream's kernel holds 8 SMs (and their shared memory) for 1.5 s, longer than any
+    wait's one-second limit, the backward must still complete correctly.  Atomic dQ mode: no block
+    waits for another.  Ordered dQ mode: blocks wait for other blocks' adds, so the launch is
+    cooperative and its blocks run only once they can all be resident."""
     import torch
     import attention_backward_02_gb300 as ab
     lib = ab._lib.load()
@@ -55,7 +56,7 @@ def test_backward_while_other_work_holds_some_sms():
     torch.cuda.synchronize()
     ab.check(lib.attn_selftest_occupy(8, 120 * 1024, C.c_double(1.5), C.c_void_p(other.cuda_stream)),
              "attn_selftest_occupy")
-    dq, dk, dv = H.run_gpu_bwd(p, o_bits, lse)  # asserts a clean device status (no timeout)
+    dq, dk, dv = H.run_gpu_bwd(p, o_bits, lse, deterministic=mode)  # asserts a clean device status
     torch.cuda.synchronize()
     for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         H.assert_close(g, r, name)
