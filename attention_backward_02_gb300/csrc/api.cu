@@ -159,7 +159,15 @@ attn_status_t cuda_status(cudaError_t e)
 
 thread_local cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
 
-cudaError_t mark(cudaEvent_t ev, cudaStream_t s) { return ev ? cudaEventRecord(ev, s) : cudaSuccess; }
+// Records a timing event; under stream capture as an external event node, so replays record it.
+cudaError_t mark(cudaEvent_t ev, cudaStream_t s)
+{
+    if (!ev) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return e;
+    return cudaEventRecordWithFlags(ev, s, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0);
+}
 
 }  // namespace
 
