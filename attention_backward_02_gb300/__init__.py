@@ -189,7 +189,8 @@ def nsa_fwd_workspace_size(desc):
 def nsa_selected_attn_fwd(desc, q, k, v, topk, o, softmax_max, softmax_sum, *, workspace=None, stream=None):
     """NSA selected-attention forward on contiguous TND CUDA tensors: q [T1, n1, d], k [T2, n2, d],
     v [T2, n2, d_v], topk [T1, n2, block_count] int32 -> o [T1, n1, d_v] (input dtype), softmax_max /
-    softmax_sum [T1, n1, 8] fp32.  Asynchronous on `stream`; returns the workspace (status word)."""
+    softmax_sum [T1, n1, 8] fp32.  Asynchronous on `stream`; returns the workspace (its first word is the
+    device status)."""
     ws = _workspace(nsa_fwd_workspace_size(desc), q.device, workspace)
     fp = lambda t: C.cast(C.c_void_p(t.data_ptr()), C.POINTER(C.c_float))
     st = _lib.load().nsa_selected_attn_fwd(

@@ -383,6 +383,42 @@ NsaLayout nsa_layout(const attn_nsa_desc_t *d, const NsaShape &sh)
     return L;
 }
 
+// The forward runs on the tensor cores for d = d_v = 128 and blocks of 64 (the backward's block lists,
+// its lse2 / dvec rows for the row maxima and sums and its dQ accumulator for O); otherwise on CUDA
+// cores, which need the status word alone.
+bool nsa_fwd_on_tc(const attn_nsa_desc_t *d, const NsaShape &sh)
+{
+    return d->d == 128 && sh.dv == 128 && d->block_size == 64;
+}
+
+NsaLayout nsa_fwd_layout(const attn_nsa_desc_t *d, const NsaShape &sh)
+{
+    attn_nsa_desc_t c = *d;
+    c.deterministic = 0;  // no per-slot partials in the forward
+    return nsa_layout(&c, sh);
+}
+
+size_t nsa_fwd_bytes(const attn_nsa_desc_t *d, const NsaShape &sh)
+{
+    return nsa_fwd_on_tc(d, sh) ? nsa_fwd_layout(d, sh).total : Workspace::align(64 * sizeof(uint32_t));
+}
+
+void nsa_ws_pointers(NsaArgs *a, const NsaLayout &L, void *workspace)
+{
+    char *ws = static_cast<char *>(workspace);
+    a->status = reinterpret_cast<uint32_t *>(ws + L.status);
+    a->lse2 = reinterpret_cast<float *>(ws + L.lse2);
+    a->dvec = reinterpret_cast<float *>(ws + L.dvec);
+    a->bitmap = reinterpret_cast<uint32_t *>(ws + L.bitmap);
+    a->offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    a->tokens = reinterpret_cast<int32_t *>(ws + L.tokens);
+    a->pieces = reinterpret_cast<int32_t *>(ws + L.pieces);
+    a->dqacc = reinterpret_cast<float *>(ws + L.dqacc);
+    a->dkacc = reinterpret_cast<float *>(ws + L.dkacc);
+    a->dvacc = reinterpret_cast<float *>(ws + L.dvacc);
+    a->dqpart = reinterpret_cast<float *>(ws + L.dqpart);
+}
+
 }  // namespace
 
 attn_status_t nsa_workspace_size(const attn_nsa_desc_t *desc, size_t *bytes)
@@ -460,7 +496,7 @@ attn_status_t nsa_fwd_workspace_size(const attn_nsa_desc_t *desc, size_t *bytes)
     attn_status_t st = check_nsa_desc(desc, &sh);
     if (st) return st;
     if (!bytes) return ATTN_ERR_NULLPTR;
-    *bytes = Workspace::align(64 * sizeof(uint32_t));
+    *bytes = nsa_fwd_bytes(desc, sh);
     return ATTN_OK;
 }
 
@@ -478,10 +514,18 @@ attn_status_t nsa_selected_attn_fwd(const attn_nsa_desc_t *desc, const void *q, 
     if ((topk && (reinterpret_cast<uintptr_t>(topk) & 3)) || (softmax_max && !aligned16(softmax_max)) ||
         (softmax_sum && !aligned16(softmax_sum)))
         return ATTN_ERR_ALIGN;
-    if ((st = check_ws(workspace, workspace_bytes, Workspace::align(64 * sizeof(uint32_t))))) return st;
+    if ((st = check_ws(workspace, workspace_bytes, nsa_fwd_bytes(desc, sh)))) return st;
     if (sh.t1 == 0) return ATTN_OK;
     NsaArgs a;
     std::memset(&a, 0, sizeof a);
+    if (nsa_fwd_on_tc(desc, sh)) {
+        const NsaLayout L = nsa_fwd_layout(desc, sh);
+        a.t1_pad = L.t1_pad;
+        a.nblk_max = sh.nblk_max; a.words_max = sh.words_max; a.nrows = L.nrows;
+        nsa_ws_pointers(&a, L, workspace);
+    } else {
+        a.status = static_cast<uint32_t *>(workspace);
+    }
     a.dtype = desc->dtype;
     a.nseq = desc->b; a.n1 = desc->n1; a.n2 = desc->n2; a.d = desc->d; a.dv = sh.dv;
     a.bs = desc->block_size; a.cnt = desc->block_count;
@@ -491,7 +535,6 @@ attn_status_t nsa_selected_attn_fwd(const attn_nsa_desc_t *desc, const void *q, 
     a.sparse_mode = desc->sparse_mode;
     a.q = q; a.k = k; a.v = v; a.topk = topk;
     a.o_out = o; a.smax_out = softmax_max; a.ssum_out = softmax_sum;
-    a.status = static_cast<uint32_t *>(workspace);
     static thread_local PackedGeo pg;
     pg.nseq = desc->b;
     pg.cu_q[0] = pg.cu_kv[0] = 0;

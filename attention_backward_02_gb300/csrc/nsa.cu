@@ -637,6 +637,46 @@ cudaError_t run_nsa(const NsaArgs &a0, const PackedGeo &g, cudaStream_t s, cudaE
     return cudaSuccess;
 }
 
+// ------------------------------------------------- forward on the tensor cores
+// Before the two passes: every row's maximum at -inf (as the order-preserving
+// int of the atomicMax), its sum and the fp32 O accumulator at 0.
+__global__ void __launch_bounds__(256) nsa_fwd_init_kernel(NsaArgs a)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int64_t nthr = int64_t(gridDim.x) * blockDim.x, tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int32_t neg_inf = int32_t(0x807FFFFF);  // -inf (0xFF800000) with its magnitude bits flipped
+    for (int64_t r = tid; r < a.t1 * a.n1; r += nthr) {
+        reinterpret_cast<int32_t *>(a.lse2)[r] = neg_inf;
+        a.dvec[r] = 0.f;
+    }
+    zero_words(reinterpret_cast<uint32_t *>(a.dqacc), a.t1 * a.n1 * a.dv, tid, nthr);
+}
+
+// After them: O = O_acc / sum (0 where the row sees no key), softmaxMax = the maximum in natural units
+// (-inf where none), softmaxSum = the sum, the stats in all 8 lanes.  A warp per (token, query head) row.
+template <class T>
+__global__ void __launch_bounds__(256) nsa_fwd_finalize_kernel(NsaArgs a)
+{
+    pdl_wait();
+    const int lane = threadIdx.x % 32;
+    for (int64_t w = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) / 32; w < a.t1 * a.n1;
+         w += int64_t(gridDim.x) * blockDim.x / 32) {
+        const float sum = a.dvec[w], inv = sum > 0.f ? 1.f / sum : 0.f;
+        for (int64_t x = lane * 4; x < a.dv; x += 128) {
+            const float4 v = *reinterpret_cast<const float4 *>(a.dqacc + w * a.dv + x);
+            T *o = static_cast<T *>(a.o_out) + w * a.dv + x;
+            *reinterpret_cast<uint2 *>(o) = make_uint2(pack2<T>(v.x * inv, v.y * inv), pack2<T>(v.z * inv, v.w * inv));
+        }
+        if (lane < 8) {
+            const int32_t mi = reinterpret_cast<const int32_t *>(a.lse2)[w];
+            const float m = __int_as_float(mi >= 0 ? mi : mi ^ 0x7FFFFFFF);
+            a.smax_out[w * 8 + lane] = m == -INFINITY ? -INFINITY : m / kLog2e;
+            a.ssum_out[w * 8 + lane] = sum;
+        }
+    }
+}
+
 template <class T, int DQK, int DV> cudaError_t run_nsa_fwd_t(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
 {
     auto k = nsa_fwd_simt_kernel<T, DQK, DV>;
@@ -649,8 +689,22 @@ template <class T, int DQK, int DV> cudaError_t run_nsa_fwd_t(const NsaArgs &a, 
     return cudaGetLastError();
 }
 
-template <class T> cudaError_t run_nsa_fwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
+template <class T> cudaError_t run_nsa_fwd(const NsaArgs &a0, const PackedGeo &g, cudaStream_t s)
 {
+    if (nsa_tc_supported(a0)) {  // tensor cores: block lists, init, row maxima, sums and O, finalize
+        NsaArgs a = a0;
+        a.zero_dq = 0;
+        cudaError_t e;
+        const int64_t words = a.nrows * a.words_max;
+        const unsigned blocks = unsigned(words > 0 ? (words / 4 + 255) / 256 < 1024 ? (words / 4 + 255) / 256 : 1024 : 1);
+        nsa_init_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = block_lists<T>(a, g, s, true, false)) != cudaSuccess) return e;
+        if ((e = launch_kernel(nsa_fwd_init_kernel, dim3(1024), dim3(256), 0, s, true, a)) != cudaSuccess) return e;
+        if ((e = launch_nsa_tc(a, g, s, true)) != cudaSuccess) return e;
+        return launch_kernel(nsa_fwd_finalize_kernel<T>, dim3(1024), dim3(256), 0, s, true, a);
+    }
+    const NsaArgs &a = a0;
     if (a.d == 128 && a.dv == 128) return run_nsa_fwd_t<T, 128, 128>(a, g, s);
     if (a.d == 192 && a.dv == 128) return run_nsa_fwd_t<T, 192, 128>(a, g, s);
     if (a.d == 128 && a.dv == 192) return run_nsa_fwd_t<T, 128, 192>(a, g, s);

@@ -29,6 +29,15 @@
 // ring in shared memory with its own barriers.
 // TMEM: S 64 + dP 64 + dV^T 64 + dK^T 64 + dQ 128 = 384 columns.
 //
+// The same kernel runs the NSA forward (the Function / Formula's attention over
+// the gathered blocks) in two passes over the same work units, since a
+// token's softmax spans blocks that different CTAs hold: kFwdMax computes S
+// and each row's maximum over the block (atomicMax into the workspace);
+// kFwdSum computes P = exp2(S scale log2 e - max), adds each row's sum of P
+// into the workspace (atomicAdd) and O += P V_blk (M=128 rows, N=128, K=64,
+// A=P K-major, B=V MN-major) through the dQ path's TMA reduce-adds; a finalize
+// divides O by the sum.
+//
 // Roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer, warps 2..9
 // element-wise work (warp w reads TMEM lanes 32 (w % 4) .. + 31; two warps
 // per lane group split the columns) and the piece's dK / dV, warps 10..13 the
@@ -50,6 +59,15 @@ using namespace tc;
 namespace {
 
 constexpr int kD = 128, kBS = 64, kRows = 128, kNst = 2, kMaxSlots = 16, kSlotInts = 4, kSlotRing = 4;
+enum : int { kBwd = 0, kFwdMax = 1, kFwdSum = 2 };  // what a launch of the kernel computes
+
+// Order-preserving map of a float onto int32 (an involution), for atomicMax on floats.
+__device__ __forceinline__ int32_t ord_f32(float x)
+{
+    const int32_t b = __float_as_int(x);
+    return b >= 0 ? b : b ^ 0x7FFFFFFF;
+}
+__device__ __forceinline__ float unord_f32(int32_t v) { return __int_as_float(v >= 0 ? v : v ^ 0x7FFFFFFF); }
 constexpr int kPieceChunks = 32;  // chunks per work unit at most
 
 struct NsaCfg {
@@ -94,8 +112,8 @@ __device__ __forceinline__ int64_t piece_row(const int32_t *piece_off, int64_t n
     return lo;
 }
 
-template <class T>
-__global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constant__ NsaTcParams p, const PackedGeo geo)
+template <class T, int kMode>
+__global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ NsaTcParams p, const PackedGeo geo)
 {
     using Cfg = NsaCfg;
     constexpr int kType = std::is_same<T, __half>::value ? 0 : 1;
@@ -183,10 +201,10 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                 if (ok && lane == 0) {
                     kv_armed = kt + 1;
                     const int krow = int(geo.cu_kv[b] + blk * kBS);
-                    mbar_arrive_expect_tx(kv_full, 2 * Cfg::KV_BYTES);
+                    mbar_arrive_expect_tx(kv_full, (kMode == kFwdMax ? 1 : 2) * Cfg::KV_BYTES);
                     for (int c = 0; c < kD / 64; ++c) {
                         tma_load_3d(sK + c * kBS * 128, &p.tm_k, kv_full, c * 64, int(g), krow);
-                        tma_load_3d(sV + c * kBS * 128, &p.tm_v, kv_full, c * 64, int(g), krow);
+                        if (kMode != kFwdMax) tma_load_3d(sV + c * kBS * 128, &p.tm_v, kv_full, c * 64, int(g), krow);
                     }
                 }
                 // lane u's token of the next chunk, loaded one chunk ahead
@@ -224,7 +242,8 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                     if (lane == 0) {
                         mbar_arrive(&slot_full[rs]);  // the token list is written
                         q_armed = ci + 1;
-                        mbar_arrive_expect_tx(&q_full[st], uint32_t(tpc * G * 512));  // Q and dO, d = 128, 16-bit
+                        // Q (and dO in the backward): d = 128, 16-bit
+                        mbar_arrive_expect_tx(&q_full[st], uint32_t(tpc * G * (kMode == kBwd ? 512 : 256)));
                     }
                     __syncwarp();  // the expected bytes are registered before any copy lands
                     uint8_t *sQ = smem + Cfg::OFF_Q + st * Cfg::Q_BYTES, *sdO = smem + Cfg::OFF_DO + st * Cfg::Q_BYTES;
@@ -232,7 +251,8 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                         const int qrow = t >= 0 ? int(int64_t(t) * a.n1 + g * G) : int(a.t1 * a.n1);  // past the end: zeros
                         for (int c = 0; c < kD / 64; ++c) {
                             tma_load_2d(sQ + c * kRows * 128 + u * R * 128, &p.tm_q, &q_full[st], c * 64, qrow);
-                            tma_load_2d(sdO + c * kRows * 128 + u * R * 128, &p.tm_do, &q_full[st], c * 64, qrow);
+                            if (kMode == kBwd)
+                                tma_load_2d(sdO + c * kRows * 128 + u * R * 128, &p.tm_do, &q_full[st], c * 64, qrow);
                         }
                     }
                 }
@@ -256,6 +276,7 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
             const uint64_t mK = desc_mn(smem_u32(sK), kBS, 0);
             const uint64_t mP = desc_mn(smem_u32(sP), kRows, 0), mdS = desc_mn(smem_u32(sdS), kRows, 0);
             const uint64_t kdS = desc_kmaj(smem_u32(sdS), kRows, 0);
+            const uint64_t kP = desc_kmaj(smem_u32(sP), kRows, 0), mV = desc_mn(smem_u32(sV), kBS, 0);
             bool ok = true;
             int64_t kt = 0, ci = 0;
             for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
@@ -274,14 +295,23 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
 #pragma unroll
                         for (int kk = 0; kk < kD / 16; ++kk)
                             mma_f16_ss(tmem + Cfg::T_S, kmaj_step(kQ, kRows, kk), kmaj_step(kK, kBS, kk), idS, kk > 0);
+                        if (kMode == kBwd)
 #pragma unroll
-                        for (int kk = 0; kk < kD / 16; ++kk)
-                            mma_f16_ss(tmem + Cfg::T_DP, kmaj_step(kdO, kRows, kk), kmaj_step(kV, kBS, kk), idS, kk > 0);
+                            for (int kk = 0; kk < kD / 16; ++kk)
+                                mma_f16_ss(tmem + Cfg::T_DP, kmaj_step(kdO, kRows, kk), kmaj_step(kV, kBS, kk), idS,
+                                           kk > 0);
                         mma_commit(s_full);
                     }
                     if (ok && !(ok = mbar_wait(p_ready, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
                     tc_fence_after();
-                    if (ok) {
+                    if (kMode == kFwdMax) {  // the row maxima are all this pass needs
+                        if (ok) {
+                            mma_commit(&q_empty[st]);
+                            if (ch == nchunks - 1) mma_commit(kv_empty);
+                        }
+                        continue;
+                    }
+                    if (kMode == kBwd && ok) {
 #pragma unroll
                         for (int kk = 0; kk < kRows / 16; ++kk)
                             mma_f16_ss(tmem + Cfg::T_DV, mn_step(mdO, kk), mn_step(mP, kk), idT, ch > 0 || kk > 0);
@@ -292,10 +322,14 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                     // the dQ warps have read the previous chunk's dQ
                     if (ci > 0 && ok && !(ok = mbar_wait(dq_free, uint32_t(ci - 1) & 1, abort))) flag_abort(abort, a.status);
                     tc_fence_after();
-                    if (ok) {
+                    if (ok) {  // backward: dQ = dS K; forward: O = P V
 #pragma unroll
-                        for (int kk = 0; kk < kBS / 16; ++kk)
-                            mma_f16_ss(tmem + Cfg::T_DQ, kmaj_step(kdS, kRows, kk), mn_step(mK, kk), idQ, kk > 0);
+                        for (int kk = 0; kk < kBS / 16; ++kk) {
+                            if (kMode == kBwd)
+                                mma_f16_ss(tmem + Cfg::T_DQ, kmaj_step(kdS, kRows, kk), mn_step(mK, kk), idQ, kk > 0);
+                            else
+                                mma_f16_ss(tmem + Cfg::T_DQ, kmaj_step(kP, kRows, kk), mn_step(mV, kk), idQ, kk > 0);
+                        }
                         mma_commit(mma_done);
                         mma_commit(&q_empty[st]);  // this Q / dO stage may be refilled
                         if (ch == nchunks - 1) mma_commit(kv_empty);
@@ -330,8 +364,17 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&slot_empty[rs]);
                 const int64_t qrow = int64_t(tok) * a.n1 + g * G + r % R;
-                const float lse = i_loc < 0 ? INFINITY : a.lse2[qrow];
-                const float dvv = i_loc < 0 ? 0.f : a.dvec[qrow];
+                // backward: LSE (log2 units); forward sum pass: the row's maximum over all its blocks
+                // (+inf where there is none, so every P is 0)
+                float lse = INFINITY, dvv = 0.f;
+                if (kMode == kBwd && i_loc >= 0) {
+                    lse = a.lse2[qrow];
+                    dvv = a.dvec[qrow];
+                } else if (kMode == kFwdSum && i_loc >= 0) {
+                    const float m = unord_f32(reinterpret_cast<const int32_t *>(a.lse2)[qrow]);
+                    lse = m == -INFINITY ? INFINITY : m;
+                }
+                float rmax = -INFINITY, rsum = 0.f;  // forward: this thread's part of the row
                 if (ok && !(ok = mbar_wait(s_full, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
@@ -346,6 +389,35 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc) {
                         const int col0 = half * 32 + cc * 16;
+                        if (kMode != kBwd) {  // forward passes: S only
+                            uint32_t s[16];
+                            tmem_ld16(tmem + lane_addr + Cfg::T_S + col0, s);
+                            tmem_ld_wait_regs(s);
+                            uint32_t pk[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int c = col0 + 2 * e;
+                                float x0 = __uint_as_float(s[2 * e]) * sc, x1 = __uint_as_float(s[2 * e + 1]) * sc;
+                                if (any_mask) {
+                                    x0 = c <= cmax && !(mrow && mrow[c]) ? x0 : -INFINITY;
+                                    x1 = c + 1 <= cmax && !(mrow && mrow[c + 1]) ? x1 : -INFINITY;
+                                }
+                                if (kMode == kFwdMax) {
+                                    rmax = fmaxf(rmax, fmaxf(x0, x1));
+                                } else {
+                                    const float p0 = ex2(x0 - lse), p1 = ex2(x1 - lse);
+                                    rsum += p0 + p1;
+                                    pk[e] = pack2<T>(p0, p1);
+                                }
+                            }
+                            if (kMode == kFwdSum)
+#pragma unroll
+                                for (int q = 0; q < 2; ++q) {
+                                    const uint32_t off = sw128_offset(uint32_t(r), uint32_t(col0 + 8 * q), kRows);
+                                    st_shared_v4(aP + off, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                                }
+                            continue;
+                        }
                         uint32_t s[16], dp[16];
                         tmem_ld16(tmem + lane_addr + Cfg::T_S + col0, s);
                         tmem_ld16(tmem + lane_addr + Cfg::T_DP + col0, dp);
@@ -371,13 +443,21 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                         }
                     }
                 }
+                // forward: fold this half row into the row's maximum / sum over all blocks
+                if (kMode == kFwdMax && i_loc >= 0 && rmax != -INFINITY)
+                    atomicMax(reinterpret_cast<int32_t *>(a.lse2) + qrow, ord_f32(rmax));
+                if (kMode == kFwdSum && i_loc >= 0 && rsum > 0.f) atomicAdd(a.dvec + qrow, rsum);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_ready);
             }
             // ---- dV^T, dK^T of this piece (this thread: head dim r, 32 of the 64 keys), once its
-            // last chunk's GEMMs have completed
+            // last chunk's GEMMs have completed (backward only)
+            if (kMode != kBwd) {
+                ++kt;
+                continue;
+            }
             if (ok && !(ok = mbar_wait(mma_done, uint32_t(ci - 1) & 1, abort))) flag_abort(abort, a.status);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
@@ -421,6 +501,7 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&slot_empty[rs]);
+                if (kMode == kFwdMax) continue;  // no GEMM output to add in this pass
                 if (ok && !(ok = mbar_wait(mma_done, uint32_t(ci) & 1, abort))) flag_abort(abort, a.status);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
@@ -456,7 +537,7 @@ __global__ void __launch_bounds__(448, 1) nsa_bwd_tc_kernel(const __grid_constan
                             if (ok && t >= 0) {
                                 const int box = hr * 2 + bx;
                                 const uint8_t *src = sDQS + bx * (kRows * 128) + lane * R * 128;
-                                if (a.deterministic) {  // its own partial rows, written once (summed in slot order later)
+                                if (kMode == kBwd && a.deterministic) {  // own partial rows (summed in slot order later)
                                     const int prow = int(((int64_t(t) * a.n2 + g) * a.cnt + slot) * G);
                                     tma_store_2d(&p.tm_dqpart, src, box * 32, prow);
                                 } else {
@@ -566,13 +647,14 @@ bool nsa_tc_supported(const NsaArgs &a)
     return a.d == kD && a.dv == kD && a.bs == kBS && G >= 1 && G <= 32;
 }
 
-cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
+cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, bool forward)
 {
     NsaTcParams prm;
     prm.a = a;
     const int G = int(a.n1 / a.n2);
     // deterministic: a whole block list per work unit, so every dK / dV element has one writer
-    prm.a.piece_tokens = a.deterministic ? (int64_t(1) << 30) : int64_t(kPieceChunks) * (kRows / ((G + 7) / 8 * 8));
+    const bool whole = a.deterministic && !forward;
+    prm.a.piece_tokens = whole ? (int64_t(1) << 30) : int64_t(kPieceChunks) * (kRows / ((G + 7) / 8 * 8));
     cudaError_t e = launch_kernel(nsa_piece_scan_kernel, dim3(1), dim3(1024), 0, s, true, prm.a);
     if (e != cudaSuccess) return e;
     if (a.t1 == 0) return cudaSuccess;
@@ -581,7 +663,8 @@ cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
         cuuint64_t dims[2] = {cuuint64_t(kD), cuuint64_t(a.t1 * a.n1)};
         cuuint64_t strides[1] = {cuuint64_t(kD * 2)};
         cuuint32_t box[2] = {64, cuuint32_t(G)};
-        if (!encode(&prm.tm_q, dt, 2, a.q, dims, strides, box) || !encode(&prm.tm_do, dt, 2, a.dO, dims, strides, box))
+        if (!encode(&prm.tm_q, dt, 2, a.q, dims, strides, box) ||
+            !encode(&prm.tm_do, dt, 2, forward ? a.q : a.dO, dims, strides, box))  // the forward reads no dO
             return cudaErrorInvalidValue;
     }
     {   // K, V: (d, kv head, token); box 64 x 1 x block
@@ -598,16 +681,27 @@ cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s)
         if (!encode(&prm.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dqacc, dims, strides, box))
             return cudaErrorInvalidValue;
         prm.tm_dqpart = prm.tm_dq;
-        if (a.deterministic) {  // fp32 partials: rows (token, kv head, slot, head of group) x d
+        if (whole) {  // fp32 partials: rows (token, kv head, slot, head of group) x d
             cuuint64_t pdims[2] = {cuuint64_t(kD), cuuint64_t(a.t1 * a.n1 * a.cnt)};
             if (!encode(&prm.tm_dqpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dqpart, pdims, strides, box))
                 return cudaErrorInvalidValue;
         }
     }
-    auto k = a.dtype == ATTN_F16 ? nsa_bwd_tc_kernel<__half> : nsa_bwd_tc_kernel<__nv_bfloat16>;
-    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, NsaCfg::SMEM_ALLOC)) != cudaSuccess)
+    const dim3 grid = dim3(unsigned(nsa_sm_count()));
+    if (!forward) {
+        auto k = a.dtype == ATTN_F16 ? nsa_tc_kernel<__half, kBwd> : nsa_tc_kernel<__nv_bfloat16, kBwd>;
+        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, NsaCfg::SMEM_ALLOC)) != cudaSuccess)
+            return e;
+        return launch_kernel(k, grid, dim3(NsaCfg::THREADS), NsaCfg::SMEM_ALLOC, s, true, prm, g);
+    }
+    // forward: the row maxima, then the sums and O, over the same work units
+    auto k1 = a.dtype == ATTN_F16 ? nsa_tc_kernel<__half, kFwdMax> : nsa_tc_kernel<__nv_bfloat16, kFwdMax>;
+    auto k2 = a.dtype == ATTN_F16 ? nsa_tc_kernel<__half, kFwdSum> : nsa_tc_kernel<__nv_bfloat16, kFwdSum>;
+    if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, NsaCfg::SMEM_ALLOC)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, NsaCfg::SMEM_ALLOC)) != cudaSuccess)
         return e;
-    return launch_kernel(k, dim3(unsigned(nsa_sm_count())), dim3(NsaCfg::THREADS), NsaCfg::SMEM_ALLOC, s, true, prm, g);
+    if ((e = launch_kernel(k1, grid, dim3(NsaCfg::THREADS), NsaCfg::SMEM_ALLOC, s, true, prm, g)) != cudaSuccess) return e;
+    return launch_kernel(k2, grid, dim3(NsaCfg::THREADS), NsaCfg::SMEM_ALLOC, s, true, prm, g);
 }
 
 }  // namespace attn

@@ -110,7 +110,8 @@ cudaError_t launch_nsa_bwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s,
                            cudaEvent_t after);
 cudaError_t launch_nsa_block_lists(const NsaArgs &a, const PackedGeo &g, cudaStream_t s);
 bool nsa_tc_supported(const NsaArgs &a);
-cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s);
+// forward: the two forward passes (row maxima; sums and O into a.lse2 / a.dvec / a.dqacc)
+cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, bool forward = false);
 // NSA forward: a.o, a.smax, a.ssum are written (o is the output here).
 cudaError_t launch_nsa_fwd(const NsaArgs &a, const PackedGeo &g, cudaStream_t s);
 

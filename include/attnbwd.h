@@ -230,7 +230,9 @@ typedef struct {
  * sees no key has O = 0, softmax_max = -inf, softmax_sum = 0.
  *   q : [T1][n1][d]  k : [T2][n2][d]  v : [T2][n2][d_v]  o : [T1][n1][d_v]
  *   topk : as for the backward; invalid indices are skipped and flagged.
- * The workspace holds the device status word: nsa_fwd_workspace_size bytes. */
+ * Workspace: nsa_fwd_workspace_size bytes (d = d_v = 128 with blocks of 64
+ * runs on the tensor cores and needs the backward's block lists and fp32
+ * row / O accumulators; other shapes need the device status word alone). */
 attn_status_t nsa_fwd_workspace_size(const attn_nsa_desc_t *desc, size_t *bytes);
 attn_status_t nsa_selected_attn_fwd(const attn_nsa_desc_t *desc, const void *q, const void *k, const void *v,
                                     const int32_t *topk, void *o, float *softmax_max, float *softmax_sum,

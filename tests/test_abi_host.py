@@ -126,6 +126,17 @@ def test_nsa_descriptor_rejections(ab, kw, code):
     assert ab._lib.load().nsa_workspace_size(C.byref(_nsa(ab, **kw)), C.byref(n)) == code
 
 
+def test_nsa_fwd_workspace_size(ab):
+    """The tensor-core forward (d = d_v = 128, blocks of 64) uses the backward's workspace layout without
+    deterministic partials; the CUDA-core forward (a head dim of 192) the status word alone."""
+    lib = ab._lib.load()
+    fwd, bwd = C.c_size_t(), C.c_size_t()
+    assert lib.nsa_fwd_workspace_size(C.byref(_nsa(ab, deterministic=True)), C.byref(fwd)) == 0
+    assert lib.nsa_workspace_size(C.byref(_nsa(ab)), C.byref(bwd)) == 0
+    assert fwd.value == bwd.value
+    assert lib.nsa_fwd_workspace_size(C.byref(_nsa(ab, d=192)), C.byref(fwd)) == 0 and fwd.value == 256
+
+
 def test_nsa_fwd_rejects_before_launch(ab):
     lib = ab._lib.load()
     desc = _nsa(ab)

@@ -35,8 +35,10 @@ def _fwd_parity(p):
 
 
 @pytest.mark.parametrize("sparse_mode", [0, 2])
-@pytest.mark.parametrize("n1,n2", [(16, 2), (4, 1), (32, 1)])
+@pytest.mark.parametrize("n1,n2", [(16, 2), (4, 1), (32, 1), (1, 1), (3, 1), (12, 1), (20, 2)])
 def test_nsa_forward_parity(sparse_mode, n1, n2):
+    """The tensor-core forward (two passes over the block lists: row maxima, then sums and O) for full
+    and padded head groups, both sparse modes."""
     _fwd_parity(_problem(sparse_mode, n1=n1, n2=n2, seed=40 + n1 + sparse_mode))
 
 
