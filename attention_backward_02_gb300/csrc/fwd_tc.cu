@@ -265,22 +265,29 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             const int64_t lim64 = kmax - int64_t(j) * BN;  // columns <= lim are visible
             const int lim = int(lim64 < -1 ? -1 : (lim64 > BN ? BN : lim64));
             wait(&s_full[sb], uint32_t(j >> 1) & 1);
-            // pass 1: the tile's row max (this half, then both halves through shared memory)
+            // this half row of S, scaled to log2 units and masked, into registers; the S buffer is free
+            // for the tile after next as soon as it has been read.  Then the row max (this half, then both
+            // halves through shared memory).
+            static_assert(HC == 64, "two chunks of 32 columns per half row");
+            float x[HC];
             float mx = -INFINITY;
             if (ok) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tS + half * HC, v0);
+                tmem_ld32(tS + half * HC + 32, v1);
+                tmem_ld_wait_regs(v0);
+                tmem_ld_wait_regs(v1);
 #pragma unroll
-                for (int ch = 0; ch < HC / 32; ++ch) {
-                    const int c0 = half * HC + ch * 32;
-                    uint32_t v[32];
-                    tmem_ld32(tS + c0, v);
-                    tmem_ld_wait_regs(v);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float x = c0 + e <= lim ? __uint_as_float(v[e]) * c : -INFINITY;
-                        mx = fmaxf(mx, x);
-                    }
+                for (int e = 0; e < 32; ++e) {
+                    x[e] = half * HC + e <= lim ? __uint_as_float(v0[e]) * c : -INFINITY;
+                    x[32 + e] = half * HC + 32 + e <= lim ? __uint_as_float(v1[e]) * c : -INFINITY;
                 }
+#pragma unroll
+                for (int e = 0; e < HC; ++e) mx = fmaxf(mx, x[e]);
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[sb]);
             {
                 float *slot = xm + (j & 1) * 256;  // alternate by tile: the other half may still read the last
                 slot[half * 128 + r] = mx;
@@ -323,15 +330,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
                 for (int ch = 0; ch < HC / 32; ++ch) {
                     const int c0 = half * HC + ch * 32;
-                    uint32_t v[32];
-                    tmem_ld32(tS + c0, v);
-                    tmem_ld_wait_regs(v);
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float x0 = c0 + e <= lim ? __uint_as_float(v[e]) * c - m_use : -INFINITY;
-                        const float x1 = c0 + e + 1 <= lim ? __uint_as_float(v[e + 1]) * c - m_use : -INFINITY;
-                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        const float p0 = ex2(x[ch * 32 + e] - m_use), p1 = ex2(x[ch * 32 + e + 1] - m_use);
                         l += p0 + p1;
                         pk[e / 2] = pack2<T>(p0, p1);
                     }
@@ -348,10 +350,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&s_free[sb]);
-                mbar_arrive(&p_full[sb]);
-            }
+            if (lane == 0) mbar_arrive(&p_full[sb]);
         }
         // ---- epilogue: O / l (16-bit, row per thread, this half's columns) and LSE (natural log)
         {
