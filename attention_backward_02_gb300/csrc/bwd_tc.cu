@@ -945,9 +945,9 @@ void plan_ordered(TcSched &S, const DenseArgs &a, const Geo &g, int64_t units, i
 // balanced groupings of the causal workloads' regular unit sizes that greedy misses by up to a
 // tile; it is used when its makespan is at least 3 % shorter.  Each CTA takes its units longest
 // first.  The plan of the last shape is kept
-// (planning is host work on every call).  Leaves on = 0 (snake order) in deterministic mode, for
-// varlen batches (sorted by length, the units running together would be one long sequence's,
-// adding into the same dQ rows) or when the plan does not fit.
+// (planning is host work on every call).  Varlen batches take only the head-local plan below, when
+// its makespan is within 5 % of the snake order's; otherwise, in the split deterministic mode or
+// when the plan does not fit, on = 0 (snake order).
 template <int BM, int BN, class Geo>
 void plan_units(TcSched &S, const DenseArgs &a, const Geo &g, int64_t units, int64_t ctas)
 {
@@ -956,19 +956,28 @@ void plan_units(TcSched &S, const DenseArgs &a, const Geo &g, int64_t units, int
         plan_ordered<BM, BN>(S, a, g, units, ctas);
         return;
     }
-    if (IsPacked<Geo>::value || a.deterministic || units > kSchedUnits || ctas > kSchedCtas || ctas < 1) return;
+    constexpr bool packed = IsPacked<Geo>::value;
+    if (a.deterministic || units > kSchedUnits || ctas > kSchedCtas || ctas < 1) return;
     struct Key {
         int64_t nseq, h, h_kv, s_q, s_kv, units, ctas;
         int mask;
+        uint64_t lens;  // packed batches: a hash of the sequence lengths
         bool operator==(const Key &o) const
         {
             return nseq == o.nseq && h == o.h && h_kv == o.h_kv && s_q == o.s_q && s_kv == o.s_kv && units == o.units &&
-                   ctas == o.ctas && mask == o.mask;
+                   ctas == o.ctas && mask == o.mask && lens == o.lens;
         }
     };
-    static thread_local Key last_key = {-1, 0, 0, 0, 0, 0, 0, 0};
+    uint64_t lens = 1469598103934665603ull;  // FNV-1a over the (query, key) lengths
+    if (packed)
+        for (int64_t b = 0; b < a.nseq; ++b)
+            for (const int64_t l : {g.q_len(b), g.kv_len(b)}) {
+                lens ^= uint64_t(l);
+                lens *= 1099511628211ull;
+            }
+    static thread_local Key last_key = {-1, 0, 0, 0, 0, 0, 0, 0, 0};
     static thread_local TcSched last_plan;
-    const Key key = {a.nseq, a.h, a.h_kv, g.q_len(0), g.kv_len(0), units, ctas, a.mask};
+    const Key key = {a.nseq, a.h, a.h_kv, g.q_len(0), g.kv_len(0), units, ctas, a.mask, lens};
     if (key == last_key) {
         S = last_plan;
         return;
@@ -1044,26 +1053,43 @@ void plan_units(TcSched &S, const DenseArgs &a, const Geo &g, int64_t units, int
     bool use_local = false;
     const int64_t ws_bytes = (a.t_q * a.h * a.d * 2 + a.t_kv * a.h_kv * a.d) * 2 + a.h * a.t_pad * a.d * 4;
     if (ws_bytes > (int64_t(64) << 20)) {
-        const int64_t ntiles = nu / nheads;
-        const int64_t pairs = (ntiles + 1) / 2, njobs = pairs * nheads;
+        // the (sequence, kv head) heads, largest first (packed batches: their lengths differ), each with
+        // its key tiles in pairs (jt, n_b - 1 - jt)
+        static thread_local int32_t heads[kSchedUnits];
+        static thread_local int64_t head_cost[kSchedUnits];
+        for (int64_t hd = 0; hd < nheads; ++hd) {
+            heads[hd] = int32_t(hd);
+            head_cost[hd] = 0;
+        }
+        for (int u = 0; u < nu; ++u) head_cost[u % nheads] += cost[u];
+        std::stable_sort(heads, heads + nheads, [&](int32_t x, int32_t y) { return head_cost[x] > head_cost[y]; });
+        int64_t njobs = 0;
+        for (int64_t hd = 0; hd < nheads; ++hd) {
+            const int64_t nt = (g.kv_len(hd / a.h_kv) + BN - 1) / BN;
+            njobs += (nt + 1) / 2;
+        }
         const int64_t full = njobs / n > 1 ? njobs / n - 1 : 0;
         for (int c = 0; c < n; ++c) load[c] = 0;
+        for (int u = 0; u < nu; ++u) local_of[u] = -1;
         int32_t rank = 0;
         int ntail = 0;
-        for (int64_t job = 0; job < njobs; ++job) {
-            const int64_t head = job / pairs, pj = job % pairs;
-            const int64_t ua = pj * nheads + head, ub = (ntiles - 1 - pj) * nheads + head;
-            for (int k = 0; k < (ua == ub ? 1 : 2); ++k) {
-                const int64_t u = k == 0 ? ua : ub;
-                local_of[u] = -1;
-                if (cost[u] == 0) continue;
-                if (job < full * n) {
-                    const int c = int(job % n);
-                    local_of[u] = c;
-                    local_rank[u] = rank++;
-                    load[c] += cost[u];
-                } else {
-                    tail[ntail++] = int32_t(u);
+        int64_t job = 0;
+        for (int64_t k = 0; k < nheads; ++k) {
+            const int64_t head = heads[k];
+            const int64_t nt = (g.kv_len(head / a.h_kv) + BN - 1) / BN;
+            for (int64_t pj = 0; pj < (nt + 1) / 2; ++pj, ++job) {
+                const int64_t ua = pj * nheads + head, ub = (nt - 1 - pj) * nheads + head;
+                for (int kk = 0; kk < (ua == ub ? 1 : 2); ++kk) {
+                    const int64_t u = kk == 0 ? ua : ub;
+                    if (cost[u] == 0) continue;
+                    if (job < full * n) {
+                        const int c = int(job % n);
+                        local_of[u] = c;
+                        local_rank[u] = rank++;
+                        load[c] += cost[u];
+                    } else {
+                        tail[ntail++] = int32_t(u);
+                    }
                 }
             }
         }
@@ -1080,6 +1106,21 @@ void plan_units(TcSched &S, const DenseArgs &a, const Geo &g, int64_t units, int
         int64_t local_max = 0;
         for (int c = 0; c < n; ++c) local_max = load[c] > local_max ? load[c] : local_max;
         use_local = 100 * local_max <= 105 * best;
+        if (packed) {  // against the snake order packed batches take otherwise
+            for (int c = 0; c < n; ++c) load[c] = 0;
+            for (int u = 0; u < nu; ++u) {
+                const int r = u / n, c = u % n;
+                load[(r & 1) ? n - 1 - c : c] += cost[u];
+            }
+            int64_t snake_max = 0;
+            for (int c = 0; c < n; ++c) snake_max = load[c] > snake_max ? load[c] : snake_max;
+            use_local = 100 * local_max <= 105 * snake_max;
+        }
+    }
+    if (packed && !use_local) {  // snake order (units running together would add into one long sequence's rows)
+        last_plan = S;
+        last_key = key;
+        return;
     }
     if (use_local)
         for (int u = 0; u < nu; ++u) cta_of[u] = local_of[u];
