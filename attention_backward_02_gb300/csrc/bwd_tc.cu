@@ -32,9 +32,11 @@
 // warps turn tile i's S/dP into P/dS.  Two 32 KB shared buffers alternate
 // per query tile: tile i writes its dS into one while tile i-1's GEMMs read
 // their dS from the other.  P (16-bit, packed) waits in registers until tile
-// i-1's dV GEMM has released the P columns of TMEM.  Q, dO and the LSE / D
-// vectors stream through a 3-stage ring.  Fixed-length batches take their
-// work units in a longest-first order planned on the host.
+// i-1's dV GEMM has released the P columns of TMEM.  At d = 128 the softmax
+// warps copy S^T / dP^T into registers and release them before computing, so
+// tile i+1's S/dP GEMMs run during tile i's element-wise work.  Q, dO and the
+// LSE / D vectors stream through a 3-stage ring.  Fixed-length batches take
+// their work units in a longest-first order planned on the host.
 //
 // Roles (14 warps): warp 0 issues TMA loads, warp 1 the MMAs, warps 2..9 do
 // the element-wise work (warp w reads TMEM lanes 32 (w % 4) .. + 31; the two
@@ -513,21 +515,47 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                     else if (q == 0) tc_fence_after();
                     const int c0 = q * (BM / NG) + half * GW;
                     uint32_t pk[GW / 2];  // P^T of this column group, packed
-                    if (ok) {
-                        const bool any_mask = __any_sync(0xffffffffu, cmin > c0);
-                        // chunks of 16 columns; the TMEM loads of chunk cc + 1 are issued before
-                        // chunk cc is computed
-                        constexpr int NCH = GW / 16;
-                        uint32_t sbuf[2][16], dbuf[2][16];
+                    // S^T / dP^T of the group in chunks of 16 columns.  With one group a thread (d = 128)
+                    // the whole group is loaded at once and its TMEM columns released before P / dS are
+                    // computed, so the next tile's S^T / dP^T GEMMs overlap this tile's element-wise work;
+                    // with two (d = 64) chunk cc + 1 is loaded while chunk cc is computed and the columns
+                    // are released after the group (the early release measured slower there)
+                    constexpr int NCH = GW / 16;
+                    constexpr bool kEarlyFree = NG == 1 && NCH == 2;
+                    uint32_t sbuf[2][16], dbuf[2][16];
+                    auto release = [&]() {
+                        if (NH == NG || q == NG - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&s_free[rel]);  // these columns may be overwritten
+                        }
+                    };
+                    if (kEarlyFree) {
+                        if (ok) {
+#pragma unroll
+                            for (int cc = 0; cc < NCH; ++cc) {
+                                tmem_ld16(tmem + lane_addr + Cfg::T_S + c0 + 16 * cc, sbuf[cc & 1]);
+                                tmem_ld16(tmem + lane_addr + Cfg::T_DP + c0 + 16 * cc, dbuf[cc & 1]);
+                            }
+                            tmem_ld_wait_regs(sbuf[0], dbuf[0]);
+                            tmem_ld_wait_regs(sbuf[1], dbuf[1]);
+                        }
+                        release();
+                    } else if (ok) {
                         tmem_ld16(tmem + lane_addr + Cfg::T_S + c0, sbuf[0]);
                         tmem_ld16(tmem + lane_addr + Cfg::T_DP + c0, dbuf[0]);
+                    }
+                    if (ok) {
+                        const bool any_mask = __any_sync(0xffffffffu, cmin > c0);
 #pragma unroll
                         for (int cc = 0; cc < NCH; ++cc) {
                             const int col0 = c0 + cc * 16, cur = cc & 1;
-                            tmem_ld_wait_regs(sbuf[cur], dbuf[cur]);
-                            if (cc + 1 < NCH) {
-                                tmem_ld16(tmem + lane_addr + Cfg::T_S + col0 + 16, sbuf[cur ^ 1]);
-                                tmem_ld16(tmem + lane_addr + Cfg::T_DP + col0 + 16, dbuf[cur ^ 1]);
+                            if (!kEarlyFree) {
+                                tmem_ld_wait_regs(sbuf[cur], dbuf[cur]);
+                                if (cc + 1 < NCH) {
+                                    tmem_ld16(tmem + lane_addr + Cfg::T_S + col0 + 16, sbuf[cur ^ 1]);
+                                    tmem_ld16(tmem + lane_addr + Cfg::T_DP + col0 + 16, dbuf[cur ^ 1]);
+                                }
                             }
                             uint32_t dk[8];
 #pragma unroll
@@ -556,11 +584,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                             }
                         }
                     }
-                    if (NH == NG || q == NG - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&s_free[rel]);  // these columns may be overwritten
-                    }
+                    if (!kEarlyFree) release();
                     // P^T into TMEM once the previous tile's dV GEMM has read it
                     if (q == 0) {
                         const uint32_t t_p = qi > 0 ? mbar_test_wait(p_free, (qi - 1) & 1) : 1u;
