@@ -101,7 +101,7 @@ struct TcCfg {
     static constexpr int OFF_LSE = OFF_DQS + DQS_BYTES;       // NST x BM floats
     static constexpr int OFF_DVEC = OFF_LSE + NST * BM * 4;   // NST x BM floats
     static constexpr int OFF_BAR = OFF_DVEC + NST * BM * 4;
-    static constexpr int OFF_MISC = OFF_BAR + 24 * 8;
+    static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
     static constexpr int SMEM = OFF_MISC + 64;
     static constexpr int SMEM_ALLOC = SMEM + 1024;            // room to align the base to 1024
     static constexpr int T_S = 0, T_DP = BM, T_P = 2 * BM, T_DV = 2 * BM + BM / 2, T_DK = T_DV + D,
@@ -117,6 +117,7 @@ struct TcCfg {
 // Work units of each CTA, chosen on the host (see plan_units).  on = 0: the CTAs
 // take the units in snake order instead.
 constexpr int kSchedCtas = 160;
+constexpr int kMailbox = 4;  // ordered dQ mode: counters in flight from the dQ leader to the publishing warp
 constexpr int kSchedUnits = 4096;
 struct TcSched {
     int32_t on;
@@ -167,7 +168,8 @@ template <> struct IsPacked<PackedGeo> : std::true_type {};
 // kOrdered: ordered dQ mode (one accumulator, each query tile's adds in a fixed order; needs the planned
 // unit order and a cooperative launch).  A template parameter, so the other modes carry none of its code.
 template <class T, int D, class Geo, bool kOrdered>
-__global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(const __grid_constant__ TcParams p, const Geo geo)
+__global__ void __launch_bounds__(TcCfg<D>::THREADS + (kOrdered ? 32 : 0), 1)
+    dense_bwd_tc_kernel(const __grid_constant__ TcParams p, const Geo geo)
 {
     using Cfg = TcCfg<D>;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, NST = Cfg::NST, NH = Cfg::NH, NG = Cfg::NG;
@@ -188,8 +190,11 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
     uint64_t *ds_free = s_full + 8;          // [2] dS buffer: the GEMMs that read it have completed
     uint64_t *acc_free = s_full + 10;        // the dK / dV accumulators have been read out
     uint64_t *drain = s_full + 11;
+    // ordered dQ mode: counters handed from the dQ leader to the warp that publishes them
+    uint64_t *mb_full = s_full + 12, *mb_empty = s_full + 12 + kMailbox;  // [kMailbox]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 8);
+    uint32_t **mailbox = reinterpret_cast<uint32_t **>(smem + Cfg::OFF_MISC + 16);  // [kMailbox]
     const DenseArgs &a = p.a;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -213,6 +218,11 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
         mbar_init(&ds_free[1], 1);
         mbar_init(acc_free, 4);
         mbar_init(drain, 1);
+        if (kOrdered)
+            for (int k = 0; k < kMailbox; ++k) {
+                mbar_init(&mb_full[k], 1);
+                mbar_init(&mb_empty[k], 1);
+            }
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, Cfg::T_COLS);
@@ -617,8 +627,26 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
         }
         ATTN_END_UNITS
         pdl_trigger();
+    } else if (kOrdered && warp == 2 + Cfg::NSW + 4) {
+        // ================================================= ordered dQ mode: add counts (warp 14)
+        // A GPU-scope release stalls the warp that issues it for about a microsecond; the dQ leader
+        // hands each counter over (after its adds have landed and a proxy fence) and goes on, and
+        // this warp publishes it.  A null counter ends the list.
+        if (lane == 0) {
+            for (uint32_t n = 0;; ++n) {
+                const int k = int(n % kMailbox);
+                if (!mbar_wait(&mb_full[k], (n / kMailbox) & 1, abort)) {
+                    if (!*abort) flag_abort(abort, a.status);
+                    break;
+                }
+                uint32_t *const ctr = mailbox[k];
+                mbar_arrive(&mb_empty[k]);
+                if (!ctr) break;
+                red_release_gpu_add(ctr, 1u);
+            }
+        }
     } else {
-        // ================================================= dQ reduce, dK / dV epilogue (last 4 warps)
+        // ================================================= dQ reduce, dK / dV epilogue (warps 10..13)
         const int lg = warp & 3;
         const uint32_t lane_addr = uint32_t(lg * 32) << 16;
         const int r = lg * 32 + lane;  // TMEM lane of this thread
@@ -629,6 +657,17 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
         bool ok = true;
         uint32_t qi = 0;
         uint32_t *pend = nullptr;  // ordered dQ mode: counter of the tile whose adds are still to be counted
+        uint32_t n_post = 0;       // ... and the counters handed to the publishing warp so far
+        auto post = [&](uint32_t *ctr) {
+            const int k = int(n_post % kMailbox);
+            if (n_post >= kMailbox && ok && !(ok = mbar_wait(&mb_empty[k], ((n_post / kMailbox) - 1) & 1, abort)))
+                flag_abort(abort, a.status);
+            if (ok) {
+                mailbox[k] = ctr;
+                mbar_arrive(&mb_full[k]);
+            }
+            ++n_post;
+        };
         pdl_wait();  // the dQ accumulator (and the ordered mode's counters) have been zeroed
 
         ATTN_FOR_EACH_UNIT
@@ -809,13 +848,13 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
                         if (pend) {
                             bulk_wait2();
                             fence_proxy_async_global();
-                            red_release_gpu_add(pend, 1u);
+                            post(pend);
                             pend = nullptr;
                         }
                         if (it == n_iter - 1) {
                             bulk_wait0();
                             fence_proxy_async_global();
-                            red_release_gpu_add(sem_of(), 1u);
+                            post(sem_of());
                         } else {
                             pend = sem_of();
                         }
@@ -826,6 +865,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1) dense_bwd_tc_kernel(cons
             if (leader && a.deterministic) bulk_wait0();
         }
         ATTN_END_UNITS
+        if (kOrdered && leader) post(nullptr);  // the publishing warp may exit
         if (leader) bulk_wait0();  // the reduce-adds have read the staging buffer (and landed) before the exit
         pdl_trigger();  // the dQ finalize may start launching; it waits for this grid
     }
@@ -1203,8 +1243,8 @@ template <class T, int D, class Geo> cudaError_t run_tc(const DenseArgs &a, cons
     plan_units<Cfg::BM, Cfg::BN>(prm.sched, prm.a, g, prm.a.tc_units, units);
     if (a.ordered && !prm.sched.on) return cudaErrorNotSupported;  // the waits need the planned order
     // ordered dQ mode waits across CTAs: a cooperative launch puts all of them on the GPU at once
-    return launch_kernel_ex(k, dim3(unsigned(units)), dim3(Cfg::THREADS), Cfg::SMEM_ALLOC, s, true, a.ordered != 0,
-                            prm, g);
+    return launch_kernel_ex(k, dim3(unsigned(units)), dim3(Cfg::THREADS + (a.ordered ? 32 : 0)), Cfg::SMEM_ALLOC, s,
+                            true, a.ordered != 0, prm, g);
 }
 
 template <class Geo> cudaError_t dispatch(const DenseArgs &a, const Geo &g, cudaStream_t s)
