@@ -41,7 +41,8 @@
 // Roles (14 warps): warp 0 issues TMA loads, warp 1 the MMAs, warps 2..9 do
 // the element-wise work (warp w reads TMEM lanes 32 (w % 4) .. + 31; the two
 // warps on the same lanes split the columns), warps 10..13 the dQ staging and
-// the dK / dV epilogue.
+// the dK / dV epilogue.  The ordered dQ mode adds warp 14, which publishes the
+// per-tile add counts.
 //
 // Causal masking: query tiles entirely before the first query that sees the
 // key tile are skipped; the rest are masked per element when needed.  Key
