@@ -31,12 +31,13 @@ __device__ __forceinline__ int64_t seq_lse(const DenseArgs &a, const PackedGeo &
     return h * a.t_q + g.cu_q[b] + i;
 }
 
-// Rows of a preprocess / finalize work unit: a quarter of the workspace row
-// alignment, so a unit lies within one sequence and the grid has enough blocks.
-constexpr int kUnitRows = int(kWsRowAlign) / 4;
+// Rows of a preprocess / finalize work unit: half the workspace row alignment,
+// so a unit lies within one sequence, each thread has two (d = 64) or four
+// (d = 128) rows' loads in flight, and workload-sized grids fit one wave.
+constexpr int kUnitRows = int(kWsRowAlign) / 2;
 
 // ------------------------------------------------------------- preprocess
-// Work unit = (head, 32 workspace rows); a unit lies within one sequence, so
+// Work unit = (head, 64 workspace rows); a unit lies within one sequence, so
 // it is located once.  d/8 threads per row (8 elements each),
 // 256-thread blocks striding over the units in one resident wave.  Covers
 // every workspace row: padding rows get LSE2 = +inf (so P = 0) and D = 0.
