@@ -79,7 +79,8 @@ def nsa_desc(*, dtype, cu_seqlens_q, cu_seqlens_kv, n1, n2, d, scale, block_size
     key lengths, n1 query and n2 kv heads, query / key head dim d and value head dim d_v (0: d),
     scaleValue, selectedBlockSize / Count, sparseMode 0 (selection only) or 2 (also causal,
     bottom-right per sequence); deterministic makes dq, dk, dv bitwise reproducible (tensor-core head
-    groups only); grad_fp32 makes dq, dk, dv fp32; atten_mask (attenMaskOptional) is a 2-D uint8 CUDA
+    groups only): False / 0 atomic adds, True / 1 per-slot dQ partials summed in slot order, 2 one dQ
+    accumulator whose adds per token go in decreasing block order (ATTN_DQ_ORDERED); grad_fp32 makes dq, dk, dv fp32; atten_mask (attenMaskOptional) is a 2-D uint8 CUDA
     tensor [rows, cols] over local (query, key) positions, nonzero = key removed, covering every
     sequence (held by the descriptor)."""
     keep = _Keep()
@@ -89,7 +90,7 @@ def nsa_desc(*, dtype, cu_seqlens_q, cu_seqlens_kv, n1, n2, d, scale, block_size
         keep.items.append(atten_mask)
     desc = attn_nsa_desc_t(int(dtype), len(cu_seqlens_q), _cu_array(keep, cu_seqlens_q),
                            _cu_array(keep, cu_seqlens_kv), int(n1), int(n2), int(d), float(scale),
-                           int(block_size), int(block_count), int(sparse_mode), int(bool(deterministic)),
+                           int(block_size), int(block_count), int(sparse_mode), int(deterministic),
                            int(d_v), int(bool(grad_fp32)),
                            atten_mask.data_ptr() if atten_mask is not None else None,
                            int(atten_mask.shape[0]) if atten_mask is not None else 0,

@@ -329,7 +329,7 @@ attn_status_t check_nsa_desc(const attn_nsa_desc_t *d, NsaShape *sh)
     if (d->block_count < 1 || d->block_count > 128 || d->block_count * d->block_size >= 8192)
         return ATTN_ERR_INVALID;
     if (d->sparse_mode != 0 && d->sparse_mode != 2) return ATTN_ERR_INVALID;
-    if (d->deterministic != 0 && d->deterministic != 1) return ATTN_ERR_INVALID;
+    if (d->deterministic < 0 || d->deterministic > 2) return ATTN_ERR_INVALID;
     if (d->d != 128 && d->d != 192) return ATTN_ERR_INVALID;
     if (d->d_v != 0 && d->d_v != 128 && d->d_v != 192) return ATTN_ERR_INVALID;
     if (d->grad_fp32 != 0 && d->grad_fp32 != 1) return ATTN_ERR_INVALID;
@@ -356,7 +356,7 @@ attn_status_t check_nsa_desc(const attn_nsa_desc_t *d, NsaShape *sh)
 }
 
 struct NsaLayout {
-    size_t status, lse2, dvec, bitmap, offsets, pieces, tokens, dqacc, dkacc, dvacc, dqpart, total;
+    size_t status, lse2, dvec, bitmap, offsets, pieces, tokens, dqacc, dkacc, dvacc, dqpart, sem, rank, total;
     int64_t t1_pad, nrows;
 };
 
@@ -377,9 +377,14 @@ NsaLayout nsa_layout(const attn_nsa_desc_t *d, const NsaShape &sh)
     L.dkacc = L.dqacc + Workspace::align(rows * size_t(d->d) * sizeof(float));
     L.dvacc = L.dkacc + Workspace::align(size_t(sh.t2) * size_t(d->n2 * d->d) * sizeof(float));
     L.dqpart = L.dvacc + Workspace::align(size_t(sh.t2) * size_t(d->n2 * sh.dv) * sizeof(float));
-    const size_t part_bytes =
-        d->deterministic ? size_t(sh.t1) * size_t(d->n1) * size_t(d->block_count) * size_t(d->d) * sizeof(float) : 0;
-    L.total = L.dqpart + Workspace::align(part_bytes);
+    // deterministic 1: dQ per (token, selected slot); 2: one add counter per (token, kv head)
+    const size_t part_bytes = d->deterministic == 1
+                                  ? size_t(sh.t1) * size_t(d->n1) * size_t(d->block_count) * size_t(d->d) * sizeof(float)
+                                  : 0;
+    L.sem = L.dqpart + Workspace::align(part_bytes);
+    const bool ord = d->deterministic == 2;
+    L.rank = L.sem + (ord ? Workspace::align(size_t(sh.t1) * size_t(d->n2) * sizeof(uint32_t)) : 0);
+    L.total = L.rank + (ord ? Workspace::align(size_t(sh.t1) * size_t(d->n2 * d->block_count) * sizeof(int32_t)) : 0);
     return L;
 }
 
@@ -394,7 +399,7 @@ bool nsa_fwd_on_tc(const attn_nsa_desc_t *d, const NsaShape &sh)
 NsaLayout nsa_fwd_layout(const attn_nsa_desc_t *d, const NsaShape &sh)
 {
     attn_nsa_desc_t c = *d;
-    c.deterministic = 0;  // no per-slot partials in the forward
+    c.deterministic = 0;  // no per-slot partials or add counters in the forward
     return nsa_layout(&c, sh);
 }
 
@@ -417,6 +422,8 @@ void nsa_ws_pointers(NsaArgs *a, const NsaLayout &L, void *workspace)
     a->dkacc = reinterpret_cast<float *>(ws + L.dkacc);
     a->dvacc = reinterpret_cast<float *>(ws + L.dvacc);
     a->dqpart = reinterpret_cast<float *>(ws + L.dqpart);
+    a->sem = reinterpret_cast<uint32_t *>(ws + L.sem);
+    a->rank = reinterpret_cast<int32_t *>(ws + L.rank);
 }
 
 }  // namespace
@@ -478,6 +485,8 @@ attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, 
     a.dkacc = reinterpret_cast<float *>(ws + L.dkacc);
     a.dvacc = reinterpret_cast<float *>(ws + L.dvacc);
     a.dqpart = reinterpret_cast<float *>(ws + L.dqpart);
+    a.sem = reinterpret_cast<uint32_t *>(ws + L.sem);
+    a.rank = reinterpret_cast<int32_t *>(ws + L.rank);
     // the CUDA-core kernel (a head dim of 192) adds dK / dV atomically from many blocks
     if (a.deterministic && !nsa_tc_supported(a)) return ATTN_ERR_UNSUPPORTED;
     static thread_local PackedGeo pg;

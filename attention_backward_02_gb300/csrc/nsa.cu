@@ -60,6 +60,7 @@ __device__ __forceinline__ void nsa_preprocess_block(const NsaArgs &a, int64_t p
         zero_words(reinterpret_cast<uint32_t *>(a.dkacc), a.t2 * a.n2 * a.d, tid, nthr);
         zero_words(reinterpret_cast<uint32_t *>(a.dvacc), a.t2 * a.n2 * a.dv, tid, nthr);
         if (a.zero_dq) zero_words(reinterpret_cast<uint32_t *>(a.dqacc), a.t1 * a.n1 * a.d, tid, nthr);
+        if (a.deterministic == 2) zero_words(a.sem, a.t1 * a.n2, tid, nthr);  // no dQ add has landed yet
     }
     const int64_t gx = nblk / a.n1, bx = pb % gx, h = pb / gx;
     const int lane = threadIdx.x % 16;
@@ -133,6 +134,18 @@ __global__ void nsa_mark_kernel(NsaArgs a, PackedGeo geo)
     if (a.sparse_mode == 2 && !visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, int64_t(blk) * a.bs, lq, lkv)) return;
     const int64_t row = (b * a.n2 + g) * a.nblk_max + blk;
     atomicOr(a.bitmap + row * a.words_max + i / 32, 1u << (i % 32));
+    if (a.deterministic == 2) {  // ordered dQ: the token's kept blocks above this one add before it
+        int32_t above = 0;
+        for (int64_t c2 = 0; c2 < a.cnt; ++c2) {
+            const int32_t id = ids[c2];
+            if (id <= blk || int64_t(id) >= nblk) continue;
+            bool first = true;
+            for (int64_t c3 = 0; c3 < c2 && first; ++c3) first = ids[c3] != id;
+            if (first && (a.sparse_mode != 2 || visible(ATTN_CAUSAL_BOTTOM_RIGHT, i, int64_t(id) * a.bs, lq, lkv)))
+                ++above;
+        }
+        a.rank[idx * a.cnt + c] = above;
+    }
 }
 
 // Count: one warp per row; counts land in offsets[row + 1].
@@ -605,7 +618,7 @@ cudaError_t run_nsa(const NsaArgs &a0, const PackedGeo &g, cudaStream_t s, cudaE
     cudaError_t e;
     const bool tc = nsa_tc_supported(a0);
     NsaArgs a = a0;
-    a.zero_dq = tc && !a.deterministic ? 1 : 0;
+    a.zero_dq = tc && a.deterministic != 1 ? 1 : 0;
     // init (status word, bitmap) first, ordinarily; then the block lists with the preprocess riding in
     // the emit launch; every kernel after init is chained with programmatic dependent launch
     {
@@ -620,7 +633,7 @@ cudaError_t run_nsa(const NsaArgs &a0, const PackedGeo &g, cudaStream_t s, cudaE
         if ((e = launch_nsa_tc(a, g, s)) != cudaSuccess) return e;
         if (after && (e = cudaEventRecord(after, s)) != cudaSuccess) return e;
         // the dQ finalize converts dK / dV too
-        if (a.t1 > 0 && a.deterministic)
+        if (a.t1 > 0 && a.deterministic == 1)
             e = launch_kernel(nsa_dq_finalize_det_kernel<OutT>, dim3(1024), dim3(256), 0, s, true, a, g, 1);
         else if (a.t1 > 0)
             e = launch_kernel(nsa_dq_finalize_kernel<OutT>, dim3(1024), dim3(256), 0, s, true, a, 1);

@@ -59,6 +59,7 @@ using namespace tc;
 namespace {
 
 constexpr int kD = 128, kBS = 64, kRows = 128, kNst = 2, kMaxSlots = 16, kSlotInts = 4, kSlotRing = 4;
+constexpr int kMailbox = 2;  // ordered mode: chunks of add counters in flight to the publishing warp
 enum : int { kBwd = 0, kFwdMax = 1, kFwdSum = 2 };  // what a launch of the kernel computes
 
 // Order-preserving map of a float onto int32 (an involution), for atomicMax on floats.
@@ -83,7 +84,8 @@ struct NsaCfg {
     static constexpr int OFF_DS = OFF_P + PS_BYTES;
     static constexpr int OFF_DQS = OFF_DS + PS_BYTES;
     static constexpr int OFF_SLOT = OFF_DQS + DQS_BYTES;    // kSlotRing x kMaxSlots x {local index, token, topk slot, -}
-    static constexpr int OFF_BAR = OFF_SLOT + kSlotRing * kMaxSlots * kSlotInts * 4;
+    static constexpr int OFF_MBOX = OFF_SLOT + kSlotRing * kMaxSlots * kSlotInts * 4;  // ordered mode: counters
+    static constexpr int OFF_BAR = OFF_MBOX + kMailbox * kMaxSlots * 8;
     static constexpr int OFF_MISC = OFF_BAR + 24 * 8;
     static constexpr int THREADS = 448;
     static constexpr int SMEM = OFF_MISC + 64;
@@ -112,8 +114,10 @@ __device__ __forceinline__ int64_t piece_row(const int32_t *piece_off, int64_t n
     return lo;
 }
 
-template <class T, int kMode>
-__global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ NsaTcParams p, const PackedGeo geo)
+// kOrd: backward in the ordered deterministic mode (a publishing warp, pieces in decreasing order)
+template <class T, int kMode, bool kOrd>
+__global__ void __launch_bounds__(kOrd ? 480 : 448, 1)
+    nsa_tc_kernel(const __grid_constant__ NsaTcParams p, const PackedGeo geo)
 {
     using Cfg = NsaCfg;
     constexpr int kType = std::is_same<T, __half>::value ? 0 : 1;
@@ -124,6 +128,9 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
     uint64_t *s_full = bars + 2 + 2 * kNst, *p_ready = s_full + 1, *mma_done = s_full + 2, *drain = s_full + 3;
     uint64_t *dq_free = s_full + 4;  // the dQ warps have read the dQ accumulator
     uint64_t *slot_full = s_full + 5, *slot_empty = s_full + 5 + kSlotRing;  // [kSlotRing] token lists
+    // ordered mode: chunks of add counters from the dQ issuer to the publishing warp
+    uint64_t *mb_full = s_full + 5 + 2 * kSlotRing, *mb_empty = mb_full + kMailbox;  // [kMailbox]
+    uint32_t **mbox = reinterpret_cast<uint32_t **>(smem + Cfg::OFF_MBOX);           // [kMailbox][kMaxSlots]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 8);
     int32_t *slots = reinterpret_cast<int32_t *>(smem + Cfg::OFF_SLOT);  // [ring][slot][kSlotInts]
@@ -146,6 +153,10 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
     pdl_wait();     // statistics, block lists, pieces and the zeroed accumulators are ready
     pdl_trigger();  // the finalize kernels may start launching; they wait for this grid
     const int64_t n_pieces = a.pieces[a.nrows];
+    // Work units: the pieces, in block-list row order.  Ordered mode (whole block lists): every row, in
+    // decreasing block order (then sequence and kv head), empty rows skipped; so each CTA's rows have
+    // decreasing blocks, every wait is for a higher block, and no cycle of waits can form.
+    const int64_t n_units = kOrd ? a.nrows : n_pieces;
 
     if (threadIdx.x == 0) {
         *abort = 0;
@@ -164,6 +175,11 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
             mbar_init(&slot_full[k], 1);
             mbar_init(&slot_empty[k], 8 + 4);  // P / dS warps, dQ warps
         }
+        if (kOrd)
+            for (int k = 0; k < kMailbox; ++k) {
+                mbar_init(&mb_full[k], 1);
+                mbar_init(&mb_empty[k], 1);
+            }
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, Cfg::T_COLS);
@@ -176,14 +192,17 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
 
     // the work unit of piece pc: block-list row, token range, sequence / head / block
 #define NSA_PIECE_DECODE                                                                         \
-    const int64_t row = piece_row(a.pieces, a.nrows, pc);                                       \
-    const int64_t lp = pc - a.pieces[row];                                                      \
+    const int64_t nbg = a.nseq * a.n2;                                                          \
+    const int64_t row = kOrd ? (pc % nbg) * a.nblk_max + (a.nblk_max - 1 - pc / nbg)          \
+                             : piece_row(a.pieces, a.nrows, pc);                                \
+    const int64_t lp = kOrd ? 0 : pc - a.pieces[row];                                          \
     const int64_t tok_begin = a.offsets[row] + lp * a.piece_tokens;                            \
     const int64_t tok_end_full = a.offsets[row + 1];                                            \
     const int64_t tok_end = tok_begin + a.piece_tokens < tok_end_full ? tok_begin + a.piece_tokens : tok_end_full; \
     const int nchunks = int((tok_end - tok_begin + tpc - 1) / tpc);                            \
     const int64_t b = row / (a.n2 * a.nblk_max), g = (row / a.nblk_max) % a.n2, blk = row % a.nblk_max; \
-    (void)b; (void)g; (void)blk; (void)nchunks;
+    (void)b; (void)g; (void)blk; (void)nchunks;                                                 \
+    if (kOrd && nchunks == 0) continue;
 
     if (warp == 0) {
         // ================================================= TMA producer (the whole warp: lane u
@@ -194,7 +213,7 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
             }
             bool ok = true;
             int64_t kt = 0, ci = 0, q_armed = 0, kv_armed = 0;
-            for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
+            for (int64_t pc = blockIdx.x; pc < n_units; pc += gridDim.x) {
                 NSA_PIECE_DECODE
                 if (kt > 0 && ok && !(ok = mbar_wait(kv_empty, uint32_t(kt - 1) & 1, abort))) flag_abort(abort, a.status);
                 ok = __all_sync(0xffffffffu, ok);
@@ -225,11 +244,15 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
                     const int u = lane;  // this lane's token slot
                     const int32_t t = t_next;
                     if (u < tpc) {
-                        int32_t slot = -1;  // deterministic mode: position of this block in the token's topk
-                        if (a.deterministic && t >= 0) {
+                        // deterministic mode 1: position of this block in the token's topk (its first
+                        // occurrence, the one the block lists keep); mode 2: how many of the token's kept
+                        // blocks above this one add before it (worked out with the block lists)
+                        int32_t slot = -1;
+                        if (a.deterministic != 0 && t >= 0) {
                             const int32_t *ids = a.topk + (int64_t(t) * a.n2 + g) * a.cnt;
                             for (int64_t c = a.cnt - 1; c >= 0; --c)
                                 if (ids[c] == blk) slot = int32_t(c);
+                            if (kOrd && slot >= 0) slot = a.rank[(int64_t(t) * a.n2 + g) * a.cnt + slot];
                         }
                         int32_t *sl = slots + (rs * kMaxSlots + u) * kSlotInts;
                         sl[0] = t >= 0 ? int32_t(t - geo.cu_q[b]) : -1;
@@ -279,7 +302,7 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
             const uint64_t kP = desc_kmaj(smem_u32(sP), kRows, 0), mV = desc_mn(smem_u32(sV), kBS, 0);
             bool ok = true;
             int64_t kt = 0, ci = 0;
-            for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
+            for (int64_t pc = blockIdx.x; pc < n_units; pc += gridDim.x) {
                 NSA_PIECE_DECODE
                 if (ok && !(ok = mbar_wait(kv_full, uint32_t(kt) & 1, abort))) flag_abort(abort, a.status);
                 tc_fence_after();
@@ -350,7 +373,7 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
         const uint32_t aP = smem_u32(sP), adS = smem_u32(sdS);
         bool ok = true;
         int64_t kt = 0, ci = 0;
-        for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
+        for (int64_t pc = blockIdx.x; pc < n_units; pc += gridDim.x) {
             NSA_PIECE_DECODE
             const int64_t shift = geo.kv_len(b) - geo.q_len(b);
             for (int ch = 0; ch < nchunks; ++ch, ++ci) {
@@ -477,6 +500,25 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
             tc_fence_before();
             ++kt;
         }
+    } else if (kOrd && warp == 14) {
+        // ================================================= ordered mode: add counts (warp 14)
+        // A GPU-scope release stalls the warp that issues it for about a microsecond; the dQ issuer
+        // hands each chunk's counters over once their adds have landed, and this warp publishes them.
+        uint32_t *const end_mark = reinterpret_cast<uint32_t *>(uintptr_t(1));
+        for (uint32_t n = 0;; ++n) {
+            const int k = int(n % kMailbox);
+            const bool got = __all_sync(0xffffffffu, mbar_wait(&mb_full[k], (n / kMailbox) & 1, abort));
+            if (!got) {
+                if (lane == 0 && !*abort) flag_abort(abort, a.status);
+                break;
+            }
+            uint32_t *const ctr = lane < kMaxSlots ? mbox[k * kMaxSlots + lane] : nullptr;
+            const bool end = mbox[k * kMaxSlots] == end_mark;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mb_empty[k]);
+            if (end) break;
+            if (ctr) red_release_gpu_add(ctr, 1u);
+        }
     } else {
         // ================================================= dQ of each chunk (warps 10..13)
         const int lg = warp & 3;
@@ -487,13 +529,32 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
         const uint32_t aDQS = smem_u32(sDQS);
         bool ok = true;
         int64_t ci = 0;
-        for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
+        // ordered mode (issuer warp): the counter of this lane's token in the previous chunk, whose
+        // adds are still to be counted, and the chunks handed to the publishing warp so far
+        uint32_t *pend = nullptr;
+        bool pend_set = false;
+        uint32_t n_post = 0;
+        auto post = [&](uint32_t *ctr) {  // the whole issuer warp; lanes past the chunk's tokens pass null
+            const int k = int(n_post % kMailbox);
+            bool free_ok = true;
+            if (n_post >= kMailbox) free_ok = mbar_wait(&mb_empty[k], ((n_post / kMailbox) - 1) & 1, abort);
+            if (!__all_sync(0xffffffffu, free_ok)) {
+                if (lane == 0 && !*abort) flag_abort(abort, a.status);
+                ok = false;
+            } else {
+                if (lane < kMaxSlots) mbox[k * kMaxSlots + lane] = ctr;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&mb_full[k]);
+            }
+            ++n_post;
+        };
+        for (int64_t pc = blockIdx.x; pc < n_units; pc += gridDim.x) {
             NSA_PIECE_DECODE
             for (int ch = 0; ch < nchunks; ++ch, ++ci) {
                 const int rs = int(ci % kSlotRing);
                 if (ok && !(ok = mbar_wait(&slot_full[rs], uint32_t(ci / kSlotRing) & 1, abort)))
                     flag_abort(abort, a.status);
-                int32_t t = -1, slot = -1;  // this lane's token and its topk position
+                int32_t t = -1, slot = -1;  // this lane's token and its topk position (ordered: blocks above)
                 if (ok && issuer && lane < tpc) {
                     const int32_t *sl = slots + (rs * kMaxSlots + lane) * kSlotInts;
                     t = sl[1];
@@ -534,10 +595,20 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
                         fence_proxy_async_smem();
                         ok = bar_and(2, 128, ok);
                         if (issuer) {
-                            if (ok && t >= 0) {
+                            bool add = ok && t >= 0;
+                            if (kOrd && add && hr == 0 && bx == 0) {
+                                // this token's adds from its selected blocks above this one have landed
+                                if (wait_count(a.sem + int64_t(t) * a.n2 + g, uint32_t(slot), abort)) {
+                                    fence_proxy_async_global();
+                                } else {
+                                    flag_abort(abort, a.status);
+                                    ok = add = false;
+                                }
+                            }
+                            if (add) {
                                 const int box = hr * 2 + bx;
                                 const uint8_t *src = sDQS + bx * (kRows * 128) + lane * R * 128;
-                                if (kMode == kBwd && a.deterministic) {  // own partial rows (summed in slot order later)
+                                if (kMode == kBwd && a.deterministic == 1) {  // own partial rows (summed in slot order later)
                                     const int prow = int(((int64_t(t) * a.n2 + g) * a.cnt + slot) * G);
                                     tma_store_2d(&p.tm_dqpart, src, box * 32, prow);
                                 } else {
@@ -545,11 +616,32 @@ __global__ void __launch_bounds__(448, 1) nsa_tc_kernel(const __grid_constant__ 
                                 }
                             }
                             bulk_commit();  // one group per round and lane, possibly empty
+                            if (kOrd && hr == 1 && bx == 1) {
+                                // count the previous chunk's adds once they have landed (all but this
+                                // chunk's four groups complete); a piece's last chunk is counted at once,
+                                // so the next piece (a lower block) never waits on an uncounted add here
+                                uint32_t *const cur = ok && t >= 0 ? a.sem + int64_t(t) * a.n2 + g : nullptr;
+                                if (pend_set) {
+                                    bulk_wait4();
+                                    fence_proxy_async_global();
+                                    post(pend);
+                                }
+                                if (ch == nchunks - 1) {
+                                    bulk_wait0();
+                                    fence_proxy_async_global();
+                                    post(cur);
+                                    pend_set = false;
+                                } else {
+                                    pend = cur;
+                                    pend_set = true;
+                                }
+                            }
                         }
                     }
                 }
             }
         }
+        if (kOrd && issuer) post(reinterpret_cast<uint32_t *>(uintptr_t(lane == 0)));  // the publisher may exit
         if (issuer) bulk_wait0();
     }
 #undef NSA_PIECE_DECODE
@@ -681,7 +773,7 @@ cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, 
         if (!encode(&prm.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dqacc, dims, strides, box))
             return cudaErrorInvalidValue;
         prm.tm_dqpart = prm.tm_dq;
-        if (whole) {  // fp32 partials: rows (token, kv head, slot, head of group) x d
+        if (whole && a.deterministic == 1) {  // fp32 partials: rows (token, kv head, slot, head of group) x d
             cuuint64_t pdims[2] = {cuuint64_t(kD), cuuint64_t(a.t1 * a.n1 * a.cnt)};
             if (!encode(&prm.tm_dqpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dqpart, pdims, strides, box))
                 return cudaErrorInvalidValue;
@@ -689,14 +781,18 @@ cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, 
     }
     const dim3 grid = dim3(unsigned(nsa_sm_count()));
     if (!forward) {
-        auto k = a.dtype == ATTN_F16 ? nsa_tc_kernel<__half, kBwd> : nsa_tc_kernel<__nv_bfloat16, kBwd>;
+        // ordered deterministic mode: a CTA waits for adds other CTAs make, so all of them must be resident
+        // (a cooperative launch), and a 15th warp publishes the counts
+        const bool ord = a.deterministic == 2;
+        auto k = ord ? (a.dtype == ATTN_F16 ? nsa_tc_kernel<__half, kBwd, true> : nsa_tc_kernel<__nv_bfloat16, kBwd, true>)
+                     : (a.dtype == ATTN_F16 ? nsa_tc_kernel<__half, kBwd, false> : nsa_tc_kernel<__nv_bfloat16, kBwd, false>);
         if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, NsaCfg::SMEM_ALLOC)) != cudaSuccess)
             return e;
-        return launch_kernel(k, grid, dim3(NsaCfg::THREADS), NsaCfg::SMEM_ALLOC, s, true, prm, g);
+        return launch_kernel_ex(k, grid, dim3(NsaCfg::THREADS + (ord ? 32 : 0)), NsaCfg::SMEM_ALLOC, s, true, ord, prm, g);
     }
     // forward: the row maxima, then the sums and O, over the same work units
-    auto k1 = a.dtype == ATTN_F16 ? nsa_tc_kernel<__half, kFwdMax> : nsa_tc_kernel<__nv_bfloat16, kFwdMax>;
-    auto k2 = a.dtype == ATTN_F16 ? nsa_tc_kernel<__half, kFwdSum> : nsa_tc_kernel<__nv_bfloat16, kFwdSum>;
+    auto k1 = a.dtype == ATTN_F16 ? nsa_tc_kernel<__half, kFwdMax, false> : nsa_tc_kernel<__nv_bfloat16, kFwdMax, false>;
+    auto k2 = a.dtype == ATTN_F16 ? nsa_tc_kernel<__half, kFwdSum, false> : nsa_tc_kernel<__nv_bfloat16, kFwdSum, false>;
     if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, NsaCfg::SMEM_ALLOC)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, NsaCfg::SMEM_ALLOC)) != cudaSuccess)
         return e;

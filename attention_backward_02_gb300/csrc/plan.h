@@ -64,7 +64,10 @@ struct Workspace {
 //   tokens   int32 [t1 * n2 * cnt]  block lists, ascending token ids
 //   dqacc    f32 [t1_pad][n1][d]
 //   dkacc    f32 [t2][n2][d], dvacc f32 [t2][n2][dv]
-//   dqpart   f32 [t1][n2][cnt][G][d]   deterministic mode: dQ per (token, selected slot)
+//   dqpart   f32 [t1][n2][cnt][G][d]   deterministic mode 1: dQ per (token, selected slot)
+//   sem      uint32 [t1][n2]           deterministic mode 2: dQ adds landed per (token, kv head)
+//   rank     int32 [t1][n2][cnt]       deterministic mode 2: per kept (token, slot), the token's kept
+//                                      blocks above the slot's block (the adds that go before its own)
 struct NsaArgs {
     int dtype;
     int grad_fp32;              // dq, dk, dv are fp32 (else the input dtype)
@@ -72,7 +75,8 @@ struct NsaArgs {
     int64_t t1, t2, t1_pad;
     int64_t nblk_max, words_max, nrows;   // nrows = nseq * n2 * nblk_max
     float scale;
-    int sparse_mode, deterministic, n_part;
+    int sparse_mode, n_part;
+    int deterministic;          // 0: atomic adds; 1: per-slot dQ partials; 2: ordered adds behind counters
     const void *q, *k, *v, *o, *dO;
     const uint8_t *mask;        // attenMaskOptional [..][mask_cols], nonzero = removed (NULL: none)
     int64_t mask_cols;
@@ -87,8 +91,10 @@ struct NsaArgs {
     uint32_t *bitmap;
     int32_t *offsets, *tokens, *pieces;
     float *dqacc, *dkacc, *dvacc, *dqpart;
+    uint32_t *sem;
+    int32_t *rank;
     int64_t piece_tokens;       // tokens per work unit of the tensor-core kernel (whole lists when deterministic)
-    int zero_dq;                // the preprocess also zeroes dqacc (tensor-core path, atomic dQ)
+    int zero_dq;                // the preprocess also zeroes dqacc (tensor-core path, one dQ accumulator)
 };
 
 // Maps a CUDA error to ATTN_ERR_CUDA and keeps its text for attn_last_error

@@ -240,6 +240,7 @@ __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Waits until at most two bulk groups of this thread are pending (the older ones have completed).
 __device__ __forceinline__ void bulk_wait2() { asm volatile("cp.async.bulk.wait_group 2;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait4() { asm volatile("cp.async.bulk.wait_group 4;" ::: "memory"); }
 
 // Brings a tile of a 4-D tensor into L2 ahead of its load (no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3)

@@ -604,7 +604,7 @@ def extra_workloads(args, flush, stream, lib, peak, steps=10, warmup=3):
     import torch
     out = {}
     # dQ modes: False atomic, True split partial buffers (NSA: per-slot partials), 2 ordered single buffer
-    for idx, det in ((2, False), (2, True), (2, 2), (3, False), (3, 2), (4, False), (4, True)):
+    for idx, det in ((2, False), (2, True), (2, 2), (3, False), (3, 2), (4, False), (4, True), (4, 2)):
         if idx == args.workload and det is False:
             continue
         p, flops, cfg = workload_info(idx)

@@ -200,8 +200,15 @@ typedef struct {
     int64_t block_count;    /* selectedBlockCount in [1, 128], count*size < 8192 */
     int sparse_mode;        /* 0: only the selection; 2: also causal,
                                bottom-right aligned per sequence              */
-    int deterministic;      /* 1: bitwise reproducible dQ, dK, dV; needs
-                               d = d_v = 128 (ATTN_ERR_UNSUPPORTED otherwise) */
+    int deterministic;      /* bitwise reproducible dQ, dK, dV, needing
+                               d = d_v = 128 (ATTN_ERR_UNSUPPORTED otherwise):
+                               0 off; 1 dQ per (token, selected slot) in the
+                               workspace, summed in slot order (T1 n1
+                               block_count d 4 bytes); 2 one dQ accumulator
+                               whose adds for a token go in decreasing block
+                               order behind a counter per (token, kv head)
+                               (T1 n2 (block_count + 1) 4 bytes; a
+                               cooperative launch)                            */
     int64_t d_v;            /* head dim of v, O, dO and dv: 128 or 192; 0 means
                                d ([Ascend] Constraints: D is 192 or 128, and K
                                and V may differ)                              */

@@ -120,10 +120,26 @@ def _nsa(ab, **kw):
     (dict(sparse_mode=1), 2), (dict(d=64), 2), (dict(d=192), 0), (dict(d_v=192), 0), (dict(d=192, d_v=128), 0),
     (dict(d_v=64), 2), (dict(grad_fp32=True), 0),
     (dict(cu_seqlens_kv=[4000, 8192]), 2), (dict(cu_seqlens_kv=[512, 1024], block_count=16), 2),
+    (dict(deterministic=2), 0), (dict(deterministic=3), 2), (dict(deterministic=-1), 2),
 ])
 def test_nsa_descriptor_rejections(ab, kw, code):
     n = C.c_size_t()
     assert ab._lib.load().nsa_workspace_size(C.byref(_nsa(ab, **kw)), C.byref(n)) == code
+
+
+def test_nsa_ordered_workspace(ab):
+    """Deterministic NSA modes: per-slot dQ partials (T1 n1 block_count d fp32) against one add counter per
+    (token, kv head) (T1 n2 uint32) and an int32 per (token, kv head, slot) beside the single dQ
+    accumulator."""
+    lib = ab._lib.load()
+    plain, split, ordered = C.c_size_t(), C.c_size_t(), C.c_size_t()
+    assert lib.nsa_workspace_size(C.byref(_nsa(ab)), C.byref(plain)) == 0
+    assert lib.nsa_workspace_size(C.byref(_nsa(ab, deterministic=1)), C.byref(split)) == 0
+    assert lib.nsa_workspace_size(C.byref(_nsa(ab, deterministic=2)), C.byref(ordered)) == 0
+    t1, n1, n2, cnt, d = 8192, 16, 1, 16, 128
+    align = lambda x: (x + 255) // 256 * 256
+    assert split.value == plain.value + align(t1 * n1 * cnt * d * 4)
+    assert ordered.value == plain.value + align(t1 * n2 * 4) + align(t1 * n2 * cnt * 4)
 
 
 def test_nsa_fwd_workspace_size(ab):

@@ -157,3 +157,44 @@ def test_workload4_deterministic_bitwise():
     second = H.run_gpu_nsa(p, o_bits, mx, sm, deterministic=True)
     for a, b in zip(first, second):
         np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------------ ordered deterministic mode (deterministic = 2)
+
+def _two_runs_same_bits(p, mode):
+    first = _parity(p, deterministic=mode)
+    o_bits, mx, sm = H.nsa_oracle_inputs(p)
+    second = H.run_gpu_nsa(p, o_bits, mx, sm, mode)
+    for a, b in zip(first, second):
+        np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("sparse_mode", [0, 2])
+@pytest.mark.parametrize("n1,n2", [(16, 2), (16, 1), (32, 1)])
+def test_ordered_parity_and_bitwise(sparse_mode, n1, n2):
+    """One dQ accumulator whose adds for a token go in decreasing block order behind a counter per
+    (token, kv head): oracle parity and the same bits from two calls."""
+    _two_runs_same_bits(_small(sparse_mode, seed=41 + sparse_mode, n1=n1, n2=n2), 2)
+
+
+@pytest.mark.parametrize("n1,n2", [(8, 2), (3, 1), (12, 1), (20, 2)])
+def test_ordered_padded_groups(n1, n2):
+    _two_runs_same_bits(_small(2, seed=52 + n1, n1=n1, n2=n2), 2)
+
+
+def test_ordered_bad_indices_flagged():
+    """An index out of range and a repeat are dropped by the block lists; the count of blocks a token waits
+    for must drop them too, or the waits would run out."""
+    import attention_backward_02_gb300 as ab
+    p = _small(2, seed=4)
+    bad = p.topk.copy()
+    bad[5, 0, 1] = 1000
+    bad[7, 1, 2] = bad[7, 1, 0]
+    o_bits, mx, sm = H.nsa_oracle_inputs(p)
+    H.run_gpu_nsa(p, o_bits, mx, sm, 2, topk=bad,
+                  expect_flags=ab._lib.ATTN_DEV_INDEX_RANGE | ab._lib.ATTN_DEV_INDEX_DUP)
+
+
+def test_workload4_ordered_bitwise():
+    """4 x 4096 tokens, 16 / 1 heads, d128, 16 blocks of 64, sparse mode 2: every element, two calls."""
+    _two_runs_same_bits(synth.workload(4), 2)

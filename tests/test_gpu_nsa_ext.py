@@ -75,7 +75,7 @@ def _bwd_parity(p, grad_fp32=False, deterministic=False):
 
 
 @pytest.mark.parametrize("n1,n2", [(16, 2), (4, 1)])
-@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("deterministic", [False, True, 2])
 def test_nsa_backward_fp32_gradients(n1, n2, deterministic):
     """fp32 dq / dk / dv on the tensor-core kernel: a full head group (16 / 2) and a padded one (4 / 1)."""
     p = _problem(2, n1=n1, n2=n2, seed=60 + n1)
@@ -96,12 +96,13 @@ def test_nsa_backward_unequal_dims_fp32():
     _bwd_parity(p, grad_fp32=True)
 
 
-def test_nsa_unequal_dims_deterministic_refused():
+@pytest.mark.parametrize("mode", [True, 2])
+def test_nsa_unequal_dims_deterministic_refused(mode):
     import attention_backward_02_gb300 as ab
     p = _problem(0, n1=16, n2=2, d=192, d_v=128, seed=81)
     o_bits, mx, sm = H.nsa_oracle_inputs(p)
     with pytest.raises(ab.AttnError) as e:
-        H.run_gpu_nsa(p, o_bits, mx, sm, deterministic=True)
+        H.run_gpu_nsa(p, o_bits, mx, sm, deterministic=mode)
     assert e.value.status == ab._lib.ATTN_ERR_UNSUPPORTED
 
 
@@ -129,6 +130,7 @@ def test_nsa_forward_with_mask(sparse_mode, n1, n2):
 @pytest.mark.parametrize("sparse_mode", [0, 2])
 @pytest.mark.parametrize("n1,n2,d,d_v,deterministic", [(16, 2, 128, 128, False), (4, 1, 128, 128, False),
                                                        (16, 2, 128, 128, True), (5, 1, 128, 128, True),
+                                                       (16, 2, 128, 128, 2), (5, 1, 128, 128, 2),
                                                        (8, 2, 192, 128, False)])
 def test_nsa_backward_with_mask(sparse_mode, n1, n2, d, d_v, deterministic):
     """The mask per element: on the tensor-core kernel (d = d_v = 128, both dQ modes, head groups of
