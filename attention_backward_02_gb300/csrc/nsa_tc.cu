@@ -43,6 +43,16 @@
 // per lane group split the columns) and the piece's dK / dV, warps 10..13 the
 // dQ of each chunk (TMEM -> its stage -> reduce), so the element-wise warps go
 // straight on to the next chunk.  Bounded waits as in the dense kernel.
+// Deterministic modes take whole block lists as work units (one writer per
+// dK / dV row).  Mode 1 stores each (token, slot)'s dQ rows for a finalize to
+// sum in slot order.  Mode 2 (kOrd) adds into the one accumulator in decreasing
+// block order per token: before its first add for a token the issuer lane
+// waits until the token's counter equals the number of its kept blocks above
+// this one (worked out with the block lists), and once the adds have landed
+// (one chunk later, at once for a unit's last chunk) a 15th warp increments
+// the counters with GPU-scope releases.  Units go to the CTAs in decreasing
+// block order, so every wait is for a higher block and none can close a cycle;
+// the launch is cooperative, so every CTA is resident.
 #include <cudaTypedefs.h>
 
 #include <climits>
