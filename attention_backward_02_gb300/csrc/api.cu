@@ -356,7 +356,7 @@ attn_status_t check_nsa_desc(const attn_nsa_desc_t *d, NsaShape *sh)
 }
 
 struct NsaLayout {
-    size_t status, lse2, dvec, bitmap, offsets, pieces, tokens, dqacc, dkacc, dvacc, dqpart, sem, rank, total;
+    size_t status, lse2, dvec, bitmap, offsets, pieces, tokens, dqacc, dkacc, dvacc, dqpart, sem, rank, kvpart, total;
     int64_t t1_pad, nrows;
 };
 
@@ -384,7 +384,13 @@ NsaLayout nsa_layout(const attn_nsa_desc_t *d, const NsaShape &sh)
     L.sem = L.dqpart + Workspace::align(part_bytes);
     const bool ord = d->deterministic == 2;
     L.rank = L.sem + (ord ? Workspace::align(size_t(sh.t1) * size_t(d->n2) * sizeof(uint32_t)) : 0);
-    L.total = L.rank + (ord ? Workspace::align(size_t(sh.t1) * size_t(d->n2 * d->block_count) * sizeof(int32_t)) : 0);
+    L.kvpart = L.rank + (ord ? Workspace::align(size_t(sh.t1) * size_t(d->n2 * d->block_count) * sizeof(int32_t)) : 0);
+    // deterministic mode 1: each work unit's dK / dV rows (block_size keys x (d + d_v) fp32)
+    const size_t kv_bytes = d->deterministic == 1 ? size_t(nsa_max_pieces(L.nrows, sh.t1, d->n2, d->block_count,
+                                                                           d->n1 / d->n2)) *
+                                                        size_t(d->block_size) * size_t(d->d + sh.dv) * sizeof(float)
+                                                  : 0;
+    L.total = L.kvpart + Workspace::align(kv_bytes);
     return L;
 }
 
@@ -424,6 +430,7 @@ void nsa_ws_pointers(NsaArgs *a, const NsaLayout &L, void *workspace)
     a->dqpart = reinterpret_cast<float *>(ws + L.dqpart);
     a->sem = reinterpret_cast<uint32_t *>(ws + L.sem);
     a->rank = reinterpret_cast<int32_t *>(ws + L.rank);
+    a->kvpart = reinterpret_cast<float *>(ws + L.kvpart);
 }
 
 }  // namespace
@@ -487,6 +494,7 @@ attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, 
     a.dqpart = reinterpret_cast<float *>(ws + L.dqpart);
     a.sem = reinterpret_cast<uint32_t *>(ws + L.sem);
     a.rank = reinterpret_cast<int32_t *>(ws + L.rank);
+    a.kvpart = reinterpret_cast<float *>(ws + L.kvpart);
     // the CUDA-core kernel (a head dim of 192) adds dK / dV atomically from many blocks
     if (a.deterministic && !nsa_tc_supported(a)) return ATTN_ERR_UNSUPPORTED;
     static thread_local PackedGeo pg;

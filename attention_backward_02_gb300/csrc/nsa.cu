@@ -565,6 +565,30 @@ __global__ void nsa_dq_finalize_det_kernel(NsaArgs a, PackedGeo geo, int with_kv
     if (with_kv) convert_dkdv4<OutT>(a);  // dK / dV in the same launch
 }
 
+// Deterministic mode 1: each block's dK / dV rows are the sum of its pieces' rows, taken in piece
+// order (one thread per block-list row, key and 4 of the d + d_v columns).
+__global__ void __launch_bounds__(256) nsa_kv_sum_kernel(NsaArgs a, PackedGeo geo)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int64_t w = (a.d + a.dv) / 4;
+    const int64_t n = a.nrows * a.bs * w;
+    for (int64_t x = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; x < n; x += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t row = x / (a.bs * w), key = (x / w) % a.bs, c4 = x % w;
+        const int32_t p0 = a.pieces[row], p1 = a.pieces[row + 1];
+        if (p0 == p1) continue;  // no token selected the block: its rows stay zero
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int32_t pc = p0; pc < p1; ++pc) {
+            const float4 v = reinterpret_cast<const float4 *>(a.kvpart + (int64_t(pc) * a.bs + key) * (a.d + a.dv))[c4];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        const int64_t b = row / (a.n2 * a.nblk_max), g = (row / a.nblk_max) % a.n2, blk = row % a.nblk_max;
+        const int64_t krow = (geo.cu_kv[b] + blk * a.bs + key) * a.n2 + g;
+        float *dst = c4 < a.d / 4 ? a.dkacc + krow * a.d + c4 * 4 : a.dvacc + krow * a.dv + (c4 - a.d / 4) * 4;
+        *reinterpret_cast<float4 *>(dst) = acc;
+    }
+}
+
 template <class OutT>
 __global__ void nsa_finalize_kernel(NsaArgs a)
 {
@@ -632,6 +656,9 @@ cudaError_t run_nsa(const NsaArgs &a0, const PackedGeo &g, cudaStream_t s, cudaE
         if (before && (e = cudaEventRecord(before, s)) != cudaSuccess) return e;
         if ((e = launch_nsa_tc(a, g, s)) != cudaSuccess) return e;
         if (after && (e = cudaEventRecord(after, s)) != cudaSuccess) return e;
+        if (a.t1 > 0 && a.deterministic == 1 &&
+            (e = launch_kernel(nsa_kv_sum_kernel, dim3(1024), dim3(256), 0, s, true, a, g)) != cudaSuccess)
+            return e;
         // the dQ finalize converts dK / dV too
         if (a.t1 > 0 && a.deterministic == 1)
             e = launch_kernel(nsa_dq_finalize_det_kernel<OutT>, dim3(1024), dim3(256), 0, s, true, a, g, 1);

@@ -43,16 +43,18 @@
 // per lane group split the columns) and the piece's dK / dV, warps 10..13 the
 // dQ of each chunk (TMEM -> its stage -> reduce), so the element-wise warps go
 // straight on to the next chunk.  Bounded waits as in the dense kernel.
-// Deterministic modes take whole block lists as work units (one writer per
-// dK / dV row).  Mode 1 stores each (token, slot)'s dQ rows for a finalize to
-// sum in slot order.  Mode 2 (kOrd) adds into the one accumulator in decreasing
-// block order per token: before its first add for a token the issuer lane
-// waits until the token's counter equals the number of its kept blocks above
-// this one (worked out with the block lists), and once the adds have landed
-// (one chunk later, at once for a unit's last chunk) a 15th warp increments
-// the counters with GPU-scope releases.  Units go to the CTAs in decreasing
-// block order, so every wait is for a higher block and none can close a cycle;
-// the launch is cooperative, so every CTA is resident.
+// Deterministic mode 1 stores each piece's dK / dV rows for a kernel that sums
+// them per block in piece order (in place of the fp32 atomics), and each
+// (token, slot)'s dQ rows for a finalize to sum in slot order.  Mode 2 (kOrd)
+// takes whole block lists as work units (one writer per dK / dV row) and adds
+// dQ into the one accumulator in decreasing block order per token:
+// before its first add for a token the issuer lane waits until the token's
+// counter equals the number of its kept blocks above this one (worked out with
+// the block lists), and once the adds have landed (one chunk later, at once
+// for a piece's last chunk) a 15th warp increments the counters with
+// GPU-scope releases.  Pieces go to the CTAs in decreasing block order, so
+// every wait is for a higher block and none can close a cycle; the launch is
+// cooperative, so every CTA is resident.
 #include <cudaTypedefs.h>
 
 #include <climits>
@@ -79,7 +81,7 @@ __device__ __forceinline__ int32_t ord_f32(float x)
     return b >= 0 ? b : b ^ 0x7FFFFFFF;
 }
 __device__ __forceinline__ float unord_f32(int32_t v) { return __int_as_float(v >= 0 ? v : v ^ 0x7FFFFFFF); }
-constexpr int kPieceChunks = 32;  // chunks per work unit at most
+constexpr int kPieceChunks = kNsaPieceChunks;  // chunks per work unit at most
 
 struct NsaCfg {
     static constexpr int KV_BYTES = kBS * kD * 2;       // 16 KB
@@ -162,11 +164,10 @@ __global__ void __launch_bounds__(kOrd ? 480 : 448, 1)
     }
     pdl_wait();     // statistics, block lists, pieces and the zeroed accumulators are ready
     pdl_trigger();  // the finalize kernels may start launching; they wait for this grid
+    // Work units: the pieces, in block-list row order; in the ordered mode the rows go in decreasing block
+    // order (then sequence and kv head; a.pieces is scanned in that order), so each CTA's units have
+    // non-increasing blocks, every wait is for a higher block, and no cycle of waits can form.
     const int64_t n_pieces = a.pieces[a.nrows];
-    // Work units: the pieces, in block-list row order.  Ordered mode (whole block lists): every row, in
-    // decreasing block order (then sequence and kv head), empty rows skipped; so each CTA's rows have
-    // decreasing blocks, every wait is for a higher block, and no cycle of waits can form.
-    const int64_t n_units = kOrd ? a.nrows : n_pieces;
 
     if (threadIdx.x == 0) {
         *abort = 0;
@@ -202,17 +203,15 @@ __global__ void __launch_bounds__(kOrd ? 480 : 448, 1)
 
     // the work unit of piece pc: block-list row, token range, sequence / head / block
 #define NSA_PIECE_DECODE                                                                         \
-    const int64_t nbg = a.nseq * a.n2;                                                          \
-    const int64_t row = kOrd ? (pc % nbg) * a.nblk_max + (a.nblk_max - 1 - pc / nbg)          \
-                             : piece_row(a.pieces, a.nrows, pc);                                \
-    const int64_t lp = kOrd ? 0 : pc - a.pieces[row];                                          \
+    const int64_t qrow_ = piece_row(a.pieces, a.nrows, pc);                                     \
+    const int64_t row = kOrd ? nsa_ord_row(a, qrow_) : qrow_;                                       \
+    const int64_t lp = pc - a.pieces[qrow_];                                                    \
     const int64_t tok_begin = a.offsets[row] + lp * a.piece_tokens;                            \
     const int64_t tok_end_full = a.offsets[row + 1];                                            \
     const int64_t tok_end = tok_begin + a.piece_tokens < tok_end_full ? tok_begin + a.piece_tokens : tok_end_full; \
     const int nchunks = int((tok_end - tok_begin + tpc - 1) / tpc);                            \
     const int64_t b = row / (a.n2 * a.nblk_max), g = (row / a.nblk_max) % a.n2, blk = row % a.nblk_max; \
-    (void)b; (void)g; (void)blk; (void)nchunks;                                                 \
-    if (kOrd && nchunks == 0) continue;
+    (void)b; (void)g; (void)blk; (void)nchunks;
 
     if (warp == 0) {
         // ================================================= TMA producer (the whole warp: lane u
@@ -223,7 +222,7 @@ __global__ void __launch_bounds__(kOrd ? 480 : 448, 1)
             }
             bool ok = true;
             int64_t kt = 0, ci = 0, q_armed = 0, kv_armed = 0;
-            for (int64_t pc = blockIdx.x; pc < n_units; pc += gridDim.x) {
+            for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
                 NSA_PIECE_DECODE
                 if (kt > 0 && ok && !(ok = mbar_wait(kv_empty, uint32_t(kt - 1) & 1, abort))) flag_abort(abort, a.status);
                 ok = __all_sync(0xffffffffu, ok);
@@ -312,7 +311,7 @@ __global__ void __launch_bounds__(kOrd ? 480 : 448, 1)
             const uint64_t kP = desc_kmaj(smem_u32(sP), kRows, 0), mV = desc_mn(smem_u32(sV), kBS, 0);
             bool ok = true;
             int64_t kt = 0, ci = 0;
-            for (int64_t pc = blockIdx.x; pc < n_units; pc += gridDim.x) {
+            for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
                 NSA_PIECE_DECODE
                 if (ok && !(ok = mbar_wait(kv_full, uint32_t(kt) & 1, abort))) flag_abort(abort, a.status);
                 tc_fence_after();
@@ -383,7 +382,7 @@ __global__ void __launch_bounds__(kOrd ? 480 : 448, 1)
         const uint32_t aP = smem_u32(sP), adS = smem_u32(sdS);
         bool ok = true;
         int64_t kt = 0, ci = 0;
-        for (int64_t pc = blockIdx.x; pc < n_units; pc += gridDim.x) {
+        for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
             NSA_PIECE_DECODE
             const int64_t shift = geo.kv_len(b) - geo.q_len(b);
             for (int ch = 0; ch < nchunks; ++ch, ++ci) {
@@ -499,12 +498,21 @@ __global__ void __launch_bounds__(kOrd ? 480 : 448, 1)
                 tmem_ld32(tmem + lane_addr + Cfg::T_DV + half * 32, vv);
                 tmem_ld32(tmem + lane_addr + Cfg::T_DK + half * 32, kk);
                 tmem_ld_wait();
-                const int64_t key0 = geo.cu_kv[b] + blk * kBS + half * 32;
+                if (a.deterministic == 1) {  // this piece's rows, summed per block in piece order afterwards
+                    float *dst = a.kvpart + (pc * kBS + half * 32) * (2 * kD) + r;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int64_t off = ((key0 + e) * a.n2 + g) * kD + r;
-                    atomicAdd(a.dvacc + off, __uint_as_float(vv[e]));
-                    atomicAdd(a.dkacc + off, __uint_as_float(kk[e]) * a.scale);
+                    for (int e = 0; e < 32; ++e) {
+                        dst[e * 2 * kD] = __uint_as_float(kk[e]) * a.scale;
+                        dst[e * 2 * kD + kD] = __uint_as_float(vv[e]);
+                    }
+                } else {
+                    const int64_t key0 = geo.cu_kv[b] + blk * kBS + half * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int64_t off = ((key0 + e) * a.n2 + g) * kD + r;
+                        atomicAdd(a.dvacc + off, __uint_as_float(vv[e]));
+                        atomicAdd(a.dkacc + off, __uint_as_float(kk[e]) * a.scale);
+                    }
                 }
             }
             tc_fence_before();
@@ -558,7 +566,7 @@ __global__ void __launch_bounds__(kOrd ? 480 : 448, 1)
             }
             ++n_post;
         };
-        for (int64_t pc = blockIdx.x; pc < n_units; pc += gridDim.x) {
+        for (int64_t pc = blockIdx.x; pc < n_pieces; pc += gridDim.x) {
             NSA_PIECE_DECODE
             for (int ch = 0; ch < nchunks; ++ch, ++ci) {
                 const int rs = int(ci % kSlotRing);
@@ -715,8 +723,9 @@ __global__ void __launch_bounds__(1024) nsa_piece_scan_kernel(NsaArgs a)
     const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
     if (threadIdx.x == 0) a.pieces[0] = 0;
     for (int64_t base = 0; base < a.nrows; base += 1024) {
-        const int64_t r = base + threadIdx.x;
-        const int32_t len = r < a.nrows ? a.offsets[r + 1] - a.offsets[r] : 0;
+        const int64_t r = base + threadIdx.x;  // position; the ordered mode takes the rows in its own order
+        const int64_t rr = r < a.nrows && a.deterministic == 2 ? nsa_ord_row(a, r) : r;
+        const int32_t len = r < a.nrows ? a.offsets[rr + 1] - a.offsets[rr] : 0;
         int32_t v = (len + per_piece - 1) / per_piece;
         for (int off = 1; off < 32; off <<= 1) {
             int32_t u = __shfl_up_sync(0xffffffffu, v, off);
@@ -754,9 +763,11 @@ cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, 
     NsaTcParams prm;
     prm.a = a;
     const int G = int(a.n1 / a.n2);
-    // deterministic: a whole block list per work unit, so every dK / dV element has one writer
-    const bool whole = a.deterministic && !forward;
-    prm.a.piece_tokens = whole ? (int64_t(1) << 30) : int64_t(kPieceChunks) * (kRows / ((G + 7) / 8 * 8));
+    // The block lists are split into pieces, except in the ordered mode, which takes each whole (one
+    // writer per dK / dV row; split, the pieces of a block run beside those of the blocks above it and
+    // wait on them: 1.86 against 1.30 ms at 4 x 4096 tokens).  Mode 1 stores each piece's dK / dV rows
+    // for a sum in piece order.
+    prm.a.piece_tokens = a.deterministic == 2 && !forward ? (int64_t(1) << 30) : nsa_piece_tokens(G);
     cudaError_t e = launch_kernel(nsa_piece_scan_kernel, dim3(1), dim3(1024), 0, s, true, prm.a);
     if (e != cudaSuccess) return e;
     if (a.t1 == 0) return cudaSuccess;
@@ -783,7 +794,7 @@ cudaError_t launch_nsa_tc(const NsaArgs &a, const PackedGeo &g, cudaStream_t s, 
         if (!encode(&prm.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dqacc, dims, strides, box))
             return cudaErrorInvalidValue;
         prm.tm_dqpart = prm.tm_dq;
-        if (whole && a.deterministic == 1) {  // fp32 partials: rows (token, kv head, slot, head of group) x d
+        if (!forward && a.deterministic == 1) {  // fp32 partials: rows (token, kv head, slot, head of group) x d
             cuuint64_t pdims[2] = {cuuint64_t(kD), cuuint64_t(a.t1 * a.n1 * a.cnt)};
             if (!encode(&prm.tm_dqpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dqpart, pdims, strides, box))
                 return cudaErrorInvalidValue;

@@ -68,6 +68,19 @@ struct Workspace {
 //   sem      uint32 [t1][n2]           deterministic mode 2: dQ adds landed per (token, kv head)
 //   rank     int32 [t1][n2][cnt]       deterministic mode 2: per kept (token, slot), the token's kept
 //                                      blocks above the slot's block (the adds that go before its own)
+//   kvpart   f32 [pieces][bs][dK d | dV dv]   deterministic mode 1: each piece's dK / dV rows, summed
+//                                      per block in piece order
+// Chunks of 128 rows per work unit ("piece") of the tensor-core NSA kernel, and the most units a call
+// can have: every block-list row's tokens in pieces of kNsaPieceChunks chunks of 128 / R tokens
+// (R = 8 ceil(G / 8) rows per token).
+constexpr int kNsaPieceChunks = 32;
+inline int64_t nsa_piece_tokens(int64_t G) { return int64_t(kNsaPieceChunks) * (128 / ((G + 7) / 8 * 8)); }
+inline int64_t nsa_max_pieces(int64_t nrows, int64_t t1, int64_t n2, int64_t cnt, int64_t G)
+{
+    const int64_t pt = nsa_piece_tokens(G);
+    return nrows + (t1 * n2 * cnt + pt - 1) / pt;
+}
+
 struct NsaArgs {
     int dtype;
     int grad_fp32;              // dq, dk, dv are fp32 (else the input dtype)
@@ -93,9 +106,18 @@ struct NsaArgs {
     float *dqacc, *dkacc, *dvacc, *dqpart;
     uint32_t *sem;
     int32_t *rank;
+    float *kvpart;
     int64_t piece_tokens;       // tokens per work unit of the tensor-core kernel (whole lists when deterministic)
     int zero_dq;                // the preprocess also zeroes dqacc (tensor-core path, one dQ accumulator)
 };
+
+// Ordered deterministic NSA mode: the block-list rows in decreasing block order (then sequence and kv
+// head); the row at position q.
+__host__ __device__ inline int64_t nsa_ord_row(const NsaArgs &a, int64_t q)
+{
+    const int64_t nbg = a.nseq * a.n2;
+    return (q % nbg) * a.nblk_max + (a.nblk_max - 1 - q / nbg);
+}
 
 // Maps a CUDA error to ATTN_ERR_CUDA and keeps its text for attn_last_error
 // (this host thread); cudaSuccess maps to ATTN_OK.

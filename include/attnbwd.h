@@ -204,7 +204,8 @@ typedef struct {
                                d = d_v = 128 (ATTN_ERR_UNSUPPORTED otherwise):
                                0 off; 1 dQ per (token, selected slot) in the
                                workspace, summed in slot order (T1 n1
-                               block_count d 4 bytes); 2 one dQ accumulator
+                               block_count d 4 bytes, plus the dK / dV rows of
+                               every work unit); 2 one dQ accumulator
                                whose adds for a token go in decreasing block
                                order behind a counter per (token, kv head)
                                (T1 n2 (block_count + 1) 4 bytes; a

@@ -130,15 +130,19 @@ def test_nsa_descriptor_rejections(ab, kw, code):
 def test_nsa_ordered_workspace(ab):
     """Deterministic NSA modes: per-slot dQ partials (T1 n1 block_count d fp32) against one add counter per
     (token, kv head) (T1 n2 uint32) and an int32 per (token, kv head, slot) beside the single dQ
-    accumulator."""
+    accumulator; the first also keeps each work unit's dK / dV rows (block_size keys x (d + d_v) fp32) for
+    a sum in unit order, for at most one unit per block-list row plus one per 32 chunks of 128 / R
+    tokens."""
     lib = ab._lib.load()
     plain, split, ordered = C.c_size_t(), C.c_size_t(), C.c_size_t()
     assert lib.nsa_workspace_size(C.byref(_nsa(ab)), C.byref(plain)) == 0
     assert lib.nsa_workspace_size(C.byref(_nsa(ab, deterministic=1)), C.byref(split)) == 0
     assert lib.nsa_workspace_size(C.byref(_nsa(ab, deterministic=2)), C.byref(ordered)) == 0
-    t1, n1, n2, cnt, d = 8192, 16, 1, 16, 128
+    t1, n1, n2, cnt, d, bs, nrows = 8192, 16, 1, 16, 128, 64, 2 * 1 * 64
     align = lambda x: (x + 255) // 256 * 256
-    assert split.value == plain.value + align(t1 * n1 * cnt * d * 4)
+    tokens_per_unit = 32 * (128 // 16)  # G = 16: rows per token R = 16
+    kv = align((nrows + -(-t1 * n2 * cnt // tokens_per_unit)) * bs * 2 * d * 4)
+    assert split.value == plain.value + align(t1 * n1 * cnt * d * 4) + kv
     assert ordered.value == plain.value + align(t1 * n2 * 4) + align(t1 * n2 * cnt * 4)
 
 
