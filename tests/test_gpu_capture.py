@@ -89,3 +89,46 @@ def test_forward_replayed_from_a_cuda_graph():
     torch.cuda.synchronize()
     np.testing.assert_array_equal(H.gpu_to_f64(o), o_direct)  # one writer per element: the same bits
     np.testing.assert_array_equal(lse.cpu().numpy(), lse_direct)
+
+
+@pytest.mark.parametrize("mode", [False, True, 2])
+def test_nsa_backward_replayed_from_a_cuda_graph(mode):
+    """nsa_selected_attn_bwd captured in a CUDA graph (the ordered mode's cooperative launch becomes a graph
+    node too): the replay gives the direct call's bits in the deterministic modes and oracle parity in all."""
+    import torch
+    import attention_backward_02_gb300 as ab
+    p = synth.nsa_problem("graph_nsa", dtype=synth.BF16, lens_q=[300, 129], lens_kv=[512, 256], n1=16, n2=2,
+                          d=128, block_size=64, block_count=4, sparse_mode=2, seed=63)
+    o_bits, mx, sm = H.nsa_oracle_inputs(p)
+    q, k, v, do, o = (H.bits_to_gpu(x, p.dtype) for x in (p.q, p.k, p.v, p.do, o_bits))
+    mx8 = torch.from_numpy(np.repeat(mx[..., None], 8, -1).astype(np.float32)).cuda()
+    sm8 = torch.from_numpy(np.repeat(sm[..., None], 8, -1).astype(np.float32)).cuda()
+    tk = torch.from_numpy(np.ascontiguousarray(p.topk, np.int32)).cuda()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    desc = H.nsa_desc(p, mode)
+    ws = torch.empty(ab.nsa_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        ab.nsa_selected_attn_bwd(desc, q, k, v, o, do, mx8, sm8, tk, dq, dk, dv, workspace=ws)
+    torch.cuda.synchronize()
+    direct = [H.gpu_to_f64(t) for t in (dq, dk, dv)]
+    assert ab.attn_query_status(ws) == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        ab.nsa_selected_attn_bwd(desc, q, k, v, o, do, mx8, sm8, tk, dq, dk, dv, workspace=ws)
+    for t in (dq, dk, dv):
+        t.fill_(float("nan"))
+    torch.cuda.synchronize()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert ab.attn_query_status(ws) == 0
+    replayed = [H.gpu_to_f64(t) for t in (dq, dk, dv)]
+    ref = oracle.nsa_bwd(p.f64("q"), p.f64("k"), p.f64("v"), synth.bits_to_f64(o_bits, p.dtype), p.f64("do"),
+                         mx.astype(np.float64), sm.astype(np.float64), p.topk, p.cu_q, p.cu_kv, p.scale,
+                         p.block_size, p.sparse_mode)
+    for name, a, b, r in zip(("dQ", "dK", "dV"), direct, replayed, ref):
+        if mode:
+            np.testing.assert_array_equal(a, b)
+        H.assert_close(b, r, name)
