@@ -60,3 +60,27 @@ def test_backward_while_other_work_holds_some_sms(mode):
     torch.cuda.synchronize()
     for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         H.assert_close(g, r, name)
+
+
+@pytest.mark.parametrize("mode", [False, 2])
+def test_nsa_backward_while_other_work_holds_some_sms(mode):
+    """The NSA backward beside a kernel that holds 8 SMs for 1.5 s: atomic dQ (no block waits for another)
+    and the ordered deterministic mode (blocks wait for other blocks' adds; a cooperative launch) both
+    complete with oracle parity and a clean status."""
+    import torch
+    import attention_backward_02_gb300 as ab
+    lib = ab._lib.load()
+    p = synth.nsa_problem("shared_gpu_nsa", dtype=synth.BF16, lens_q=[1024, 700], lens_kv=[1024, 768], n1=16,
+                          n2=2, d=128, block_size=64, block_count=6, sparse_mode=2, seed=44)
+    o_bits, mx, sm = H.nsa_oracle_inputs(p)
+    ref = oracle.nsa_bwd(p.f64("q"), p.f64("k"), p.f64("v"), synth.bits_to_f64(o_bits, p.dtype), p.f64("do"),
+                         mx.astype(np.float64), sm.astype(np.float64), p.topk, p.cu_q, p.cu_kv, p.scale,
+                         p.block_size, p.sparse_mode)
+    other = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    ab.check(lib.attn_selftest_occupy(8, 120 * 1024, C.c_double(1.5), C.c_void_p(other.cuda_stream)),
+             "attn_selftest_occupy")
+    got = H.run_gpu_nsa(p, o_bits, mx, sm, mode)  # asserts a clean device status
+    torch.cuda.synchronize()
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        H.assert_close(g, r, name)
