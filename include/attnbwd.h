@@ -148,8 +148,10 @@ attn_status_t sdpa_fwd_stats(const attn_sdpa_desc_t *desc, attn_view_t q, attn_v
  * lse as sdpa_fwd_stats writes it.  dQ / dK / dV may have any strides that
  * follow the 16-byte rule (the sample allocates them empty_like the inputs).
  * Outputs have the input dtype, rounded to nearest even.  No block of any
- * kernel waits for another block, so the call is safe next to other work on
- * the device (other streams, other processes).                              */
+ * kernel waits for another block (in ATTN_DQ_ORDERED, blocks wait for one
+ * another under a cooperative launch, which starts once all of them can be
+ * resident), so the call is safe next to other work on the device (other
+ * streams, other processes).                                                */
 attn_status_t sdpa_bwd(const attn_sdpa_desc_t *desc, attn_view_t q, attn_view_t k, attn_view_t v,
                        attn_view_t o, attn_view_t dO, const float *lse, attn_view_t dQ, attn_view_t dK,
                        attn_view_t dV, void *workspace, size_t workspace_bytes, void *stream);
@@ -264,7 +266,9 @@ attn_status_t nsa_workspace_size(const attn_nsa_desc_t *desc, size_t *bytes);
  *   topk : [T1][n2][block_count] int32 block ids local to the token's
  *       sequence, each in [0, S2_b / block_size), distinct per (token, head).
  * Every selected block must lie inside its sequence: S2_b % block_size == 0
- * and S2_b >= block_count * block_size for every sequence.                   */
+ * and S2_b >= block_count * block_size for every sequence.  As for sdpa_bwd,
+ * blocks wait for one another only in deterministic mode 2, under a
+ * cooperative launch.                                                        */
 attn_status_t nsa_selected_attn_bwd(const attn_nsa_desc_t *desc, const void *q, const void *k,
                                     const void *v, const void *o, const void *dO,
                                     const float *softmax_max, const float *softmax_sum,
