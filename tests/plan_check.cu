@@ -52,8 +52,33 @@ PackedGeo packed(const std::vector<int64_t> &lq, const std::vector<int64_t> &lkv
     return g;
 }
 
+// The NSA ordered deterministic mode's unit order (nsa_ord_row): a permutation of the block-list rows in
+// which blocks never increase, so the pieces dealt to a CTA (every grid-th one, in that order) take
+// non-increasing blocks and every wait points to a block above.
+void check_nsa_order(int64_t nseq, int64_t n2, int64_t nblk)
+{
+    NsaArgs a;
+    memset(&a, 0, sizeof a);
+    a.nseq = nseq; a.n2 = n2; a.nblk_max = nblk; a.nrows = nseq * n2 * nblk;
+    std::vector<int> seen(size_t(a.nrows), 0);
+    bool perm = true, mono = true;
+    int64_t prev_blk = INT64_MAX;
+    for (int64_t q = 0; q < a.nrows; ++q) {
+        const int64_t row = nsa_ord_row(a, q);
+        if (row < 0 || row >= a.nrows || seen[size_t(row)]++) perm = false;
+        const int64_t blk = row % nblk;
+        if (blk > prev_blk) mono = false;
+        prev_blk = blk;
+    }
+    printf("nsa_order_%lldx%lldx%lld on 1 perm %d mono %d\n", (long long)nseq, (long long)n2, (long long)nblk,
+           perm ? 1 : 0, mono ? 1 : 0);
+}
+
 int main()
 {
+    check_nsa_order(4, 1, 64);
+    check_nsa_order(3, 2, 17);
+    check_nsa_order(1, 8, 5);
     DenseArgs a;
     for (int mode = 0; mode < 3; ++mode) {  // atomic, split (8 partial buffers), ordered
         const char *tag = mode == 0 ? "atomic" : mode == 1 ? "split" : "ordered";

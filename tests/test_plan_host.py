@@ -2,7 +2,7 @@
 program built with nvcc plans the benchmark shapes and some edge shapes in the atomic, split and
 ordered dQ modes.  Every plan must end, take every unit with work exactly once, and in the ordered
 mode give each CTA its units in non-increasing key-tile order (the condition under which its waits
-cannot form a cycle)."""
+cannot form a cycle); the NSA ordered mode's unit order is checked the same way."""
 import os
 import shutil
 import subprocess
@@ -34,8 +34,9 @@ def plan_lines():
 
 
 def test_every_shape_planned(plan_lines):
-    assert len(plan_lines) == 15
-    for name, r in plan_lines.items():
+    dense = {k: v for k, v in plan_lines.items() if not k.startswith("nsa_order")}
+    assert len(dense) == 15
+    for name, r in dense.items():
         if name.startswith("varlen") and name.endswith("_split"):
             assert r["on"] in (0, 1), name  # packed split batches may keep the snake order
         if r["on"]:
@@ -52,3 +53,12 @@ def test_ordered_lists_take_key_tiles_in_decreasing_order(plan_lines):
     for name, r in plan_lines.items():
         if name.endswith("_ordered"):
             assert r["on"] == 1 and r["ordered_ok"] == 1, (name, r)
+
+
+def test_nsa_ordered_unit_order(plan_lines):
+    """NSA ordered deterministic mode: the rows in decreasing block order form a permutation and the blocks
+    never increase along it."""
+    rows = {k: v for k, v in plan_lines.items() if k.startswith("nsa_order")}
+    assert len(rows) == 3
+    for name, r in rows.items():
+        assert r["perm"] == 1 and r["mono"] == 1, (name, r)
